@@ -1,0 +1,16 @@
+"""GB300 (sm_103a) SSD layer forward: C-ABI library + thin Python binding.
+
+``ssd_forward`` and friends are resolved lazily so that importing
+``mamba_ssd_layer_gb300.inputs`` does not load the CUDA library.
+"""
+from __future__ import annotations
+
+__all__ = ["ssd_forward", "ssd_forward_host", "ssd_workspace_size", "ssd_status",
+           "ssd_status_string", "library_path", "SSDError"]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)
