@@ -1,0 +1,329 @@
+"""Benchmark of the SSD layer forward on GB300.
+
+One step = one full SSD forward (chunk table, chunk states, state pass, chunk outputs)
+over the long-sequence workload b=1, T=16384, H=80, P=64, N=128, G=1, chunk 256, bf16
+x/B/C with fp32 dt/A/D. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded sample of
+the same workload (the slow baseline the GPU path is checked against).
+Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
+problems, no collective on the data path); value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SSD fwd tokens/s and % of bf16 tensor/HBM roofline, T=2K–16K, N=128"
+UNIT = "tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def algorithmic_bytes(w, batch_rows, nseq) -> int:
+    """Bytes the forward must move at minimum: x in, y out (bf16), B, C in (bf16), dt in (fp32),
+    A, D, and the initial/final states when used (fp32)."""
+    T, H, P, N, G = batch_rows, w.nheads, w.headdim, w.dstate, w.ngroups
+    e = 2 if w.dtype == "bf16" else 4
+    by = 2 * T * H * P * e + 2 * T * G * N * e + 4 * T * H + 8 * H
+    by += nseq * H * P * N * 4 * (2 if w.init_state else 1)
+    return int(by)
+
+
+def algorithmic_flops(w, batch_rows) -> int:
+    """Useful FLOPs of the chunked algorithm per the pages' cost model: causal C B^T per group
+    (Q+1)N/2 MACs per token, masked (L o CB^T) X per head (Q+1)P/2 MACs, chunk state and
+    C.state per head N*P MACs each -> 2 FLOP per MAC."""
+    Q, H, P, N, G = w.chunk, w.nheads, w.headdim, w.dstate, w.ngroups
+    macs_per_token = G * (Q + 1) * N / 2 + H * ((Q + 1) * P / 2 + 2 * N * P)
+    return int(2 * macs_per_token * batch_rows)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+        else:
+            self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, w):
+    """The oracle on the host cores, bounded: each step runs a sample of the workload."""
+    import oracle
+    from mamba_ssd_layer_gb300.inputs import make_inputs, small_variant
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    # sample: every head, the first `tokens` tokens of the sequence (~several seconds per step)
+    tokens = min(w.seqlen, args.ref_tokens)
+    ws = small_variant(w, seqlen=tokens, nheads=w.nheads, batch=1) if not w.varlen_total else \
+        small_variant(w, seqlen=tokens, nheads=w.nheads)
+    d = make_inputs(ws)
+    threads = oracle.default_threads()
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle.ssd_recurrence(d["x"][:, :64], d["dt"][:, :64], d["A"], d["B"][:, :64], d["C"][:, :64], d["D"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
+                              d["cu_seqlens"], nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    tot = float(np.sum(times))
+    val = tokens * args.steps / tot
+    sample = f"{tokens} of {w.seqlen} tokens, all {w.nheads} heads, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+            "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (2 rotating input sets of ~350 MB each)"}
+
+
+def cpu_baseline(w, budget_tokens: int):
+    import oracle
+    from mamba_ssd_layer_gb300.inputs import make_inputs, small_variant
+    tokens = min(w.seqlen, budget_tokens)
+    d = make_inputs(small_variant(w, seqlen=tokens, nheads=w.nheads, batch=1))
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"], nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {tokens} of {w.seqlen} tokens, all {w.nheads} heads, 1 run ({dt:.1f} s)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_n128")
+    ap.add_argument("--ref-tokens", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    from mamba_ssd_layer_gb300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mamba_ssd_layer_gb300 import binding as bd
+    from mamba_ssd_layer_gb300 import ssd_forward, ssd_forward_host
+
+    d = make_inputs(w)
+    rows = d["x"].shape[0] * d["x"].shape[1]
+    nseq = (len(d["cu_seqlens"]) - 1) if d["cu_seqlens"] is not None else d["x"].shape[0]
+
+    def dev_inputs():
+        t = {}
+        for k in ("x", "B", "C"):
+            t[k] = torch.from_numpy(d[k]).to(dev, torch.bfloat16)
+        for k in ("dt", "A", "D"):
+            t[k] = torch.from_numpy(d[k]).to(dev, torch.float32)
+        t["init"] = None if d["initial_state"] is None else torch.from_numpy(d["initial_state"]).to(dev)
+        t["cu"] = None if d["cu_seqlens"] is None else torch.from_numpy(d["cu_seqlens"]).to(dev)
+        t["y"] = torch.empty_like(t["x"])
+        t["final"] = torch.empty((nseq, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+        return t
+
+    sets = [dev_inputs(), dev_inputs()]          # two rotating sets: the previous step's data is out of L2
+    ws_bytes = bd.ssd_workspace_size(1 if d["cu_seqlens"] is not None else d["x"].shape[0], d["x"].shape[1],
+                                     w.nheads, w.headdim, w.dstate, w.ngroups, bd.SSD_BF16, w.chunk,
+                                     nseq if d["cu_seqlens"] is not None else 0)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        t = sets[i % 2]
+        ssd_forward(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], chunk=w.chunk, initial_state=t["init"],
+                    cu_seqlens=t["cu"], y=t["y"], final_state=t["final"], workspace=workspace, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    status = bd.ssd_status(workspace)
+    if status != bd.SSD_OK:
+        raise RuntimeError(f"device status after warm-up: {bd.ssd_status_string(status)}")
+
+    if world > 1:
+        torch.distributed.barrier()
+    bd.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    bd.profile_enable(False)
+    kern_ms, kern_n = bd.profile_read()
+    ms = ev0.elapsed_time(ev1)
+    status = bd.ssd_status(workspace)
+    if status != bd.SSD_OK:
+        raise RuntimeError(f"device status after timing: {bd.ssd_status_string(status)}")
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_per_step = ms / args.steps
+    value = world * rows * args.steps / (ms / 1e3)
+
+    # end to end through the host entry point: pinned inputs in, y and final states out
+    hx = {k: torch.from_numpy(d[k]).to(torch.bfloat16).pin_memory() for k in ("x", "B", "C")}
+    hf = {k: torch.from_numpy(d[k]).pin_memory() for k in ("dt", "A", "D")}
+    hinit = None if d["initial_state"] is None else torch.from_numpy(d["initial_state"]).pin_memory()
+    hcu = None if d["cu_seqlens"] is None else torch.from_numpy(d["cu_seqlens"])
+    hy = torch.empty_like(hx["x"]).pin_memory()
+    hfin = torch.empty((nseq, w.nheads, w.headdim, w.dstate), dtype=torch.float32).pin_memory()
+    need = bd.load_library().ssd_host_buffer_size
+    devbuf = None
+
+    def e2e_step():
+        nonlocal devbuf
+        _, _ = ssd_forward_host(hx["x"], hf["dt"], hf["A"], hx["B"], hx["C"], hf["D"], chunk=w.chunk,
+                                initial_state=hinit, cu_seqlens=hcu, y=hy, final_state=hfin,
+                                device_buffer=devbuf, stream=stream)
+
+    import ctypes
+    shp = bd._shape(1 if hcu is not None else d["x"].shape[0], d["x"].shape[1], w.nheads, w.headdim, w.dstate,
+                    w.ngroups)
+    devbuf = torch.empty(int(need(ctypes.byref(shp), bd.SSD_BF16, w.chunk, nseq if hcu is not None else 0)),
+                         dtype=torch.uint8, device=dev)
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for t in (hx["x"], hx["B"], hx["C"], hf["dt"], hf["A"], hf["D"]))
+    h2d += 0 if hinit is None else hinit.numel() * 4
+    h2d += 0 if hcu is None else hcu.numel() * 4
+    d2h = hy.numel() * 2 + hfin.numel() * 4
+
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    alg_bytes = algorithmic_bytes(w, rows, nseq)
+    alg_flops = algorithmic_flops(w, rows)
+    kern_avg_ms = kern_ms / max(kern_n, 1)
+    # roofline of the dominant kernel: the algorithmic bytes of the whole pass over its launch time
+    achieved = alg_bytes / (kern_avg_ms / 1e3) / 1e9 if kern_n else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
+                     "peak_source": src, "kernel": "ssd_chunk_out (dominant)", "kernel_ms": kern_avg_ms,
+                     "alg_bytes_per_launch": alg_bytes,
+                     "step_frac": alg_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
+        "tflops": alg_flops / (ms_per_step / 1e3) / 1e12,
+        "e2e": {"value": world * rows * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.ref_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

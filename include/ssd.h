@@ -1,0 +1,135 @@
+/*
+ * ssd.h -- C ABI of the GB300 (sm_103a) SSD layer forward pass.
+ *
+ * The operation (one call = one layer forward over a batch):
+ *
+ *   for every sequence s, head h (group g = h / (H/G)) and token t of s:
+ *     a_t = exp(dt[t,h] * A[h])
+ *     S   = a_t * S + x[t,h,:] (outer) B[t,g,:]          S: (P, N), starts at initial_state[s,h] or 0
+ *     y[t,h,:] = S . C[t,g,:] + D[h] * x[t,h,:]
+ *   final_state[s,h] = S after the last token of s
+ *
+ * equivalently Y = (L o C B^T) X + D X with the 1-semiseparable mask
+ * L_ij = exp(sum_{k=j+1..i} dt_k A) (i >= j). It is computed with the chunked block
+ * decomposition: per-chunk cumulative sums of dt*A, diagonal blocks in the
+ * quadratic (masked attention) form, chunk states B^T X, an inter-chunk
+ * scalar-decay recurrence over the states, and C . state outputs plus the D skip.
+ *
+ * Sources: recurrence and scalar-identity A -- "Mamba-2 状态空间对偶性理论" §1.2
+ * and "LLM(十一)——Mamba" §3.1.1-3.1.2; quadratic form -- "LLM(十一)——Mamba"
+ * §3.1.3; the chunked algorithm (diagonal blocks, right/center/left factors) --
+ * "LLM(十一)——Mamba" §3.5 (3.5.1 Diagonal Blocks, 3.5.2 Low-Rank Blocks, the ssd
+ * listing in 3.5.3); variable length by state reset -- "LLM(十一)——Mamba" §3.7.3;
+ * grouped B/C heads -- "LLM(十一)——Mamba" §3.6.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (except in ssd_forward_host), row-major
+ *     and contiguous, 16-byte aligned. The caller owns every buffer and the stream.
+ *   - The library allocates no device memory. Scratch lives in the caller's workspace.
+ *   - Work is enqueued on `stream`; no call synchronises the stream except
+ *     ssd_status and ssd_forward_host.
+ *   - Return value: SSD_OK or one of the SSD_ERR_* codes below; nothing is launched
+ *     when an argument check fails. Errors raised on the device (a bounded wait that
+ *     timed out) are recorded in the workspace and read back by ssd_status.
+ */
+#ifndef SSD_GB300_H
+#define SSD_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage type of x, B, C and y. dt, A, D and the states are always fp32. */
+typedef enum { SSD_F32 = 0, SSD_BF16 = 1 } ssd_dtype;
+
+#define SSD_OK               0
+#define SSD_ERR_INVALID_ARG  1  /* bad shape, NULL pointer, misalignment, H % G, cu_seqlens with batch != 1 */
+#define SSD_ERR_UNSUPPORTED  2  /* chunk or head/state size outside the kernel set, or not an sm_103 device */
+#define SSD_ERR_CUDA         3  /* a CUDA runtime call or launch failed */
+#define SSD_ERR_TIMEOUT      4  /* a bounded device-side wait gave up (reported by ssd_status) */
+#define SSD_ERR_WORKSPACE    5  /* workspace NULL, misaligned or smaller than ssd_workspace_size() */
+
+/*
+ * Problem shape. batch rows of seqlen tokens each (dense), or, with cu_seqlens,
+ * batch == 1 and seqlen = total number of packed tokens.
+ *   nheads  H  -- heads; headdim P -- channels per head; dstate N -- state size;
+ *   ngroups G  -- B/C groups, G divides H, heads [g*H/G, (g+1)*H/G) share group g.
+ */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups;
+} ssd_shape;
+
+/*
+ * Bytes of device workspace ssd_forward needs for this shape, dtype, chunk and
+ * number of sequences (nseq = number of cu_seqlens segments, or 0 for a dense batch).
+ * Returns 0 when the arguments are invalid or unsupported.
+ */
+size_t ssd_workspace_size(const ssd_shape *shape, ssd_dtype dtype, int chunk, int nseq);
+
+/*
+ * One forward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ *   x             (batch, seqlen, H, P)  dtype
+ *   dt            (batch, seqlen, H)     fp32, expected > 0 (used as given: no softplus, no bias)
+ *   A             (H)                    fp32, expected < 0
+ *   B, C          (batch, seqlen, G, N)  dtype
+ *   D             (H)                    fp32, or NULL for no skip term
+ *   chunk         block length Q of the decomposition: 64, 128 or 256. The result does not
+ *                 depend on it beyond rounding; it sets the granularity of the state pass.
+ *   initial_state (nseq_or_batch, H, P, N) fp32, or NULL for zero states
+ *   cu_seqlens    (nseq + 1) int32 DEVICE array of segment offsets into the packed row
+ *                 (first 0, last seqlen, non-decreasing), or NULL for a dense batch.
+ *                 Requires batch == 1. No state crosses a segment boundary.
+ *   nseq          number of segments when cu_seqlens != NULL, else ignored
+ *   y             (batch, seqlen, H, P)  dtype, written
+ *   final_state   (nseq_or_batch, H, P, N) fp32, written, or NULL
+ *   workspace     device scratch of at least ssd_workspace_size(...) bytes, 256-byte aligned;
+ *                 its contents on entry do not matter
+ *
+ * Supported sizes: dtype SSD_F32 -- any P <= 256, N <= 256 (SIMT fp32 kernels);
+ * dtype SSD_BF16 -- P == 64, N in {64, 128, 256}, H/G even (tcgen05 kernels).
+ * y must not alias any input. Inputs must be finite.
+ */
+int ssd_forward(const ssd_shape *shape, ssd_dtype dtype,
+                const void *x, const float *dt, const float *A,
+                const void *B, const void *C, const float *D,
+                int chunk, const float *initial_state,
+                const int32_t *cu_seqlens, int nseq,
+                void *y, float *final_state,
+                void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/*
+ * The same forward pass on HOST buffers: copies the inputs to device memory
+ * carved out of `device_buffer`, runs ssd_forward, copies y and final_state back,
+ * and synchronises `stream`. Host buffers should be pinned for full copy speed.
+ * cu_seqlens is a HOST array here. device_buffer must hold at least
+ * ssd_host_buffer_size(...) bytes (inputs, outputs and workspace).
+ */
+size_t ssd_host_buffer_size(const ssd_shape *shape, ssd_dtype dtype, int chunk, int nseq);
+int ssd_forward_host(const ssd_shape *shape, ssd_dtype dtype,
+                     const void *x, const float *dt, const float *A,
+                     const void *B, const void *C, const float *D,
+                     int chunk, const float *initial_state,
+                     const int32_t *cu_seqlens, int nseq,
+                     void *y, float *final_state,
+                     void *device_buffer, size_t device_buffer_bytes,
+                     void *stream);
+
+/*
+ * Synchronises `stream`, then returns the device-side status recorded in the
+ * workspace by the last ssd_forward that used it (SSD_OK or SSD_ERR_TIMEOUT),
+ * or SSD_ERR_CUDA if the copy itself fails.
+ */
+int ssd_status(const void *workspace, void *stream);
+
+/* Static, NUL-terminated description of a return code. */
+const char *ssd_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSD_GB300_H */

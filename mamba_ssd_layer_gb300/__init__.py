@@ -6,7 +6,7 @@
 from __future__ import annotations
 
 __all__ = ["ssd_forward", "ssd_forward_host", "ssd_workspace_size", "ssd_status",
-           "ssd_status_string", "library_path", "SSDError"]
+           "ssd_status_string", "library_path", "SSDError", "profile_enable", "profile_read"]
 
 
 def __getattr__(name):

@@ -1,0 +1,216 @@
+"""Thin Python binding of the SSD C ABI (``include/ssd.h``), via ctypes.
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library. PyTorch supplies device memory and the current stream. If the library
+has not been built, importing the entry points raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_WORKSPACE = range(6)
+SSD_F32, SSD_BF16 = 0, 1
+
+_lib = None
+
+
+class SSDError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {ssd_status_string(code)} (code {code})")
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64), ("nheads", ctypes.c_int64),
+                ("headdim", ctypes.c_int64), ("dstate", ctypes.c_int64), ("ngroups", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load ``_lib/libssd_gb300.so`` and declare its signatures (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"SSD CUDA library not built ({path} missing); run mamba_ssd_layer_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, fp, sz, i32 = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    shp = ctypes.POINTER(_Shape)
+    lib.ssd_workspace_size.argtypes = [shp, i32, i32, i32]
+    lib.ssd_workspace_size.restype = sz
+    lib.ssd_host_buffer_size.argtypes = [shp, i32, i32, i32]
+    lib.ssd_host_buffer_size.restype = sz
+    fwd_args = [shp, i32, vp, fp, fp, vp, vp, fp, i32, fp, vp, i32, vp, fp, vp, sz, vp]
+    lib.ssd_forward.argtypes = fwd_args
+    lib.ssd_forward.restype = i32
+    lib.ssd_forward_host.argtypes = fwd_args
+    lib.ssd_forward_host.restype = i32
+    lib.ssd_status.argtypes = [vp, vp]
+    lib.ssd_status.restype = i32
+    lib.ssd_profile_enable.argtypes = [i32]
+    lib.ssd_profile_enable.restype = i32
+    lib.ssd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+    lib.ssd_profile_read.restype = i32
+    lib.ssd_status_string.argtypes = [i32]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def ssd_status_string(code: int) -> str:
+    return load_library().ssd_status_string(int(code)).decode()
+
+
+def _shape(batch, seqlen, H, P, N, G) -> _Shape:
+    return _Shape(int(batch), int(seqlen), int(H), int(P), int(N), int(G))
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return SSD_F32
+    if t.dtype == torch.bfloat16:
+        return SSD_BF16
+    raise TypeError(f"x/B/C must be float32 or bfloat16, got {t.dtype}")
+
+
+def ssd_workspace_size(batch, seqlen, nheads, headdim, dstate, ngroups, dtype_code, chunk, nseq=0) -> int:
+    return int(load_library().ssd_workspace_size(ctypes.byref(_shape(batch, seqlen, nheads, headdim, dstate, ngroups)),
+                                                 int(dtype_code), int(chunk), int(nseq)))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, shape, dtype, device):
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+def ssd_forward(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu_seqlens=None,
+                return_final_state: bool = True, y=None, final_state=None, workspace=None, stream=None):
+    """SSD forward through the C ABI on CUDA tensors.
+
+    x (batch, T, H, P) and B, C (batch, T, G, N) in float32 or bfloat16 (the same);
+    dt (batch, T, H), A (H,), D (H,) or None, initial_state (nseq, H, P, N) or None: float32.
+    cu_seqlens: int32 (nseq + 1,) on the device, batch must be 1. Returns (y, final_state),
+    final_state None when return_final_state is False. The work is enqueued on `stream`
+    (default: torch's current stream); nothing is synchronised.
+    """
+    import torch
+    batch, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    dev = x.device
+    code = _dtype_code(x)
+    _check(x, "x", (batch, T, H, P), x.dtype, dev)
+    _check(dt, "dt", (batch, T, H), torch.float32, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(B, "B", (batch, T, G, N), x.dtype, dev)
+    _check(C, "C", (batch, T, G, N), x.dtype, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    nseq = 0
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.device != dev:
+            raise TypeError("cu_seqlens must be an int32 tensor on the same device")
+        nseq = cu_seqlens.shape[0] - 1
+    nseq_eff = nseq if cu_seqlens is not None else batch
+    _check(initial_state, "initial_state", (nseq_eff, H, P, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((nseq_eff, H, P, N), dtype=torch.float32, device=dev)
+    shape = _shape(batch, T, H, P, N, G)
+    lib = load_library()
+    ws_bytes = int(lib.ssd_workspace_size(ctypes.byref(shape), code, int(chunk), int(nseq)))
+    if ws_bytes == 0:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_workspace_size")
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ssd_forward(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                         int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
+                         _ptr(final_state) if return_final_state else None,
+                         workspace.data_ptr(), ws_bytes, ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_forward")
+    return y, (final_state if return_final_state else None)
+
+
+def ssd_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the device status word of `workspace`."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return int(load_library().ssd_status(workspace.data_ptr(), ctypes.c_void_p(stream.cuda_stream)))
+
+
+def ssd_forward_host(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu_seqlens=None,
+                     return_final_state: bool = True, y=None, final_state=None, device_buffer=None,
+                     stream=None):
+    """The same forward pass on HOST (CPU, ideally pinned) tensors through ``ssd_forward_host``:
+    host->device copies, the kernels and the device->host copies all happen inside the C call,
+    which synchronises the stream before returning."""
+    import torch
+    batch, T, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    code = _dtype_code(x)
+    cpu = torch.device("cpu")
+    for t, name in ((x, "x"), (dt, "dt"), (A, "A"), (B, "B"), (C, "C"), (D, "D"), (initial_state, "initial_state"),
+                    (cu_seqlens, "cu_seqlens")):
+        if t is not None and (t.device != cpu or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    nseq = 0 if cu_seqlens is None else cu_seqlens.shape[0] - 1
+    nseq_eff = nseq if cu_seqlens is not None else batch
+    if y is None:
+        y = torch.empty_like(x)
+    if return_final_state and final_state is None:
+        final_state = torch.empty((nseq_eff, H, P, N), dtype=torch.float32)
+    shape = _shape(batch, T, H, P, N, G)
+    lib = load_library()
+    need = int(lib.ssd_host_buffer_size(ctypes.byref(shape), code, int(chunk), int(nseq)))
+    if need == 0:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_host_buffer_size")
+    if device_buffer is None or device_buffer.numel() < need:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(device_buffer.device)
+    rc = lib.ssd_forward_host(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                              int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
+                              _ptr(final_state) if return_final_state else None,
+                              device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_forward_host")
+    return y, (final_state if return_final_state else None)
+
+
+def profile_enable(on: bool = True) -> None:
+    """Record CUDA events around the dominant kernel of every later ssd_forward on this thread."""
+    load_library().ssd_profile_enable(1 if on else 0)
+
+
+def profile_read():
+    """(summed milliseconds, launches) of the dominant kernel since the last read; resets."""
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_int(0)
+    rc = load_library().ssd_profile_read(ctypes.byref(ms), ctypes.byref(n))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_profile_read")
+    return ms.value, n.value

@@ -1,0 +1,97 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every entry point the
+header declares, sizes workspaces, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mamba_ssd_layer_gb300 import build as B
+from mamba_ssd_layer_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return bd.load_library()
+
+
+def header_functions():
+    inc = os.path.join(ROOT, "include")
+    txt = "\n".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char)\s*\*?\s*(ssd_\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_header_declares_entry_points():
+    names = header_functions()
+    assert {"ssd_forward", "ssd_workspace_size", "ssd_status", "ssd_status_string",
+            "ssd_forward_host", "ssd_host_buffer_size"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def shape(batch=1, T=256, H=4, P=64, N=128, G=1):
+    return bd._Shape(batch, T, H, P, N, G)
+
+
+def test_workspace_size(lib):
+    s = shape(batch=2, T=1000, H=4, P=64, N=128)
+    ws = lib.ssd_workspace_size(ctypes.byref(s), bd.SSD_BF16, 256, 0)
+    chunks = 2 * 4  # ceil(1000/256) per row
+    assert ws >= chunks * 4 * 64 * 128 * 4
+    # varlen bound: ceil(rows/Q) + nseq chunks
+    s1 = shape(batch=1, T=1000)
+    wv = lib.ssd_workspace_size(ctypes.byref(s1), bd.SSD_BF16, 256, 5)
+    assert wv >= (4 + 5) * 4 * 64 * 128 * 4
+    # unsupported chunk / shapes give 0
+    assert lib.ssd_workspace_size(ctypes.byref(s), bd.SSD_BF16, 100, 0) == 0
+    assert lib.ssd_workspace_size(ctypes.byref(shape(P=32)), bd.SSD_BF16, 256, 0) == 0
+    assert lib.ssd_workspace_size(ctypes.byref(shape(H=3, G=2)), bd.SSD_F32, 64, 0) == 0
+    assert lib.ssd_workspace_size(ctypes.byref(shape(P=16, N=16)), bd.SSD_F32, 64, 0) > 0
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert isinstance(bd.ssd_status_string(code), str) and bd.ssd_status_string(code)
+    assert bd.ssd_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every case below fails host-side checks
+
+
+def call(lib, s, dtype=bd.SSD_BF16, chunk=256, x=FAKE, ws=FAKE, ws_bytes=1 << 40, cu=None, nseq=0, A=FAKE):
+    return lib.ssd_forward(ctypes.byref(s), dtype, x, FAKE, A, FAKE, FAKE, None, chunk, None, cu, nseq,
+                           FAKE, None, ws, ws_bytes, None)
+
+
+def test_argument_errors_before_any_device_work(lib):
+    s = shape()
+    assert call(lib, shape(H=3, G=2)) == bd.SSD_ERR_INVALID_ARG            # H % G
+    assert call(lib, s, chunk=100) == bd.SSD_ERR_UNSUPPORTED                 # chunk
+    assert call(lib, shape(P=32)) == bd.SSD_ERR_UNSUPPORTED                  # bf16 needs P == 64
+    assert call(lib, shape(N=96)) == bd.SSD_ERR_UNSUPPORTED
+    assert call(lib, s, x=FAKE + 2) == bd.SSD_ERR_INVALID_ARG                # misaligned
+    assert call(lib, s, x=None) == bd.SSD_ERR_INVALID_ARG                    # NULL input
+    assert call(lib, s, A=None) == bd.SSD_ERR_INVALID_ARG
+    assert call(lib, s, ws=None) == bd.SSD_ERR_WORKSPACE
+    assert call(lib, s, ws=FAKE + 16) == bd.SSD_ERR_WORKSPACE               # not 256-aligned
+    assert call(lib, s, ws_bytes=16) == bd.SSD_ERR_WORKSPACE
+    assert call(lib, shape(batch=2), cu=FAKE, nseq=2) == bd.SSD_ERR_INVALID_ARG  # varlen needs batch 1
+    assert call(lib, s, cu=FAKE, nseq=0) == bd.SSD_ERR_INVALID_ARG
+    assert call(lib, s, dtype=7) == bd.SSD_ERR_INVALID_ARG
+
+
+def test_no_gpu_reports_cuda_or_unsupported(lib):
+    # valid arguments on a machine without a usable sm_103 device: an error code, never a crash
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    s = shape()
+    rc = call(lib, s)
+    assert rc in (bd.SSD_ERR_CUDA, bd.SSD_ERR_UNSUPPORTED)

@@ -1,0 +1,129 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same
+seeded inputs. Tolerances (normwise max|out - ref| / max|ref|): 1e-4 for the fp32
+path, 1e-2 for the bf16 path (fp32 accumulation), for y and the final states alike."""
+import numpy as np
+import pytest
+
+from mamba_ssd_layer_gb300.inputs import WORKLOADS, make_inputs, small_variant
+from ssd_util import TOL, normwise, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def check(d, dtype, chunk, heads=None, use_D=True):
+    y, f = run_gpu(d, dtype, chunk, use_D=use_D)
+    yr, fr = run_oracle(d, heads=heads, use_D=use_D)
+    if heads is not None:
+        y, f = y[:, :, heads], f[:, heads]
+    ey, ef = normwise(y, yr), normwise(f, fr)
+    print(f"[parity] {dtype} chunk={chunk} y_err={ey:.3e} final_err={ef:.3e}")
+    assert np.isfinite(y).all() and np.isfinite(f).all()
+    assert ey <= TOL[dtype], f"y error {ey:.3e}"
+    assert ef <= TOL[dtype], f"final state error {ef:.3e}"
+    return ey, ef
+
+
+# ---------------------------------------------------------------- fp32 path
+def test_fp32_tiny_workload():
+    d = make_inputs(WORKLOADS["fp32_tiny"])
+    check(d, "f32", 64)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+def test_fp32_chunk_sizes_ragged(chunk):
+    w = WORKLOADS["fp32_tiny"].with_(batch=2, seqlen=700, nheads=4, init_state=True, seed=77)
+    check(make_inputs(w), "f32", chunk)
+
+
+def test_fp32_odd_sizes_groups():
+    w = WORKLOADS["fp32_tiny"].with_(batch=3, seqlen=131, nheads=6, headdim=12, dstate=20, ngroups=3,
+                                     init_state=True, seed=78)
+    check(make_inputs(w), "f32", 64)
+
+
+# ---------------------------------------------------------------- bf16 path, small (whole output vs oracle)
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("N", [64, 128])
+def test_bf16_chunk_sizes_ragged(chunk, N):
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=1000, nheads=4, batch=2).with_(dstate=N, seed=90 + N)
+    check(make_inputs(w), "bf16", chunk)
+
+
+def test_bf16_chunk_invariance():
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=777, nheads=2, batch=1).with_(seed=91)
+    d = make_inputs(w)
+    outs = [run_gpu(d, "bf16", q) for q in (64, 128, 256)]
+    for (y, f) in outs[1:]:
+        assert normwise(y, outs[0][0]) <= TOL["bf16"]
+        assert normwise(f, outs[0][1]) <= TOL["bf16"]
+
+
+def test_bf16_no_skip_no_init():
+    w = small_variant(WORKLOADS["m2_130m"], seqlen=512, nheads=4, batch=2).with_(seed=92)
+    check(make_inputs(w), "bf16", 256, use_D=False)
+
+
+@pytest.mark.parametrize("T", [1, 17, 128, 129, 255, 256, 257])
+def test_bf16_short_and_boundary_lengths(T):
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=T, nheads=2, batch=3).with_(seed=93 + T)
+    check(make_inputs(w), "bf16", 256)
+
+
+def test_bf16_grouped_heads():
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=600, nheads=8, batch=1).with_(ngroups=2, seed=94)
+    check(make_inputs(w), "bf16", 128)
+
+
+def test_bf16_varlen_small():
+    w = small_variant(WORKLOADS["varlen"], seqlen=3000, nheads=4).with_(seg_min=1, seg_max=700, seed=95,
+                                                                      init_state=True)
+    d = make_inputs(w)
+    assert len(d["cu_seqlens"]) > 4
+    check(d, "bf16", 256)
+
+
+def test_fp32_varlen_small():
+    w = small_variant(WORKLOADS["varlen"], seqlen=900, nheads=2).with_(headdim=16, dstate=16, dtype="f32",
+                                                                     seg_min=1, seg_max=200, seed=96,
+                                                                     init_state=True)
+    check(make_inputs(w), "f32", 64)
+
+
+def test_empty_sequence():
+    import torch
+    from mamba_ssd_layer_gb300 import ssd_forward
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=0, nheads=2, batch=2).with_(seed=97)
+    d = make_inputs(w)
+    from ssd_util import to_device
+    t = to_device(d, "bf16")
+    y, f = ssd_forward(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], chunk=256,
+                       initial_state=t["initial_state"])
+    torch.cuda.synchronize()
+    assert y.shape[1] == 0
+    assert torch.equal(f.cpu(), t["initial_state"].cpu())
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import torch
+    from mamba_ssd_layer_gb300 import ssd_forward_host
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=512, nheads=4, batch=2).with_(seed=98)
+    d = make_inputs(w)
+    y_dev, f_dev = run_gpu(d, "bf16", 256)
+    h = {k: (torch.from_numpy(d[k]).bfloat16() if k in ("x", "B", "C") else torch.from_numpy(d[k]))
+         for k in ("x", "dt", "A", "B", "C", "D", "initial_state")}
+    y, f = ssd_forward_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], chunk=256,
+                            initial_state=h["initial_state"])
+    assert np.array_equal(y.float().numpy(), y_dev.astype(np.float32))
+    assert np.array_equal(f.numpy(), f_dev.astype(np.float32))
+
+
+# ---------------------------------------------------------------- full workloads, sampled heads
+FULL = [("m2_130m", [0, 11, 23]), ("m2_2p7b", [0, 41, 79]), ("long_n64", [3, 77]),
+        ("long_n128", [0, 40, 79]), ("varlen", [0, 31])]
+
+
+@pytest.mark.parametrize("name,heads", FULL, ids=[f[0] for f in FULL])
+def test_full_workload_sampled_heads(name, heads):
+    w = WORKLOADS[name]
+    d = make_inputs(w)
+    check(d, "bf16", w.chunk, heads=heads)
