@@ -129,6 +129,14 @@ int ssd_status(const void *workspace, void *stream);
 /* Static, NUL-terminated description of a return code. */
 const char *ssd_status_string(int code);
 
+/*
+ * Detail of the most recent SSD_ERR_CUDA returned to the calling host thread: the
+ * failing step and the CUDA runtime's error name (e.g. "fused launch:
+ * cudaErrorInvalidValue"), or "" if none. The string stays valid until the next call
+ * from the same thread.
+ */
+const char *ssd_last_error_detail(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,13 @@ _lib = None
 class SSDError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {ssd_status_string(code)} (code {code})")
+        detail = ""
+        if code == SSD_ERR_CUDA:
+            try:
+                detail = load_library().ssd_last_error_detail().decode()
+            except Exception:
+                pass
+        super().__init__(f"{where}: {ssd_status_string(code)} (code {code})" + (f" [{detail}]" if detail else ""))
 
 
 class _Shape(ctypes.Structure):
@@ -59,6 +65,8 @@ def load_library():
     lib.ssd_profile_enable.restype = i32
     lib.ssd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
     lib.ssd_profile_read.restype = i32
+    lib.ssd_last_error_detail.argtypes = []
+    lib.ssd_last_error_detail.restype = ctypes.c_char_p
     lib.ssd_status_string.argtypes = [i32]
     lib.ssd_status_string.restype = ctypes.c_char_p
     _lib = lib

@@ -2,6 +2,7 @@
 // argument checks, workspace carving, device checks and dispatch to the fp32
 // (SIMT) or bf16 (tcgen05) kernels. Nothing here allocates device memory.
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <cuda_runtime.h>
 
@@ -40,7 +41,7 @@ size_t elt(ssd_dtype d) { return d == SSD_F32 ? 4 : 2; }
 // The kernels are built for sm_103a only.
 int check_device(int* num_sms) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SSD_ERR_CUDA;
+    if (note_cuda_error("cudaGetDevice", cudaGetDevice(&dev)) != cudaSuccess) return SSD_ERR_CUDA;
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -56,10 +57,19 @@ struct ProfState {
     size_t used = 0;               // events recorded since the last read
 };
 thread_local ProfState g_prof;
+thread_local char g_err_detail[160] = "";
 
 }  // namespace
 
 namespace ssd {
+cudaError_t note_cuda_error(const char* step, cudaError_t e) {
+    if (e != cudaSuccess) {
+        snprintf(g_err_detail, sizeof(g_err_detail), "%s: %s", step, cudaGetErrorName(e));
+        (void)cudaGetLastError();
+    }
+    return e;
+}
+
 void prof_begin(cudaStream_t s) {
     if (!g_prof.on) return;
     if (g_prof.used + 2 > g_prof.ev.size()) {
@@ -106,7 +116,7 @@ int ssd_profile_read(double* total_ms, int* launches) {
 size_t ssd_workspace_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int nseq) {
     const bool varlen = nseq > 0;
     if (check_shape(s, dtype, chunk, nseq, varlen) != SSD_OK) return 0;
-    return ws_layout(*s, chunk, varlen ? nseq : s->batch, varlen).total;
+    return ws_layout(*s, dtype, chunk, varlen ? nseq : s->batch, varlen).total;
 }
 
 int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
@@ -124,10 +134,11 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
         if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
     if (varlen && nseq <= 0) return SSD_ERR_INVALID_ARG;
     const int64_t nseq_eff = varlen ? nseq : s->batch;
-    const WsLayout L = ws_layout(*s, chunk, nseq_eff, varlen);
+    const WsLayout L = ws_layout(*s, dtype, chunk, nseq_eff, varlen);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
         return SSD_ERR_WORKSPACE;
     int num_sms = 0;
+    g_err_detail[0] = '\0';
     rc = check_device(&num_sms);
     if (rc != SSD_OK) return rc;
 
@@ -148,8 +159,18 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
     p.stream = static_cast<cudaStream_t>(stream);
     p.num_sms = num_sms;
 
-    cudaError_t e = launch_prep(p);
-    if (e == cudaSuccess) e = (dtype == SSD_F32) ? launch_f32_path(p) : launch_bf16_path(p);
+    cudaError_t e;
+    if (L.fused) {
+        const int64_t np = fused_pieces(p);
+        if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;   // more SMs than the workspace bound allows
+        e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.flags(), np));
+        if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p));
+    } else {
+        e = note_cuda_error("prep launch", launch_prep(p, chunk, nullptr, 0));
+        if (e == cudaSuccess)
+            e = note_cuda_error(dtype == SSD_F32 ? "fp32 launch" : "bf16 launch",
+                                (dtype == SSD_F32) ? launch_f32_path(p) : launch_bf16_path(p));
+    }
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
@@ -238,6 +259,8 @@ int ssd_status(const void* workspace, void* stream) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
     return v;
 }
+
+const char* ssd_last_error_detail(void) { return g_err_detail; }
 
 const char* ssd_status_string(int code) {
     switch (code) {

@@ -22,12 +22,13 @@ namespace ssd {
 __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ cu, int64_t nseq,
                                                     int64_t seqlen, int64_t rows, int Q,
                                                     int* header, ChunkDesc* chunks, int32_t* seqoff,
-                                                    int64_t max_chunks) {
+                                                    int64_t max_chunks, int* flags, int64_t nflags) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     __shared__ int bad;
     const int tid = threadIdx.x;
     if (tid == 0) { carry = 0; bad = 0; }
+    for (int64_t i = tid; i < nflags; i += blockDim.x) flags[i] = 0;
     __syncthreads();
     // pass 1: validate
     for (int64_t s = tid; s < nseq; s += blockDim.x) {
@@ -89,12 +90,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
         seqoff[nseq] = carry;
         header[0] = SSD_OK;
         header[1] = carry;
+        header[2] = 0;   // first device-side timeout location (diagnostic), 0 = none
+        header[3] = 0;
     }
 }
 
-cudaError_t launch_prep(const Problem& p) {
+cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags) {
     prep_kernel<<<1, 1024, 0, p.stream>>>(p.varlen ? p.cu_seqlens : nullptr, p.nseq, p.s.seqlen, p.rows,
-                                          p.chunk, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks);
+                                          q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks, flags, nflags);
     return cudaGetLastError();
 }
 

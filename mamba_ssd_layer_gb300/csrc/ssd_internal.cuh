@@ -16,34 +16,62 @@ struct ChunkDesc {
 };
 
 // Workspace layout (byte offsets, every section 256-byte aligned).
-//   header  : int32 status, int32 number of chunks actually built
-//   chunks  : ChunkDesc[max_chunks]
+//   header  : int32 status, int32 number of chunks (tiles) actually built, int32 location
+//             code of the first device-side timeout (0 = none), int32 spare
+//   chunks  : ChunkDesc[max_chunks]  (chunks of `chunk` tokens; 128-token tiles on the fused path)
 //   seqoff  : int32[nseq + 1], first chunk of every sequence
+// three-kernel path:
 //   decay   : float[max_chunks * H], exp(sum of dt*A over the chunk)
 //   states  : float[max_chunks * H * P * N]; the chunk-state kernel writes each chunk's
 //             local end state here and the state pass overwrites it in place with the
 //             true state entering the chunk
+// fused path (bf16, P = 64, N <= 128):
+//   flags   : int32[max_pieces]  0 = nothing published, 1 = aggregate, 2 = inclusive state
+//   pdecay  : float[max_pieces * 2], decay of each piece's published segment per head
+//   agg     : float[max_pieces * 128 * N], local end state of the piece's last segment
+//   incl    : float[max_pieces * 128 * N], true end state of that segment
+constexpr int kFusedTile = 128;
+constexpr int kFusedMaxGrid = 256;
+constexpr int kFusedPieceTiles = 8;
+
 struct WsLayout {
-    size_t header, chunks, seqoff, decay, states, total;
-    int64_t max_chunks, nseq;
+    size_t header, chunks, seqoff, decay, states, flags, pdecay, agg, incl, total;
+    int64_t max_chunks, nseq, max_pieces;
+    bool fused;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(const ssd_shape& s, int chunk, int64_t nseq_eff, bool varlen) {
+inline bool use_fused_path(const ssd_shape& s, ssd_dtype dtype) {
+    return dtype == SSD_BF16 && s.headdim == 64 && (s.dstate == 64 || s.dstate == 128) &&
+           ((s.nheads / s.ngroups) % 2 == 0);
+}
+
+inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_t nseq_eff, bool varlen) {
     WsLayout w{};
+    w.fused = use_fused_path(s, dtype);
+    const int q = w.fused ? kFusedTile : chunk;
     const int64_t rows = s.batch * s.seqlen;
     w.nseq = nseq_eff;
     if (varlen)
-        w.max_chunks = (rows + chunk - 1) / chunk + nseq_eff;
+        w.max_chunks = (rows + q - 1) / q + nseq_eff;
     else
-        w.max_chunks = s.batch * ((s.seqlen + chunk - 1) / chunk);
+        w.max_chunks = s.batch * ((s.seqlen + q - 1) / q);
     size_t off = 0;
     w.header = off; off = align256(off + 16);
     w.chunks = off; off = align256(off + sizeof(ChunkDesc) * (size_t)(w.max_chunks > 0 ? w.max_chunks : 1));
     w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
-    w.decay = off;  off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads));
-    w.states = off; off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads * s.headdim * s.dstate));
+    if (w.fused) {
+        const int64_t L = (s.nheads / 2) * w.max_chunks;
+        w.max_pieces = L / kFusedPieceTiles + kFusedMaxGrid;
+        w.flags = off;  off = align256(off + sizeof(int32_t) * (size_t)w.max_pieces);
+        w.pdecay = off; off = align256(off + sizeof(float) * 2 * (size_t)w.max_pieces);
+        w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * s.dstate));
+        w.incl = off;   off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * s.dstate));
+    } else {
+        w.decay = off;  off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads));
+        w.states = off; off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads * s.headdim * s.dstate));
+    }
     w.total = off;
     return w;
 }
@@ -77,19 +105,26 @@ struct Problem {
     int32_t* seqoff() const { return reinterpret_cast<int32_t*>(ws + L.seqoff); }
     float* decay() const { return reinterpret_cast<float*>(ws + L.decay); }
     float* states() const { return reinterpret_cast<float*>(ws + L.states); }
+    int* flags() const { return reinterpret_cast<int*>(ws + L.flags); }
 };
 
+// ssd_api.cu: records the failing step of an SSD_ERR_CUDA for ssd_last_error_detail
+// and clears the runtime's sticky "last error" so later calls do not inherit it.
+cudaError_t note_cuda_error(const char* step, cudaError_t e);
 // ssd_api.cu: optional event pair around the dominant kernel (see ssd_profile.h)
 void prof_begin(cudaStream_t s);
 void prof_end(cudaStream_t s);
 
-// ssd_common.cu
-cudaError_t launch_prep(const Problem& p);
+// ssd_common.cu: chunk (tile) table of `q` tokens; zeroes `nflags` piece flags
+cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags);
 cudaError_t launch_state_pass(const Problem& p);
 // ssd_f32.cu
 cudaError_t launch_f32_path(const Problem& p);
-// ssd_tc.cu
+// ssd_tc.cu (three-kernel tcgen05 path)
 cudaError_t launch_bf16_path(const Problem& p);
 bool bf16_path_supports(const ssd_shape& s, int chunk);
+// ssd_fused.cu (single-pass tcgen05 path)
+int64_t fused_pieces(const Problem& p);
+cudaError_t launch_fused(const Problem& p);
 
 }  // namespace ssd

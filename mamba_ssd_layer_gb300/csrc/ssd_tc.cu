@@ -178,7 +178,10 @@ chunk_state_tc(const __grid_constant__ TcMaps maps, const int* __restrict__ head
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, (uint32_t)(N < 32 ? 32 : N));
+    if (warp == 0) {
+        __syncwarp();
+        tmem_dealloc(tmem, (uint32_t)(N < 32 ? 32 : N));
+    }
 }
 
 // ----------------------------------------------------------------------------
@@ -213,12 +216,21 @@ chunk_out_tc(const __grid_constant__ TcMaps maps, const int* __restrict__ header
              const ChunkDesc* __restrict__ chunks, const float* __restrict__ dt, const float* __restrict__ A,
              const float* __restrict__ D, float* __restrict__ states, __nv_bfloat16* __restrict__ y,
              int H, int N, int G, int Q) {
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ float cs[2][256];
-
+    // all shared memory is dynamic: swizzled regions first (1024-byte aligned), then the
+    // cumsums, barriers and the TMEM address
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (header_in[0] != SSD_OK || (int)blockIdx.x >= header_in[1]) return;
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0) record_status(status, SSD_ERR_UNSUPPORTED);
+        return;
+    }
+    const int nb_ = N / 64;
+    uint8_t* tail = smem_raw + (size_t)(2 + 2 * nb_ + (nb_ > 2 ? nb_ : 2)) * kRegion;
+    float (*cs)[256] = reinterpret_cast<float (*)[256]>(tail);
+    uint64_t& bar_tma = *reinterpret_cast<uint64_t*>(tail + 2048);
+    uint64_t& bar_mma = *reinterpret_cast<uint64_t*>(tail + 2056);
+    uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(tail + 2064);
+
     const ChunkDesc d = chunks[blockIdx.x];
     const int h0 = 2 * blockIdx.y;
     const int g = h0 / (H / G);
@@ -228,8 +240,7 @@ chunk_out_tc(const __grid_constant__ TcMaps maps, const int* __restrict__ header
     const int lane = threadIdx.x & 31;
     const int row = threadIdx.x;   // accumulator lane = tile row (or (head, channel) for S)
 
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* xs = base;
+    uint8_t* xs = smem_raw;
     uint8_t* bs = xs + 2 * kRegion;
     uint8_t* csm = bs + (size_t)nb * kRegion;
     uint8_t* rs = csm + (size_t)nb * kRegion;
@@ -444,7 +455,10 @@ chunk_out_tc(const __grid_constant__ TcMaps maps, const int* __restrict__ header
     }
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) {
+        __syncwarp();
+        tmem_dealloc(tmem, 512);
+    }
     (void)lane;
 }
 
@@ -483,8 +497,8 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64
 }  // namespace
 
 bool bf16_path_supports(const ssd_shape& s, int chunk) {
-    return s.headdim == 64 && (s.dstate == 64 || s.dstate == 128) && ((s.nheads / s.ngroups) % 2 == 0) &&
-           (chunk == 64 || chunk == 128 || chunk == 256);
+    return s.headdim == 64 && (s.dstate == 64 || s.dstate == 128 || s.dstate == 256) &&
+           ((s.nheads / s.ngroups) % 2 == 0) && (chunk == 64 || chunk == 128 || chunk == 256);
 }
 
 cudaError_t launch_bf16_path(const Problem& p) {
@@ -507,7 +521,7 @@ cudaError_t launch_bf16_path(const Problem& p) {
     e = launch_state_pass(p);
     if (e != cudaSuccess) return e;
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns the SM
-    size_t smem_c = 1024 + (size_t)(2 + 2 * nb + (nb > 2 ? nb : 2)) * kRegion;
+    size_t smem_c = (size_t)(2 + 2 * nb + (nb > 2 ? nb : 2)) * kRegion + 2048 + 64;
     if (smem_c < 120 * 1024) smem_c = 120 * 1024;
     cudaFuncSetAttribute(chunk_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
     prof_begin(p.stream);

@@ -36,12 +36,22 @@ def to_device(d: dict, dtype: str, device="cuda"):
 
 def run_gpu(d: dict, dtype: str, chunk: int, use_D=True, return_final=True):
     import torch
+    from mamba_ssd_layer_gb300 import binding as bd
     from mamba_ssd_layer_gb300 import ssd_forward
     t = to_device(d, dtype)
+    x = t["x"]
+    nseq = 0 if t["cu_seqlens"] is None else t["cu_seqlens"].shape[0] - 1
+    ws_bytes = bd.ssd_workspace_size(x.shape[0], x.shape[1], x.shape[2], x.shape[3], t["B"].shape[3],
+                                     t["B"].shape[2], bd.SSD_F32 if dtype == "f32" else bd.SSD_BF16, chunk, nseq)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
     y, f = ssd_forward(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"] if use_D else None, chunk=chunk,
                        initial_state=t["initial_state"], cu_seqlens=t["cu_seqlens"],
-                       return_final_state=return_final)
+                       return_final_state=return_final, workspace=ws)
     torch.cuda.synchronize()
+    st = bd.ssd_status(ws)
+    if st != bd.SSD_OK:
+        hdr = ws[:16].cpu().numpy().view(np.int32)
+        raise AssertionError(f"device status: {bd.ssd_status_string(st)}; header {hdr.tolist()}")
     return (y.float().cpu().numpy().astype(np.float64),
             None if f is None else f.cpu().numpy().astype(np.float64))
 

@@ -43,7 +43,7 @@ def test_fp32_odd_sizes_groups():
 
 # ---------------------------------------------------------------- bf16 path, small (whole output vs oracle)
 @pytest.mark.parametrize("chunk", [64, 128, 256])
-@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("N", [64, 128, 256])
 def test_bf16_chunk_sizes_ragged(chunk, N):
     w = small_variant(WORKLOADS["m2_2p7b"], seqlen=1000, nheads=4, batch=2).with_(dstate=N, seed=90 + N)
     check(make_inputs(w), "bf16", chunk)
@@ -67,6 +67,21 @@ def test_bf16_no_skip_no_init():
 def test_bf16_short_and_boundary_lengths(T):
     w = small_variant(WORKLOADS["m2_2p7b"], seqlen=T, nheads=2, batch=3).with_(seed=93 + T)
     check(make_inputs(w), "bf16", 256)
+
+
+@pytest.mark.parametrize("T,H,batch", [(8192, 2, 1), (3000, 4, 3), (20000, 2, 1)])
+def test_bf16_long_chains_few_heads(T, H, batch):
+    # few head pairs and long sequences: many pieces per chain, deep look-back
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=T, nheads=H, batch=batch).with_(seed=99 + T)
+    check(make_inputs(w), "bf16", 256)
+
+
+def test_bf16_deterministic():
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=5000, nheads=4, batch=1).with_(seed=101)
+    d = make_inputs(w)
+    y1, f1 = run_gpu(d, "bf16", 256)
+    y2, f2 = run_gpu(d, "bf16", 256)
+    assert np.array_equal(y1, y2) and np.array_equal(f1, f2)
 
 
 def test_bf16_grouped_heads():
@@ -119,7 +134,7 @@ def test_host_entry_point_matches_device_entry_point():
 
 # ---------------------------------------------------------------- full workloads, sampled heads
 FULL = [("m2_130m", [0, 11, 23]), ("m2_2p7b", [0, 41, 79]), ("long_n64", [3, 77]),
-        ("long_n128", [0, 40, 79]), ("varlen", [0, 31])]
+        ("long_n128", [0, 40, 79]), ("long_n256", [1, 78]), ("varlen", [0, 31])]
 
 
 @pytest.mark.parametrize("name,heads", FULL, ids=[f[0] for f in FULL])
