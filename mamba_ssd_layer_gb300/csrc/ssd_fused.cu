@@ -100,6 +100,24 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32])
     tmem_st16(taddr + 16, b);
 }
 
+// TMEM -> registers without waiting; pair with tmem_wait_ld() before using the values
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -127,9 +145,25 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 // Barrier slots in shared memory
 enum {
     kBarFull0 = 0, kBarFull1, kBarEmpty0, kBarEmpty1,
-    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarS, kBarYFree, kBarAgg, kBarMath,
+    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree, kBarAgg, kBarMath,
+    kBarGrpL, kBarGrpS,
     kNumBars
 };
+
+// Pass-1 weights use one barrier per stage (kBarWX1a + stage): the math warps may weight the
+// next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
+// barrier before the first was waited for would make the waiter miss a phase.
+// Expected arrivals per phase: full = producer's expect_tx + its "cumsum written" arrival;
+// pass-2 signals from one math group (4 warps); pass-1 weights and the shared barrier from
+// both groups (8 warps); MMA commits 1.
+__device__ __forceinline__ uint32_t bar_count(int i) {
+    switch (i) {
+        case kBarFull0: case kBarFull1: return 2;
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarGrpL: case kBarGrpS: return 4;
+        case kBarWX1a: case kBarWX1b: case kBarMath: return 8;
+        default: return 1;
+    }
+}
 
 struct Smem {
     uint8_t* base;
@@ -139,10 +173,13 @@ struct Smem {
     __device__ uint8_t* b(int s) const { return base + s * stage_bytes() + 2 * kRegion; }
     __device__ uint8_t* c(int s) const { return base + s * stage_bytes() + 2 * kRegion + (N / 64) * kRegion; }
     __device__ uint8_t* hs() const { return base + 2 * stage_bytes(); }
-    __device__ float* cs() const { return reinterpret_cast<float*>(hs() + (N / 64) * kRegion); }      // [2][128] (x log2 e)
-    __device__ float* vtab() const { return cs() + 256; }                                             // [2][64]
-    __device__ float* misc() const { return vtab() + 128; }                                           // [64]
-    __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(misc() + 64); }          // [kNumBars]
+    // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
+    // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
+    __device__ float* cs(int s) const { return reinterpret_cast<float*>(hs() + (N / 64) * kRegion) + s * 260; }
+    __device__ float* stage_misc(int s) const { return cs(s) + 256; }
+    __device__ float* vtab() const { return cs(0) + 520; }                                            // [2][64]
+    __device__ float* misc() const { return vtab() + 128; }                                           // [8]
+    __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(misc() + 8); }           // [kNumBars]
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
 };
@@ -184,31 +221,52 @@ __device__ __forceinline__ void warp_arrive(const Smem& sm, int idx) {
 }
 
 // ---------------------------------------------------------------- work decomposition
+// A cursor over the chain-major tile list: sequence s, head pair hp, tile t of the sequence,
+// the sequence's first row and length, and how many tiles of this chain the piece still holds.
 struct Cursor {
-    int s, hp, t, nt;      // sequence, head pair, tile index in the sequence, tiles of the sequence
-    int64_t run;           // tiles of this chain left inside the piece
+    int s, hp, t, nt;
+    int64_t run;
+    int32_t seq_row0, seq_len;
 };
 
 __device__ __forceinline__ int64_t piece_begin(int64_t q, int64_t L, int64_t np) { return (q * L) / np; }
 
-__device__ __forceinline__ Cursor locate(int64_t g, int64_t g_end, const int32_t* seqoff, int nseq, int npairs) {
-    // sequence s with npairs*seqoff[s] <= g < npairs*seqoff[s+1]
+__device__ __forceinline__ Cursor locate(int64_t g, int64_t g_end, const int32_t* seqoff, const ChunkDesc* tiles,
+                                         int nseq, int npairs) {
+    // the sequence s with npairs*seqoff[s] <= g < npairs*seqoff[s+1]; empty sequences share the next
+    // sequence's offset, so the largest such s is the non-empty one holding g
     int lo = 0, hi = nseq - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if ((int64_t)npairs * seqoff[mid] <= g) lo = mid; else hi = mid - 1;
     }
-    // the largest such s is the non-empty sequence holding g (empty ones share its offset)
-    const int s = lo;
     Cursor c;
-    c.s = s;
-    c.nt = seqoff[s + 1] - seqoff[s];
-    const int64_t local = g - (int64_t)npairs * seqoff[s];
+    c.s = lo;
+    const int32_t f0 = seqoff[lo], f1 = seqoff[lo + 1];
+    c.nt = f1 - f0;
+    const int64_t local = g - (int64_t)npairs * f0;
     c.hp = (int)(local / c.nt);
     c.t = (int)(local % c.nt);
     const int64_t left = c.nt - c.t;
     c.run = (g_end - g) < left ? (g_end - g) : left;
+    const ChunkDesc first = tiles[f0], last = tiles[f1 - 1];
+    c.seq_row0 = first.row0;
+    c.seq_len = last.row0 + last.len - first.row0;
     return c;
+}
+
+__device__ __forceinline__ int tile_row0(const Cursor& c, int t) { return c.seq_row0 + kTile * t; }
+__device__ __forceinline__ int tile_len(const Cursor& c, int t) {
+    const int rem = c.seq_len - kTile * t;
+    return rem < kTile ? rem : kTile;
+}
+
+// The last chain segment of a piece (the one whose state may continue into the next piece).
+__device__ __forceinline__ Cursor last_segment(int64_t g0, int64_t g1, const FusedArgs& a) {
+    int64_t g = g0;
+    Cursor last{};
+    while (g < g1) { last = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs); g += last.run; }
+    return last;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -243,10 +301,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         return;
     }
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kBarLG || i == kBarST || i == kBarWX || i == kBarYFree || i == kBarMath) ? 8u : 1u;
-            mbar_init(sm.bars() + i, cnt);
-        }
+        for (int i = 0; i < kNumBars; ++i) mbar_init(sm.bars() + i, bar_count(i));
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
@@ -258,59 +313,112 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *sm.tmem_slot();
-
     const int64_t np = a.npieces;
 
     if (warp == 0) {
-        // ============================================================ TMA producer
-        if (lane == 0) {
-            uint32_t ph_empty = 0;   // parity bits, one per barrier index
-            uint32_t issued = 0;     // bit s: stage s has been filled before
-            int stage = 0;
-            auto load_tile = [&](const Cursor& c, int t, bool with_c) -> bool {
-                if ((issued >> stage) & 1u) {
-                    if (!wait_bar(sm, kBarEmpty0 + stage, ph_empty, a)) return false;
-                }
-                issued |= 1u << stage;
-                const ChunkDesc d = a.tiles[a.seqoff[c.s] + t];
-                const int h0 = 2 * c.hp;
+        // ============================================================ producer warp
+        // TMA for x (both heads), B and C (lane 0); dt for both heads -> the tile-local cumsum of
+        // dt*A (x log2 e), plus the segment carry in pass 1 (all lanes), written into the stage.
+        uint32_t ph = 0;
+        uint32_t issued = 0;
+        int stage = 0;
+        bool ok = true;
+        auto load_tile = [&](const Cursor& c, int t, bool pass1, float tot0, float tot1, float& carry0,
+                             float& carry1) -> bool {
+            if ((issued >> stage) & 1u) {
+                const bool w = wait_bar(sm, kBarEmpty0 + stage, ph, a);
+                if (!__all_sync(0xffffffffu, w)) return false;
+            }
+            issued |= 1u << stage;
+            const int row0 = tile_row0(c, t), len = tile_len(c, t);
+            const int h0 = 2 * c.hp;
+            uint64_t* full = sm.bars() + kBarFull0 + stage;
+            if (lane == 0) {
                 const int g = h0 / (a.H / a.G);
-                uint64_t* full = sm.bars() + kBarFull0 + stage;
-                mbar_arrive_expect_tx(full, (uint32_t)((2 + (with_c ? 2 : 1) * NB) * kRegion));
-                tma_load_3d(sm.x(stage, 0), &maps.x, full, 0, h0, d.row0);
-                tma_load_3d(sm.x(stage, 1), &maps.x, full, 0, h0 + 1, d.row0);
+                mbar_arrive_expect_tx(full, (uint32_t)((2 + (pass1 ? 1 : 2) * NB) * kRegion));
+                tma_load_3d(sm.x(stage, 0), &maps.x, full, 0, h0, row0);
+                tma_load_3d(sm.x(stage, 1), &maps.x, full, 0, h0 + 1, row0);
                 for (int k = 0; k < NB; ++k) {
-                    tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, full, 64 * k, g, d.row0);
-                    if (with_c) tma_load_3d(sm.c(stage) + k * kRegion, &maps.c, full, 64 * k, g, d.row0);
+                    tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, full, 64 * k, g, row0);
+                    if (!pass1) tma_load_3d(sm.c(stage) + k * kRegion, &maps.c, full, 64 * k, g, row0);
                 }
-                stage ^= 1;
-                return true;
-            };
-            bool ok = true;
-            for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
-                const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
-                if (g0 >= g1) continue;
-                // pass 1: last segment, if it continues past the piece
-                {
-                    int64_t g = g0;
-                    Cursor last{};
-                    while (g < g1) { last = locate(g, g1, a.seqoff, a.nseq, a.npairs); g += last.run; }
-                    if (last.t + last.run < last.nt)
-                        for (int t = last.t; t < last.t + last.run && ok; ++t) ok = load_tile(last, t, false);
+            }
+            float v[2][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int l = 4 * lane + k;
+                    v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
                 }
-                for (int64_t g = g0; g < g1 && ok;) {
-                    const Cursor c = locate(g, g1, a.seqoff, a.nseq, a.npairs);
-                    for (int t = c.t; t < c.t + c.run && ok; ++t) ok = load_tile(c, t, true);
-                    g += c.run;
+            float* cs = sm.cs(stage);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float A2 = __ldg(a.A + h0 + hh) * kLog2e;
+                float p[4];
+                p[0] = v[hh][0] * A2;
+#pragma unroll
+                for (int k = 1; k < 4; ++k) p[k] = p[k - 1] + v[hh][k] * A2;
+                float sc = p[3];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float tt = __shfl_up_sync(0xffffffffu, sc, o);
+                    if (lane >= o) sc += tt;
                 }
+                const float base = sc - p[3] + (pass1 ? (hh ? carry1 : carry0) : 0.f);
+                float4 o4 = make_float4(base + p[0], base + p[1], base + p[2], base + p[3]);
+                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = o4;
+                const float tile_total = __shfl_sync(0xffffffffu, sc, 31);
+                if (pass1) { if (hh) carry1 += tile_total; else carry0 += tile_total; }
+            }
+            if (lane == 0) {
+                float* m = sm.stage_misc(stage);
+                m[0] = tot0;
+                m[1] = tot1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full);
+            stage ^= 1;
+            return true;
+        };
+        for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
+            const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
+            if (g0 >= g1) continue;
+            const Cursor last = last_segment(g0, g1, a);
+            if (last.t + last.run < last.nt) {
+                // pass 1: the segment's total dt*A first (its tokens' weights are decays to its end)
+                const int h0 = 2 * last.hp;
+                const int r0 = tile_row0(last, last.t);
+                const int ntok = tile_row0(last, last.t + (int)last.run - 1) + tile_len(last, last.t + (int)last.run - 1) - r0;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+                for (int l = lane; l < ntok; l += 32) {
+                    const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
+                    s0 += d2.x;
+                    s1 += d2.y;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                }
+                const float tot0 = s0 * __ldg(a.A + h0) * kLog2e, tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
+                float c0 = 0.f, c1 = 0.f;
+                for (int t = last.t; t < last.t + last.run && ok; ++t) ok = load_tile(last, t, true, tot0, tot1, c0, c1);
+            }
+            for (int64_t g = g0; g < g1 && ok;) {
+                const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
+                float c0 = 0.f, c1 = 0.f;
+                for (int t = c.t; t < c.t + c.run && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
+                g += c.run;
             }
         }
     } else if (warp == 1) {
-        // ============================================================ MMA issuer
+        // ============================================================ MMA issuer (lane 0)
         if (lane == 0) {
-            uint32_t ph = {};
+            uint32_t ph = 0;
             int stage = 0;
-            bool have_prev_tile = false;   // a pass-2 tile was issued before (Yd / Y regions in use)
+            bool have_prev_tile = false;   // a pass-2 tile's Y regions are still being read
             const uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yo = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
@@ -323,134 +431,119 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || accumulate_first) ? 1u : 0u);
                 }
             };
+            auto issue_g = [&](int st) {
+                for (int ks = 0; ks < N / 16; ++ks) {
+                    const int k = ks / 4, off = (ks % 4) * 32;
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + k * kRegion + off), 0, 1024);
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + k * kRegion + off), 0, 1024);
+                    mma_bf16_ss(tmem + kColG, ad, bd, id_g, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(sm.bars() + kBarG);
+            };
             for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
                 const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
                 if (g0 >= g1) continue;
-                {
-                    int64_t g = g0;
-                    Cursor last{};
-                    while (g < g1) { last = locate(g, g1, a.seqoff, a.nseq, a.npairs); g += last.run; }
-                    if (last.t + last.run < last.nt) {
-                        for (int i = 0; i < last.run && ok; ++i) {
-                            ok = wait_bar(sm, kBarFull0 + stage, ph, a) &&
-                                 wait_bar(sm, kBarWX, ph, a);
-                            if (!ok) break;
-                            tc_fence_after_sync();
-                            issue_s(stage, i > 0);
-                            mma_commit(sm.bars() + kBarEmpty0 + stage);
-                            stage ^= 1;
-                        }
-                        if (ok) mma_commit(sm.bars() + kBarAgg);
-                    }
-                }
-                for (int64_t g = g0; g < g1 && ok;) {
-                    const Cursor c = locate(g, g1, a.seqoff, a.nseq, a.npairs);
-                    for (int i = 0; i < c.run && ok; ++i) {
-                        ok = wait_bar(sm, kBarFull0 + stage, ph, a);
-                        if (ok && have_prev_tile) ok = wait_bar(sm, kBarYD, ph, a);   // LG(t-1) consumed
+                const Cursor last = last_segment(g0, g1, a);
+                if (last.t + last.run < last.nt) {
+                    for (int i = 0; i < last.run && ok; ++i) {
+                        ok = wait_bar(sm, kBarFull0 + stage, ph, a) && wait_bar(sm, kBarWX1a + stage, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        // G = C B^T
-                        for (int ks = 0; ks < N / 16; ++ks) {
-                            const int k = ks / 4, off = (ks % 4) * 32;
-                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(stage) + k * kRegion + off), 0, 1024);
-                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(stage) + k * kRegion + off), 0, 1024);
-                            mma_bf16_ss(tmem + kColG, ad, bd, id_g, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(sm.bars() + kBarG);
-                        // Yo = C h^T  (needs the staged state and a free Y region)
-                        ok = wait_bar(sm, kBarST, ph, a);
-                        if (ok && have_prev_tile) ok = wait_bar(sm, kBarYFree, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        for (int ks = 0; ks < N / 16; ++ks) {
-                            const int k = ks / 4, off = (ks % 4) * 32;
-                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(stage) + k * kRegion + off), 0, 1024);
-                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + k * kRegion + off), 0, 1024);
-                            mma_bf16_ss(tmem + kColYO, ad, bd, id_yo, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(sm.bars() + kBarYO);
-                        // Yd_h = (L o G)_h X_h, A operand in TMEM
-                        ok = wait_bar(sm, kBarLG, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        for (int h = 0; h < 2; ++h) {
-                            for (int ks = 0; ks < 8; ++ks) {
-                                const uint32_t acol = kColG + 32 * (ks / 2) + 16 * h + 8 * (ks % 2);
-                                const uint64_t bd = smem_desc_sw128(smem_u32(sm.x(stage, h) + ks * 2048), kRegion, 1024);
-                                mma_bf16_ts(tmem + kColYD + 64 * h, tmem + acol, bd, id_yd, ks > 0 ? 1u : 0u);
-                            }
-                        }
-                        mma_commit(sm.bars() + kBarYD);
-                        // S: state += (w o X)^T B
-                        ok = wait_bar(sm, kBarWX, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        issue_s(stage, true);
-                        mma_commit(sm.bars() + kBarS);
+                        issue_s(stage, i > 0);
                         mma_commit(sm.bars() + kBarEmpty0 + stage);
                         stage ^= 1;
-                        have_prev_tile = true;
                     }
-                    g += c.run;
+                    if (ok) mma_commit(sm.bars() + kBarAgg);
+                }
+                // pass 2, per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an
+                // earlier one's reads of the same TMEM):
+                //   Yd(t), both heads interleaved       needs L o G(t), Y regions free
+                //   G(t+1)                              needs the next stage; runs while the S warps
+                //                                       stage the state and weight x
+                //   Yo(t) and S(t), interleaved         needs the staged state and the weights
+                const int64_t ntiles = g1 - g0;
+                for (int64_t k = 0; k < ntiles && ok; ++k) {
+                    const int st = stage;
+                    if (k == 0) {
+                        ok = wait_bar(sm, kBarFull0 + st, ph, a);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        issue_g(st);
+                    }
+                    ok = wait_bar(sm, kBarLG, ph, a);
+                    if (ok && have_prev_tile) ok = wait_bar(sm, kBarYFree, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    for (int ks = 0; ks < 8; ++ks) {
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t acol = kColG + 32 * (ks / 2) + 16 * h + 8 * (ks % 2);
+                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.x(st, h) + ks * 2048), kRegion, 1024);
+                            mma_bf16_ts(tmem + kColYD + 64 * h, tmem + acol, bd, id_yd, ks > 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(sm.bars() + kBarYD);
+                    if (k + 1 < ntiles) {
+                        ok = wait_bar(sm, kBarFull0 + (st ^ 1), ph, a);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        issue_g(st ^ 1);
+                    }
+                    ok = wait_bar(sm, kBarST, ph, a) && wait_bar(sm, kBarWX, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    for (int ks = 0; ks < 8; ++ks) {
+                        if (ks < N / 16) {
+                            const int kk = ks / 4, off = (ks % 4) * 32;
+                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + kk * kRegion + off), 0, 1024);
+                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
+                            mma_bf16_ss(tmem + kColYO, ad, bd, id_yo, ks > 0 ? 1u : 0u);
+                        }
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
+                        mma_bf16_ss(tmem + kColST, ad, bd, id_s, 1u);
+                    }
+                    mma_commit(sm.bars() + kBarYO);
+                    mma_commit(sm.bars() + kBarS);
+                    mma_commit(sm.bars() + kBarEmpty0 + st);
+                    stage ^= 1;
+                    have_prev_tile = true;
                 }
             }
         }
     } else {
         // ============================================================ math warps
+        // warps 2-5 ("L" group): L o G in pass 2; warps 6-9 ("S" group): state steps, weights and
+        // the epilogue in pass 2. Both groups share pass 1, publishing and the look-back.
         const int mt = tid - 64;                 // 0..255
+        const bool grpL = warp < 6;
+        const int gt = mt & 127;                 // thread index within its group
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int ch = (warp - 2) >> 2;          // column half (0: warps 2-5, 1: warps 6-9)
+        const int ch = grpL ? 0 : 1;             // column half in the shared phases
         const int row = 32 * qd + lane;          // TMEM lane = tile row / (head, channel) row
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        const int hrow = row >> 6, prow = row & 63;   // (head, channel) of this state row
-        constexpr int NH = N / 2;                // state columns owned by this thread
+        const int hrow = row >> 6, prow = row & 63;
+        constexpr int NH = N / 2;
         const int n0 = ch * NH;
-        uint32_t ph = {};
+        uint32_t ph = 0;
         int stage = 0;
-        float* cs = sm.cs();
         float* vt = sm.vtab();
         float* misc = sm.misc();
         bool ok = true;
-        // bounded barrier over the 8 math warps (an mbarrier, so an aborting CTA cannot hang here)
-        auto math_bar = [&]() {
+        auto math_bar = [&]() {    // all 8 math warps
             warp_arrive(sm, kBarMath);
             if (!wait_bar_warp(sm, kBarMath, ph, a)) ok = false;
         };
-
-        // state registers: h[n0 .. n0+NH) of row (hrow, prow)
-        float hreg[NH];
-
-        // tile-local cumsum of dt*A (times log2 e) for both heads; warps 2 and 3 (mt < 64)
-        auto tile_cumsum = [&](const ChunkDesc& d, int h0, float carry_scale_unused) {
-            (void)carry_scale_unused;
-            if (mt < 64) {
-                const int hh = mt >> 5;
-                const int h = h0 + hh;
-                const float Ah = __ldg(a.A + h) * kLog2e;
-                float carry = 0.f;
-                for (int base = 0; base < kTile; base += 32) {
-                    const int l = base + lane;
-                    float v = (l < d.len) ? __ldg(a.dt + (int64_t)(d.row0 + l) * a.H + h) * Ah : 0.f;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float t = __shfl_up_sync(0xffffffffu, v, o);
-                        if (lane >= o) v += t;
-                    }
-                    v += carry;
-                    cs[hh * 128 + l] = v;
-                    carry = __shfl_sync(0xffffffffu, v, 31);
-                }
-            }
+        auto group_bar = [&]() {   // the 4 warps of this group
+            warp_arrive(sm, grpL ? kBarGrpL : kBarGrpS);
+            if (!wait_bar_warp(sm, grpL ? kBarGrpL : kBarGrpS, ph, a)) ok = false;
         };
-
-        // scale the staged x tile in place: row l of head h by w_h(l) (0 beyond len)
-        auto weight_x = [&](int st, int len, float last0, float last1, float base0, float base1) {
-            // w = exp2(last_h - cs_h(l) - base_h): the segment-end (or tile-end) decay of token l
-            for (int qq = mt; qq < 2 * kTile * 8; qq += kMathThreads) {
+        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)) (0 past len)
+        auto weight_x = [&](int st, int len, float last0, float last1, int first, int stride) {
+            const float* cs = sm.cs(st);
+            for (int qq = first; qq < 2 * kTile * 8; qq += stride) {
                 const int hh = qq >> 10;
                 const int l = (qq & 1023) >> 3;
-                const float w = (l < len) ? ex2((hh ? last1 : last0) - (hh ? base1 : base0) - cs[hh * 128 + l]) : 0.f;
+                const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
                 uint4* p = reinterpret_cast<uint4*>(sm.x(st, 0) + (size_t)qq * 16);
                 uint4 v = *p;
                 uint32_t* u = reinterpret_cast<uint32_t*>(&v);
@@ -462,56 +555,35 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 *p = v;
             }
         };
+        float hreg[NH];
 
         for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
             const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
             if (g0 >= g1) continue;
-            const Cursor first = locate(g0, g1, a.seqoff, a.nseq, a.npairs);
-            Cursor last{};
-            {
-                int64_t g = g0;
-                while (g < g1) { last = locate(g, g1, a.seqoff, a.nseq, a.npairs); g += last.run; }
-            }
+            const Cursor first = locate(g0, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
+            const Cursor last = last_segment(g0, g1, a);
             const bool first_cont = first.t > 0;
             const bool last_cont = last.t + last.run < last.nt;
             const bool single = (first.s == last.s && first.hp == last.hp);
 
-            // ------------------------------------------------ pass 1: local end state of the last segment
+            // ------------------------------------------------ pass 1 (both groups)
             if (last_cont) {
                 const int h0 = 2 * last.hp;
-                // total dt*A (x log2 e) of the segment per head
-                if (mt < 64) {
-                    const int hh = mt >> 5;
-                    const float Ah = __ldg(a.A + h0 + hh) * kLog2e;
-                    float acc = 0.f;
-                    for (int t = last.t; t < last.t + last.run; ++t) {
-                        const ChunkDesc d = a.tiles[a.seqoff[last.s] + t];
-                        for (int l = lane; l < d.len; l += 32)
-                            acc += __ldg(a.dt + (int64_t)(d.row0 + l) * a.H + h0 + hh) * Ah;
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                    if (lane == 0) { misc[kMiscTot0 + hh] = acc; misc[kMiscCarry0 + hh] = 0.f; }
-                }
                 for (int t = last.t; t < last.t + last.run && ok; ++t) {
-                    const ChunkDesc d = a.tiles[a.seqoff[last.s] + t];
-                    math_bar();
-                    tile_cumsum(d, h0, 0.f);
-                    math_bar();
                     ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
                     if (!ok) break;
-                    weight_x(stage, d.len, misc[kMiscTot0], misc[kMiscTot1], misc[kMiscCarry0], misc[kMiscCarry1]);
+                    const float* m = sm.stage_misc(stage);
+                    const float tot0 = m[0], tot1 = m[1];
+                    if (t == last.t && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
+                    weight_x(stage, tile_len(last, t), tot0, tot1, mt, kMathThreads);
                     fence_proxy_async_smem();
-                    warp_arrive(sm, kBarWX);
-                    math_bar();
-                    if (mt < 64 && lane == 0) misc[kMiscCarry0 + (mt >> 5)] += cs[(mt >> 5) * 128 + d.len - 1];
+                    warp_arrive(sm, kBarWX1a + stage);
                     stage ^= 1;
                 }
                 if (!ok) break;
                 ok = wait_bar_warp(sm, kBarAgg, ph, a);
                 if (!ok) break;
                 tc_fence_after_sync();
-                // publish the aggregate rows (they stay in TMEM for the inclusive state below)
                 const float dec = ex2(misc[kMiscTot0 + hrow]);
                 const int64_t slot = (q * 128 + row) * N + n0;
                 const bool starts_chain = last.t == 0;
@@ -527,7 +599,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     for (int k = 0; k < 32; k += 4) {
                         float4 o = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
                         if (ip) {
-                            // the segment starts its chain: inclusive state = dec * init + aggregate
                             const float4 i4 = *reinterpret_cast<const float4*>(ip + c0 + k);
                             o.x = fmaf(dec, i4.x, o.x); o.y = fmaf(dec, i4.y, o.y);
                             o.z = fmaf(dec, i4.z, o.z); o.w = fmaf(dec, i4.w, o.w);
@@ -542,26 +613,24 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tc_fence_before_sync();
             }
 
-            // ------------------------------------------------ look-back for the first segment
-            float* hin = hreg;   // the entering state of the first segment
+            // ------------------------------------------------ look-back (both groups)
             if (first_cont) {
 #pragma unroll
-                for (int k = 0; k < NH; ++k) hin[k] = 0.f;
+                for (int k = 0; k < NH; ++k) hreg[k] = 0.f;
                 float mult = 1.f;
                 for (int64_t qq = q - 1; qq >= 0; --qq) {
                     if (piece_begin(qq, L, np) == piece_begin(qq + 1, L, np)) continue;   // empty pieces publish nothing
                     int f = 0;
                     const uint64_t t0 = global_timer_ns();
                     while (true) {
-                        // lane 0 polls and decides; the warp follows its decision (no divergence)
-                        int verdict = 0;   // 0 keep waiting, 1 published, 2 give up
+                        int verdict = 0;   // lane 0 polls and decides; the warp follows (no divergence)
                         if (lane == 0) {
                             f = ld_acquire(a.flags + qq);
                             if (f != 0) verdict = 1;
                             else if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) verdict = 2;
                             else if (global_timer_ns() - t0 > kWaitLimitNs) {
                                 record_status(a.status, SSD_ERR_TIMEOUT);
-                                atomicCAS(a.status + 2, 0, 0x200);   // a look-back gave up (diagnostic)
+                                atomicCAS(a.status + 2, 0, 0x200);
                                 verdict = 2;
                             }
                         }
@@ -575,21 +644,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
                     for (int k = 0; k < NH; k += 4) {
                         const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k));
-                        hin[k] = fmaf(mult, v.x, hin[k]);
-                        hin[k + 1] = fmaf(mult, v.y, hin[k + 1]);
-                        hin[k + 2] = fmaf(mult, v.z, hin[k + 2]);
-                        hin[k + 3] = fmaf(mult, v.w, hin[k + 3]);
+                        hreg[k] = fmaf(mult, v.x, hreg[k]);
+                        hreg[k + 1] = fmaf(mult, v.y, hreg[k + 1]);
+                        hreg[k + 2] = fmaf(mult, v.z, hreg[k + 2]);
+                        hreg[k + 3] = fmaf(mult, v.w, hreg[k + 3]);
                     }
                     if (f == 2) break;
                     mult *= __ldcg(a.decay + qq * 2 + hrow);
                 }
-                if (!ok) {
-                    *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
-                    break;
-                }
+                if (!ok) break;
+                tc_fence_after_sync();
                 if (last_cont && single) {
-                    // this piece lies inside one chain: inclusive = dec * h_in + aggregate (still in TMEM)
-                    tc_fence_after_sync();
+                    // the piece lies inside one chain: inclusive = dec * h_in + aggregate (still in TMEM)
                     const float dec = ex2(misc[kMiscTot0 + hrow]);
                     float* dst = a.incl + (q * 128 + row) * N + n0;
 #pragma unroll
@@ -598,38 +664,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         tmem_ld32(lane_base + kColST + n0 + c0, v);
 #pragma unroll
                         for (int k = 0; k < 32; k += 4) {
-                            const float4 o = make_float4(fmaf(dec, hin[c0 + k], v[k]), fmaf(dec, hin[c0 + k + 1], v[k + 1]),
-                                                         fmaf(dec, hin[c0 + k + 2], v[k + 2]), fmaf(dec, hin[c0 + k + 3], v[k + 3]));
+                            const float4 o = make_float4(fmaf(dec, hreg[c0 + k], v[k]), fmaf(dec, hreg[c0 + k + 1], v[k + 1]),
+                                                         fmaf(dec, hreg[c0 + k + 2], v[k + 2]), fmaf(dec, hreg[c0 + k + 3], v[k + 3]));
                             __stcg(reinterpret_cast<float4*>(dst + c0 + k), o);
                         }
                     }
                     __threadfence();
-                    math_bar();
-                    if (mt == 0) st_release(a.flags + q, 2);
-                    tc_fence_before_sync();
                 }
-            }
-
-            // ------------------------------------------------ pass 2: outputs, state chained on chip
-            for (int64_t g = g0; g < g1 && ok;) {
-                const Cursor c = locate(g, g1, a.seqoff, a.nseq, a.npairs);
-                const int h0 = 2 * c.hp;
-                const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
-                const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
-                // initial state of the segment -> hreg (the look-back already left it there)
-                if (g == g0 && first_cont) {
-                } else if (c.t == 0 && a.init) {
-                    const float* ip = a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0;
-#pragma unroll
-                    for (int k = 0; k < NH; k += 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(ip + k);
-                        hreg[k] = v.x; hreg[k + 1] = v.y; hreg[k + 2] = v.z; hreg[k + 3] = v.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int k = 0; k < NH; ++k) hreg[k] = 0.f;
-                }
-                // park it in the TMEM state columns; every tile's state step reads it from there
+                // park h_in in the TMEM state columns for the first segment
 #pragma unroll
                 for (int c0 = 0; c0 < NH; c0 += 32) {
                     float v[32];
@@ -638,71 +680,44 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     tmem_st32f(lane_base + kColST + n0 + c0, v);
                 }
                 tmem_wait_st();
-                for (int i = 0; i < c.run && ok; ++i) {
-                    const int t = c.t + i;
-                    const ChunkDesc d = a.tiles[a.seqoff[c.s] + t];
-                    const bool seg_first = (i == 0);
-                    math_bar();
-                    tile_cumsum(d, h0, 0.f);
-                    math_bar();
-                    if (mt < 128) {
-                        const int hh = mt >> 6, j = mt & 63;
-                        vt[hh * 64 + j] = ex2(cs[hh * 128 + 63] - cs[hh * 128 + j]);   // exp(cs_63 - cs_j)
-                    }
-                    if (mt < 2) misc[kMiscA0 + mt] = ex2(cs[mt * 128 + d.len - 1]);
-                    math_bar();
-                    // ---- state step: stage h_{t-1} (bf16) for Yo and put a_t h_{t-1} in TMEM for S
-                    if (!seg_first) {
-                        ok = wait_bar_warp(sm, kBarS, ph, a);
+                tc_fence_before_sync();
+                math_bar();
+                if (last_cont && single && mt == 0) st_release(a.flags + q, 2);
+            } else if (last_cont) {
+                math_bar();   // the aggregate was read by both groups before the S group parks a state
+            }
+            if (!ok) break;
+
+            // ------------------------------------------------ pass 2, L group: L o G (+ D on the diagonal)
+            if (grpL) {
+                for (int64_t g = g0; g < g1 && ok;) {
+                    const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
+                    const int h0 = 2 * c.hp;
+                    const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
+                    const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
+                    for (int t = c.t; t < c.t + c.run && ok; ++t) {
+                        const int len = tile_len(c, t);
+                        ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
                         if (!ok) break;
-                    }
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int c0 = 0; c0 < NH; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(lane_base + kColST + n0 + c0, v);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) hreg[c0 + k] = v[k];
-                    }
-                    {
-                        const float at = misc[kMiscA0 + hrow];
-                        // bf16 copy (K-major, 128-byte swizzle, n-blocks of 64)
-#pragma unroll
-                        for (int k = 0; k < NH; k += 8) {
-                            const int n = n0 + k;
-                            uint4 v;
-                            v.x = pack_bf16x2(hreg[k], hreg[k + 1]);
-                            v.y = pack_bf16x2(hreg[k + 2], hreg[k + 3]);
-                            v.z = pack_bf16x2(hreg[k + 4], hreg[k + 5]);
-                            v.w = pack_bf16x2(hreg[k + 6], hreg[k + 7]);
-                            *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = v;
+                        const float* cs = sm.cs(stage);
+                        group_bar();   // everyone is done with the previous tile's vt
+                        {
+                            const int hh = gt >> 6, j = gt & 63;
+                            vt[hh * 64 + j] = ex2(cs[hh * 128 + 63] - cs[hh * 128 + j]);   // exp(cs_63 - cs_j)
                         }
-#pragma unroll
-                        for (int c0 = 0; c0 < NH; c0 += 32) {
-                            float v[32];
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) v[k] = at * hreg[c0 + k];
-                            tmem_st32f(lane_base + kColST + n0 + c0, v);
-                        }
-                        tmem_wait_st();
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before_sync();
-                    warp_arrive(sm, kBarST);
-                    // ---- L o G (+ D on the diagonal) over G, in place, both heads
-                    ok = wait_bar_warp(sm, kBarG, ph, a);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    {
+                        group_bar();
+                        ok = ok && wait_bar_warp(sm, kBarG, ph, a);
+                        if (!ok) break;
+                        tc_fence_after_sync();
                         const int i = row;
-                        const bool rv = i < d.len;
+                        const bool rv = i < len;
                         const float csi0 = cs[i], csi1 = cs[128 + i];
+                        const float u0 = ex2(csi0 - cs[63]), u1 = ex2(csi1 - cs[128 + 63]);
 #pragma unroll
-                        for (int b = 0; b < 2; ++b) {
-                            const int jb = 64 * ch + 32 * b;
+                        for (int b = 0; b < 4; ++b) {
+                            const int jb = 32 * b;
                             uint32_t p0[16], p1[16];
-                            // tcgen05.ld is warp-collective: the whole warp loads if any lane needs the block
-                            const bool need = rv && jb <= i;
+                            const bool need = rv && jb <= i;   // tcgen05.ld is warp-collective
                             if (!__any_sync(0xffffffffu, need)) {
 #pragma unroll
                                 for (int k = 0; k < 16; ++k) { p0[k] = 0u; p1[k] = 0u; }
@@ -713,9 +728,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
                                     for (int k = 0; k < 32; ++k) gv[k] = 0.f;
                                 }
-                                if (ch == 0 && i >= 64) {
+                                if (jb < 64 && i >= 64) {
                                     // lower-left block: exp(cs_i - cs_63) exp(cs_63 - cs_j)
-                                    const float u0 = ex2(csi0 - cs[63]), u1 = ex2(csi1 - cs[128 + 63]);
 #pragma unroll
                                     for (int k = 0; k < 16; ++k) {
                                         const int j = jb + 2 * k;
@@ -743,65 +757,134 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                             tmem_st16(lane_base + kColG + jb + 16, p1);
                         }
                         tmem_wait_st();
+                        tc_fence_before_sync();
+                        warp_arrive(sm, kBarLG);
+                        stage ^= 1;
                     }
-                    tc_fence_before_sync();
-                    warp_arrive(sm, kBarLG);
-                    // ---- weights for S: x scaled in place by exp(cs_last - cs_l) once Yd is done with x
-                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a) &&
-                         wait_bar_warp(sm, kBarYD, ph, a);
-                    if (!ok) break;
-                    weight_x(stage, d.len, cs[d.len - 1], cs[128 + d.len - 1], 0.f, 0.f);
-                    fence_proxy_async_smem();
-                    warp_arrive(sm, kBarWX);
-                    // ---- epilogue: y = Yd + exp(cs_i) Yo, head ch, row i
-                    ok = wait_bar_warp(sm, kBarYO, ph, a);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    {
-                        const int i = row;
-                        const float e = ex2(cs[ch * 128 + i]);
-                        __nv_bfloat16* yrow = a.y + ((int64_t)(d.row0 + i) * a.H + h0 + ch) * 64;
+                    g += c.run;
+                }
+            } else {
+                // ------------------------------------------------ pass 2, S group: state, weights, epilogue
+                for (int64_t g = g0; g < g1 && ok;) {
+                    const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
+                    const int h0 = 2 * c.hp;
+                    if (!(g == g0 && first_cont)) {
+                        // the segment starts its chain: initial state (or zero) into the TMEM state columns
+                        const float* ip = (c.t == 0 && a.init) ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N : nullptr;
 #pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 32) {
-                            float yd[32], yo[32];
-                            tmem_ld32(lane_base + kColYD + 64 * ch + c0, yd);
-                            tmem_ld32(lane_base + kColYO + 64 * ch + c0, yo);
-                            if (i < d.len) {
+                        for (int c0 = 0; c0 < N; c0 += 32) {
+                            float v[32];
 #pragma unroll
-                                for (int k = 0; k < 32; k += 8) {
-                                    uint4 v;
-                                    v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
-                                    v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
-                                    v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
-                                    v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
-                                    *reinterpret_cast<uint4*>(yrow + c0 + k) = v;
+                            for (int k = 0; k < 32; k += 4) {
+                                const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + c0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                                v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
+                            }
+                            tmem_st32f(lane_base + kColST + c0, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    for (int t = c.t; t < c.t + c.run && ok; ++t) {
+                        const int len = tile_len(c, t);
+                        const int row0 = tile_row0(c, t);
+                        ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+                        if (!ok) break;
+                        const float* cs = sm.cs(stage);
+                        const float at = ex2(cs[hrow * 128 + len - 1]);     // decay of this row's head over the tile
+                        const float e0 = ex2(cs[row]), e1 = ex2(cs[128 + row]);   // exp(cs_i) for both heads
+                        const float last0 = cs[len - 1], last1 = cs[128 + len - 1];
+                        // ---- state step: stage h_{t-1} (bf16) for Yo and leave a_t h_{t-1} in TMEM for S
+                        if (t != c.t) {
+                            ok = wait_bar_warp(sm, kBarS, ph, a);
+                            if (!ok) break;
+                        }
+                        tc_fence_after_sync();
+#pragma unroll
+                        for (int c0 = 0; c0 < N; c0 += 64) {
+                            float v[64];
+                            tmem_ld32_nowait(lane_base + kColST + c0, v);
+                            tmem_ld32_nowait(lane_base + kColST + c0 + 32, v + 32);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 64; k += 8) {
+                                const int n = c0 + k;
+                                uint4 pk;
+                                pk.x = pack_bf16x2(v[k], v[k + 1]);
+                                pk.y = pack_bf16x2(v[k + 2], v[k + 3]);
+                                pk.z = pack_bf16x2(v[k + 4], v[k + 5]);
+                                pk.w = pack_bf16x2(v[k + 6], v[k + 7]);
+                                *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
+                            }
+#pragma unroll
+                            for (int k = 0; k < 64; ++k) v[k] *= at;
+                            tmem_st32f(lane_base + kColST + c0, *reinterpret_cast<float(*)[32]>(v));
+                            tmem_st32f(lane_base + kColST + c0 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+                        }
+                        tmem_wait_st();
+                        fence_proxy_async_smem();
+                        tc_fence_before_sync();
+                        warp_arrive(sm, kBarST);
+                        // ---- weights for S: x scaled in place once Yd has read it
+                        ok = wait_bar_warp(sm, kBarYD, ph, a);
+                        if (!ok) break;
+                        weight_x(stage, len, last0, last1, gt, 128);
+                        fence_proxy_async_smem();
+                        warp_arrive(sm, kBarWX);
+                        // ---- epilogue: y = Yd + exp(cs_i) Yo for both heads of row i
+                        ok = wait_bar_warp(sm, kBarYO, ph, a);
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        {
+                            const int i = row;
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const float e = hh ? e1 : e0;
+                                __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64;
+#pragma unroll
+                                for (int c0 = 0; c0 < 64; c0 += 32) {
+                                    float yd[32], yo[32];
+                                    tmem_ld32_nowait(lane_base + kColYD + 64 * hh + c0, yd);
+                                    tmem_ld32_nowait(lane_base + kColYO + 64 * hh + c0, yo);
+                                    tmem_wait_ld();
+                                    if (i < len) {
+#pragma unroll
+                                        for (int k = 0; k < 32; k += 8) {
+                                            uint4 v;
+                                            v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
+                                            v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
+                                            v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
+                                            v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
+                                            *reinterpret_cast<uint4*>(yrow + c0 + k) = v;
+                                        }
+                                    }
                                 }
                             }
                         }
+                        tc_fence_before_sync();
+                        warp_arrive(sm, kBarYFree);
+                        stage ^= 1;
+                    }
+                    if (!ok) break;
+                    // end of segment: the last S, then the final state at a chain end
+                    ok = wait_bar_warp(sm, kBarS, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    if (c.t + c.run == c.nt && a.final_state) {
+                        float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N;
+#pragma unroll
+                        for (int c0 = 0; c0 < N; c0 += 32) {
+                            float v[32];
+                            tmem_ld32(lane_base + kColST + c0, v);
+#pragma unroll
+                            for (int k = 0; k < 32; k += 4)
+                                *reinterpret_cast<float4*>(fp + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                        }
                     }
                     tc_fence_before_sync();
-                    warp_arrive(sm, kBarYFree);
-                    stage ^= 1;
+                    g += c.run;
                 }
-                if (!ok) break;
-                // end of segment: wait for the last S, write the final state at a chain end
-                ok = wait_bar_warp(sm, kBarS, ph, a);
-                if (!ok) break;
-                tc_fence_after_sync();
-                if (c.t + c.run == c.nt && a.final_state) {
-                    float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0;
-#pragma unroll
-                    for (int c0 = 0; c0 < NH; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(lane_base + kColST + n0 + c0, v);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4)
-                            *reinterpret_cast<float4*>(fp + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                    }
-                }
-                tc_fence_before_sync();
-                g += c.run;
             }
+            // both groups finish the piece before the next one's shared phases
+            math_bar();
         }
         if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
     }
@@ -840,7 +923,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 template <int N>
 size_t fused_smem_bytes() {
     const size_t stage = 2 * kRegion + 2 * (N / 64) * kRegion;
-    return 2 * stage + (N / 64) * kRegion + (256 + 128 + 64) * 4 + kNumBars * 8 + 16;
+    return 2 * stage + (N / 64) * kRegion + (520 + 128 + 8) * 4 + kNumBars * 8 + 16;
 }
 
 template <int N>
