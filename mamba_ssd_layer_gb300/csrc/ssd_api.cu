@@ -161,10 +161,12 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
 
     cudaError_t e;
     if (L.fused) {
-        const int64_t np = fused_pieces(p);
-        if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;   // more SMs than the workspace bound allows
-        e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.flags(), np));
-        if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p));
+        int K = 0;
+        int64_t np = 0;
+        fused_plan(p, &K, &np);
+        if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;
+        e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.flags(), np, varlen ? p.woff() : nullptr, K));
+        if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np));
     } else {
         e = note_cuda_error("prep launch", launch_prep(p, chunk, nullptr, 0));
         if (e == cudaSuccess)

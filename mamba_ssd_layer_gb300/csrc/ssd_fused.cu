@@ -41,14 +41,15 @@ namespace {
 
 constexpr int kTile = kFusedTile;
 constexpr int kRegion = kTile * 128;          // one 128-row x 128-byte swizzled box (16 KB)
-constexpr int kThreads = 320;
-constexpr int kMathThreads = 256;
-constexpr int kPieceTiles = kFusedPieceTiles;  // target tiles per piece
+constexpr int kThreads = 576;        // 2 + 8 + 8 warps
+constexpr int kMathThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column map (512 allocated)
 constexpr uint32_t kColST = 0;     // state / aggregate: rows (head, channel), N columns
-constexpr uint32_t kColG = 128;    // C B^T (fp32), then L o C B^T (bf16 pairs) in place
+constexpr uint32_t kColG = 128;    // C B^T (fp32), then L o C B^T (bf16 pairs) in place: the 16 fp32
+                                   // columns 16c..16c+15 become 8 packed columns of head 0 followed by
+                                   // 8 of head 1, both covering tokens j = 16c..16c+15
 constexpr uint32_t kColYD = 256;   // Yd, head 0 then head 1 (64 columns each)
 constexpr uint32_t kColYO = 384;   // Yo, rows = tokens, columns = (head, channel)
 
@@ -71,8 +72,14 @@ struct FusedArgs {
     float* decay;               // per piece: [2] per-head decay of the published segment
     float* agg;                 // per piece: [128][N]
     float* incl;                // per piece: [128][N]
+    const int32_t* woff;        // packed batch: first window of each sequence
     int H, G, nseq, npairs;
-    int64_t npieces;
+    int64_t npieces;            // pieces to dispatch (exact for a dense batch, a bound for a packed one)
+    int K;                      // tiles per window
+    int dense;                  // 1: batch of equal sequences (pieces decoded arithmetically)
+    int64_t seqlen;             // dense: tokens per sequence
+    int nt_dense;               // dense: tiles per sequence
+    int W_dense;                // dense: windows per sequence
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -112,6 +119,23 @@ __device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float* v) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -154,13 +178,13 @@ enum {
 // next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
 // barrier before the first was waited for would make the waiter miss a phase.
 // Expected arrivals per phase: full = producer's expect_tx + its "cumsum written" arrival;
-// pass-2 signals from one math group (4 warps); pass-1 weights and the shared barrier from
-// both groups (8 warps); MMA commits 1.
+// pass-2 signals from one math group (8 warps); pass-1 weights and the shared barrier from
+// both groups (16 warps); MMA commits 1.
 __device__ __forceinline__ uint32_t bar_count(int i) {
     switch (i) {
         case kBarFull0: case kBarFull1: return 2;
-        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarGrpL: case kBarGrpS: return 4;
-        case kBarWX1a: case kBarWX1b: case kBarMath: return 8;
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarGrpL: case kBarGrpS: return 8;
+        case kBarWX1a: case kBarWX1b: case kBarMath: return 16;
         default: return 1;
     }
 }
@@ -195,8 +219,9 @@ __device__ __forceinline__ bool wait_bar(const Smem& sm, int idx, uint32_t& phas
     phases ^= 1u << idx;
     if (mbar_try_wait(bar, par)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, par)) return true;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_sleep(bar, par, 20000u)) return true;   // sleeps until the phase completes
+        if ((it & 63u) != 0) continue;
         if (*reinterpret_cast<volatile int*>(sm.abort_flag())) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             record_status(a.status, SSD_ERR_TIMEOUT);
@@ -221,57 +246,66 @@ __device__ __forceinline__ void warp_arrive(const Smem& sm, int idx) {
 }
 
 // ---------------------------------------------------------------- work decomposition
-// A cursor over the chain-major tile list: sequence s, head pair hp, tile t of the sequence,
-// the sequence's first row and length, and how many tiles of this chain the piece still holds.
-struct Cursor {
-    int s, hp, t, nt;
-    int64_t run;
-    int32_t seq_row0, seq_len;
+// A piece is one window of K consecutive 128-token tiles of one chain (sequence s, head pair hp).
+// Pieces are numbered chain-major (q = first window of the chain + w) for the published states;
+// a dense batch is dispatched window-major (all chains' window 0, then window 1, ...), so that the
+// pieces of one chain that run at the same time are few and a look-back stays short.
+struct Piece {
+    int64_t q;                 // published-state slot
+    int s, hp, w;              // sequence, head pair, window
+    int t0, t1, nt;            // tiles [t0, t1) of the sequence's nt tiles
+    int32_t seq_row0, seq_len; // first packed row and length of the sequence
+    bool valid;
 };
 
-__device__ __forceinline__ int64_t piece_begin(int64_t q, int64_t L, int64_t np) { return (q * L) / np; }
-
-__device__ __forceinline__ Cursor locate(int64_t g, int64_t g_end, const int32_t* seqoff, const ChunkDesc* tiles,
-                                         int nseq, int npairs) {
-    // the sequence s with npairs*seqoff[s] <= g < npairs*seqoff[s+1]; empty sequences share the next
-    // sequence's offset, so the largest such s is the non-empty one holding g
-    int lo = 0, hi = nseq - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)npairs * seqoff[mid] <= g) lo = mid; else hi = mid - 1;
+__device__ __forceinline__ Piece decode_piece(int64_t d, const FusedArgs& a) {
+    Piece p;
+    p.valid = true;
+    if (a.dense) {
+        const int64_t nchains = (int64_t)a.nseq * a.npairs;
+        const int64_t w = d / nchains, c = d % nchains;
+        p.w = (int)w;
+        p.s = (int)(c / a.npairs);
+        p.hp = (int)(c % a.npairs);
+        p.q = c * a.W_dense + w;
+        p.nt = a.nt_dense;
+        p.seq_row0 = (int32_t)(p.s * a.seqlen);
+        p.seq_len = (int32_t)a.seqlen;
+    } else {
+        const int64_t total = (int64_t)a.header[3] * a.npairs;
+        if (d >= total) { p.valid = false; return p; }
+        int lo = 0, hi = a.nseq - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)a.npairs * a.woff[mid] <= d) lo = mid; else hi = mid - 1;
+        }
+        const int32_t w0 = a.woff[lo], w1 = a.woff[lo + 1];
+        const int64_t local = d - (int64_t)a.npairs * w0;
+        const int Ws = w1 - w0;
+        p.s = lo;
+        p.hp = (int)(local / Ws);
+        p.w = (int)(local % Ws);
+        p.q = d;
+        const int32_t f0 = a.seqoff[lo], f1 = a.seqoff[lo + 1];
+        p.nt = f1 - f0;
+        const ChunkDesc first = a.tiles[f0], last = a.tiles[f1 - 1];
+        p.seq_row0 = first.row0;
+        p.seq_len = last.row0 + last.len - first.row0;
     }
-    Cursor c;
-    c.s = lo;
-    const int32_t f0 = seqoff[lo], f1 = seqoff[lo + 1];
-    c.nt = f1 - f0;
-    const int64_t local = g - (int64_t)npairs * f0;
-    c.hp = (int)(local / c.nt);
-    c.t = (int)(local % c.nt);
-    const int64_t left = c.nt - c.t;
-    c.run = (g_end - g) < left ? (g_end - g) : left;
-    const ChunkDesc first = tiles[f0], last = tiles[f1 - 1];
-    c.seq_row0 = first.row0;
-    c.seq_len = last.row0 + last.len - first.row0;
-    return c;
+    p.t0 = p.w * a.K;
+    p.t1 = p.t0 + a.K < p.nt ? p.t0 + a.K : p.nt;
+    return p;
 }
 
-__device__ __forceinline__ int tile_row0(const Cursor& c, int t) { return c.seq_row0 + kTile * t; }
-__device__ __forceinline__ int tile_len(const Cursor& c, int t) {
+__device__ __forceinline__ int tile_row0(const Piece& c, int t) { return c.seq_row0 + kTile * t; }
+__device__ __forceinline__ int tile_len(const Piece& c, int t) {
     const int rem = c.seq_len - kTile * t;
     return rem < kTile ? rem : kTile;
 }
 
-// The last chain segment of a piece (the one whose state may continue into the next piece).
-__device__ __forceinline__ Cursor last_segment(int64_t g0, int64_t g1, const FusedArgs& a) {
-    int64_t g = g0;
-    Cursor last{};
-    while (g < g1) { last = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs); g += last.run; }
-    return last;
-}
-
 // ---------------------------------------------------------------- the kernel
 template <int N>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
 ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem sm;
@@ -282,8 +316,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
 
     if (a.header[0] != SSD_OK) return;
-    const int total_tiles = a.header[1];
-    const int64_t L = (int64_t)a.npairs * total_tiles;
 
     // sequences without tokens: the final state is the initial state (or zero)
     if (a.final_state) {
@@ -294,7 +326,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 a.final_state[(int64_t)s * n + e] = a.init ? a.init[(int64_t)s * n + e] : 0.f;
         }
     }
-    if (L == 0) return;
+    const int64_t np = a.npieces;
+    if (np == 0 || (a.dense && a.nt_dense == 0)) return;
 
     if ((smem_u32(smem_raw) & 1023u) != 0) {      // layout needs a 1024-byte aligned base
         if (tid == 0) record_status(a.status, SSD_ERR_UNSUPPORTED);
@@ -313,17 +346,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *sm.tmem_slot();
-    const int64_t np = a.npieces;
 
     if (warp == 0) {
         // ============================================================ producer warp
         // TMA for x (both heads), B and C (lane 0); dt for both heads -> the tile-local cumsum of
-        // dt*A (x log2 e), plus the segment carry in pass 1 (all lanes), written into the stage.
+        // dt*A (x log2 e), plus the window carry in pass 1 (all lanes), written into the stage.
         uint32_t ph = 0;
         uint32_t issued = 0;
         int stage = 0;
         bool ok = true;
-        auto load_tile = [&](const Cursor& c, int t, bool pass1, float tot0, float tot1, float& carry0,
+        auto load_tile = [&](const Piece& c, int t, bool pass1, float tot0, float tot1, float& carry0,
                              float& carry1) -> bool {
             if ((issued >> stage) & 1u) {
                 const bool w = wait_bar(sm, kBarEmpty0 + stage, ph, a);
@@ -366,8 +398,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (lane >= o) sc += tt;
                 }
                 const float base = sc - p[3] + (pass1 ? (hh ? carry1 : carry0) : 0.f);
-                float4 o4 = make_float4(base + p[0], base + p[1], base + p[2], base + p[3]);
-                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = o4;
+                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) =
+                    make_float4(base + p[0], base + p[1], base + p[2], base + p[3]);
                 const float tile_total = __shfl_sync(0xffffffffu, sc, 31);
                 if (pass1) { if (hh) carry1 += tile_total; else carry0 += tile_total; }
             }
@@ -381,15 +413,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             stage ^= 1;
             return true;
         };
-        for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
-            const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
-            if (g0 >= g1) continue;
-            const Cursor last = last_segment(g0, g1, a);
-            if (last.t + last.run < last.nt) {
-                // pass 1: the segment's total dt*A first (its tokens' weights are decays to its end)
-                const int h0 = 2 * last.hp;
-                const int r0 = tile_row0(last, last.t);
-                const int ntok = tile_row0(last, last.t + (int)last.run - 1) + tile_len(last, last.t + (int)last.run - 1) - r0;
+        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+            const Piece c = decode_piece(d, a);
+            if (!c.valid) break;
+            if (c.t1 < c.nt) {
+                // pass 1: the window's total dt*A first (its tokens' weights are decays to its end)
+                const int h0 = 2 * c.hp;
+                const int r0 = tile_row0(c, c.t0);
+                const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
                 for (int l = lane; l < ntok; l += 32) {
@@ -404,14 +435,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 const float tot0 = s0 * __ldg(a.A + h0) * kLog2e, tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
                 float c0 = 0.f, c1 = 0.f;
-                for (int t = last.t; t < last.t + last.run && ok; ++t) ok = load_tile(last, t, true, tot0, tot1, c0, c1);
+                for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, true, tot0, tot1, c0, c1);
             }
-            for (int64_t g = g0; g < g1 && ok;) {
-                const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
-                float c0 = 0.f, c1 = 0.f;
-                for (int t = c.t; t < c.t + c.run && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
-                g += c.run;
-            }
+            float c0 = 0.f, c1 = 0.f;
+            for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
         }
     } else if (warp == 1) {
         // ============================================================ MMA issuer (lane 0)
@@ -424,13 +451,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t id_s = idesc_bf16_f32(128, N, 1, 1);
             bool ok = true;
-            auto issue_s = [&](int st, bool accumulate_first) {
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
-                    mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || accumulate_first) ? 1u : 0u);
-                }
-            };
             auto issue_g = [&](int st) {
                 for (int ks = 0; ks < N / 16; ++ks) {
                     const int k = ks / 4, off = (ks % 4) * 32;
@@ -440,16 +460,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 mma_commit(sm.bars() + kBarG);
             };
-            for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
-                const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
-                if (g0 >= g1) continue;
-                const Cursor last = last_segment(g0, g1, a);
-                if (last.t + last.run < last.nt) {
-                    for (int i = 0; i < last.run && ok; ++i) {
+            for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+                const Piece c = decode_piece(d, a);
+                if (!c.valid) break;
+                if (c.t1 < c.nt) {
+                    for (int t = c.t0; t < c.t1 && ok; ++t) {
                         ok = wait_bar(sm, kBarFull0 + stage, ph, a) && wait_bar(sm, kBarWX1a + stage, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        issue_s(stage, i > 0);
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(stage, 0) + ks * 2048), kRegion, 1024);
+                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(stage) + ks * 2048), kRegion, 1024);
+                            mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || t > c.t0) ? 1u : 0u);
+                        }
                         mma_commit(sm.bars() + kBarEmpty0 + stage);
                         stage ^= 1;
                     }
@@ -461,10 +484,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 //   G(t+1)                              needs the next stage; runs while the S warps
                 //                                       stage the state and weight x
                 //   Yo(t) and S(t), interleaved         needs the staged state and the weights
-                const int64_t ntiles = g1 - g0;
-                for (int64_t k = 0; k < ntiles && ok; ++k) {
+                for (int t = c.t0; t < c.t1 && ok; ++t) {
                     const int st = stage;
-                    if (k == 0) {
+                    if (t == c.t0) {
                         ok = wait_bar(sm, kBarFull0 + st, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
@@ -476,13 +498,13 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     tc_fence_after_sync();
                     for (int ks = 0; ks < 8; ++ks) {
                         for (int h = 0; h < 2; ++h) {
-                            const uint32_t acol = kColG + 32 * (ks / 2) + 16 * h + 8 * (ks % 2);
+                            const uint32_t acol = kColG + 32 * (ks / 2) + 16 * (ks % 2) + 8 * h;
                             const uint64_t bd = smem_desc_sw128(smem_u32(sm.x(st, h) + ks * 2048), kRegion, 1024);
                             mma_bf16_ts(tmem + kColYD + 64 * h, tmem + acol, bd, id_yd, ks > 0 ? 1u : 0u);
                         }
                     }
                     mma_commit(sm.bars() + kBarYD);
-                    if (k + 1 < ntiles) {
+                    if (t + 1 < c.t1) {
                         ok = wait_bar(sm, kBarFull0 + (st ^ 1), ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
@@ -512,30 +534,47 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         }
     } else {
         // ============================================================ math warps
-        // warps 2-5 ("L" group): L o G in pass 2; warps 6-9 ("S" group): state steps, weights and
-        // the epilogue in pass 2. Both groups share pass 1, publishing and the look-back.
-        const int mt = tid - 64;                 // 0..255
-        const bool grpL = warp < 6;
-        const int gt = mt & 127;                 // thread index within its group
+        // warps 2-9 ("L" group, two per TMEM lane quadrant, each half of the columns): L o G in
+        // pass 2; warps 10-17 ("S" group, two per quadrant): state steps, weights and the epilogue.
+        // All 16 share pass 1, publishing and the look-back, a quarter of the state columns each.
+        const int mt = tid - 64;                 // 0..511
+        const bool grpL = warp < 10;
+        const int gw = grpL ? warp - 2 : warp - 10;   // warp index within its group, 0..7
+        const int gt = gw * 32 + lane;           // thread index within its group, 0..255
+        const int half = gw >> 2;                // which half of the columns (group phases)
         const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int ch = grpL ? 0 : 1;             // column half in the shared phases
+        const int quarter = (warp - 2) >> 2;     // column quarter in the shared phases
         const int row = 32 * qd + lane;          // TMEM lane = tile row / (head, channel) row
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const int hrow = row >> 6, prow = row & 63;
-        constexpr int NH = N / 2;
-        const int n0 = ch * NH;
+        constexpr int NQ = N / 4;                // state columns per thread in the shared phases
+        constexpr int NH = N / 2;                // state columns per thread in the S group
+        const int nq0 = quarter * NQ;
         uint32_t ph = 0;
         int stage = 0;
         float* vt = sm.vtab();
         float* misc = sm.misc();
         bool ok = true;
-        auto math_bar = [&]() {    // all 8 math warps
+        auto math_bar = [&]() {    // all 16 math warps
             warp_arrive(sm, kBarMath);
             if (!wait_bar_warp(sm, kBarMath, ph, a)) ok = false;
         };
-        auto group_bar = [&]() {   // the 4 warps of this group
-            warp_arrive(sm, grpL ? kBarGrpL : kBarGrpS);
-            if (!wait_bar_warp(sm, grpL ? kBarGrpL : kBarGrpS, ph, a)) ok = false;
+        auto group_bar = [&]() {   // the 8 warps of the L group
+            warp_arrive(sm, kBarGrpL);
+            if (!wait_bar_warp(sm, kBarGrpL, ph, a)) ok = false;
+        };
+        // TMEM state columns [c0, c0 + cnt) of this thread's row, cnt a multiple of 16
+        auto st_load = [&](int c0, int cnt, float* v) {
+            for (int k = 0; k < cnt; k += 16) tmem_ld16_nowait(lane_base + kColST + c0 + k, v + k);
+            tmem_wait_ld();
+        };
+        auto st_store = [&](int c0, int cnt, const float* v) {
+            for (int k = 0; k < cnt; k += 16) {
+                uint32_t r[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(v[k + e]);
+                tmem_st16(lane_base + kColST + c0 + k, r);
+            }
         };
         // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)) (0 past len)
         auto weight_x = [&](int st, int len, float last0, float last1, int first, int stride) {
@@ -555,27 +594,25 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 *p = v;
             }
         };
-        float hreg[NH];
+        float hreg[NQ];
 
-        for (int64_t q = blockIdx.x; q < np && ok; q += gridDim.x) {
-            const int64_t g0 = piece_begin(q, L, np), g1 = piece_begin(q + 1, L, np);
-            if (g0 >= g1) continue;
-            const Cursor first = locate(g0, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
-            const Cursor last = last_segment(g0, g1, a);
-            const bool first_cont = first.t > 0;
-            const bool last_cont = last.t + last.run < last.nt;
-            const bool single = (first.s == last.s && first.hp == last.hp);
+        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+            const Piece c = decode_piece(d, a);
+            if (!c.valid) break;
+            const int h0 = 2 * c.hp;
+            const bool first_cont = c.w > 0;
+            const bool last_cont = c.t1 < c.nt;
+            const int64_t q = c.q;
 
-            // ------------------------------------------------ pass 1 (both groups)
+            // ------------------------------------------------ pass 1 (all math warps)
             if (last_cont) {
-                const int h0 = 2 * last.hp;
-                for (int t = last.t; t < last.t + last.run && ok; ++t) {
+                for (int t = c.t0; t < c.t1 && ok; ++t) {
                     ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
                     if (!ok) break;
                     const float* m = sm.stage_misc(stage);
                     const float tot0 = m[0], tot1 = m[1];
-                    if (t == last.t && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
-                    weight_x(stage, tile_len(last, t), tot0, tot1, mt, kMathThreads);
+                    if (t == c.t0 && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
+                    weight_x(stage, tile_len(c, t), tot0, tot1, mt, kMathThreads);
                     fence_proxy_async_smem();
                     warp_arrive(sm, kBarWX1a + stage);
                     stage ^= 1;
@@ -585,304 +622,329 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (!ok) break;
                 tc_fence_after_sync();
                 const float dec = ex2(misc[kMiscTot0 + hrow]);
-                const int64_t slot = (q * 128 + row) * N + n0;
-                const bool starts_chain = last.t == 0;
-                const float* ip = (starts_chain && a.init)
-                                      ? a.init + (((int64_t)last.s * a.H + h0 + hrow) * 64 + prow) * N + n0
+                const float* ip = (!first_cont && a.init)
+                                      ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0
                                       : nullptr;
-                float* dst = (starts_chain ? a.incl : a.agg) + slot;
+                float* dst = (!first_cont ? a.incl : a.agg) + (q * 128 + row) * N + nq0;
+                float v[NQ];
+                st_load(nq0, NQ, v);
 #pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(lane_base + kColST + n0 + c0, v);
-#pragma unroll
-                    for (int k = 0; k < 32; k += 4) {
-                        float4 o = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                        if (ip) {
-                            const float4 i4 = *reinterpret_cast<const float4*>(ip + c0 + k);
-                            o.x = fmaf(dec, i4.x, o.x); o.y = fmaf(dec, i4.y, o.y);
-                            o.z = fmaf(dec, i4.z, o.z); o.w = fmaf(dec, i4.w, o.w);
-                        }
-                        __stcg(reinterpret_cast<float4*>(dst + c0 + k), o);
+                for (int k = 0; k < NQ; k += 4) {
+                    float4 o = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                    if (ip) {
+                        // the window starts its chain: inclusive state = dec * init + aggregate
+                        const float4 i4 = *reinterpret_cast<const float4*>(ip + k);
+                        o.x = fmaf(dec, i4.x, o.x); o.y = fmaf(dec, i4.y, o.y);
+                        o.z = fmaf(dec, i4.z, o.z); o.w = fmaf(dec, i4.w, o.w);
                     }
+                    __stcg(reinterpret_cast<float4*>(dst + k), o);
                 }
-                if (!starts_chain && mt < 2) a.decay[q * 2 + mt] = ex2(misc[kMiscTot0 + mt]);
+                if (first_cont && mt < 2) a.decay[q * 2 + mt] = ex2(misc[kMiscTot0 + mt]);
                 __threadfence();
                 math_bar();
-                if (mt == 0) st_release(a.flags + q, starts_chain ? 2 : 1);
+                if (mt == 0) st_release(a.flags + q, first_cont ? 1 : 2);
                 tc_fence_before_sync();
             }
 
-            // ------------------------------------------------ look-back (both groups)
+            // ------------------------------------------------ look-back (all math warps)
             if (first_cont) {
+                // lanes poll up to 32 predecessors at once; the state entering this window is
+                //   h_in = agg(q-1) + dec(q-1) (agg(q-2) + dec(q-2) (... + incl(q-m)))
+                // with q-m the nearest predecessor that has published its inclusive state.
 #pragma unroll
-                for (int k = 0; k < NH; ++k) hreg[k] = 0.f;
+                for (int k = 0; k < NQ; ++k) hreg[k] = 0.f;
                 float mult = 1.f;
-                for (int64_t qq = q - 1; qq >= 0; --qq) {
-                    if (piece_begin(qq, L, np) == piece_begin(qq + 1, L, np)) continue;   // empty pieces publish nothing
+                int64_t qq = q - 1;                      // next predecessor to fold in
+                const int64_t qfirst = q - c.w;          // the chain's first window (always inclusive)
+                const uint64_t t0 = global_timer_ns();
+                while (ok && qq >= qfirst) {
+                    const int64_t mine = qq - lane;
                     int f = 0;
-                    const uint64_t t0 = global_timer_ns();
-                    while (true) {
-                        int verdict = 0;   // lane 0 polls and decides; the warp follows (no divergence)
+                    if (mine >= qfirst) f = ld_acquire(a.flags + mine);
+                    const unsigned incl_mask = __ballot_sync(0xffffffffu, f == 2);
+                    const unsigned none_mask = __ballot_sync(0xffffffffu, mine >= qfirst && f == 0);
+                    const int m = incl_mask ? (__ffs(incl_mask) - 1) : 32;     // nearest inclusive lane
+                    const unsigned need = (m >= 31) ? 0xffffffffu : ((2u << m) - 1u);
+                    if (none_mask & need) {
+                        // something up to the nearest inclusive state is not published yet: spin
+                        int verdict = 0;
                         if (lane == 0) {
-                            f = ld_acquire(a.flags + qq);
-                            if (f != 0) verdict = 1;
-                            else if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) verdict = 2;
+                            if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) verdict = 2;
                             else if (global_timer_ns() - t0 > kWaitLimitNs) {
                                 record_status(a.status, SSD_ERR_TIMEOUT);
                                 atomicCAS(a.status + 2, 0, 0x200);
                                 verdict = 2;
                             }
                         }
-                        verdict = __shfl_sync(0xffffffffu, verdict, 0);
-                        f = __shfl_sync(0xffffffffu, f, 0);
-                        if (verdict == 1) break;
-                        if (verdict == 2) { ok = false; break; }
+                        if (__shfl_sync(0xffffffffu, verdict, 0) == 2) ok = false;
+                        continue;
                     }
-                    if (!ok) break;
-                    const float* src = (f == 2 ? a.incl : a.agg) + (qq * 128 + row) * N + n0;
+                    __threadfence();   // the flags were seen set: order the state reads after them
+                    const int cnt = (m < 32) ? m + 1 : 32;
+                    float dec_l = 0.f;
+                    if (lane < cnt && (m == 32 || lane < m)) dec_l = __ldcg(a.decay + (qq - lane) * 2 + hrow);
+                    for (int j = 0; j < cnt; ++j) {
+                        const int64_t qj = qq - j;
+                        const bool is_incl = (j == m);
+                        const float* src = (is_incl ? a.incl : a.agg) + (qj * 128 + row) * N + nq0;
 #pragma unroll
-                    for (int k = 0; k < NH; k += 4) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k));
-                        hreg[k] = fmaf(mult, v.x, hreg[k]);
-                        hreg[k + 1] = fmaf(mult, v.y, hreg[k + 1]);
-                        hreg[k + 2] = fmaf(mult, v.z, hreg[k + 2]);
-                        hreg[k + 3] = fmaf(mult, v.w, hreg[k + 3]);
+                        for (int k = 0; k < NQ; k += 4) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k));
+                            hreg[k] = fmaf(mult, v.x, hreg[k]);
+                            hreg[k + 1] = fmaf(mult, v.y, hreg[k + 1]);
+                            hreg[k + 2] = fmaf(mult, v.z, hreg[k + 2]);
+                            hreg[k + 3] = fmaf(mult, v.w, hreg[k + 3]);
+                        }
+                        if (!is_incl) mult *= __shfl_sync(0xffffffffu, dec_l, j);
                     }
-                    if (f == 2) break;
-                    mult *= __ldcg(a.decay + qq * 2 + hrow);
+                    if (m < 32) break;
+                    qq -= 32;
                 }
                 if (!ok) break;
                 tc_fence_after_sync();
-                if (last_cont && single) {
-                    // the piece lies inside one chain: inclusive = dec * h_in + aggregate (still in TMEM)
+                if (last_cont) {
+                    // inclusive = dec * h_in + aggregate (still in TMEM)
                     const float dec = ex2(misc[kMiscTot0 + hrow]);
-                    float* dst = a.incl + (q * 128 + row) * N + n0;
+                    float* dst = a.incl + (q * 128 + row) * N + nq0;
+                    float v[NQ];
+                    st_load(nq0, NQ, v);
 #pragma unroll
-                    for (int c0 = 0; c0 < NH; c0 += 32) {
-                        float v[32];
-                        tmem_ld32(lane_base + kColST + n0 + c0, v);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 o = make_float4(fmaf(dec, hreg[c0 + k], v[k]), fmaf(dec, hreg[c0 + k + 1], v[k + 1]),
-                                                         fmaf(dec, hreg[c0 + k + 2], v[k + 2]), fmaf(dec, hreg[c0 + k + 3], v[k + 3]));
-                            __stcg(reinterpret_cast<float4*>(dst + c0 + k), o);
-                        }
+                    for (int k = 0; k < NQ; k += 4) {
+                        const float4 o = make_float4(fmaf(dec, hreg[k], v[k]), fmaf(dec, hreg[k + 1], v[k + 1]),
+                                                     fmaf(dec, hreg[k + 2], v[k + 2]), fmaf(dec, hreg[k + 3], v[k + 3]));
+                        __stcg(reinterpret_cast<float4*>(dst + k), o);
                     }
                     __threadfence();
                 }
-                // park h_in in the TMEM state columns for the first segment
-#pragma unroll
-                for (int c0 = 0; c0 < NH; c0 += 32) {
-                    float v[32];
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = hreg[c0 + k];
-                    tmem_st32f(lane_base + kColST + n0 + c0, v);
-                }
+                st_store(nq0, NQ, hreg);   // park h_in in the TMEM state columns
                 tmem_wait_st();
                 tc_fence_before_sync();
                 math_bar();
-                if (last_cont && single && mt == 0) st_release(a.flags + q, 2);
+                if (last_cont && mt == 0) st_release(a.flags + q, 2);
             } else if (last_cont) {
-                math_bar();   // the aggregate was read by both groups before the S group parks a state
+                math_bar();   // every warp read the aggregate before the S group parks a state
             }
             if (!ok) break;
 
-            // ------------------------------------------------ pass 2, L group: L o G (+ D on the diagonal)
             if (grpL) {
-                for (int64_t g = g0; g < g1 && ok;) {
-                    const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
-                    const int h0 = 2 * c.hp;
-                    const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
-                    const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
-                    for (int t = c.t; t < c.t + c.run && ok; ++t) {
-                        const int len = tile_len(c, t);
-                        ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
-                        if (!ok) break;
-                        const float* cs = sm.cs(stage);
-                        group_bar();   // everyone is done with the previous tile's vt
-                        {
-                            const int hh = gt >> 6, j = gt & 63;
-                            vt[hh * 64 + j] = ex2(cs[hh * 128 + 63] - cs[hh * 128 + j]);   // exp(cs_63 - cs_j)
+                // ------------------------------------------------ pass 2, L group: L o G (+ D on the diagonal)
+                // thread (row i, half lh) owns columns jb + 16 lh .. + 16 of each 32-column block jb;
+                // both halves read a block pair before either overwrites it in place.
+                const int lh = half;
+                const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
+                const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
+                for (int t = c.t0; t < c.t1 && ok; ++t) {
+                    const int len = tile_len(c, t);
+                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+                    if (!ok) break;
+                    const float* cs = sm.cs(stage);
+                    group_bar();   // everyone is done with the previous tile's vt
+                    if (gt < 128) {
+                        const int hh = gt >> 6, j = gt & 63;
+                        vt[hh * 64 + j] = ex2(cs[hh * 128 + 63] - cs[hh * 128 + j]);   // exp(cs_63 - cs_j)
+                    }
+                    group_bar();
+                    ok = ok && wait_bar_warp(sm, kBarG, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int i = row;
+                    const bool rv = i < len;
+                    const float csi0 = cs[i], csi1 = cs[128 + i];
+                    const float u0 = ex2(csi0 - cs[63]), u1 = ex2(csi1 - cs[128 + 63]);
+                    const int r_lo = 32 * qd, r_hi = 32 * qd + 31;    // rows of this warp
+#pragma unroll
+                    for (int bp = 0; bp < 4; bp += 2) {
+                        // this thread's 16 columns of blocks bp and bp+1 (each read and then
+                        // overwritten by this thread only)
+                        float g[2][16];
+                        bool load[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int jc = 32 * (bp + u) + 16 * lh;
+                            load[u] = jc <= r_hi;
+                            if (load[u]) tmem_ld16_nowait(lane_base + kColG + jc, g[u]);
                         }
-                        group_bar();
-                        ok = ok && wait_bar_warp(sm, kBarG, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        const int i = row;
-                        const bool rv = i < len;
-                        const float csi0 = cs[i], csi1 = cs[128 + i];
-                        const float u0 = ex2(csi0 - cs[63]), u1 = ex2(csi1 - cs[128 + 63]);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int b = 0; b < 4; ++b) {
-                            const int jb = 32 * b;
-                            uint32_t p0[16], p1[16];
-                            const bool need = rv && jb <= i;   // tcgen05.ld is warp-collective
-                            if (!__any_sync(0xffffffffu, need)) {
+                        for (int u = 0; u < 2; ++u) {
+                            const int jb = 32 * (bp + u), jc = jb + 16 * lh;
+                            uint32_t p[2][8];   // [head][packed pairs]
+                            if (!load[u]) {
 #pragma unroll
-                                for (int k = 0; k < 16; ++k) { p0[k] = 0u; p1[k] = 0u; }
-                            } else {
-                                float gv[32];
-                                tmem_ld32(lane_base + kColG + jb, gv);
-                                if (!need) {
+                                for (int k = 0; k < 8; ++k) { p[0][k] = 0u; p[1][k] = 0u; }
+                            } else if (jb < 64 && r_lo >= 64) {
+                                // lower-left block: exp(cs_i - cs_63) exp(cs_63 - cs_j), no exponentials
+                                const float4* v0 = reinterpret_cast<const float4*>(vt + jc);
+                                const float4* v1 = reinterpret_cast<const float4*>(vt + 64 + jc);
 #pragma unroll
-                                    for (int k = 0; k < 32; ++k) gv[k] = 0.f;
+                                for (int k4 = 0; k4 < 4; ++k4) {
+                                    const float4 a4 = v0[k4], b4 = v1[k4];
+                                    p[0][2 * k4] = pack_bf16x2(g[u][4 * k4] * (u0 * a4.x), g[u][4 * k4 + 1] * (u0 * a4.y));
+                                    p[0][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * (u0 * a4.z), g[u][4 * k4 + 3] * (u0 * a4.w));
+                                    p[1][2 * k4] = pack_bf16x2(g[u][4 * k4] * (u1 * b4.x), g[u][4 * k4 + 1] * (u1 * b4.y));
+                                    p[1][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * (u1 * b4.z), g[u][4 * k4 + 3] * (u1 * b4.w));
                                 }
-                                if (jb < 64 && i >= 64) {
-                                    // lower-left block: exp(cs_i - cs_63) exp(cs_63 - cs_j)
+                            } else if (jc + 15 < r_lo) {
+                                // diagonal 64-block, strictly below the diagonal for every row: exp(cs_i - cs_j)
+                                const float4* c0p = reinterpret_cast<const float4*>(cs + jc);
+                                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + jc);
 #pragma unroll
-                                    for (int k = 0; k < 16; ++k) {
-                                        const int j = jb + 2 * k;
-                                        p0[k] = pack_bf16x2(gv[2 * k] * u0 * vt[j], gv[2 * k + 1] * u0 * vt[j + 1]);
-                                        p1[k] = pack_bf16x2(gv[2 * k] * u1 * vt[64 + j], gv[2 * k + 1] * u1 * vt[64 + j + 1]);
-                                    }
-                                } else {
-                                    // diagonal block: exp(cs_i - cs_j) for j <= i
+                                for (int k4 = 0; k4 < 4; ++k4) {
+                                    const float4 a4 = c0p[k4], b4 = c1p[k4];
+                                    p[0][2 * k4] = pack_bf16x2(g[u][4 * k4] * ex2(csi0 - a4.x), g[u][4 * k4 + 1] * ex2(csi0 - a4.y));
+                                    p[0][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * ex2(csi0 - a4.z), g[u][4 * k4 + 3] * ex2(csi0 - a4.w));
+                                    p[1][2 * k4] = pack_bf16x2(g[u][4 * k4] * ex2(csi1 - b4.x), g[u][4 * k4 + 1] * ex2(csi1 - b4.y));
+                                    p[1][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * ex2(csi1 - b4.z), g[u][4 * k4 + 3] * ex2(csi1 - b4.w));
+                                }
+                            } else {
+                                // the diagonal itself: mask j > i, D on j == i
+                                const float4* c0p = reinterpret_cast<const float4*>(cs + jc);
+                                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + jc);
 #pragma unroll
-                                    for (int k = 0; k < 16; ++k) {
-                                        const int j = jb + 2 * k;
-                                        float l00 = 0.f, l01 = 0.f, l10 = 0.f, l11 = 0.f;
-                                        if (j <= i) { l00 = ex2(csi0 - cs[j]); l10 = ex2(csi1 - cs[128 + j]); }
-                                        if (j + 1 <= i) { l01 = ex2(csi0 - cs[j + 1]); l11 = ex2(csi1 - cs[128 + j + 1]); }
-                                        float a0 = gv[2 * k] * l00, a1 = gv[2 * k + 1] * l01;
-                                        float b0 = gv[2 * k] * l10, b1 = gv[2 * k + 1] * l11;
-                                        if (j == i) { a0 += Dlg0; b0 += Dlg1; }
-                                        if (j + 1 == i) { a1 += Dlg0; b1 += Dlg1; }
-                                        p0[k] = pack_bf16x2(a0, a1);
-                                        p1[k] = pack_bf16x2(b0, b1);
+                                for (int k4 = 0; k4 < 4; ++k4) {
+                                    const float4 a4 = c0p[k4], b4 = c1p[k4];
+                                    const float ca[4] = {a4.x, a4.y, a4.z, a4.w};
+                                    const float cb[4] = {b4.x, b4.y, b4.z, b4.w};
+                                    float r0[4], r1[4];
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int j = jc + 4 * k4 + e;
+                                        r0[e] = (j <= i) ? g[u][4 * k4 + e] * ex2(csi0 - ca[e]) : 0.f;
+                                        r1[e] = (j <= i) ? g[u][4 * k4 + e] * ex2(csi1 - cb[e]) : 0.f;
+                                        if (j == i) { r0[e] += Dlg0; r1[e] += Dlg1; }
                                     }
+                                    p[0][2 * k4] = pack_bf16x2(r0[0], r0[1]);
+                                    p[0][2 * k4 + 1] = pack_bf16x2(r0[2], r0[3]);
+                                    p[1][2 * k4] = pack_bf16x2(r1[0], r1[1]);
+                                    p[1][2 * k4 + 1] = pack_bf16x2(r1[2], r1[3]);
                                 }
                             }
-                            tmem_st16(lane_base + kColG + jb, p0);
-                            tmem_st16(lane_base + kColG + jb + 16, p1);
+                            if (!rv) {
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) { p[0][k] = 0u; p[1][k] = 0u; }
+                            }
+                            tmem_st8(lane_base + kColG + jc, p[0]);       // head 0, tokens jc .. jc+15
+                            tmem_st8(lane_base + kColG + jc + 8, p[1]);   // head 1, same tokens
                         }
-                        tmem_wait_st();
-                        tc_fence_before_sync();
-                        warp_arrive(sm, kBarLG);
-                        stage ^= 1;
                     }
-                    g += c.run;
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    warp_arrive(sm, kBarLG);
+                    stage ^= 1;
                 }
             } else {
                 // ------------------------------------------------ pass 2, S group: state, weights, epilogue
-                for (int64_t g = g0; g < g1 && ok;) {
-                    const Cursor c = locate(g, g1, a.seqoff, a.tiles, a.nseq, a.npairs);
-                    const int h0 = 2 * c.hp;
-                    if (!(g == g0 && first_cont)) {
-                        // the segment starts its chain: initial state (or zero) into the TMEM state columns
-                        const float* ip = (c.t == 0 && a.init) ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N : nullptr;
+                const int sh = half;             // state columns [sh N/2, +N/2); epilogue head sh
+                const int n0 = sh * NH;
+                if (!first_cont) {
+                    // the window starts its chain: initial state (or zero) into the TMEM state columns
+                    const float* ip = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0 : nullptr;
 #pragma unroll
-                        for (int c0 = 0; c0 < N; c0 += 32) {
-                            float v[32];
+                    for (int cc = 0; cc < NH; cc += 32) {
+                        float v[32];
 #pragma unroll
-                            for (int k = 0; k < 32; k += 4) {
-                                const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + c0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
-                            }
-                            tmem_st32f(lane_base + kColST + c0, v);
+                        for (int k = 0; k < 32; k += 4) {
+                            const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + cc + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
                         }
-                        tmem_wait_st();
+                        st_store(n0 + cc, 32, v);
                     }
-                    for (int t = c.t; t < c.t + c.run && ok; ++t) {
-                        const int len = tile_len(c, t);
-                        const int row0 = tile_row0(c, t);
-                        ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+                    tmem_wait_st();
+                }
+                for (int t = c.t0; t < c.t1 && ok; ++t) {
+                    const int len = tile_len(c, t);
+                    const int row0 = tile_row0(c, t);
+                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+                    if (!ok) break;
+                    const float* cs = sm.cs(stage);
+                    const float at = ex2(cs[hrow * 128 + len - 1]);     // decay of this row's head over the tile
+                    const float e = ex2(cs[sh * 128 + row]);              // exp(cs_i), head sh
+                    const float last0 = cs[len - 1], last1 = cs[128 + len - 1];
+                    // ---- state step: stage h_{t-1} (bf16) for Yo and leave a_t h_{t-1} in TMEM for S
+                    if (t != c.t0) {
+                        ok = wait_bar_warp(sm, kBarS, ph, a);
                         if (!ok) break;
-                        const float* cs = sm.cs(stage);
-                        const float at = ex2(cs[hrow * 128 + len - 1]);     // decay of this row's head over the tile
-                        const float e0 = ex2(cs[row]), e1 = ex2(cs[128 + row]);   // exp(cs_i) for both heads
-                        const float last0 = cs[len - 1], last1 = cs[128 + len - 1];
-                        // ---- state step: stage h_{t-1} (bf16) for Yo and leave a_t h_{t-1} in TMEM for S
-                        if (t != c.t) {
-                            ok = wait_bar_warp(sm, kBarS, ph, a);
-                            if (!ok) break;
-                        }
-                        tc_fence_after_sync();
+                    }
+                    tc_fence_after_sync();
 #pragma unroll
-                        for (int c0 = 0; c0 < N; c0 += 64) {
-                            float v[64];
-                            tmem_ld32_nowait(lane_base + kColST + c0, v);
-                            tmem_ld32_nowait(lane_base + kColST + c0 + 32, v + 32);
+                    for (int cc = 0; cc < NH; cc += 32) {
+                        float v[32];
+                        st_load(n0 + cc, 32, v);
+#pragma unroll
+                        for (int k = 0; k < 32; k += 8) {
+                            const int n = n0 + cc + k;
+                            uint4 pk;
+                            pk.x = pack_bf16x2(v[k], v[k + 1]);
+                            pk.y = pack_bf16x2(v[k + 2], v[k + 3]);
+                            pk.z = pack_bf16x2(v[k + 4], v[k + 5]);
+                            pk.w = pack_bf16x2(v[k + 6], v[k + 7]);
+                            *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] *= at;
+                        st_store(n0 + cc, 32, v);
+                    }
+                    tmem_wait_st();
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    warp_arrive(sm, kBarST);
+                    // ---- weights for S: x scaled in place once Yd has read it
+                    ok = wait_bar_warp(sm, kBarYD, ph, a);
+                    if (!ok) break;
+                    weight_x(stage, len, last0, last1, gt, 256);
+                    fence_proxy_async_smem();
+                    warp_arrive(sm, kBarWX);
+                    // ---- epilogue: y = Yd + exp(cs_i) Yo, row i, head sh
+                    ok = wait_bar_warp(sm, kBarYO, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    {
+                        const int i = row;
+                        __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + sh) * 64;
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 16) {
+                            float yd[16], yo[16];
+                            tmem_ld16_nowait(lane_base + kColYD + 64 * sh + c0, yd);
+                            tmem_ld16_nowait(lane_base + kColYO + 64 * sh + c0, yo);
                             tmem_wait_ld();
+                            if (i < len) {
 #pragma unroll
-                            for (int k = 0; k < 64; k += 8) {
-                                const int n = c0 + k;
-                                uint4 pk;
-                                pk.x = pack_bf16x2(v[k], v[k + 1]);
-                                pk.y = pack_bf16x2(v[k + 2], v[k + 3]);
-                                pk.z = pack_bf16x2(v[k + 4], v[k + 5]);
-                                pk.w = pack_bf16x2(v[k + 6], v[k + 7]);
-                                *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
-                            }
-#pragma unroll
-                            for (int k = 0; k < 64; ++k) v[k] *= at;
-                            tmem_st32f(lane_base + kColST + c0, *reinterpret_cast<float(*)[32]>(v));
-                            tmem_st32f(lane_base + kColST + c0 + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-                        }
-                        tmem_wait_st();
-                        fence_proxy_async_smem();
-                        tc_fence_before_sync();
-                        warp_arrive(sm, kBarST);
-                        // ---- weights for S: x scaled in place once Yd has read it
-                        ok = wait_bar_warp(sm, kBarYD, ph, a);
-                        if (!ok) break;
-                        weight_x(stage, len, last0, last1, gt, 128);
-                        fence_proxy_async_smem();
-                        warp_arrive(sm, kBarWX);
-                        // ---- epilogue: y = Yd + exp(cs_i) Yo for both heads of row i
-                        ok = wait_bar_warp(sm, kBarYO, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        {
-                            const int i = row;
-#pragma unroll
-                            for (int hh = 0; hh < 2; ++hh) {
-                                const float e = hh ? e1 : e0;
-                                __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64;
-#pragma unroll
-                                for (int c0 = 0; c0 < 64; c0 += 32) {
-                                    float yd[32], yo[32];
-                                    tmem_ld32_nowait(lane_base + kColYD + 64 * hh + c0, yd);
-                                    tmem_ld32_nowait(lane_base + kColYO + 64 * hh + c0, yo);
-                                    tmem_wait_ld();
-                                    if (i < len) {
-#pragma unroll
-                                        for (int k = 0; k < 32; k += 8) {
-                                            uint4 v;
-                                            v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
-                                            v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
-                                            v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
-                                            v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
-                                            *reinterpret_cast<uint4*>(yrow + c0 + k) = v;
-                                        }
-                                    }
+                                for (int k = 0; k < 16; k += 8) {
+                                    uint4 v;
+                                    v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
+                                    v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
+                                    v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
+                                    v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
+                                    *reinterpret_cast<uint4*>(yrow + c0 + k) = v;
                                 }
                             }
                         }
-                        tc_fence_before_sync();
-                        warp_arrive(sm, kBarYFree);
-                        stage ^= 1;
-                    }
-                    if (!ok) break;
-                    // end of segment: the last S, then the final state at a chain end
-                    ok = wait_bar_warp(sm, kBarS, ph, a);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    if (c.t + c.run == c.nt && a.final_state) {
-                        float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N;
-#pragma unroll
-                        for (int c0 = 0; c0 < N; c0 += 32) {
-                            float v[32];
-                            tmem_ld32(lane_base + kColST + c0, v);
-#pragma unroll
-                            for (int k = 0; k < 32; k += 4)
-                                *reinterpret_cast<float4*>(fp + c0 + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                        }
                     }
                     tc_fence_before_sync();
-                    g += c.run;
+                    warp_arrive(sm, kBarYFree);
+                    stage ^= 1;
+                }
+                if (ok) {
+                    // end of the window: the last S, then the final state at a chain end
+                    ok = wait_bar_warp(sm, kBarS, ph, a);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        if (c.t1 == c.nt && a.final_state) {
+                            float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0;
+#pragma unroll
+                            for (int cc = 0; cc < NH; cc += 32) {
+                                float v[32];
+                                st_load(n0 + cc, 32, v);
+#pragma unroll
+                                for (int k = 0; k < 32; k += 4)
+                                    *reinterpret_cast<float4*>(fp + cc + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                            }
+                        }
+                        tc_fence_before_sync();
+                    }
                 }
             }
+            if (!ok) break;
             // both groups finish the piece before the next one's shared phases
             math_bar();
         }
@@ -953,16 +1015,35 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
 }  // namespace
 
 
-int64_t fused_pieces(const Problem& p) {
+void fused_plan(const Problem& p, int* K_out, int64_t* np_out) {
     const int64_t npairs = p.s.nheads / 2;
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
-    const int64_t L = npairs * p.L.max_chunks;
-    int64_t rounds = L / ((int64_t)grid * kPieceTiles);
-    if (rounds < 1) rounds = 1;
-    return rounds * grid;
+    if (!p.varlen) {
+        // dense: pick the window K (tiles per piece) that balances the rounds best; a piece costs
+        // its K tiles plus about one tile of fixed work (look-back, pass-1 set-up)
+        const int64_t nt = (p.s.seqlen + kFusedTile - 1) / kFusedTile;
+        const int64_t nchains = p.s.batch * npairs;
+        int bestK = kFusedMinWindow;
+        double best = 1e300;
+        for (int K = kFusedMinWindow; K <= kFusedMaxWindow; ++K) {
+            const int64_t W = (nt + K - 1) / K;
+            const int64_t np = nchains * W;
+            const int64_t rounds = (np + grid - 1) / grid;
+            const double cost = (double)rounds * (K + 1.0);
+            if (cost < best - 1e-9) { best = cost; bestK = K; }
+        }
+        *K_out = bestK;
+        *np_out = nchains * ((nt + bestK - 1) / bestK);
+    } else {
+        // packed batch: windows of 8 tiles; the piece count is bounded here, exact on the device
+        const int K = 8;
+        *K_out = K;
+        const int64_t max_tiles = p.L.max_chunks;
+        *np_out = npairs * ((max_tiles - p.nseq + K - 1) / K + p.nseq);
+    }
 }
 
-cudaError_t launch_fused(const Problem& p) {
+cudaError_t launch_fused(const Problem& p, int K, int64_t np) {
     const int H = (int)p.s.nheads, N = (int)p.s.dstate, G = (int)p.s.ngroups;
     const int64_t npairs = H / 2;
     FusedMaps maps;
@@ -970,21 +1051,18 @@ cudaError_t launch_fused(const Problem& p) {
         !make_map_fused(&maps.c, p.C, N, G, p.rows))
         return note_cuda_error("fused tensor maps", cudaErrorInvalidValue);
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
-    // pieces: ~kPieceTiles tiles each (sized from the tile-count bound; the kernel cuts the
-    // actual list), a whole number of rounds over the grid
-    const int64_t np = fused_pieces(p);
     FusedArgs fa;
     fa.header = p.status();
     fa.status = p.status();
     fa.tiles = p.chunks();
     fa.seqoff = p.seqoff();
+    fa.woff = p.varlen ? p.woff() : nullptr;
     fa.dt = p.dt;
     fa.A = p.A;
     fa.D = p.D;
     fa.init = p.init;
     fa.final_state = p.final_state;
     fa.y = (__nv_bfloat16*)p.y;
-    if (np > p.L.max_pieces) return cudaErrorInvalidValue;
     fa.flags = p.flags();
     fa.decay = reinterpret_cast<float*>(p.ws + p.L.pdecay);
     fa.agg = reinterpret_cast<float*>(p.ws + p.L.agg);
@@ -994,6 +1072,11 @@ cudaError_t launch_fused(const Problem& p) {
     fa.nseq = (int)p.nseq;
     fa.npairs = (int)npairs;
     fa.npieces = np;
+    fa.K = K;
+    fa.dense = p.varlen ? 0 : 1;
+    fa.seqlen = p.s.seqlen;
+    fa.nt_dense = (int)((p.s.seqlen + kFusedTile - 1) / kFusedTile);
+    fa.W_dense = (fa.nt_dense + K - 1) / K;
     cudaError_t e;
     prof_begin(p.stream);
     e = (N == 64) ? launch_fused_n<64>(p, fa, maps, grid) : launch_fused_n<128>(p, fa, maps, grid);

@@ -32,10 +32,11 @@ struct ChunkDesc {
 //   incl    : float[max_pieces * 128 * N], true end state of that segment
 constexpr int kFusedTile = 128;
 constexpr int kFusedMaxGrid = 256;
-constexpr int kFusedPieceTiles = 8;
+constexpr int kFusedMinWindow = 4;    // tiles per piece, lower bound (bounds the workspace)
+constexpr int kFusedMaxWindow = 16;
 
 struct WsLayout {
-    size_t header, chunks, seqoff, decay, states, flags, pdecay, agg, incl, total;
+    size_t header, chunks, seqoff, woff, decay, states, flags, pdecay, agg, incl, total;
     int64_t max_chunks, nseq, max_pieces;
     bool fused;
 };
@@ -62,8 +63,11 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
     w.chunks = off; off = align256(off + sizeof(ChunkDesc) * (size_t)(w.max_chunks > 0 ? w.max_chunks : 1));
     w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
     if (w.fused) {
-        const int64_t L = (s.nheads / 2) * w.max_chunks;
-        w.max_pieces = L / kFusedPieceTiles + kFusedMaxGrid;
+        // pieces are windows of >= kFusedMinWindow tiles of one (sequence, head pair)
+        const int64_t per_seq = varlen ? ((w.max_chunks - nseq_eff) + kFusedMinWindow - 1) / kFusedMinWindow + nseq_eff
+                                       : s.batch * ((((s.seqlen + q - 1) / q) + kFusedMinWindow - 1) / kFusedMinWindow);
+        w.max_pieces = (s.nheads / 2) * (per_seq > 0 ? per_seq : 1);
+        w.woff = off;   off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
         w.flags = off;  off = align256(off + sizeof(int32_t) * (size_t)w.max_pieces);
         w.pdecay = off; off = align256(off + sizeof(float) * 2 * (size_t)w.max_pieces);
         w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * s.dstate));
@@ -106,6 +110,7 @@ struct Problem {
     float* decay() const { return reinterpret_cast<float*>(ws + L.decay); }
     float* states() const { return reinterpret_cast<float*>(ws + L.states); }
     int* flags() const { return reinterpret_cast<int*>(ws + L.flags); }
+    int32_t* woff() const { return reinterpret_cast<int32_t*>(ws + L.woff); }
 };
 
 // ssd_api.cu: records the failing step of an SSD_ERR_CUDA for ssd_last_error_detail
@@ -115,16 +120,18 @@ cudaError_t note_cuda_error(const char* step, cudaError_t e);
 void prof_begin(cudaStream_t s);
 void prof_end(cudaStream_t s);
 
-// ssd_common.cu: chunk (tile) table of `q` tokens; zeroes `nflags` piece flags
-cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags);
+// ssd_common.cu: chunk (tile) table of `q` tokens; zeroes `nflags` piece flags; with woff,
+// also the per-sequence offsets of windows of K chunks
+cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags, int32_t* woff = nullptr, int K = 1);
 cudaError_t launch_state_pass(const Problem& p);
 // ssd_f32.cu
 cudaError_t launch_f32_path(const Problem& p);
 // ssd_tc.cu (three-kernel tcgen05 path)
 cudaError_t launch_bf16_path(const Problem& p);
 bool bf16_path_supports(const ssd_shape& s, int chunk);
-// ssd_fused.cu (single-pass tcgen05 path)
-int64_t fused_pieces(const Problem& p);
-cudaError_t launch_fused(const Problem& p);
+// ssd_fused.cu (single-pass tcgen05 path): the window size K (tiles per piece) and the number of
+// pieces (exact for a dense batch, an upper bound for a packed batch)
+void fused_plan(const Problem& p, int* K, int64_t* npieces);
+cudaError_t launch_fused(const Problem& p, int K, int64_t npieces);
 
 }  // namespace ssd
