@@ -120,6 +120,33 @@ int ssd_forward_host(const ssd_shape *shape, ssd_dtype dtype,
                      void *stream);
 
 /*
+ * ssd_forward for callers that cannot allocate device memory (for example code that runs
+ * before its allocator is set up, or inside a context whose memory it does not own). There
+ * is no counterpart on the pages: this entry point only changes where scratch comes from.
+ *
+ * Arguments and results are those of ssd_forward without the workspace: the scratch is a
+ * file-scope device array of 16 MiB inside this library, which every GPU that loads the
+ * library holds until the process exits. Problems whose ssd_workspace_size exceeds it are
+ * rejected with SSD_ERR_WORKSPACE before anything is launched (ssd_last_error_detail gives
+ * both sizes). Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+ * Nothing in the array has to start at zero: the first kernel of every call clears the
+ * status word, counters and look-back flags that the later kernels read.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it; make that first call before any stream capture on that device.
+ * Every call shares the one array: calls whose work overlaps on the GPU (different
+ * streams, or host threads without ordering) race and corrupt each other's results.
+ * Device-side status (a bounded wait that timed out) is not readable for these calls.
+ */
+int ssd_forward_noalloc(const ssd_shape *shape, ssd_dtype dtype,
+                        const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D,
+                        int chunk, const float *initial_state,
+                        const int32_t *cu_seqlens, int nseq,
+                        void *y, float *final_state,
+                        void *stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last ssd_forward that used it (SSD_OK or SSD_ERR_TIMEOUT),
  * or SSD_ERR_CUDA if the copy itself fails.
