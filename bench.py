@@ -1,8 +1,9 @@
 """Benchmark of the SSD layer forward on GB300.
 
-One step = one full SSD forward (chunk table, chunk states, state pass, chunk outputs)
-over the long-sequence workload b=1, T=16384, H=80, P=64, N=128, G=1, chunk 256, bf16
-x/B/C with fp32 dt/A/D. Prints ONE JSON line (rank 0).
+One step = one full SSD forward (chunk cumsums, diagonal blocks, chunk states, inter-chunk
+state pass, off-diagonal outputs and the D skip) over the long-sequence workload b=1,
+T=16384, H=80, P=64, N=128, G=1, chunk 256, bf16 x/B/C with fp32 dt/A/D. Prints ONE JSON
+line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -14,6 +15,7 @@ problems, no collective on the data path); value = all ranks' tokens / max time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -28,6 +30,41 @@ sys.path.insert(0, ROOT)
 METRIC = "SSD fwd tokens/s and % of bf16 tensor/HBM roofline, T=2K–16K, N=128"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
+# workload, with a stamp of the kernel's sources at capture time. A stamp that no longer
+# matches the sources means the kernel changed since: the traffic is then reported as null.
+KERNEL_SOURCES = ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
+                  "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh")
+NCU_TRAFFIC = {
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 274485760 + 209124352, "stamp": "b47e893736c61106"},
+}
+
+
+def kernel_source_stamp() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str, kernel: str):
+    rec = NCU_TRAFFIC.get(workload)
+    if rec is None or rec["kernel"] != kernel or rec["stamp"] != kernel_source_stamp():
+        return None
+    return rec["bytes"]
+
+
+def reduce_over_ranks(ms: float, tokens_per_rank: int, steps: int, world: int, device):
+    """Slowest rank's timed region (max over ranks) and the whole-job tokens/s it gives."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * tokens_per_rank * steps / (ms / 1e3)
 
 
 def load_peaks():
@@ -63,7 +100,7 @@ def algorithmic_flops(w, batch_rows) -> int:
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -75,7 +112,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
         return self
@@ -91,19 +128,28 @@ class ClockSampler:
         else:
             self.out = ""
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen; with (t0, t1) (time.time() around the
+        timed region) only the samples taken inside it count, when there are any."""
+        import datetime
+        rows = []
         for line in (self.out or "").strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for nm, v in zip(names, f[5:9]):
+        if t0 is not None and any(t0 <= r[0] <= t1 for r in rows):
+            rows = [r for r in rows if t0 <= r[0] <= t1]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, s, m, flags in rows:
+            sm.append(s)
+            mx.append(m)
+            for nm, v in zip(names, flags):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
@@ -158,27 +204,33 @@ def config_dict(w):
             "l2": "inputs larger than L2 (2 rotating input sets of ~350 MB each)"}
 
 
-def cpu_baseline(w, budget_tokens: int):
+def cpu_baseline(w, budget_tokens: int, min_seconds: float = 10.0, max_runs: int = 50):
+    """The oracle as it stands on the host cores: one sequence of the workload (all heads),
+    run repeatedly until about `min_seconds` of CPU work has been timed."""
     import oracle
     from mamba_ssd_layer_gb300.inputs import make_inputs, small_variant
     tokens = min(w.seqlen, budget_tokens)
     d = make_inputs(small_variant(w, seqlen=tokens, nheads=w.nheads, batch=1))
     threads = oracle.default_threads()
-    t0 = time.perf_counter()
-    oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"], nthreads=threads)
+    runs, t0 = 0, time.perf_counter()
+    while runs < max_runs and (runs == 0 or time.perf_counter() - t0 < min_seconds):
+        oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
+                              d["cu_seqlens"], nthreads=threads)
+        runs += 1
     dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {tokens} of {w.seqlen} tokens, all {w.nheads} heads, 1 run ({dt:.1f} s)"}
+    return {"value": tokens * runs / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{tokens} of {w.seqlen * w.batch} tokens (one sequence, all {w.nheads} heads), "
+                      f"{runs} runs in {dt:.1f} s"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_n128")
-    ap.add_argument("--ref-tokens", type=int, default=4096)
+    ap.add_argument("--ref-tokens", type=int, default=16384)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
 
@@ -244,23 +296,23 @@ def main():
     with ClockSampler(dev.index) as clk:
         time.sleep(0.3)
         torch.cuda.synchronize()
+        wall0 = time.time()
         ev0.record(stream)
         for i in range(args.steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
+        wall1 = time.time()
     bd.profile_enable(False)
     kern_ms, kern_n = bd.profile_read()
     ms = ev0.elapsed_time(ev1)
     status = bd.ssd_status(workspace)
     if status != bd.SSD_OK:
         raise RuntimeError(f"device status after timing: {bd.ssd_status_string(status)}")
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    launches = bd.profile_kernel_launches()
+    kernel = bd.profile_kernel_name()
+    ms, value = reduce_over_ranks(ms, rows, args.steps, world, dev)
     ms_per_step = ms / args.steps
-    value = world * rows * args.steps / (ms / 1e3)
 
     # end to end through the host entry point: pinned inputs in, y and final states out
     hx = {k: torch.from_numpy(d[k]).to(torch.bfloat16).pin_memory() for k in ("x", "B", "C")}
@@ -307,15 +359,16 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if achieved else None, "traffic": None,
-                     "peak_source": src, "kernel": "ssd_chunk_out (dominant)", "kernel_ms": kern_avg_ms,
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": measured_traffic(w.name, kernel),
+                     "peak_source": src, "kernel": kernel, "kernel_ms": kern_avg_ms,
                      "alg_bytes_per_launch": alg_bytes,
                      "step_frac": alg_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
         "tflops": alg_flops / (ms_per_step / 1e3) / 1e12,
         "e2e": {"value": world * rows * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 4 * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "clocks": clk.summary(wall0, wall1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.ref_tokens)

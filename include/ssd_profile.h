@@ -7,7 +7,7 @@
  * events come from a pool the library creates on first use and keeps until exit;
  * no device memory is allocated. ssd_profile_read synchronises on the recorded events,
  * returns the summed elapsed time and the number of recorded launches, and resets
- * the pool for reuse.
+ * the pool for reuse. The library also counts every kernel it launches while recording.
  */
 #ifndef SSD_GB300_PROFILE_H
 #define SSD_GB300_PROFILE_H
@@ -23,6 +23,13 @@ int ssd_profile_enable(int on);
 /* Sum of elapsed milliseconds over the recorded launches and their count; resets the
  * record. Returns SSD_OK, or SSD_ERR_CUDA if an event query fails. */
 int ssd_profile_read(double *total_ms, int *launches);
+
+/* Kernels of this library launched from the calling host thread since recording was last
+ * enabled (all of them, not only the timed one). */
+long long ssd_profile_kernel_launches(void);
+
+/* Name of the kernel the events bracket (static string; "" before the first recorded call). */
+const char *ssd_profile_kernel_name(void);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,10 @@ def load_library():
     lib.ssd_profile_enable.restype = i32
     lib.ssd_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
     lib.ssd_profile_read.restype = i32
+    lib.ssd_profile_kernel_launches.argtypes = []
+    lib.ssd_profile_kernel_launches.restype = ctypes.c_longlong
+    lib.ssd_profile_kernel_name.argtypes = []
+    lib.ssd_profile_kernel_name.restype = ctypes.c_char_p
     lib.ssd_last_error_detail.argtypes = []
     lib.ssd_last_error_detail.restype = ctypes.c_char_p
     lib.ssd_status_string.argtypes = [i32]
@@ -222,3 +226,13 @@ def profile_read():
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_profile_read")
     return ms.value, n.value
+
+
+def profile_kernel_launches() -> int:
+    """Kernels the library launched on this thread since recording was last enabled."""
+    return int(load_library().ssd_profile_kernel_launches())
+
+
+def profile_kernel_name() -> str:
+    """Name of the kernel the recorded events bracket."""
+    return load_library().ssd_profile_kernel_name().decode()

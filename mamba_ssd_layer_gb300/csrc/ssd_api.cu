@@ -55,6 +55,8 @@ struct ProfState {
     bool on = false;
     std::vector<cudaEvent_t> ev;   // begin/end pairs
     size_t used = 0;               // events recorded since the last read
+    long long launches = 0;        // kernels launched since recording was enabled
+    const char* kernel = "";       // the kernel the events bracket
 };
 thread_local ProfState g_prof;
 thread_local char g_err_detail[160] = "";
@@ -70,8 +72,13 @@ cudaError_t note_cuda_error(const char* step, cudaError_t e) {
     return e;
 }
 
-void prof_begin(cudaStream_t s) {
+void prof_launch() {
+    if (g_prof.on) ++g_prof.launches;
+}
+
+void prof_begin(cudaStream_t s, const char* kernel) {
     if (!g_prof.on) return;
+    g_prof.kernel = kernel;
     if (g_prof.used + 2 > g_prof.ev.size()) {
         for (int i = 0; i < 2; ++i) {
             cudaEvent_t e;
@@ -91,7 +98,7 @@ void prof_end(cudaStream_t s) {
 extern "C" {
 
 int ssd_profile_enable(int on) {
-    if (on && !g_prof.on) g_prof.used = 0;
+    if (on && !g_prof.on) { g_prof.used = 0; g_prof.launches = 0; }
     g_prof.on = on != 0;
     return SSD_OK;
 }
@@ -112,6 +119,10 @@ int ssd_profile_read(double* total_ms, int* launches) {
     if (launches) *launches = n;
     return SSD_OK;
 }
+
+long long ssd_profile_kernel_launches(void) { return g_prof.launches; }
+
+const char* ssd_profile_kernel_name(void) { return g_prof.kernel; }
 
 size_t ssd_workspace_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int nseq) {
     const bool varlen = nseq > 0;

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
 }
 
 cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags, int32_t* woff, int K) {
+    prof_launch();
     prep_kernel<<<1, 1024, 0, p.stream>>>(p.varlen ? p.cu_seqlens : nullptr, p.nseq, p.s.seqlen, p.rows,
                                           q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks, flags, nflags,
                                           woff, K);
@@ -205,6 +206,7 @@ cudaError_t launch_state_pass(const Problem& p) {
     const bool vec4 = (PN % 4) == 0;
     const int64_t units = vec4 ? PN / 4 : PN;
     dim3 grid((unsigned)((units + 255) / 256), (unsigned)p.s.nheads, (unsigned)p.nseq);
+    prof_launch();
     if (vec4)
         state_pass_kernel<4><<<grid, 256, 0, p.stream>>>(p.status(), p.seqoff(), p.decay(), p.states(),
                                                          p.init, p.final_state, (int)p.s.nheads, PN);

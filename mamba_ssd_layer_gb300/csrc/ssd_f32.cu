@@ -150,13 +150,15 @@ cudaError_t launch_f32_path(const Problem& p) {
     const int H = (int)p.s.nheads, P = (int)p.s.headdim, N = (int)p.s.dstate, G = (int)p.s.ngroups;
     if (p.L.max_chunks == 0) return launch_state_pass(p);
     dim3 grid((unsigned)p.L.max_chunks, (unsigned)H);
+    prof_launch();
     chunk_state_f32<<<grid, 256, 0, p.stream>>>(p.status(), p.chunks(), (const float*)p.x, p.dt, p.A,
                                                 (const float*)p.B, p.decay(), p.states(), H, P, N, G);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_state_pass(p);
     if (e != cudaSuccess) return e;
-    prof_begin(p.stream);
+    prof_launch();
+    prof_begin(p.stream, "chunk_out_f32");
     chunk_out_f32<<<grid, kThreads, 0, p.stream>>>(p.status(), p.chunks(), (const float*)p.x, p.dt, p.A,
                                                    (const float*)p.B, (const float*)p.C, p.D, p.states(),
                                                    (float*)p.y, H, P, N, G);

@@ -1009,6 +1009,7 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    prof_launch();
     return note_cuda_error("fused cooperative launch", cudaLaunchKernelEx(&cfg, ssd_fused_kernel<N>, maps, fa));
 }
 
@@ -1078,7 +1079,7 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np) {
     fa.nt_dense = (int)((p.s.seqlen + kFusedTile - 1) / kFusedTile);
     fa.W_dense = (fa.nt_dense + K - 1) / K;
     cudaError_t e;
-    prof_begin(p.stream);
+    prof_begin(p.stream, "ssd_fused_kernel");
     e = (N == 64) ? launch_fused_n<64>(p, fa, maps, grid) : launch_fused_n<128>(p, fa, maps, grid);
     prof_end(p.stream);
     return e;

@@ -116,8 +116,10 @@ struct Problem {
 // ssd_api.cu: records the failing step of an SSD_ERR_CUDA for ssd_last_error_detail
 // and clears the runtime's sticky "last error" so later calls do not inherit it.
 cudaError_t note_cuda_error(const char* step, cudaError_t e);
-// ssd_api.cu: optional event pair around the dominant kernel (see ssd_profile.h)
-void prof_begin(cudaStream_t s);
+// ssd_api.cu: optional event pair around the dominant kernel (see ssd_profile.h), and a count
+// of every kernel launch (each launcher calls prof_launch once per launch it makes)
+void prof_launch();
+void prof_begin(cudaStream_t s, const char* kernel);
 void prof_end(cudaStream_t s);
 
 // ssd_common.cu: chunk (tile) table of `q` tokens; zeroes `nflags` piece flags; with woff,

@@ -514,6 +514,7 @@ cudaError_t launch_bf16_path(const Problem& p) {
 
     const size_t smem_a = 1024 + (size_t)(2 + nb) * ntiles * kRegion;
     cudaFuncSetAttribute(chunk_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a);
+    prof_launch();
     chunk_state_tc<<<grid, kThreads, smem_a, p.stream>>>(maps, p.status(), p.status(), p.chunks(), p.dt, p.A,
                                                          p.decay(), p.states(), H, N, G, Q);
     cudaError_t e = cudaGetLastError();
@@ -524,7 +525,8 @@ cudaError_t launch_bf16_path(const Problem& p) {
     size_t smem_c = (size_t)(2 + 2 * nb + (nb > 2 ? nb : 2)) * kRegion + 2048 + 64;
     if (smem_c < 120 * 1024) smem_c = 120 * 1024;
     cudaFuncSetAttribute(chunk_out_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_c);
-    prof_begin(p.stream);
+    prof_launch();
+    prof_begin(p.stream, "chunk_out_tc");
     chunk_out_tc<<<grid, kThreads, smem_c, p.stream>>>(maps, p.status(), p.status(), p.chunks(), p.dt, p.A, p.D,
                                                        p.states(), (__nv_bfloat16*)p.y, H, N, G, Q);
     prof_end(p.stream);
