@@ -30,6 +30,7 @@
 // warps 2..9 = math (masks, state updates, weights, epilogue, look-back).
 // Every wait is bounded; a timeout records SSD_ERR_TIMEOUT and the CTA winds down.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kTile = kFusedTile;
 constexpr int kRegion = kTile * 128;          // one 128-row x 128-byte swizzled box (16 KB)
-constexpr int kThreads = 576;        // 2 + 8 + 8 warps
+constexpr int kThreads = 576;        // producer warp, MMA warp, 16 math warps
 constexpr int kMathThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -168,23 +169,22 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 
 // Barrier slots in shared memory
 enum {
-    kBarFull0 = 0, kBarFull1, kBarEmpty0, kBarEmpty1,
+    kBarFullX0 = 0, kBarFullX1, kBarFullBC0, kBarFullBC1, kBarEmpty0, kBarEmpty1,
     kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree, kBarAgg, kBarMath,
-    kBarGrpL, kBarGrpS,
     kNumBars
 };
 
 // Pass-1 weights use one barrier per stage (kBarWX1a + stage): the math warps may weight the
 // next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
 // barrier before the first was waited for would make the waiter miss a phase.
-// Expected arrivals per phase: full = producer's expect_tx + its "cumsum written" arrival;
-// pass-2 signals from one math group (8 warps); pass-1 weights and the shared barrier from
-// both groups (16 warps); MMA commits 1.
+// Expected arrivals per phase: the x barrier = producer's expect_tx + its "cumsum written"
+// arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16);
+// MMA commits 1.
 __device__ __forceinline__ uint32_t bar_count(int i) {
     switch (i) {
-        case kBarFull0: case kBarFull1: return 2;
-        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarGrpL: case kBarGrpS: return 8;
-        case kBarWX1a: case kBarWX1b: case kBarMath: return 16;
+        case kBarFullX0: case kBarFullX1: return 2;
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarWX1a: case kBarWX1b: case kBarMath:
+            return 16;
         default: return 1;
     }
 }
@@ -201,8 +201,9 @@ struct Smem {
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(hs() + (N / 64) * kRegion) + s * 260; }
     __device__ float* stage_misc(int s) const { return cs(s) + 256; }
-    __device__ float* vtab() const { return cs(0) + 520; }                                            // [2][64]
-    __device__ float* misc() const { return vtab() + 128; }                                           // [8]
+    // exp(cs_p - cs_j) per head and token j (p = last token of j's 16-token group), fp16 pairs [2][64]
+    __device__ __half2* vt() const { return reinterpret_cast<__half2*>(cs(0) + 520); }
+    __device__ float* misc() const { return cs(0) + 520 + 128; }                                     // [8]
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(misc() + 8); }           // [kNumBars]
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
@@ -349,10 +350,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 
     if (warp == 0) {
         // ============================================================ producer warp
-        // TMA for x (both heads), B and C (lane 0); dt for both heads -> the tile-local cumsum of
-        // dt*A (x log2 e), plus the window carry in pass 1 (all lanes), written into the stage.
+        // TMA (lane 0): pass 1 loads x and B on the stage's x barrier; pass 2 loads B and C on the
+        // B/C barrier (they feed C B^T first) and x on the x barrier. All lanes: dt for both heads
+        // -> the tile-local cumsum of dt*A (x log2 e), with the window carry in pass 1. In pass 2
+        // also the table v_j = exp(cs_p - cs_j), p the last token of j's 16-token group, once the
+        // previous tile's L o G (its only reader) is done.
         uint32_t ph = 0;
         uint32_t issued = 0;
+        uint32_t p2 = 0;   // pass-2 tiles loaded so far
         int stage = 0;
         bool ok = true;
         auto load_tile = [&](const Piece& c, int t, bool pass1, float tot0, float tot1, float& carry0,
@@ -364,16 +369,24 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             issued |= 1u << stage;
             const int row0 = tile_row0(c, t), len = tile_len(c, t);
             const int h0 = 2 * c.hp;
-            uint64_t* full = sm.bars() + kBarFull0 + stage;
+            uint64_t* fullx = sm.bars() + kBarFullX0 + stage;
             if (lane == 0) {
                 const int g = h0 / (a.H / a.G);
-                mbar_arrive_expect_tx(full, (uint32_t)((2 + (pass1 ? 1 : 2) * NB) * kRegion));
-                tma_load_3d(sm.x(stage, 0), &maps.x, full, 0, h0, row0);
-                tma_load_3d(sm.x(stage, 1), &maps.x, full, 0, h0 + 1, row0);
-                for (int k = 0; k < NB; ++k) {
-                    tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, full, 64 * k, g, row0);
-                    if (!pass1) tma_load_3d(sm.c(stage) + k * kRegion, &maps.c, full, 64 * k, g, row0);
+                if (pass1) {
+                    mbar_arrive_expect_tx(fullx, (uint32_t)((2 + NB) * kRegion));
+                    for (int k = 0; k < NB; ++k)
+                        tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, fullx, 64 * k, g, row0);
+                } else {
+                    uint64_t* fullbc = sm.bars() + kBarFullBC0 + stage;
+                    mbar_arrive_expect_tx(fullbc, (uint32_t)(2 * NB * kRegion));
+                    for (int k = 0; k < NB; ++k) {
+                        tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, fullbc, 64 * k, g, row0);
+                        tma_load_3d(sm.c(stage) + k * kRegion, &maps.c, fullbc, 64 * k, g, row0);
+                    }
+                    mbar_arrive_expect_tx(fullx, (uint32_t)(2 * kRegion));
                 }
+                tma_load_3d(sm.x(stage, 0), &maps.x, fullx, 0, h0, row0);
+                tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
             }
             float v[2][4];
 #pragma unroll
@@ -384,6 +397,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
                 }
             float* cs = sm.cs(stage);
+            float cv[2][4];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const float A2 = __ldg(a.A + h0 + hh) * kLog2e;
@@ -398,8 +412,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (lane >= o) sc += tt;
                 }
                 const float base = sc - p[3] + (pass1 ? (hh ? carry1 : carry0) : 0.f);
-                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) =
-                    make_float4(base + p[0], base + p[1], base + p[2], base + p[3]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cv[hh][k] = base + p[k];
+                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
                 const float tile_total = __shfl_sync(0xffffffffu, sc, 31);
                 if (pass1) { if (hh) carry1 += tile_total; else carry0 += tile_total; }
             }
@@ -408,8 +423,26 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 m[0] = tot0;
                 m[1] = tot1;
             }
+            if (!pass1) {
+                if (p2 > 0) {
+                    const bool w = wait_bar(sm, kBarLG, ph, a);
+                    if (!__all_sync(0xffffffffu, w)) return false;
+                }
+                ++p2;
+                __half2* vt = sm.vt();
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float piv = __shfl_sync(0xffffffffu, cv[hh][3], lane | 3);
+                    const __half2 lo = __floats2half2_rn(ex2(piv - cv[hh][0]), ex2(piv - cv[hh][1]));
+                    const __half2 hi = __floats2half2_rn(ex2(piv - cv[hh][2]), ex2(piv - cv[hh][3]));
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(vt + hh * 64 + 2 * lane) = pk;
+                }
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(full);
+            if (lane == 0) mbar_arrive(fullx);
             stage ^= 1;
             return true;
         };
@@ -460,19 +493,22 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 mma_commit(sm.bars() + kBarG);
             };
+            auto issue_s = [&](int st, bool first) {
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
+                    mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || !first) ? 1u : 0u);
+                }
+            };
             for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
                 const Piece c = decode_piece(d, a);
                 if (!c.valid) break;
                 if (c.t1 < c.nt) {
                     for (int t = c.t0; t < c.t1 && ok; ++t) {
-                        ok = wait_bar(sm, kBarFull0 + stage, ph, a) && wait_bar(sm, kBarWX1a + stage, ph, a);
+                        ok = wait_bar(sm, kBarFullX0 + stage, ph, a) && wait_bar(sm, kBarWX1a + stage, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(stage, 0) + ks * 2048), kRegion, 1024);
-                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(stage) + ks * 2048), kRegion, 1024);
-                            mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || t > c.t0) ? 1u : 0u);
-                        }
+                        issue_s(stage, t == c.t0);
                         mma_commit(sm.bars() + kBarEmpty0 + stage);
                         stage ^= 1;
                     }
@@ -480,19 +516,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 // pass 2, per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an
                 // earlier one's reads of the same TMEM):
-                //   Yd(t), both heads interleaved       needs L o G(t), Y regions free
-                //   G(t+1)                              needs the next stage; runs while the S warps
-                //                                       stage the state and weight x
-                //   Yo(t) and S(t), interleaved         needs the staged state and the weights
+                //   Yd(t), both heads interleaved      needs L o G(t), the Y regions free
+                //   Yo(t)                              needs the staged state h_{t-1}
+                //   G(t+1)                             needs the next stage's B and C
+                //   S(t)                               needs the weighted x
                 for (int t = c.t0; t < c.t1 && ok; ++t) {
                     const int st = stage;
                     if (t == c.t0) {
-                        ok = wait_bar(sm, kBarFull0 + st, ph, a);
+                        ok = wait_bar(sm, kBarFullBC0 + st, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
                         issue_g(st);
                     }
-                    ok = wait_bar(sm, kBarLG, ph, a);
+                    ok = wait_bar(sm, kBarLG, ph, a) && wait_bar(sm, kBarFullX0 + st, ph, a);
                     if (ok && have_prev_tile) ok = wait_bar(sm, kBarYFree, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -504,27 +540,26 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         }
                     }
                     mma_commit(sm.bars() + kBarYD);
+                    ok = wait_bar(sm, kBarST, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    for (int ks = 0; ks < N / 16; ++ks) {
+                        const int kk = ks / 4, off = (ks % 4) * 32;
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + kk * kRegion + off), 0, 1024);
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
+                        mma_bf16_ss(tmem + kColYO, ad, bd, id_yo, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(sm.bars() + kBarYO);
                     if (t + 1 < c.t1) {
-                        ok = wait_bar(sm, kBarFull0 + (st ^ 1), ph, a);
+                        ok = wait_bar(sm, kBarFullBC0 + (st ^ 1), ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
                         issue_g(st ^ 1);
                     }
-                    ok = wait_bar(sm, kBarST, ph, a) && wait_bar(sm, kBarWX, ph, a);
+                    ok = wait_bar(sm, kBarWX, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    for (int ks = 0; ks < 8; ++ks) {
-                        if (ks < N / 16) {
-                            const int kk = ks / 4, off = (ks % 4) * 32;
-                            const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + kk * kRegion + off), 0, 1024);
-                            const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
-                            mma_bf16_ss(tmem + kColYO, ad, bd, id_yo, ks > 0 ? 1u : 0u);
-                        }
-                        const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
-                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
-                        mma_bf16_ss(tmem + kColST, ad, bd, id_s, 1u);
-                    }
-                    mma_commit(sm.bars() + kBarYO);
+                    issue_s(st, false);
                     mma_commit(sm.bars() + kBarS);
                     mma_commit(sm.bars() + kBarEmpty0 + st);
                     stage ^= 1;
@@ -534,34 +569,26 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         }
     } else {
         // ============================================================ math warps
-        // warps 2-9 ("L" group, two per TMEM lane quadrant, each half of the columns): L o G in
-        // pass 2; warps 10-17 ("S" group, two per quadrant): state steps, weights and the epilogue.
-        // All 16 share pass 1, publishing and the look-back, a quarter of the state columns each.
+        // 16 warps, four per TMEM lane quadrant qd (the rows 32 qd .. 32 qd + 31 a warp may access);
+        // kq (0..3) picks the warp's share of the columns in every phase:
+        //   L o G       column block 32 kq .. 32 kq + 31 (both heads)
+        //   state       state columns kq N/4 .. (kq + 1) N/4
+        //   epilogue    head kq / 2, channels 32 (kq % 2) .. + 31
         const int mt = tid - 64;                 // 0..511
-        const bool grpL = warp < 10;
-        const int gw = grpL ? warp - 2 : warp - 10;   // warp index within its group, 0..7
-        const int gt = gw * 32 + lane;           // thread index within its group, 0..255
-        const int half = gw >> 2;                // which half of the columns (group phases)
-        const int qd = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int quarter = (warp - 2) >> 2;     // column quarter in the shared phases
+        const int qd = warp & 3;
+        const int kq = (warp - 2) >> 2;
         const int row = 32 * qd + lane;          // TMEM lane = tile row / (head, channel) row
         const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
         const int hrow = row >> 6, prow = row & 63;
-        constexpr int NQ = N / 4;                // state columns per thread in the shared phases
-        constexpr int NH = N / 2;                // state columns per thread in the S group
-        const int nq0 = quarter * NQ;
+        constexpr int NQ = N / 4;                // state columns per thread
+        const int nq0 = kq * NQ;
         uint32_t ph = 0;
         int stage = 0;
-        float* vt = sm.vtab();
         float* misc = sm.misc();
         bool ok = true;
         auto math_bar = [&]() {    // all 16 math warps
             warp_arrive(sm, kBarMath);
             if (!wait_bar_warp(sm, kBarMath, ph, a)) ok = false;
-        };
-        auto group_bar = [&]() {   // the 8 warps of the L group
-            warp_arrive(sm, kBarGrpL);
-            if (!wait_bar_warp(sm, kBarGrpL, ph, a)) ok = false;
         };
         // TMEM state columns [c0, c0 + cnt) of this thread's row, cnt a multiple of 16
         auto st_load = [&](int c0, int cnt, float* v) {
@@ -576,14 +603,17 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tmem_st16(lane_base + kColST + c0 + k, r);
             }
         };
-        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)) (0 past len)
-        auto weight_x = [&](int st, int len, float last0, float last1, int first, int stride) {
+        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)), 0 past len.
+        // Thread mt takes half a row; its four 16-byte chunks are visited in a row-rotated order so
+        // that a warp's accesses spread over all banks.
+        auto weight_x = [&](int st, int len, float last0, float last1) {
             const float* cs = sm.cs(st);
-            for (int qq = first; qq < 2 * kTile * 8; qq += stride) {
-                const int hh = qq >> 10;
-                const int l = (qq & 1023) >> 3;
-                const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
-                uint4* p = reinterpret_cast<uint4*>(sm.x(st, 0) + (size_t)qq * 16);
+            const int pr = mt >> 1, hh = pr >> 7, l = pr & 127, hf = mt & 1;
+            const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
+            uint8_t* rowp = sm.x(st, hh) + l * 128 + 64 * hf;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint4* p = reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & 3));
                 uint4 v = *p;
                 uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
@@ -592,6 +622,143 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     u[k] = pack_bf16x2(f.x * w, f.y * w);
                 }
                 *p = v;
+            }
+        };
+        // L o G (+ D on the diagonal) of stage st, in place over C B^T in TMEM. This thread: row i,
+        // columns j = 32 kq .. 32 kq + 31, written as packed bf16 (per 16 tokens: 8 columns of head 0,
+        // then 8 of head 1). Blocks above the diagonal are zero; strictly-lower 16-token groups use
+        // exp(cs_i - cs_p) exp(cs_p - cs_j) with p the group's last token (both factors <= 1, no
+        // subtraction of distant cumsums); the diagonal block takes exp(cs_i - cs_j) directly.
+        auto lg_tile = [&](int st, int len, float D0, float D1) {
+            const float* cs = sm.cs(st);
+            const int i = row;
+            const bool rv = i < len;
+            const uint32_t col = lane_base + kColG + 32 * kq;
+            if (kq > qd || !__any_sync(0xffffffffu, rv)) {
+                uint32_t z[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) z[e] = 0u;
+                tmem_st16(col, z);
+                tmem_st16(col + 16, z);
+                return;
+            }
+            float g[32];
+            tmem_ld16_nowait(col, g);
+            tmem_ld16_nowait(col + 16, g + 16);
+            const float ci0 = cs[i], ci1 = cs[128 + i];
+            if (kq < qd) {
+                const int jp = 32 * kq;
+                const float u00 = ex2(ci0 - cs[jp + 15]), u01 = ex2(ci0 - cs[jp + 31]);
+                const float u10 = ex2(ci1 - cs[128 + jp + 15]), u11 = ex2(ci1 - cs[128 + jp + 31]);
+                const uint4* v0 = reinterpret_cast<const uint4*>(sm.vt() + 16 * kq);
+                const uint4* v1 = reinterpret_cast<const uint4*>(sm.vt() + 64 + 16 * kq);
+                tmem_wait_ld();
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {
+                    const float ua = gg ? u01 : u00, ub = gg ? u11 : u10;
+                    uint32_t p0[8], p1[8];
+#pragma unroll
+                    for (int w4 = 0; w4 < 2; ++w4) {
+                        const uint4 a4 = v0[2 * gg + w4], b4 = v1[2 * gg + w4];
+                        const uint32_t av[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 va = __half22float2(*reinterpret_cast<const __half2*>(&av[m]));
+                            const float2 vb = __half22float2(*reinterpret_cast<const __half2*>(&bv[m]));
+                            const int e = 16 * gg + 8 * w4 + 2 * m;
+                            p0[4 * w4 + m] = pack_bf16x2(g[e] * (ua * va.x), g[e + 1] * (ua * va.y));
+                            p1[4 * w4 + m] = pack_bf16x2(g[e] * (ub * vb.x), g[e + 1] * (ub * vb.y));
+                        }
+                    }
+                    if (!rv) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
+                    }
+                    tmem_st8(col + 16 * gg, p0);
+                    tmem_st8(col + 16 * gg + 8, p1);
+                }
+            } else {
+                const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * kq);
+                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * kq);
+                tmem_wait_ld();
+#pragma unroll
+                for (int gg = 0; gg < 2; ++gg) {
+                    uint32_t p0[8], p1[8];
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 a4 = c0p[4 * gg + k4], b4 = c1p[4 * gg + k4];
+                        const float ca[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const float cb[4] = {b4.x, b4.y, b4.z, b4.w};
+                        float r0[4], r1[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int jl = 16 * gg + 4 * k4 + e;
+                            const int j = 32 * kq + jl;
+                            r0[e] = (j <= i) ? g[jl] * ex2(ci0 - ca[e]) : 0.f;
+                            r1[e] = (j <= i) ? g[jl] * ex2(ci1 - cb[e]) : 0.f;
+                            if (j == i) { r0[e] += D0; r1[e] += D1; }
+                        }
+                        p0[2 * k4] = pack_bf16x2(r0[0], r0[1]);
+                        p0[2 * k4 + 1] = pack_bf16x2(r0[2], r0[3]);
+                        p1[2 * k4] = pack_bf16x2(r1[0], r1[1]);
+                        p1[2 * k4 + 1] = pack_bf16x2(r1[2], r1[3]);
+                    }
+                    if (!rv) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
+                    }
+                    tmem_st8(col + 16 * gg, p0);
+                    tmem_st8(col + 16 * gg + 8, p1);
+                }
+            }
+        };
+        // state step of stage st: h_{t-1} (this thread's state columns) to bf16 in the staging area for
+        // Yo, and a_t h_{t-1} back into TMEM for S(t) to accumulate onto
+        auto state_step = [&](int st, int len) {
+            const float* cs = sm.cs(st);
+            const float at = ex2(cs[hrow * 128 + len - 1]);
+            float v[NQ];
+            st_load(nq0, NQ, v);
+#pragma unroll
+            for (int cc = 0; cc < NQ; cc += 8) {
+                const int n = nq0 + cc;
+                uint4 pk;
+                pk.x = pack_bf16x2(v[cc], v[cc + 1]);
+                pk.y = pack_bf16x2(v[cc + 2], v[cc + 3]);
+                pk.z = pack_bf16x2(v[cc + 4], v[cc + 5]);
+                pk.w = pack_bf16x2(v[cc + 6], v[cc + 7]);
+                *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
+            }
+#pragma unroll
+            for (int e = 0; e < NQ; ++e) v[e] *= at;
+            st_store(nq0, NQ, v);
+            tmem_wait_st();
+        };
+        // y = Yd + exp(cs_i) Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31
+        auto epilogue = [&](int st, int len, int row0, int h0) {
+            const float* cs = sm.cs(st);
+            const int hh = kq >> 1, c0 = 32 * (kq & 1);
+            const int i = row;
+            const float e = ex2(cs[hh * 128 + i]);
+            __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64 + c0;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float yd[16], yo[16];
+                tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0 + 16 * hf, yd);
+                tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0 + 16 * hf, yo);
+                tmem_wait_ld();
+                if (i < len) {
+#pragma unroll
+                    for (int k = 0; k < 16; k += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
+                        v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
+                        v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
+                        v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
+                        *reinterpret_cast<uint4*>(yrow + 16 * hf + k) = v;
+                    }
+                }
             }
         };
         float hreg[NQ];
@@ -604,15 +771,15 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const bool last_cont = c.t1 < c.nt;
             const int64_t q = c.q;
 
-            // ------------------------------------------------ pass 1 (all math warps)
+            // ------------------------------------------------ pass 1 (right factors of the window)
             if (last_cont) {
                 for (int t = c.t0; t < c.t1 && ok; ++t) {
-                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+                    ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a);
                     if (!ok) break;
                     const float* m = sm.stage_misc(stage);
                     const float tot0 = m[0], tot1 = m[1];
                     if (t == c.t0 && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
-                    weight_x(stage, tile_len(c, t), tot0, tot1, mt, kMathThreads);
+                    weight_x(stage, tile_len(c, t), tot0, tot1);
                     fence_proxy_async_smem();
                     warp_arrive(sm, kBarWX1a + stage);
                     stage ^= 1;
@@ -646,7 +813,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tc_fence_before_sync();
             }
 
-            // ------------------------------------------------ look-back (all math warps)
+            // ------------------------------------------------ look-back (center factors)
             if (first_cont) {
                 // lanes poll up to 32 predecessors at once; the state entering this window is
                 //   h_in = agg(q-1) + dec(q-1) (agg(q-2) + dec(q-2) (... + incl(q-m)))
@@ -716,236 +883,87 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                     __threadfence();
                 }
-                st_store(nq0, NQ, hreg);   // park h_in in the TMEM state columns
+                st_store(nq0, NQ, hreg);   // park h_in in this thread's TMEM state columns
                 tmem_wait_st();
                 tc_fence_before_sync();
                 math_bar();
                 if (last_cont && mt == 0) st_release(a.flags + q, 2);
-            } else if (last_cont) {
-                math_bar();   // every warp read the aggregate before the S group parks a state
+            } else {
+                // the window starts its chain: initial state (or zero) into this thread's state columns
+                // (the same columns it published from, so no barrier is needed in between)
+                const float* ip = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0 : nullptr;
+                float v[NQ];
+#pragma unroll
+                for (int k = 0; k < NQ; k += 4) {
+                    const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
+                }
+                st_store(nq0, NQ, v);
+                tmem_wait_st();
             }
             if (!ok) break;
 
-            if (grpL) {
-                // ------------------------------------------------ pass 2, L group: L o G (+ D on the diagonal)
-                // thread (row i, half lh) owns columns jb + 16 lh .. + 16 of each 32-column block jb;
-                // both halves read a block pair before either overwrites it in place.
-                const int lh = half;
-                const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
-                const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
-                for (int t = c.t0; t < c.t1 && ok; ++t) {
-                    const int len = tile_len(c, t);
-                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
+            // ------------------------------------------------ pass 2 (diagonal blocks, left factors, state)
+            const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
+            const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
+            ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
+            if (!ok) break;
+            tc_fence_after_sync();
+            lg_tile(stage, tile_len(c, c.t0), Dlg0, Dlg1);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            warp_arrive(sm, kBarLG);
+            for (int t = c.t0; t < c.t1 && ok; ++t) {
+                const int st = stage;
+                const int len = tile_len(c, t);
+                const int row0 = tile_row0(c, t);
+                const float* cs = sm.cs(st);
+                if (t != c.t0) {
+                    ok = wait_bar_warp(sm, kBarS, ph, a);
                     if (!ok) break;
-                    const float* cs = sm.cs(stage);
-                    group_bar();   // everyone is done with the previous tile's vt
-                    if (gt < 128) {
-                        const int hh = gt >> 6, j = gt & 63;
-                        vt[hh * 64 + j] = ex2(cs[hh * 128 + 63] - cs[hh * 128 + j]);   // exp(cs_63 - cs_j)
-                    }
-                    group_bar();
-                    ok = ok && wait_bar_warp(sm, kBarG, ph, a);
+                }
+                tc_fence_after_sync();
+                state_step(st, len);
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                warp_arrive(sm, kBarST);
+                ok = wait_bar_warp(sm, kBarYD, ph, a);
+                if (!ok) break;
+                weight_x(st, len, cs[len - 1], cs[128 + len - 1]);
+                fence_proxy_async_smem();
+                warp_arrive(sm, kBarWX);
+                ok = wait_bar_warp(sm, kBarYO, ph, a);
+                if (!ok) break;
+                tc_fence_after_sync();
+                epilogue(st, len, row0, h0);
+                tc_fence_before_sync();
+                warp_arrive(sm, kBarYFree);
+                if (t + 1 < c.t1) {
+                    ok = wait_bar_warp(sm, kBarFullX0 + (st ^ 1), ph, a) && wait_bar_warp(sm, kBarG, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const int i = row;
-                    const bool rv = i < len;
-                    const float csi0 = cs[i], csi1 = cs[128 + i];
-                    const float u0 = ex2(csi0 - cs[63]), u1 = ex2(csi1 - cs[128 + 63]);
-                    const int r_lo = 32 * qd, r_hi = 32 * qd + 31;    // rows of this warp
-#pragma unroll
-                    for (int bp = 0; bp < 4; bp += 2) {
-                        // this thread's 16 columns of blocks bp and bp+1 (each read and then
-                        // overwritten by this thread only)
-                        float g[2][16];
-                        bool load[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int jc = 32 * (bp + u) + 16 * lh;
-                            load[u] = jc <= r_hi;
-                            if (load[u]) tmem_ld16_nowait(lane_base + kColG + jc, g[u]);
-                        }
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int jb = 32 * (bp + u), jc = jb + 16 * lh;
-                            uint32_t p[2][8];   // [head][packed pairs]
-                            if (!load[u]) {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) { p[0][k] = 0u; p[1][k] = 0u; }
-                            } else if (jb < 64 && r_lo >= 64) {
-                                // lower-left block: exp(cs_i - cs_63) exp(cs_63 - cs_j), no exponentials
-                                const float4* v0 = reinterpret_cast<const float4*>(vt + jc);
-                                const float4* v1 = reinterpret_cast<const float4*>(vt + 64 + jc);
-#pragma unroll
-                                for (int k4 = 0; k4 < 4; ++k4) {
-                                    const float4 a4 = v0[k4], b4 = v1[k4];
-                                    p[0][2 * k4] = pack_bf16x2(g[u][4 * k4] * (u0 * a4.x), g[u][4 * k4 + 1] * (u0 * a4.y));
-                                    p[0][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * (u0 * a4.z), g[u][4 * k4 + 3] * (u0 * a4.w));
-                                    p[1][2 * k4] = pack_bf16x2(g[u][4 * k4] * (u1 * b4.x), g[u][4 * k4 + 1] * (u1 * b4.y));
-                                    p[1][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * (u1 * b4.z), g[u][4 * k4 + 3] * (u1 * b4.w));
-                                }
-                            } else if (jc + 15 < r_lo) {
-                                // diagonal 64-block, strictly below the diagonal for every row: exp(cs_i - cs_j)
-                                const float4* c0p = reinterpret_cast<const float4*>(cs + jc);
-                                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + jc);
-#pragma unroll
-                                for (int k4 = 0; k4 < 4; ++k4) {
-                                    const float4 a4 = c0p[k4], b4 = c1p[k4];
-                                    p[0][2 * k4] = pack_bf16x2(g[u][4 * k4] * ex2(csi0 - a4.x), g[u][4 * k4 + 1] * ex2(csi0 - a4.y));
-                                    p[0][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * ex2(csi0 - a4.z), g[u][4 * k4 + 3] * ex2(csi0 - a4.w));
-                                    p[1][2 * k4] = pack_bf16x2(g[u][4 * k4] * ex2(csi1 - b4.x), g[u][4 * k4 + 1] * ex2(csi1 - b4.y));
-                                    p[1][2 * k4 + 1] = pack_bf16x2(g[u][4 * k4 + 2] * ex2(csi1 - b4.z), g[u][4 * k4 + 3] * ex2(csi1 - b4.w));
-                                }
-                            } else {
-                                // the diagonal itself: mask j > i, D on j == i
-                                const float4* c0p = reinterpret_cast<const float4*>(cs + jc);
-                                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + jc);
-#pragma unroll
-                                for (int k4 = 0; k4 < 4; ++k4) {
-                                    const float4 a4 = c0p[k4], b4 = c1p[k4];
-                                    const float ca[4] = {a4.x, a4.y, a4.z, a4.w};
-                                    const float cb[4] = {b4.x, b4.y, b4.z, b4.w};
-                                    float r0[4], r1[4];
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const int j = jc + 4 * k4 + e;
-                                        r0[e] = (j <= i) ? g[u][4 * k4 + e] * ex2(csi0 - ca[e]) : 0.f;
-                                        r1[e] = (j <= i) ? g[u][4 * k4 + e] * ex2(csi1 - cb[e]) : 0.f;
-                                        if (j == i) { r0[e] += Dlg0; r1[e] += Dlg1; }
-                                    }
-                                    p[0][2 * k4] = pack_bf16x2(r0[0], r0[1]);
-                                    p[0][2 * k4 + 1] = pack_bf16x2(r0[2], r0[3]);
-                                    p[1][2 * k4] = pack_bf16x2(r1[0], r1[1]);
-                                    p[1][2 * k4 + 1] = pack_bf16x2(r1[2], r1[3]);
-                                }
-                            }
-                            if (!rv) {
-#pragma unroll
-                                for (int k = 0; k < 8; ++k) { p[0][k] = 0u; p[1][k] = 0u; }
-                            }
-                            tmem_st8(lane_base + kColG + jc, p[0]);       // head 0, tokens jc .. jc+15
-                            tmem_st8(lane_base + kColG + jc + 8, p[1]);   // head 1, same tokens
-                        }
-                    }
+                    lg_tile(st ^ 1, tile_len(c, t + 1), Dlg0, Dlg1);
                     tmem_wait_st();
                     tc_fence_before_sync();
                     warp_arrive(sm, kBarLG);
-                    stage ^= 1;
                 }
-            } else {
-                // ------------------------------------------------ pass 2, S group: state, weights, epilogue
-                const int sh = half;             // state columns [sh N/2, +N/2); epilogue head sh
-                const int n0 = sh * NH;
-                if (!first_cont) {
-                    // the window starts its chain: initial state (or zero) into the TMEM state columns
-                    const float* ip = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0 : nullptr;
-#pragma unroll
-                    for (int cc = 0; cc < NH; cc += 32) {
-                        float v[32];
-#pragma unroll
-                        for (int k = 0; k < 32; k += 4) {
-                            const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + cc + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
-                        }
-                        st_store(n0 + cc, 32, v);
-                    }
-                    tmem_wait_st();
-                }
-                for (int t = c.t0; t < c.t1 && ok; ++t) {
-                    const int len = tile_len(c, t);
-                    const int row0 = tile_row0(c, t);
-                    ok = wait_bar_warp(sm, kBarFull0 + stage, ph, a);
-                    if (!ok) break;
-                    const float* cs = sm.cs(stage);
-                    const float at = ex2(cs[hrow * 128 + len - 1]);     // decay of this row's head over the tile
-                    const float e = ex2(cs[sh * 128 + row]);              // exp(cs_i), head sh
-                    const float last0 = cs[len - 1], last1 = cs[128 + len - 1];
-                    // ---- state step: stage h_{t-1} (bf16) for Yo and leave a_t h_{t-1} in TMEM for S
-                    if (t != c.t0) {
-                        ok = wait_bar_warp(sm, kBarS, ph, a);
-                        if (!ok) break;
-                    }
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int cc = 0; cc < NH; cc += 32) {
-                        float v[32];
-                        st_load(n0 + cc, 32, v);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 8) {
-                            const int n = n0 + cc + k;
-                            uint4 pk;
-                            pk.x = pack_bf16x2(v[k], v[k + 1]);
-                            pk.y = pack_bf16x2(v[k + 2], v[k + 3]);
-                            pk.z = pack_bf16x2(v[k + 4], v[k + 5]);
-                            pk.w = pack_bf16x2(v[k + 6], v[k + 7]);
-                            *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
-                        }
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] *= at;
-                        st_store(n0 + cc, 32, v);
-                    }
-                    tmem_wait_st();
-                    fence_proxy_async_smem();
-                    tc_fence_before_sync();
-                    warp_arrive(sm, kBarST);
-                    // ---- weights for S: x scaled in place once Yd has read it
-                    ok = wait_bar_warp(sm, kBarYD, ph, a);
-                    if (!ok) break;
-                    weight_x(stage, len, last0, last1, gt, 256);
-                    fence_proxy_async_smem();
-                    warp_arrive(sm, kBarWX);
-                    // ---- epilogue: y = Yd + exp(cs_i) Yo, row i, head sh
-                    ok = wait_bar_warp(sm, kBarYO, ph, a);
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    {
-                        const int i = row;
-                        __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + sh) * 64;
-#pragma unroll
-                        for (int c0 = 0; c0 < 64; c0 += 16) {
-                            float yd[16], yo[16];
-                            tmem_ld16_nowait(lane_base + kColYD + 64 * sh + c0, yd);
-                            tmem_ld16_nowait(lane_base + kColYO + 64 * sh + c0, yo);
-                            tmem_wait_ld();
-                            if (i < len) {
-#pragma unroll
-                                for (int k = 0; k < 16; k += 8) {
-                                    uint4 v;
-                                    v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
-                                    v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
-                                    v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
-                                    v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
-                                    *reinterpret_cast<uint4*>(yrow + c0 + k) = v;
-                                }
-                            }
-                        }
-                    }
-                    tc_fence_before_sync();
-                    warp_arrive(sm, kBarYFree);
-                    stage ^= 1;
-                }
-                if (ok) {
-                    // end of the window: the last S, then the final state at a chain end
-                    ok = wait_bar_warp(sm, kBarS, ph, a);
-                    if (ok) {
-                        tc_fence_after_sync();
-                        if (c.t1 == c.nt && a.final_state) {
-                            float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + n0;
-#pragma unroll
-                            for (int cc = 0; cc < NH; cc += 32) {
-                                float v[32];
-                                st_load(n0 + cc, 32, v);
-#pragma unroll
-                                for (int k = 0; k < 32; k += 4)
-                                    *reinterpret_cast<float4*>(fp + cc + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                            }
-                        }
-                        tc_fence_before_sync();
-                    }
-                }
+                stage ^= 1;
             }
             if (!ok) break;
-            // both groups finish the piece before the next one's shared phases
+            // end of the window: the last S, then the final state at a chain end
+            ok = wait_bar_warp(sm, kBarS, ph, a);
+            if (!ok) break;
+            tc_fence_after_sync();
+            if (c.t1 == c.nt && a.final_state) {
+                float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0;
+                float v[NQ];
+                st_load(nq0, NQ, v);
+#pragma unroll
+                for (int k = 0; k < NQ; k += 4)
+                    *reinterpret_cast<float4*>(fp + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+            }
+            tc_fence_before_sync();
+            // every warp is done with the piece before the next one's shared phases
             math_bar();
         }
         if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
