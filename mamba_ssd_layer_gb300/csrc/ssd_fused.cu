@@ -30,7 +30,6 @@
 // warps 2..9 = math (masks, state updates, weights, epilogue, look-back).
 // Every wait is bounded; a timeout records SSD_ERR_TIMEOUT and the CTA winds down.
 #include <cuda.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "ptx.cuh"
@@ -170,20 +169,24 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 // Barrier slots in shared memory
 enum {
     kBarFullX0 = 0, kBarFullX1, kBarFullBC0, kBarFullBC1, kBarEmpty0, kBarEmpty1,
-    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree, kBarAgg, kBarMath,
+    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree0, kBarYFree1, kBarAgg,
+    kBarMath,
     kNumBars
 };
 
 // Pass-1 weights use one barrier per stage (kBarWX1a + stage): the math warps may weight the
 // next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
-// barrier before the first was waited for would make the waiter miss a phase.
+// barrier before the first was waited for would make the waiter miss a phase. The epilogue's
+// release (kBarYFree0 + stage: Y regions read, y staged) is per stage for the same reason: the
+// producer waits it only when it next refills that stage.
 // Expected arrivals per phase: the x barrier = producer's expect_tx + its "cumsum written"
 // arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16);
 // MMA commits 1.
 __device__ __forceinline__ uint32_t bar_count(int i) {
     switch (i) {
         case kBarFullX0: case kBarFullX1: return 2;
-        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarWX1a: case kBarWX1b: case kBarMath:
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree0: case kBarYFree1: case kBarWX1a: case kBarWX1b:
+        case kBarMath:
             return 16;
         default: return 1;
     }
@@ -197,13 +200,19 @@ struct Smem {
     __device__ uint8_t* b(int s) const { return base + s * stage_bytes() + 2 * kRegion; }
     __device__ uint8_t* c(int s) const { return base + s * stage_bytes() + 2 * kRegion + (N / 64) * kRegion; }
     __device__ uint8_t* hs() const { return base + 2 * stage_bytes(); }
+    // y staging for the epilogue (x layout, one 16 KB region per head): the stage's C regions for
+    // N = 128 (free once Yo has read them), separate regions for N = 64
+    __device__ uint8_t* ystage(int s, int h) const {
+        return N >= 128 ? c(s) + h * kRegion : hs() + (N / 64) * kRegion + (2 * s + h) * kRegion;
+    }
+    __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 4 * kRegion); }
     // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
-    __device__ float* cs(int s) const { return reinterpret_cast<float*>(hs() + (N / 64) * kRegion) + s * 260; }
+    __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * 260; }
     __device__ float* stage_misc(int s) const { return cs(s) + 256; }
-    // exp(cs_p - cs_j) per head and token j (p = last token of j's 16-token group), fp16 pairs [2][64]
-    __device__ __half2* vt() const { return reinterpret_cast<__half2*>(cs(0) + 520); }
-    __device__ float* misc() const { return cs(0) + 520 + 128; }                                     // [8]
+    // exp(cs_p - cs_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
+    __device__ float* vt() const { return cs(0) + 520; }
+    __device__ float* misc() const { return cs(0) + 520 + 192; }                                     // [8]
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(misc() + 8); }           // [kNumBars]
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
@@ -353,22 +362,42 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         // TMA (lane 0): pass 1 loads x and B on the stage's x barrier; pass 2 loads B and C on the
         // B/C barrier (they feed C B^T first) and x on the x barrier. All lanes: dt for both heads
         // -> the tile-local cumsum of dt*A (x log2 e), with the window carry in pass 1. In pass 2
-        // also the table v_j = exp(cs_p - cs_j), p the last token of j's 16-token group, once the
-        // previous tile's L o G (its only reader) is done.
+        // also the table v_j = exp(cs_p - cs_j), p the last token of j's 32-token block (j < 96), once
+        // the previous tile's L o G (its only reader) is done.
         uint32_t ph = 0;
         uint32_t issued = 0;
         uint32_t p2 = 0;   // pass-2 tiles loaded so far
+        uint32_t ypend = 0;                       // stages whose pass-2 epilogue may still use the C region
         int stage = 0;
         bool ok = true;
+        // the epilogue of the pass-2 tile in stage st stages its y in the stage's C region: wait for
+        // its release before the stage is refilled
+        auto flush_y = [&](int st) -> bool {
+            if (!((ypend >> st) & 1u)) return true;
+            ypend &= ~(1u << st);
+            const bool w = wait_bar(sm, kBarYFree0 + st, ph, a);
+            return __all_sync(0xffffffffu, w);
+        };
         auto load_tile = [&](const Piece& c, int t, bool pass1, float tot0, float tot1, float& carry0,
                              float& carry1) -> bool {
+            const int row0 = tile_row0(c, t), len = tile_len(c, t);
+            const int h0 = 2 * c.hp;
+            // dt first: the loads are in flight while the stage drains
+            float v[2][4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int l = 4 * lane + k;
+                    v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
+                }
             if ((issued >> stage) & 1u) {
                 const bool w = wait_bar(sm, kBarEmpty0 + stage, ph, a);
                 if (!__all_sync(0xffffffffu, w)) return false;
             }
             issued |= 1u << stage;
-            const int row0 = tile_row0(c, t), len = tile_len(c, t);
-            const int h0 = 2 * c.hp;
+            if (!flush_y(stage)) return false;
+            if (!pass1) ypend |= 1u << stage;
             uint64_t* fullx = sm.bars() + kBarFullX0 + stage;
             if (lane == 0) {
                 const int g = h0 / (a.H / a.G);
@@ -388,14 +417,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tma_load_3d(sm.x(stage, 0), &maps.x, fullx, 0, h0, row0);
                 tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
             }
-            float v[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int l = 4 * lane + k;
-                    v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
-                }
             float* cs = sm.cs(stage);
             float cv[2][4];
 #pragma unroll
@@ -429,16 +450,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (!__all_sync(0xffffffffu, w)) return false;
                 }
                 ++p2;
-                __half2* vt = sm.vt();
+                float* vt = sm.vt();
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const float piv = __shfl_sync(0xffffffffu, cv[hh][3], lane | 3);
-                    const __half2 lo = __floats2half2_rn(ex2(piv - cv[hh][0]), ex2(piv - cv[hh][1]));
-                    const __half2 hi = __floats2half2_rn(ex2(piv - cv[hh][2]), ex2(piv - cv[hh][3]));
-                    uint2 pk;
-                    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-                    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                    *reinterpret_cast<uint2*>(vt + hh * 64 + 2 * lane) = pk;
+                    const float piv = __shfl_sync(0xffffffffu, cv[hh][3], lane | 7);
+                    if (lane < 24)
+                        *reinterpret_cast<float4*>(vt + hh * 96 + 4 * lane) =
+                            make_float4(ex2(piv - cv[hh][0]), ex2(piv - cv[hh][1]), ex2(piv - cv[hh][2]),
+                                        ex2(piv - cv[hh][3]));
                 }
             }
             __syncwarp();
@@ -473,12 +492,15 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             float c0 = 0.f, c1 = 0.f;
             for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
         }
+        // the last tiles' releases, oldest first (keeps the barrier phases consistent)
+        if (ok) ok = flush_y(stage);
+        if (ok) ok = flush_y(stage ^ 1);
     } else if (warp == 1) {
         // ============================================================ MMA issuer (lane 0)
         if (lane == 0) {
             uint32_t ph = 0;
             int stage = 0;
-            bool have_prev_tile = false;   // a pass-2 tile's Y regions are still being read
+            int prev_st = -1;              // stage of the previous pass-2 tile (its Y regions may still be read)
             const uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yo = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
@@ -529,7 +551,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         issue_g(st);
                     }
                     ok = wait_bar(sm, kBarLG, ph, a) && wait_bar(sm, kBarFullX0 + st, ph, a);
-                    if (ok && have_prev_tile) ok = wait_bar(sm, kBarYFree, ph, a);
+                    if (ok && prev_st >= 0) ok = wait_bar(sm, kBarYFree0 + prev_st, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
                     for (int ks = 0; ks < 8; ++ks) {
@@ -563,7 +585,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     mma_commit(sm.bars() + kBarS);
                     mma_commit(sm.bars() + kBarEmpty0 + st);
                     stage ^= 1;
-                    have_prev_tile = true;
+                    prev_st = st;
                 }
             }
         }
@@ -603,31 +625,31 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tmem_st16(lane_base + kColST + c0 + k, r);
             }
         };
-        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)), 0 past len.
-        // Thread mt takes half a row; its four 16-byte chunks are visited in a row-rotated order so
-        // that a warp's accesses spread over all banks.
+        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)), 0 past len
+        // (bf16 products of the bf16 inputs and the weight rounded to bf16). Thread mt takes half a
+        // row; its four 16-byte chunks are visited in a row-rotated order so that a warp's accesses
+        // spread over all banks.
         auto weight_x = [&](int st, int len, float last0, float last1) {
             const float* cs = sm.cs(st);
             const int pr = mt >> 1, hh = pr >> 7, l = pr & 127, hf = mt & 1;
             const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
+            const __nv_bfloat162 ww = __float2bfloat162_rn(w);
             uint8_t* rowp = sm.x(st, hh) + l * 128 + 64 * hf;
+            uint4 v[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) v[cc] = *reinterpret_cast<const uint4*>(rowp + 16 * ((cc + l) & 3));
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                uint4* p = reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & 3));
-                uint4 v = *p;
-                uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+                __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v[cc]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float2 f = unpack_bf16x2(u[k]);
-                    u[k] = pack_bf16x2(f.x * w, f.y * w);
-                }
-                *p = v;
+                for (int k = 0; k < 4; ++k) b[k] = __hmul2(b[k], ww);
+                *reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & 3)) = v[cc];
             }
         };
         // L o G (+ D on the diagonal) of stage st, in place over C B^T in TMEM. This thread: row i,
         // columns j = 32 kq .. 32 kq + 31, written as packed bf16 (per 16 tokens: 8 columns of head 0,
-        // then 8 of head 1). Blocks above the diagonal are zero; strictly-lower 16-token groups use
-        // exp(cs_i - cs_p) exp(cs_p - cs_j) with p the group's last token (both factors <= 1, no
+        // then 8 of head 1). Blocks above the diagonal are zero; a block strictly below takes
+        // exp(cs_i - cs_p) exp(cs_p - cs_j) with p the block's last token (both factors <= 1, no
         // subtraction of distant cumsums); the diagonal block takes exp(cs_i - cs_j) directly.
         auto lg_tile = [&](int st, int len, float D0, float D1) {
             const float* cs = sm.cs(st);
@@ -647,29 +669,27 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_ld16_nowait(col + 16, g + 16);
             const float ci0 = cs[i], ci1 = cs[128 + i];
             if (kq < qd) {
-                const int jp = 32 * kq;
-                const float u00 = ex2(ci0 - cs[jp + 15]), u01 = ex2(ci0 - cs[jp + 31]);
-                const float u10 = ex2(ci1 - cs[128 + jp + 15]), u11 = ex2(ci1 - cs[128 + jp + 31]);
-                const uint4* v0 = reinterpret_cast<const uint4*>(sm.vt() + 16 * kq);
-                const uint4* v1 = reinterpret_cast<const uint4*>(sm.vt() + 64 + 16 * kq);
+                const float u0 = ex2(ci0 - cs[32 * kq + 31]), u1 = ex2(ci1 - cs[128 + 32 * kq + 31]);
+                const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+                const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 32 * kq);
+                const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 32 * kq);
                 tmem_wait_ld();
 #pragma unroll
                 for (int gg = 0; gg < 2; ++gg) {
-                    const float ua = gg ? u01 : u00, ub = gg ? u11 : u10;
                     uint32_t p0[8], p1[8];
 #pragma unroll
-                    for (int w4 = 0; w4 < 2; ++w4) {
-                        const uint4 a4 = v0[2 * gg + w4], b4 = v1[2 * gg + w4];
-                        const uint32_t av[4] = {a4.x, a4.y, a4.z, a4.w};
-                        const uint32_t bv[4] = {b4.x, b4.y, b4.z, b4.w};
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float2 va = __half22float2(*reinterpret_cast<const __half2*>(&av[m]));
-                            const float2 vb = __half22float2(*reinterpret_cast<const __half2*>(&bv[m]));
-                            const int e = 16 * gg + 8 * w4 + 2 * m;
-                            p0[4 * w4 + m] = pack_bf16x2(g[e] * (ua * va.x), g[e + 1] * (ua * va.y));
-                            p1[4 * w4 + m] = pack_bf16x2(g[e] * (ub * vb.x), g[e + 1] * (ub * vb.y));
-                        }
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const float4 a4 = v0[4 * gg + k4], b4 = v1[4 * gg + k4];
+                        const int e = 16 * gg + 4 * k4;
+                        const float2 g0 = make_float2(g[e], g[e + 1]), g1 = make_float2(g[e + 2], g[e + 3]);
+                        const float2 ra = __fmul2_rn(g0, __fmul2_rn(uu0, make_float2(a4.x, a4.y)));
+                        const float2 rb = __fmul2_rn(g1, __fmul2_rn(uu0, make_float2(a4.z, a4.w)));
+                        const float2 rc = __fmul2_rn(g0, __fmul2_rn(uu1, make_float2(b4.x, b4.y)));
+                        const float2 rd = __fmul2_rn(g1, __fmul2_rn(uu1, make_float2(b4.z, b4.w)));
+                        p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
+                        p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
+                        p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
+                        p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
                     }
                     if (!rv) {
 #pragma unroll
@@ -681,6 +701,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             } else {
                 const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * kq);
                 const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * kq);
+                const float2 cc0 = make_float2(ci0, ci0), cc1 = make_float2(ci1, ci1), m1 = make_float2(-1.f, -1.f);
                 tmem_wait_ld();
 #pragma unroll
                 for (int gg = 0; gg < 2; ++gg) {
@@ -688,21 +709,27 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const float4 a4 = c0p[4 * gg + k4], b4 = c1p[4 * gg + k4];
-                        const float ca[4] = {a4.x, a4.y, a4.z, a4.w};
-                        const float cb[4] = {b4.x, b4.y, b4.z, b4.w};
-                        float r0[4], r1[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int jl = 16 * gg + 4 * k4 + e;
-                            const int j = 32 * kq + jl;
-                            r0[e] = (j <= i) ? g[jl] * ex2(ci0 - ca[e]) : 0.f;
-                            r1[e] = (j <= i) ? g[jl] * ex2(ci1 - cb[e]) : 0.f;
-                            if (j == i) { r0[e] += D0; r1[e] += D1; }
-                        }
-                        p0[2 * k4] = pack_bf16x2(r0[0], r0[1]);
-                        p0[2 * k4 + 1] = pack_bf16x2(r0[2], r0[3]);
-                        p1[2 * k4] = pack_bf16x2(r1[0], r1[1]);
-                        p1[2 * k4 + 1] = pack_bf16x2(r1[2], r1[3]);
+                        const int jl = 16 * gg + 4 * k4;     // column within the block; row within it = lane
+                        const float2 da = __ffma2_rn(make_float2(a4.x, a4.y), m1, cc0);
+                        const float2 db = __ffma2_rn(make_float2(a4.z, a4.w), m1, cc0);
+                        const float2 dc = __ffma2_rn(make_float2(b4.x, b4.y), m1, cc1);
+                        const float2 dd = __ffma2_rn(make_float2(b4.z, b4.w), m1, cc1);
+                        float2 ra = __fmul2_rn(make_float2(g[jl], g[jl + 1]), make_float2(ex2(da.x), ex2(da.y)));
+                        float2 rb = __fmul2_rn(make_float2(g[jl + 2], g[jl + 3]), make_float2(ex2(db.x), ex2(db.y)));
+                        float2 rc = __fmul2_rn(make_float2(g[jl], g[jl + 1]), make_float2(ex2(dc.x), ex2(dc.y)));
+                        float2 rd = __fmul2_rn(make_float2(g[jl + 2], g[jl + 3]), make_float2(ex2(dd.x), ex2(dd.y)));
+                        if (jl > lane) { ra.x = 0.f; rc.x = 0.f; }
+                        if (jl + 1 > lane) { ra.y = 0.f; rc.y = 0.f; }
+                        if (jl + 2 > lane) { rb.x = 0.f; rd.x = 0.f; }
+                        if (jl + 3 > lane) { rb.y = 0.f; rd.y = 0.f; }
+                        if (jl == lane) { ra.x += D0; rc.x += D1; }
+                        if (jl + 1 == lane) { ra.y += D0; rc.y += D1; }
+                        if (jl + 2 == lane) { rb.x += D0; rd.x += D1; }
+                        if (jl + 3 == lane) { rb.y += D0; rd.y += D1; }
+                        p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
+                        p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
+                        p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
+                        p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
                     }
                     if (!rv) {
 #pragma unroll
@@ -730,34 +757,52 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 pk.w = pack_bf16x2(v[cc + 6], v[cc + 7]);
                 *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
             }
+            const float2 aa = make_float2(at, at);
 #pragma unroll
-            for (int e = 0; e < NQ; ++e) v[e] *= at;
+            for (int e = 0; e < NQ; e += 2) {
+                const float2 s2 = __fmul2_rn(make_float2(v[e], v[e + 1]), aa);
+                v[e] = s2.x;
+                v[e + 1] = s2.y;
+            }
             st_store(nq0, NQ, v);
             tmem_wait_st();
         };
-        // y = Yd + exp(cs_i) Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31
+        // y = Yd + exp(cs_i) Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31. The warp stages its
+        // 32 rows x 64 bytes in the stage's C region (free once Yo has read it) and writes them back
+        // four lanes per row, so that each store instruction covers eight whole 64-byte row pieces.
         auto epilogue = [&](int st, int len, int row0, int h0) {
             const float* cs = sm.cs(st);
             const int hh = kq >> 1, c0 = 32 * (kq & 1);
             const int i = row;
             const float e = ex2(cs[hh * 128 + i]);
-            __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64 + c0;
+            const float2 ee = make_float2(e, e);
+            uint8_t* stg = sm.ystage(st, hh);
+            float yd[32], yo[32];
+            tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0, yd);
+            tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0, yo);
+            tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0 + 16, yd + 16);
+            tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0 + 16, yo + 16);
+            tmem_wait_ld();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float yd[16], yo[16];
-                tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0 + 16 * hf, yd);
-                tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0 + 16 * hf, yo);
-                tmem_wait_ld();
-                if (i < len) {
+            for (int k = 0; k < 32; k += 8) {
+                uint4 v;
+                uint32_t* vu = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-                    for (int k = 0; k < 16; k += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(fmaf(e, yo[k], yd[k]), fmaf(e, yo[k + 1], yd[k + 1]));
-                        v.y = pack_bf16x2(fmaf(e, yo[k + 2], yd[k + 2]), fmaf(e, yo[k + 3], yd[k + 3]));
-                        v.z = pack_bf16x2(fmaf(e, yo[k + 4], yd[k + 4]), fmaf(e, yo[k + 5], yd[k + 5]));
-                        v.w = pack_bf16x2(fmaf(e, yo[k + 6], yd[k + 6]), fmaf(e, yo[k + 7], yd[k + 7]));
-                        *reinterpret_cast<uint4*>(yrow + 16 * hf + k) = v;
-                    }
+                for (int m = 0; m < 4; ++m) {
+                    const float2 r = __ffma2_rn(ee, make_float2(yo[k + 2 * m], yo[k + 2 * m + 1]),
+                                                make_float2(yd[k + 2 * m], yd[k + 2 * m + 1]));
+                    vu[m] = pack_bf16x2(r.x, r.y);
+                }
+                *reinterpret_cast<uint4*>(stg + sw128_offset(i, (c0 + k) / 8)) = v;
+            }
+            __syncwarp();
+            const int cl = (c0 >> 3) + (lane & 3);          // 16-byte chunk of the row this lane writes
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int r = 32 * qd + 8 * pass + (lane >> 2);
+                if (r < len) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
+                    *reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl) = v;
                 }
             }
         };
@@ -807,11 +852,23 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     __stcg(reinterpret_cast<float4*>(dst + k), o);
                 }
                 if (first_cont && mt < 2) a.decay[q * 2 + mt] = ex2(misc[kMiscTot0 + mt]);
-                __threadfence();
+                // every thread's stores precede the barrier; one gpu-scope release then publishes them all
                 math_bar();
                 if (mt == 0) st_release(a.flags + q, first_cont ? 1 : 2);
                 tc_fence_before_sync();
             }
+
+            // ------------------------------------------------ L o G of the window's first tile (it does not
+            // need the entering state, so its MMA can run while the look-back waits)
+            const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
+            const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
+            ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
+            if (!ok) break;
+            tc_fence_after_sync();
+            lg_tile(stage, tile_len(c, c.t0), Dlg0, Dlg1);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            warp_arrive(sm, kBarLG);
 
             // ------------------------------------------------ look-back (center factors)
             if (first_cont) {
@@ -881,7 +938,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                                                      fmaf(dec, hreg[k + 2], v[k + 2]), fmaf(dec, hreg[k + 3], v[k + 3]));
                         __stcg(reinterpret_cast<float4*>(dst + k), o);
                     }
-                    __threadfence();
                 }
                 st_store(nq0, NQ, hreg);   // park h_in in this thread's TMEM state columns
                 tmem_wait_st();
@@ -904,15 +960,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (!ok) break;
 
             // ------------------------------------------------ pass 2 (diagonal blocks, left factors, state)
-            const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
-            const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
-            ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
-            if (!ok) break;
-            tc_fence_after_sync();
-            lg_tile(stage, tile_len(c, c.t0), Dlg0, Dlg1);
-            tmem_wait_st();
-            tc_fence_before_sync();
-            warp_arrive(sm, kBarLG);
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int st = stage;
                 const int len = tile_len(c, t);
@@ -936,8 +983,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (!ok) break;
                 tc_fence_after_sync();
                 epilogue(st, len, row0, h0);
+                fence_proxy_async_smem();
                 tc_fence_before_sync();
-                warp_arrive(sm, kBarYFree);
+                warp_arrive(sm, kBarYFree0 + st);
                 if (t + 1 < c.t1) {
                     ok = wait_bar_warp(sm, kBarFullX0 + (st ^ 1), ph, a) && wait_bar_warp(sm, kBarG, ph, a);
                     if (!ok) break;
@@ -1003,7 +1051,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 template <int N>
 size_t fused_smem_bytes() {
     const size_t stage = 2 * kRegion + 2 * (N / 64) * kRegion;
-    return 2 * stage + (N / 64) * kRegion + (520 + 128 + 8) * 4 + kNumBars * 8 + 16;
+    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 4 * kRegion) + (520 + 192 + 8) * 4 + kNumBars * 8 + 16;
 }
 
 template <int N>
