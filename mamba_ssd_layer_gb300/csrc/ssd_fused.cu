@@ -32,6 +32,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "ssd_internal.cuh"
 
@@ -47,11 +49,12 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column map (512 allocated)
 constexpr uint32_t kColST = 0;     // state / aggregate: rows (head, channel), N columns
-constexpr uint32_t kColG = 128;    // C B^T (fp32), then L o C B^T (bf16 pairs) in place: the 16 fp32
-                                   // columns 16c..16c+15 become 8 packed columns of head 0 followed by
-                                   // 8 of head 1, both covering tokens j = 16c..16c+15
-constexpr uint32_t kColYD = 256;   // Yd, head 0 then head 1 (64 columns each)
-constexpr uint32_t kColYO = 384;   // Yo, rows = tokens, columns = (head, channel)
+constexpr uint32_t kColYD = 128;   // Yd, head 0 then head 1 (64 columns each)
+constexpr uint32_t kColGB = 256;   // two 128-column buffers, alternating per tile: C B^T (fp32), then
+                                   // L o C B^T (bf16 pairs) in place -- the 16 fp32 columns 16c..16c+15
+                                   // become 8 packed columns of head 0 followed by 8 of head 1, both for
+                                   // tokens j = 16c..16c+15 -- then that tile's Yo (rows = tokens, columns =
+                                   // (head, channel))
 
 struct FusedMaps {
     CUtensorMap x, b, c;
@@ -169,24 +172,20 @@ __device__ __forceinline__ void st_release(int* p, int v) {
 // Barrier slots in shared memory
 enum {
     kBarFullX0 = 0, kBarFullX1, kBarFullBC0, kBarFullBC1, kBarEmpty0, kBarEmpty1,
-    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree0, kBarYFree1, kBarAgg,
-    kBarMath,
+    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree, kBarAgg, kBarMath,
     kNumBars
 };
 
 // Pass-1 weights use one barrier per stage (kBarWX1a + stage): the math warps may weight the
 // next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
-// barrier before the first was waited for would make the waiter miss a phase. The epilogue's
-// release (kBarYFree0 + stage: Y regions read, y staged) is per stage for the same reason: the
-// producer waits it only when it next refills that stage.
+// barrier before the first was waited for would make the waiter miss a phase.
 // Expected arrivals per phase: the x barrier = producer's expect_tx + its "cumsum written"
-// arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16);
-// MMA commits 1.
+// arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16); MMA
+// commits 1.
 __device__ __forceinline__ uint32_t bar_count(int i) {
     switch (i) {
         case kBarFullX0: case kBarFullX1: return 2;
-        case kBarLG: case kBarST: case kBarWX: case kBarYFree0: case kBarYFree1: case kBarWX1a: case kBarWX1b:
-        case kBarMath:
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarWX1a: case kBarWX1b: case kBarMath:
             return 16;
         default: return 1;
     }
@@ -200,12 +199,13 @@ struct Smem {
     __device__ uint8_t* b(int s) const { return base + s * stage_bytes() + 2 * kRegion; }
     __device__ uint8_t* c(int s) const { return base + s * stage_bytes() + 2 * kRegion + (N / 64) * kRegion; }
     __device__ uint8_t* hs() const { return base + 2 * stage_bytes(); }
-    // y staging for the epilogue (x layout, one 16 KB region per head): the stage's C regions for
-    // N = 128 (free once Yo has read them), separate regions for N = 64
-    __device__ uint8_t* ystage(int s, int h) const {
-        return N >= 128 ? c(s) + h * kRegion : hs() + (N / 64) * kRegion + (2 * s + h) * kRegion;
+    // y staging for the epilogue (x layout, one 16 KB region per head): the state staging area for
+    // N = 128 (free between Yo and the next state step, both of which each warp orders for its own
+    // bytes), separate regions for N = 64
+    __device__ uint8_t* ystage(int h) const {
+        return N >= 128 ? hs() + h * kRegion : hs() + (N / 64) * kRegion + h * kRegion;
     }
-    __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 4 * kRegion); }
+    __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion); }
     // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * 260; }
@@ -230,7 +230,7 @@ __device__ __forceinline__ bool wait_bar(const Smem& sm, int idx, uint32_t& phas
     if (mbar_try_wait(bar, par)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_sleep(bar, par, 20000u)) return true;   // sleeps until the phase completes
+        if (mbar_try_wait(bar, par)) return true;   // may block for a short, hardware-chosen time
         if ((it & 63u) != 0) continue;
         if (*reinterpret_cast<volatile int*>(sm.abort_flag())) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -247,6 +247,14 @@ __device__ __forceinline__ bool wait_bar(const Smem& sm, int idx, uint32_t& phas
 __device__ __forceinline__ bool wait_bar_warp(const Smem& sm, int idx, uint32_t& phases, const FusedArgs& a) {
     const bool ok = wait_bar(sm, idx, phases, a);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Non-blocking: true (and the phase consumed) if the phase is already complete.
+__device__ __forceinline__ bool test_bar(const Smem& sm, int idx, uint32_t& phases) {
+    const uint32_t par = (phases >> idx) & 1u;
+    if (!mbar_try_wait(sm.bars() + idx, par)) return false;
+    phases ^= 1u << idx;
+    return true;
 }
 
 // Arrive once per math warp (lane 0 after the warp's work is done).
@@ -367,17 +375,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         uint32_t ph = 0;
         uint32_t issued = 0;
         uint32_t p2 = 0;   // pass-2 tiles loaded so far
-        uint32_t ypend = 0;                       // stages whose pass-2 epilogue may still use the C region
         int stage = 0;
         bool ok = true;
-        // the epilogue of the pass-2 tile in stage st stages its y in the stage's C region: wait for
-        // its release before the stage is refilled
-        auto flush_y = [&](int st) -> bool {
-            if (!((ypend >> st) & 1u)) return true;
-            ypend &= ~(1u << st);
-            const bool w = wait_bar(sm, kBarYFree0 + st, ph, a);
-            return __all_sync(0xffffffffu, w);
-        };
         auto load_tile = [&](const Piece& c, int t, bool pass1, float tot0, float tot1, float& carry0,
                              float& carry1) -> bool {
             const int row0 = tile_row0(c, t), len = tile_len(c, t);
@@ -396,8 +395,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (!__all_sync(0xffffffffu, w)) return false;
             }
             issued |= 1u << stage;
-            if (!flush_y(stage)) return false;
-            if (!pass1) ypend |= 1u << stage;
             uint64_t* fullx = sm.bars() + kBarFullX0 + stage;
             if (lane == 0) {
                 const int g = h0 / (a.H / a.G);
@@ -492,26 +489,23 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             float c0 = 0.f, c1 = 0.f;
             for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
         }
-        // the last tiles' releases, oldest first (keeps the barrier phases consistent)
-        if (ok) ok = flush_y(stage);
-        if (ok) ok = flush_y(stage ^ 1);
     } else if (warp == 1) {
         // ============================================================ MMA issuer (lane 0)
         if (lane == 0) {
             uint32_t ph = 0;
             int stage = 0;
-            int prev_st = -1;              // stage of the previous pass-2 tile (its Y regions may still be read)
+            uint32_t kt = 0;               // pass-2 tiles issued so far (selects the C B^T buffer)
             const uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yo = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t id_s = idesc_bf16_f32(128, N, 1, 1);
             bool ok = true;
-            auto issue_g = [&](int st) {
+            auto issue_g = [&](int st, uint32_t gcol) {
                 for (int ks = 0; ks < N / 16; ++ks) {
                     const int k = ks / 4, off = (ks % 4) * 32;
                     const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + k * kRegion + off), 0, 1024);
                     const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + k * kRegion + off), 0, 1024);
-                    mma_bf16_ss(tmem + kColG, ad, bd, id_g, ks > 0 ? 1u : 0u);
+                    mma_bf16_ss(tmem + gcol, ad, bd, id_g, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(sm.bars() + kBarG);
             };
@@ -537,31 +531,40 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (ok) mma_commit(sm.bars() + kBarAgg);
                 }
                 // pass 2, per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an
-                // earlier one's reads of the same TMEM):
-                //   Yd(t), both heads interleaved      needs L o G(t), the Y regions free
-                //   Yo(t)                              needs the staged state h_{t-1}
-                //   G(t+1)                             needs the next stage's B and C
-                //   S(t)                               needs the weighted x
+                // earlier one's reads of the same TMEM). The tile's C B^T buffer gb holds C B^T, then
+                // L o C B^T, then Yo; the other buffer gn takes C B^T of the next tile.
+                //   Yd(t), both heads interleaved     needs L o G(t) in gb, the previous epilogue done
+                //   G(t+1) into gn                    as soon as the next stage's B and C are there
+                //   Yo(t) into gb                     needs the staged state h_{t-1}
+                //   S(t)                              needs the weighted x
                 for (int t = c.t0; t < c.t1 && ok; ++t) {
                     const int st = stage;
+                    const uint32_t gb = kColGB + 128 * (kt & 1), gn = kColGB + 128 * ((kt + 1) & 1);
                     if (t == c.t0) {
                         ok = wait_bar(sm, kBarFullBC0 + st, ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        issue_g(st);
+                        issue_g(st, gb);
                     }
                     ok = wait_bar(sm, kBarLG, ph, a) && wait_bar(sm, kBarFullX0 + st, ph, a);
-                    if (ok && prev_st >= 0) ok = wait_bar(sm, kBarYFree0 + prev_st, ph, a);
+                    if (ok && kt > 0) ok = wait_bar(sm, kBarYFree, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
                     for (int ks = 0; ks < 8; ++ks) {
                         for (int h = 0; h < 2; ++h) {
-                            const uint32_t acol = kColG + 32 * (ks / 2) + 16 * (ks % 2) + 8 * h;
+                            const uint32_t acol = gb + 32 * (ks / 2) + 16 * (ks % 2) + 8 * h;
                             const uint64_t bd = smem_desc_sw128(smem_u32(sm.x(st, h) + ks * 2048), kRegion, 1024);
                             mma_bf16_ts(tmem + kColYD + 64 * h, tmem + acol, bd, id_yd, ks > 0 ? 1u : 0u);
                         }
                     }
                     mma_commit(sm.bars() + kBarYD);
+                    const bool more = t + 1 < c.t1;
+                    bool g_done = false;
+                    if (more && test_bar(sm, kBarFullBC0 + (st ^ 1), ph)) {
+                        tc_fence_after_sync();
+                        issue_g(st ^ 1, gn);
+                        g_done = true;
+                    }
                     ok = wait_bar(sm, kBarST, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -569,14 +572,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         const int kk = ks / 4, off = (ks % 4) * 32;
                         const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + kk * kRegion + off), 0, 1024);
                         const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
-                        mma_bf16_ss(tmem + kColYO, ad, bd, id_yo, ks > 0 ? 1u : 0u);
+                        mma_bf16_ss(tmem + gb, ad, bd, id_yo, ks > 0 ? 1u : 0u);
                     }
                     mma_commit(sm.bars() + kBarYO);
-                    if (t + 1 < c.t1) {
+                    if (more && !g_done) {
                         ok = wait_bar(sm, kBarFullBC0 + (st ^ 1), ph, a);
                         if (!ok) break;
                         tc_fence_after_sync();
-                        issue_g(st ^ 1);
+                        issue_g(st ^ 1, gn);
                     }
                     ok = wait_bar(sm, kBarWX, ph, a);
                     if (!ok) break;
@@ -585,7 +588,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     mma_commit(sm.bars() + kBarS);
                     mma_commit(sm.bars() + kBarEmpty0 + st);
                     stage ^= 1;
-                    prev_st = st;
+                    ++kt;
                 }
             }
         }
@@ -606,6 +609,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         const int nq0 = kq * NQ;
         uint32_t ph = 0;
         int stage = 0;
+        uint32_t kt = 0;                         // pass-2 tiles done (selects the C B^T buffer)
         float* misc = sm.misc();
         bool ok = true;
         auto math_bar = [&]() {    // all 16 math warps
@@ -626,37 +630,38 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
         };
         // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)), 0 past len
-        // (bf16 products of the bf16 inputs and the weight rounded to bf16). Thread mt takes half a
-        // row; its four 16-byte chunks are visited in a row-rotated order so that a warp's accesses
-        // spread over all banks.
-        auto weight_x = [&](int st, int len, float last0, float last1) {
+        // (bf16 products of the bf16 inputs and the weight rounded to bf16). With CH = 4 a thread takes
+        // half a row (512 threads), with CH = 8 a whole row (256 threads); chunks are visited in a
+        // row-rotated order so that a warp's accesses spread over all banks.
+        auto weight_x = [&](auto chunks, int st, int len, float last0, float last1, int tix) {
+            constexpr int CH = decltype(chunks)::value;
             const float* cs = sm.cs(st);
-            const int pr = mt >> 1, hh = pr >> 7, l = pr & 127, hf = mt & 1;
+            const int pr = CH == 8 ? tix : (tix >> 1), hh = pr >> 7, l = pr & 127, hf = CH == 8 ? 0 : (tix & 1);
             const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
             const __nv_bfloat162 ww = __float2bfloat162_rn(w);
             uint8_t* rowp = sm.x(st, hh) + l * 128 + 64 * hf;
-            uint4 v[4];
+            uint4 v[CH];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) v[cc] = *reinterpret_cast<const uint4*>(rowp + 16 * ((cc + l) & 3));
+            for (int cc = 0; cc < CH; ++cc) v[cc] = *reinterpret_cast<const uint4*>(rowp + 16 * ((cc + l) & (CH - 1)));
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int cc = 0; cc < CH; ++cc) {
                 __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v[cc]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) b[k] = __hmul2(b[k], ww);
-                *reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & 3)) = v[cc];
+                *reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & (CH - 1))) = v[cc];
             }
         };
-        // L o G (+ D on the diagonal) of stage st, in place over C B^T in TMEM. This thread: row i,
-        // columns j = 32 kq .. 32 kq + 31, written as packed bf16 (per 16 tokens: 8 columns of head 0,
-        // then 8 of head 1). Blocks above the diagonal are zero; a block strictly below takes
-        // exp(cs_i - cs_p) exp(cs_p - cs_j) with p the block's last token (both factors <= 1, no
-        // subtraction of distant cumsums); the diagonal block takes exp(cs_i - cs_j) directly.
-        auto lg_tile = [&](int st, int len, float D0, float D1) {
+        // One 32-column block kb of L o G (+ D on the diagonal) of stage st, in place over C B^T in the
+        // TMEM buffer gcol. This thread: row i, columns j = 32 kb .. 32 kb + 31, written as packed bf16
+        // (per 16 tokens: 8 columns of head 0, then 8 of head 1). A block above the diagonal is zero; a
+        // block strictly below takes exp(cs_i - cs_p) exp(cs_p - cs_j) with p the block's last token (both
+        // factors <= 1, no subtraction of distant cumsums); the diagonal block takes exp(cs_i - cs_j).
+        auto lg_block = [&](int st, int len, int kb, uint32_t gcol, float D0, float D1) {
             const float* cs = sm.cs(st);
             const int i = row;
             const bool rv = i < len;
-            const uint32_t col = lane_base + kColG + 32 * kq;
-            if (kq > qd || !__any_sync(0xffffffffu, rv)) {
+            const uint32_t col = lane_base + gcol + 32 * kb;
+            if (kb > qd || !__any_sync(0xffffffffu, rv)) {
                 uint32_t z[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) z[e] = 0u;
@@ -668,11 +673,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_ld16_nowait(col, g);
             tmem_ld16_nowait(col + 16, g + 16);
             const float ci0 = cs[i], ci1 = cs[128 + i];
-            if (kq < qd) {
-                const float u0 = ex2(ci0 - cs[32 * kq + 31]), u1 = ex2(ci1 - cs[128 + 32 * kq + 31]);
+            if (kb < qd) {
+                const float u0 = ex2(ci0 - cs[32 * kb + 31]), u1 = ex2(ci1 - cs[128 + 32 * kb + 31]);
                 const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
-                const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 32 * kq);
-                const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 32 * kq);
+                const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 32 * kb);
+                const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 32 * kb);
                 tmem_wait_ld();
 #pragma unroll
                 for (int gg = 0; gg < 2; ++gg) {
@@ -699,8 +704,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     tmem_st8(col + 16 * gg + 8, p1);
                 }
             } else {
-                const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * kq);
-                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * kq);
+                const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * kb);
+                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * kb);
                 const float2 cc0 = make_float2(ci0, ci0), cc1 = make_float2(ci1, ci1), m1 = make_float2(-1.f, -1.f);
                 tmem_wait_ld();
 #pragma unroll
@@ -740,11 +745,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
             }
         };
+        // this warp's column block of L o G for stage st into buffer gcol
+        auto lg_tile = [&](int st, int len, uint32_t gcol, float D0, float D1) {
+            lg_block(st, len, kq, gcol, D0, D1);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            warp_arrive(sm, kBarLG);
+        };
         // state step of stage st: h_{t-1} (this thread's state columns) to bf16 in the staging area for
         // Yo, and a_t h_{t-1} back into TMEM for S(t) to accumulate onto
         auto state_step = [&](int st, int len) {
             const float* cs = sm.cs(st);
             const float at = ex2(cs[hrow * 128 + len - 1]);
+            const float2 aa = make_float2(at, at);
             float v[NQ];
             st_load(nq0, NQ, v);
 #pragma unroll
@@ -757,7 +770,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 pk.w = pack_bf16x2(v[cc + 6], v[cc + 7]);
                 *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(row, (n % 64) / 8)) = pk;
             }
-            const float2 aa = make_float2(at, at);
 #pragma unroll
             for (int e = 0; e < NQ; e += 2) {
                 const float2 s2 = __fmul2_rn(make_float2(v[e], v[e + 1]), aa);
@@ -767,21 +779,22 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             st_store(nq0, NQ, v);
             tmem_wait_st();
         };
-        // y = Yd + exp(cs_i) Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31. The warp stages its
-        // 32 rows x 64 bytes in the stage's C region (free once Yo has read it) and writes them back
-        // four lanes per row, so that each store instruction covers eight whole 64-byte row pieces.
-        auto epilogue = [&](int st, int len, int row0, int h0) {
-            const float* cs = sm.cs(st);
+        // y = Yd + e Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31, with e = exp(cs_i) (read
+        // from the stage before it was released: the stage may be refilled by now) and Yo in buffer gcol.
+        // The warp stages its 32 rows x 64 bytes (x layout) and writes them back four lanes per row, so
+        // that each store instruction covers eight whole 64-byte row pieces. For N = 128 the staging bytes
+        // are exactly those this warp's state step writes (state columns kq N/4 .. = head kq / 2's region,
+        // chunks 4 (kq % 2) ..), which it overwrites only after this read-back.
+        auto epilogue = [&](float e, int len, int row0, int h0, uint32_t gcol) {
             const int hh = kq >> 1, c0 = 32 * (kq & 1);
             const int i = row;
-            const float e = ex2(cs[hh * 128 + i]);
             const float2 ee = make_float2(e, e);
-            uint8_t* stg = sm.ystage(st, hh);
+            uint8_t* stg = sm.ystage(hh);
             float yd[32], yo[32];
             tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0, yd);
-            tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0, yo);
+            tmem_ld16_nowait(lane_base + gcol + 64 * hh + c0, yo);
             tmem_ld16_nowait(lane_base + kColYD + 64 * hh + c0 + 16, yd + 16);
-            tmem_ld16_nowait(lane_base + kColYO + 64 * hh + c0 + 16, yo + 16);
+            tmem_ld16_nowait(lane_base + gcol + 64 * hh + c0 + 16, yo + 16);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; k += 8) {
@@ -805,6 +818,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     *reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl) = v;
                 }
             }
+            __syncwarp();
         };
         float hreg[NQ];
 
@@ -815,6 +829,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const bool first_cont = c.w > 0;
             const bool last_cont = c.t1 < c.nt;
             const int64_t q = c.q;
+            const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
+            const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
 
             // ------------------------------------------------ pass 1 (right factors of the window)
             if (last_cont) {
@@ -824,7 +840,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     const float* m = sm.stage_misc(stage);
                     const float tot0 = m[0], tot1 = m[1];
                     if (t == c.t0 && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
-                    weight_x(stage, tile_len(c, t), tot0, tot1);
+                    weight_x(std::integral_constant<int, 4>(), stage, tile_len(c, t), tot0, tot1, mt);
                     fence_proxy_async_smem();
                     warp_arrive(sm, kBarWX1a + stage);
                     stage ^= 1;
@@ -860,15 +876,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 
             // ------------------------------------------------ L o G of the window's first tile (it does not
             // need the entering state, so its MMA can run while the look-back waits)
-            const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
-            const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
             ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
             if (!ok) break;
             tc_fence_after_sync();
-            lg_tile(stage, tile_len(c, c.t0), Dlg0, Dlg1);
-            tmem_wait_st();
-            tc_fence_before_sync();
-            warp_arrive(sm, kBarLG);
+            lg_tile(stage, tile_len(c, c.t0), kColGB + 128 * (kt & 1), Dlg0, Dlg1);
 
             // ------------------------------------------------ look-back (center factors)
             if (first_cont) {
@@ -946,7 +957,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (last_cont && mt == 0) st_release(a.flags + q, 2);
             } else {
                 // the window starts its chain: initial state (or zero) into this thread's state columns
-                // (the same columns it published from, so no barrier is needed in between)
                 const float* ip = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0 : nullptr;
                 float v[NQ];
 #pragma unroll
@@ -970,32 +980,31 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (!ok) break;
                 }
                 tc_fence_after_sync();
+                const float e_row = ex2(cs[(kq >> 1) * 128 + row]);   // for this tile's epilogue
                 state_step(st, len);
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(sm, kBarST);
                 ok = wait_bar_warp(sm, kBarYD, ph, a);
                 if (!ok) break;
-                weight_x(st, len, cs[len - 1], cs[128 + len - 1]);
+                weight_x(std::integral_constant<int, 4>(), st, len, cs[len - 1], cs[128 + len - 1], mt);
                 fence_proxy_async_smem();
                 warp_arrive(sm, kBarWX);
-                ok = wait_bar_warp(sm, kBarYO, ph, a);
-                if (!ok) break;
-                tc_fence_after_sync();
-                epilogue(st, len, row0, h0);
-                fence_proxy_async_smem();
-                tc_fence_before_sync();
-                warp_arrive(sm, kBarYFree0 + st);
                 if (t + 1 < c.t1) {
                     ok = wait_bar_warp(sm, kBarFullX0 + (st ^ 1), ph, a) && wait_bar_warp(sm, kBarG, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    lg_tile(st ^ 1, tile_len(c, t + 1), Dlg0, Dlg1);
-                    tmem_wait_st();
-                    tc_fence_before_sync();
-                    warp_arrive(sm, kBarLG);
+                    lg_tile(st ^ 1, tile_len(c, t + 1), kColGB + 128 * ((kt + 1) & 1), Dlg0, Dlg1);
                 }
+                ok = wait_bar_warp(sm, kBarYO, ph, a);
+                if (!ok) break;
+                tc_fence_after_sync();
+                epilogue(e_row, len, row0, h0, kColGB + 128 * (kt & 1));
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                warp_arrive(sm, kBarYFree);
                 stage ^= 1;
+                ++kt;
             }
             if (!ok) break;
             // end of the window: the last S, then the final state at a chain end
@@ -1011,6 +1020,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     *reinterpret_cast<float4*>(fp + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
             }
             tc_fence_before_sync();
+            if (!ok) break;
             // every warp is done with the piece before the next one's shared phases
             math_bar();
         }
@@ -1051,7 +1061,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 template <int N>
 size_t fused_smem_bytes() {
     const size_t stage = 2 * kRegion + 2 * (N / 64) * kRegion;
-    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 4 * kRegion) + (520 + 192 + 8) * 4 + kNumBars * 8 + 16;
+    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (520 + 192 + 8) * 4 + kNumBars * 8 + 16;
 }
 
 template <int N>
