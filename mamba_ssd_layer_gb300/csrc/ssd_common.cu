@@ -134,6 +134,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
         header[1] = carry;
         header[2] = 0;   // first device-side timeout location (diagnostic), 0 = none
         if (!woff) header[3] = 0;
+        header[4] = 0;   // arrival counter of the fused kernel's grid-wide barriers
+        header[5] = 0;
     }
 }
 

@@ -191,6 +191,15 @@ __device__ __forceinline__ uint32_t bar_count(int i) {
     }
 }
 
+// Phase A barriers (re-initialised for phase C): per stage a full barrier (expect_tx + cumsum
+// arrival), an empty barrier (MMA commit) and a weights barrier (one arrival per math warp), plus
+// the aggregate barrier (MMA commit after a window's last tile).
+constexpr int kBarAFull0 = 0;   // + s: full, + 3 + s: empty, + 6 + s: weights, + 9: aggregate
+
+struct Smem;
+__device__ void init_bars_a(const Smem& sm);
+__device__ void init_bars_c(const Smem& sm);
+
 struct Smem {
     uint8_t* base;
     int N;
@@ -205,6 +214,12 @@ struct Smem {
     __device__ uint8_t* ystage(int h) const {
         return N >= 128 ? hs() + h * kRegion : hs() + (N / 64) * kRegion + h * kRegion;
     }
+    // phase A: three stages of x (both heads) and B; their cumsums in a region phase A leaves unused
+    __device__ uint8_t* xa(int s, int h) const { return base + s * (2 + N / 64) * kRegion + h * kRegion; }
+    __device__ uint8_t* ba(int s) const { return xa(s, 2); }
+    __device__ float* csa(int s) const {
+        return reinterpret_cast<float*>(N >= 128 ? hs() : ystage(0)) + s * 260;
+    }
     __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion); }
     // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
@@ -217,6 +232,25 @@ struct Smem {
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
 };
+
+__device__ void init_bars_a(const Smem& sm) {
+    for (int s = 0; s < 3; ++s) {
+        mbar_init(sm.bars() + kBarAFull0 + s, 2);
+        mbar_init(sm.bars() + kBarAFull0 + 3 + s, 1);
+        mbar_init(sm.bars() + kBarAFull0 + 6 + s, 16);
+    }
+    mbar_init(sm.bars() + kBarAFull0 + 9, 1);
+}
+
+__device__ void init_bars_c(const Smem& sm) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(sm.bars() + i, bar_count(i));
+}
+
+// Grid-wide barrier number k (1, 2, ...) of this launch over the arrival counter in the workspace
+// header (zeroed by the preparation kernel): every CTA arrives, then waits, bounded, for all of them.
+// A CTA that is already aborting, or sees another CTA's error, does not wait. Returns true if the CTA
+// may go on.
+__device__ bool grid_sync(const Smem& sm, const FusedArgs& a, int k);
 
 // misc[] layout
 enum { kMiscA0 = 0, kMiscA1, kMiscTot0, kMiscTot1, kMiscCarry0, kMiscCarry1, kMiscD0, kMiscD1 };
@@ -261,6 +295,33 @@ __device__ __forceinline__ bool test_bar(const Smem& sm, int idx, uint32_t& phas
 __device__ __forceinline__ void warp_arrive(const Smem& sm, int idx) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(sm.bars() + idx);
+}
+
+__device__ bool grid_sync(const Smem& sm, const FusedArgs& a, int k) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int* ctr = a.status + 4;
+        __threadfence();
+        atomicAdd(ctr, 1);
+        volatile int* abort = sm.abort_flag();
+        if (!*abort) {
+            const int target = k * (int)gridDim.x;
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t it = 1; ld_acquire(ctr) < target; ++it) {
+                if ((it & 63u) != 0) continue;
+                if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) { *abort = 1; break; }
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    record_status(a.status, SSD_ERR_TIMEOUT);
+                    atomicCAS(a.status + 2, 0, 0x300 + k);
+                    *abort = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return !*reinterpret_cast<volatile int*>(sm.abort_flag());
 }
 
 // ---------------------------------------------------------------- work decomposition
@@ -322,6 +383,13 @@ __device__ __forceinline__ int tile_len(const Piece& c, int t) {
 }
 
 // ---------------------------------------------------------------- the kernel
+// Three phases separated by grid-wide barriers (the launch is cooperative, so every CTA is resident):
+//   A  right factors: every window that has a successor computes its aggregate -- the state at its
+//      end from a zero start, sum_t decay(t -> end) (w o X_t)^T B_t -- and the decay over it;
+//   B  center factors: a scan over each chain's windows turns the aggregates into the state entering
+//      every window (starting from the initial state);
+//   C  the window's tiles in time order from its entering state: diagonal blocks, left factors, the
+//      state carried on chip from tile to tile, y.
 template <int N>
 __global__ void __launch_bounds__(kThreads)
 ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
@@ -346,13 +414,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     }
     const int64_t np = a.npieces;
     if (np == 0 || (a.dense && a.nt_dense == 0)) return;
+    // phase A visits the windows with a successor: for a dense batch the first W - 1 window ranks of
+    // every chain (the dispatch order puts them first), for a packed batch every window, skipping ends
+    const int64_t nA = a.dense ? (int64_t)a.nseq * a.npairs * (a.W_dense - 1) : np;
 
     if ((smem_u32(smem_raw) & 1023u) != 0) {      // layout needs a 1024-byte aligned base
         if (tid == 0) record_status(a.status, SSD_ERR_UNSUPPORTED);
         return;
     }
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) mbar_init(sm.bars() + i, bar_count(i));
+        init_bars_a(sm);
         *sm.abort_flag() = 0;
         fence_mbar_init();
     }
@@ -365,44 +436,276 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     tc_fence_after_sync();
     const uint32_t tmem = *sm.tmem_slot();
 
+    // math-warp geometry (warps 2..17): four per TMEM lane quadrant qd (the rows 32 qd .. 32 qd + 31
+    // a warp may access); kq (0..3) picks the warp's share of the columns in every phase:
+    //   L o G       column block 32 kq .. 32 kq + 31 (both heads)
+    //   state       state columns kq N/4 .. (kq + 1) N/4
+    //   epilogue    head kq / 2, channels 32 (kq % 2) .. + 31
+    const int mt = tid - 64;                 // 0..511
+    const int qd = warp & 3;
+    const int kq = (warp - 2) >> 2;
+    const int row = 32 * qd + lane;          // TMEM lane = tile row / (head, channel) row
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
+    const int hrow = row >> 6, prow = row & 63;
+    constexpr int NQ = N / 4;                // state columns per thread
+    const int nq0 = kq * NQ;
+
+    // TMEM state columns [c0, c0 + cnt) of this thread's row, cnt a multiple of 16
+    auto st_load = [&](int c0, int cnt, float* v) {
+        for (int k = 0; k < cnt; k += 16) tmem_ld16_nowait(lane_base + kColST + c0 + k, v + k);
+        tmem_wait_ld();
+    };
+    auto st_store = [&](int c0, int cnt, const float* v) {
+        for (int k = 0; k < cnt; k += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(v[k + e]);
+            tmem_st16(lane_base + kColST + c0 + k, r);
+        }
+    };
+    // x of a stage (head regions x0 and x0 + 16 KB) scaled in place: row l of head h times
+    // exp2(last_h - cs_h(l)), 0 past len (bf16 products of the bf16 inputs and the weight rounded to
+    // bf16). Thread mt (0..511) takes half a row; its four 16-byte chunks are visited in a row-rotated
+    // order so that a warp's accesses spread over all banks.
+    auto weight_x = [&](uint8_t* x0, const float* cs, int len, float last0, float last1) {
+        const int pr = mt >> 1, hh = pr >> 7, l = pr & 127, hf = mt & 1;
+        const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
+        const __nv_bfloat162 ww = __float2bfloat162_rn(w);
+        uint8_t* rowp = x0 + hh * kRegion + l * 128 + 64 * hf;
+        uint4 v[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) v[cc] = *reinterpret_cast<const uint4*>(rowp + 16 * ((cc + l) & 3));
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v[cc]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) b[k] = __hmul2(b[k], ww);
+            *reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & 3)) = v[cc];
+        }
+    };
+    // producer: dt of a tile's tokens for both heads of the pair, 4 per lane (issued early)
+    auto load_dt = [&](int row0, int len, int h0, float (&v)[2][4]) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int l = 4 * lane + k;
+                v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
+            }
+    };
+    // producer: tile-local inclusive cumsum of dt*A (x log2 e) plus `carry`, written to cs[2][128];
+    // cv gets this lane's four values per head, carry advances by the tile's total
+    auto cumsum = [&](const float (&v)[2][4], int h0, float* cs, float (&carry)[2], float (&cv)[2][4]) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float A2 = __ldg(a.A + h0 + hh) * kLog2e;
+            float p[4];
+            p[0] = v[hh][0] * A2;
+#pragma unroll
+            for (int k = 1; k < 4; ++k) p[k] = p[k - 1] + v[hh][k] * A2;
+            float sc = p[3];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float tt = __shfl_up_sync(0xffffffffu, sc, o);
+                if (lane >= o) sc += tt;
+            }
+            const float base = sc - p[3] + carry[hh];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cv[hh][k] = base + p[k];
+            *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
+            carry[hh] += __shfl_sync(0xffffffffu, sc, 31);
+        }
+    };
+
+    // ==================================================================== phase A
     if (warp == 0) {
-        // ============================================================ producer warp
-        // TMA (lane 0): pass 1 loads x and B on the stage's x barrier; pass 2 loads B and C on the
-        // B/C barrier (they feed C B^T first) and x on the x barrier. All lanes: dt for both heads
-        // -> the tile-local cumsum of dt*A (x log2 e), with the window carry in pass 1. In pass 2
-        // also the table v_j = exp(cs_p - cs_j), p the last token of j's 32-token block (j < 96), once
-        // the previous tile's L o G (its only reader) is done.
-        uint32_t ph = 0;
-        uint32_t issued = 0;
-        uint32_t p2 = 0;   // pass-2 tiles loaded so far
+        // producer: per window its total dt*A first (the weights are decays to the window's end), then
+        // every tile: x (both heads) and B by TMA (lane 0), the cumsum with the window carry (all lanes)
+        uint32_t ph = 0, issued = 0;
         int stage = 0;
         bool ok = true;
-        auto load_tile = [&](const Piece& c, int t, bool pass1, float tot0, float tot1, float& carry0,
-                             float& carry1) -> bool {
-            const int row0 = tile_row0(c, t), len = tile_len(c, t);
+        for (int64_t d = blockIdx.x; d < nA && ok; d += gridDim.x) {
+            const Piece c = decode_piece(d, a);
+            if (!c.valid) break;
+            if (c.t1 >= c.nt) continue;
             const int h0 = 2 * c.hp;
-            // dt first: the loads are in flight while the stage drains
-            float v[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int l = 4 * lane + k;
-                    v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
-                }
-            if ((issued >> stage) & 1u) {
-                const bool w = wait_bar(sm, kBarEmpty0 + stage, ph, a);
-                if (!__all_sync(0xffffffffu, w)) return false;
+            const int r0 = tile_row0(c, c.t0);
+            const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+            for (int l = lane; l < ntok; l += 32) {
+                const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
+                s0 += d2.x;
+                s1 += d2.y;
             }
-            issued |= 1u << stage;
-            uint64_t* fullx = sm.bars() + kBarFullX0 + stage;
-            if (lane == 0) {
-                const int g = h0 / (a.H / a.G);
-                if (pass1) {
-                    mbar_arrive_expect_tx(fullx, (uint32_t)((2 + NB) * kRegion));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            }
+            const float tot0 = s0 * __ldg(a.A + h0) * kLog2e, tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
+            float carry[2] = {0.f, 0.f};
+            for (int t = c.t0; t < c.t1 && ok; ++t) {
+                const int row0 = tile_row0(c, t), len = tile_len(c, t);
+                float v[2][4], cv[2][4];
+                load_dt(row0, len, h0, v);
+                if ((issued >> stage) & 1u) {
+                    const bool w = wait_bar(sm, kBarAFull0 + 3 + stage, ph, a);   // the stage's empty barrier
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                issued |= 1u << stage;
+                uint64_t* full = sm.bars() + kBarAFull0 + stage;
+                if (lane == 0) {
+                    const int g = h0 / (a.H / a.G);
+                    mbar_arrive_expect_tx(full, (uint32_t)((2 + NB) * kRegion));
+                    tma_load_3d(sm.xa(stage, 0), &maps.x, full, 0, h0, row0);
+                    tma_load_3d(sm.xa(stage, 1), &maps.x, full, 0, h0 + 1, row0);
                     for (int k = 0; k < NB; ++k)
-                        tma_load_3d(sm.b(stage) + k * kRegion, &maps.b, fullx, 64 * k, g, row0);
-                } else {
+                        tma_load_3d(sm.ba(stage) + k * kRegion, &maps.b, full, 64 * k, g, row0);
+                }
+                float* cs = sm.csa(stage);
+                cumsum(v, h0, cs, carry, cv);
+                if (lane == 0) { cs[256] = tot0; cs[257] = tot1; }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full);
+                stage = stage == 2 ? 0 : stage + 1;
+            }
+        }
+        // drain: every stage's last tile consumed, so no arrival is pending when the barriers are reset
+        for (int s = 0; s < 3 && ok; ++s)
+            if ((issued >> s) & 1u) ok = __all_sync(0xffffffffu, wait_bar(sm, kBarAFull0 + 3 + s, ph, a));
+        if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
+    } else if (warp == 1) {
+        // MMA: S_agg += (w o X_t)^T B_t over the window's tiles (M = 2 heads x 64, N = state size)
+        if (lane == 0) {
+            uint32_t ph = 0;
+            int stage = 0;
+            bool ok = true;
+            const uint32_t id_s = idesc_bf16_f32(128, N, 1, 1);
+            for (int64_t d = blockIdx.x; d < nA && ok; d += gridDim.x) {
+                const Piece c = decode_piece(d, a);
+                if (!c.valid) break;
+                if (c.t1 >= c.nt) continue;
+                for (int t = c.t0; t < c.t1 && ok; ++t) {
+                    ok = wait_bar(sm, kBarAFull0 + stage, ph, a) && wait_bar(sm, kBarAFull0 + 6 + stage, ph, a);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sm.xa(stage, 0) + ks * 2048), kRegion, 1024);
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.ba(stage) + ks * 2048), kRegion, 1024);
+                        mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || t > c.t0) ? 1u : 0u);
+                    }
+                    mma_commit(sm.bars() + kBarAFull0 + 3 + stage);
+                    stage = stage == 2 ? 0 : stage + 1;
+                }
+                if (ok) mma_commit(sm.bars() + kBarAFull0 + 9);
+            }
+            if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
+        }
+    } else {
+        // math warps: weights of every tile; the window's aggregate and decay to global memory
+        uint32_t ph = 0;
+        int stage = 0;
+        bool ok = true;
+        for (int64_t d = blockIdx.x; d < nA && ok; d += gridDim.x) {
+            const Piece c = decode_piece(d, a);
+            if (!c.valid) break;
+            if (c.t1 >= c.nt) continue;
+            float tot0 = 0.f, tot1 = 0.f;
+            for (int t = c.t0; t < c.t1 && ok; ++t) {
+                ok = wait_bar_warp(sm, kBarAFull0 + stage, ph, a);
+                if (!ok) break;
+                const float* cs = sm.csa(stage);
+                tot0 = cs[256];
+                tot1 = cs[257];
+                weight_x(sm.xa(stage, 0), cs, tile_len(c, t), tot0, tot1);
+                fence_proxy_async_smem();
+                warp_arrive(sm, kBarAFull0 + 6 + stage);
+                stage = stage == 2 ? 0 : stage + 1;
+            }
+            if (!ok) break;
+            ok = wait_bar_warp(sm, kBarAFull0 + 9, ph, a);
+            if (!ok) break;
+            tc_fence_after_sync();
+            float v[NQ];
+            st_load(nq0, NQ, v);
+            float* dst = a.agg + (c.q * 128 + row) * N + nq0;
+#pragma unroll
+            for (int k = 0; k < NQ; k += 4)
+                __stcg(reinterpret_cast<float4*>(dst + k), make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]));
+            if (mt < 2) a.decay[c.q * 2 + mt] = ex2(mt ? tot1 : tot0);
+            tc_fence_before_sync();
+        }
+        if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
+    }
+
+    // ==================================================================== phase B
+    bool run = grid_sync(sm, a, 1);
+    if (run) {
+        // chain ch = (sequence s, head pair hp) with windows q0 .. q0 + W - 1; thread item = 4 floats of
+        // the (head, channel) x state matrix: h(w + 1) = decay(w) h(w) + agg(w), h(0) = initial state
+        constexpr int per_chain = 32 * N;         // float4 units in 128 x N
+        const int64_t nch = (int64_t)a.nseq * a.npairs;
+        for (int64_t it = (int64_t)blockIdx.x * blockDim.x + tid; it < nch * per_chain;
+             it += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t ch = it / per_chain;
+            const int e4 = (int)(it % per_chain);
+            const int s = (int)(ch / a.npairs), hp = (int)(ch % a.npairs);
+            int64_t q0;
+            int W;
+            if (a.dense) {
+                W = a.W_dense;
+                q0 = ch * W;
+            } else {
+                const int32_t w0 = a.woff[s];
+                W = a.woff[s + 1] - w0;
+                q0 = (int64_t)a.npairs * w0 + (int64_t)hp * W;
+            }
+            if (W <= 1) continue;
+            const int r = e4 / (N / 4), n = 4 * (e4 % (N / 4));
+            const int hr = r >> 6, pr = r & 63;
+            float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a.init) h = *reinterpret_cast<const float4*>(a.init + (((int64_t)s * a.H + 2 * hp + hr) * 64 + pr) * N + n);
+            for (int w = 0; w + 1 < W; ++w) {
+                const float dcy = __ldcg(a.decay + (q0 + w) * 2 + hr);
+                const float4 g = __ldcg(reinterpret_cast<const float4*>(a.agg + ((q0 + w) * 128 + r) * N + n));
+                h = make_float4(fmaf(dcy, h.x, g.x), fmaf(dcy, h.y, g.y), fmaf(dcy, h.z, g.z), fmaf(dcy, h.w, g.w));
+                __stcg(reinterpret_cast<float4*>(a.incl + ((q0 + w + 1) * 128 + r) * N + n), h);
+            }
+        }
+    }
+    run = grid_sync(sm, a, 2) && run;
+    if (tid == 0) {
+        init_bars_c(sm);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // ==================================================================== phase C
+    if (run && warp == 0) {
+        // producer: every window's tiles in time order -- B and C by TMA on the B/C barrier (they feed
+        // C B^T first), x on the x barrier; the tile-local cumsum of dt*A (x log2 e); the table
+        // v_j = exp(cs_p - cs_j), p the last token of j's 32-token block (j < 96), once the previous
+        // tile's L o G (its only reader) is done
+        uint32_t ph = 0, issued = 0, p2 = 0;
+        int stage = 0;
+        bool ok = true;
+        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+            const Piece c = decode_piece(d, a);
+            if (!c.valid) break;
+            const int h0 = 2 * c.hp;
+            for (int t = c.t0; t < c.t1 && ok; ++t) {
+                const int row0 = tile_row0(c, t), len = tile_len(c, t);
+                float v[2][4], cv[2][4];
+                load_dt(row0, len, h0, v);
+                if ((issued >> stage) & 1u) {
+                    const bool w = wait_bar(sm, kBarEmpty0 + stage, ph, a);
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+                }
+                issued |= 1u << stage;
+                uint64_t* fullx = sm.bars() + kBarFullX0 + stage;
+                if (lane == 0) {
+                    const int g = h0 / (a.H / a.G);
                     uint64_t* fullbc = sm.bars() + kBarFullBC0 + stage;
                     mbar_arrive_expect_tx(fullbc, (uint32_t)(2 * NB * kRegion));
                     for (int k = 0; k < NB; ++k) {
@@ -410,41 +713,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         tma_load_3d(sm.c(stage) + k * kRegion, &maps.c, fullbc, 64 * k, g, row0);
                     }
                     mbar_arrive_expect_tx(fullx, (uint32_t)(2 * kRegion));
+                    tma_load_3d(sm.x(stage, 0), &maps.x, fullx, 0, h0, row0);
+                    tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
                 }
-                tma_load_3d(sm.x(stage, 0), &maps.x, fullx, 0, h0, row0);
-                tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
-            }
-            float* cs = sm.cs(stage);
-            float cv[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float A2 = __ldg(a.A + h0 + hh) * kLog2e;
-                float p[4];
-                p[0] = v[hh][0] * A2;
-#pragma unroll
-                for (int k = 1; k < 4; ++k) p[k] = p[k - 1] + v[hh][k] * A2;
-                float sc = p[3];
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float tt = __shfl_up_sync(0xffffffffu, sc, o);
-                    if (lane >= o) sc += tt;
-                }
-                const float base = sc - p[3] + (pass1 ? (hh ? carry1 : carry0) : 0.f);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) cv[hh][k] = base + p[k];
-                *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
-                const float tile_total = __shfl_sync(0xffffffffu, sc, 31);
-                if (pass1) { if (hh) carry1 += tile_total; else carry0 += tile_total; }
-            }
-            if (lane == 0) {
-                float* m = sm.stage_misc(stage);
-                m[0] = tot0;
-                m[1] = tot1;
-            }
-            if (!pass1) {
+                float carry[2] = {0.f, 0.f};
+                cumsum(v, h0, sm.cs(stage), carry, cv);
                 if (p2 > 0) {
                     const bool w = wait_bar(sm, kBarLG, ph, a);
-                    if (!__all_sync(0xffffffffu, w)) return false;
+                    if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
                 }
                 ++p2;
                 float* vt = sm.vt();
@@ -456,45 +732,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                             make_float4(ex2(piv - cv[hh][0]), ex2(piv - cv[hh][1]), ex2(piv - cv[hh][2]),
                                         ex2(piv - cv[hh][3]));
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(fullx);
+                stage ^= 1;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(fullx);
-            stage ^= 1;
-            return true;
-        };
-        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
-            const Piece c = decode_piece(d, a);
-            if (!c.valid) break;
-            if (c.t1 < c.nt) {
-                // pass 1: the window's total dt*A first (its tokens' weights are decays to its end)
-                const int h0 = 2 * c.hp;
-                const int r0 = tile_row0(c, c.t0);
-                const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-                for (int l = lane; l < ntok; l += 32) {
-                    const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
-                    s0 += d2.x;
-                    s1 += d2.y;
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-                }
-                const float tot0 = s0 * __ldg(a.A + h0) * kLog2e, tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
-                float c0 = 0.f, c1 = 0.f;
-                for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, true, tot0, tot1, c0, c1);
-            }
-            float c0 = 0.f, c1 = 0.f;
-            for (int t = c.t0; t < c.t1 && ok; ++t) ok = load_tile(c, t, false, 0.f, 0.f, c0, c1);
         }
-    } else if (warp == 1) {
+        if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
+    } else if (run && warp == 1) {
         // ============================================================ MMA issuer (lane 0)
         if (lane == 0) {
             uint32_t ph = 0;
             int stage = 0;
-            uint32_t kt = 0;               // pass-2 tiles issued so far (selects the C B^T buffer)
+            uint32_t kt = 0;               // tiles issued so far (selects the C B^T buffer)
             const uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yo = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
@@ -509,30 +758,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 mma_commit(sm.bars() + kBarG);
             };
-            auto issue_s = [&](int st, bool first) {
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
-                    mma_bf16_ss(tmem + kColST, ad, bd, id_s, (ks > 0 || !first) ? 1u : 0u);
-                }
-            };
             for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
                 const Piece c = decode_piece(d, a);
                 if (!c.valid) break;
-                if (c.t1 < c.nt) {
-                    for (int t = c.t0; t < c.t1 && ok; ++t) {
-                        ok = wait_bar(sm, kBarFullX0 + stage, ph, a) && wait_bar(sm, kBarWX1a + stage, ph, a);
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        issue_s(stage, t == c.t0);
-                        mma_commit(sm.bars() + kBarEmpty0 + stage);
-                        stage ^= 1;
-                    }
-                    if (ok) mma_commit(sm.bars() + kBarAgg);
-                }
-                // pass 2, per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an
-                // earlier one's reads of the same TMEM). The tile's C B^T buffer gb holds C B^T, then
-                // L o C B^T, then Yo; the other buffer gn takes C B^T of the next tile.
+                // per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an earlier
+                // one's reads of the same TMEM). The tile's C B^T buffer gb holds C B^T, then L o C B^T,
+                // then Yo; the other buffer gn takes C B^T of the next tile.
                 //   Yd(t), both heads interleaved     needs L o G(t) in gb, the previous epilogue done
                 //   G(t+1) into gn                    as soon as the next stage's B and C are there
                 //   Yo(t) into gb                     needs the staged state h_{t-1}
@@ -584,73 +815,25 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     ok = wait_bar(sm, kBarWX, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_s(st, false);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
+                        mma_bf16_ss(tmem + kColST, ad, bd, id_s, 1u);
+                    }
                     mma_commit(sm.bars() + kBarS);
                     mma_commit(sm.bars() + kBarEmpty0 + st);
                     stage ^= 1;
                     ++kt;
                 }
             }
+            if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
         }
-    } else {
+    } else if (run) {
         // ============================================================ math warps
-        // 16 warps, four per TMEM lane quadrant qd (the rows 32 qd .. 32 qd + 31 a warp may access);
-        // kq (0..3) picks the warp's share of the columns in every phase:
-        //   L o G       column block 32 kq .. 32 kq + 31 (both heads)
-        //   state       state columns kq N/4 .. (kq + 1) N/4
-        //   epilogue    head kq / 2, channels 32 (kq % 2) .. + 31
-        const int mt = tid - 64;                 // 0..511
-        const int qd = warp & 3;
-        const int kq = (warp - 2) >> 2;
-        const int row = 32 * qd + lane;          // TMEM lane = tile row / (head, channel) row
-        const uint32_t lane_base = tmem + ((uint32_t)(32 * qd) << 16);
-        const int hrow = row >> 6, prow = row & 63;
-        constexpr int NQ = N / 4;                // state columns per thread
-        const int nq0 = kq * NQ;
         uint32_t ph = 0;
         int stage = 0;
-        uint32_t kt = 0;                         // pass-2 tiles done (selects the C B^T buffer)
-        float* misc = sm.misc();
+        uint32_t kt = 0;                         // tiles done (selects the C B^T buffer)
         bool ok = true;
-        auto math_bar = [&]() {    // all 16 math warps
-            warp_arrive(sm, kBarMath);
-            if (!wait_bar_warp(sm, kBarMath, ph, a)) ok = false;
-        };
-        // TMEM state columns [c0, c0 + cnt) of this thread's row, cnt a multiple of 16
-        auto st_load = [&](int c0, int cnt, float* v) {
-            for (int k = 0; k < cnt; k += 16) tmem_ld16_nowait(lane_base + kColST + c0 + k, v + k);
-            tmem_wait_ld();
-        };
-        auto st_store = [&](int c0, int cnt, const float* v) {
-            for (int k = 0; k < cnt; k += 16) {
-                uint32_t r[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(v[k + e]);
-                tmem_st16(lane_base + kColST + c0 + k, r);
-            }
-        };
-        // x of stage st scaled in place: row l of head h times exp2(last_h - cs_h(l)), 0 past len
-        // (bf16 products of the bf16 inputs and the weight rounded to bf16). With CH = 4 a thread takes
-        // half a row (512 threads), with CH = 8 a whole row (256 threads); chunks are visited in a
-        // row-rotated order so that a warp's accesses spread over all banks.
-        auto weight_x = [&](auto chunks, int st, int len, float last0, float last1, int tix) {
-            constexpr int CH = decltype(chunks)::value;
-            const float* cs = sm.cs(st);
-            const int pr = CH == 8 ? tix : (tix >> 1), hh = pr >> 7, l = pr & 127, hf = CH == 8 ? 0 : (tix & 1);
-            const float w = (l < len) ? ex2((hh ? last1 : last0) - cs[hh * 128 + l]) : 0.f;
-            const __nv_bfloat162 ww = __float2bfloat162_rn(w);
-            uint8_t* rowp = sm.x(st, hh) + l * 128 + 64 * hf;
-            uint4 v[CH];
-#pragma unroll
-            for (int cc = 0; cc < CH; ++cc) v[cc] = *reinterpret_cast<const uint4*>(rowp + 16 * ((cc + l) & (CH - 1)));
-#pragma unroll
-            for (int cc = 0; cc < CH; ++cc) {
-                __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&v[cc]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) b[k] = __hmul2(b[k], ww);
-                *reinterpret_cast<uint4*>(rowp + 16 * ((cc + l) & (CH - 1))) = v[cc];
-            }
-        };
         // One 32-column block kb of L o G (+ D on the diagonal) of stage st, in place over C B^T in the
         // TMEM buffer gcol. This thread: row i, columns j = 32 kb .. 32 kb + 31, written as packed bf16
         // (per 16 tokens: 8 columns of head 0, then 8 of head 1). A block above the diagonal is zero; a
@@ -820,156 +1003,36 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             __syncwarp();
         };
-        float hreg[NQ];
 
         for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
             const Piece c = decode_piece(d, a);
             if (!c.valid) break;
             const int h0 = 2 * c.hp;
-            const bool first_cont = c.w > 0;
-            const bool last_cont = c.t1 < c.nt;
-            const int64_t q = c.q;
             const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
             const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
 
-            // ------------------------------------------------ pass 1 (right factors of the window)
-            if (last_cont) {
-                for (int t = c.t0; t < c.t1 && ok; ++t) {
-                    ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a);
-                    if (!ok) break;
-                    const float* m = sm.stage_misc(stage);
-                    const float tot0 = m[0], tot1 = m[1];
-                    if (t == c.t0 && mt == 0) { misc[kMiscTot0] = tot0; misc[kMiscTot1] = tot1; }
-                    weight_x(std::integral_constant<int, 4>(), stage, tile_len(c, t), tot0, tot1, mt);
-                    fence_proxy_async_smem();
-                    warp_arrive(sm, kBarWX1a + stage);
-                    stage ^= 1;
-                }
-                if (!ok) break;
-                ok = wait_bar_warp(sm, kBarAgg, ph, a);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const float dec = ex2(misc[kMiscTot0 + hrow]);
-                const float* ip = (!first_cont && a.init)
-                                      ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0
-                                      : nullptr;
-                float* dst = (!first_cont ? a.incl : a.agg) + (q * 128 + row) * N + nq0;
-                float v[NQ];
-                st_load(nq0, NQ, v);
-#pragma unroll
-                for (int k = 0; k < NQ; k += 4) {
-                    float4 o = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                    if (ip) {
-                        // the window starts its chain: inclusive state = dec * init + aggregate
-                        const float4 i4 = *reinterpret_cast<const float4*>(ip + k);
-                        o.x = fmaf(dec, i4.x, o.x); o.y = fmaf(dec, i4.y, o.y);
-                        o.z = fmaf(dec, i4.z, o.z); o.w = fmaf(dec, i4.w, o.w);
-                    }
-                    __stcg(reinterpret_cast<float4*>(dst + k), o);
-                }
-                if (first_cont && mt < 2) a.decay[q * 2 + mt] = ex2(misc[kMiscTot0 + mt]);
-                // every thread's stores precede the barrier; one gpu-scope release then publishes them all
-                math_bar();
-                if (mt == 0) st_release(a.flags + q, first_cont ? 1 : 2);
-                tc_fence_before_sync();
-            }
-
-            // ------------------------------------------------ L o G of the window's first tile (it does not
-            // need the entering state, so its MMA can run while the look-back waits)
+            // L o G of the window's first tile (it does not need the entering state)
             ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
             if (!ok) break;
             tc_fence_after_sync();
             lg_tile(stage, tile_len(c, c.t0), kColGB + 128 * (kt & 1), Dlg0, Dlg1);
 
-            // ------------------------------------------------ look-back (center factors)
-            if (first_cont) {
-                // lanes poll up to 32 predecessors at once; the state entering this window is
-                //   h_in = agg(q-1) + dec(q-1) (agg(q-2) + dec(q-2) (... + incl(q-m)))
-                // with q-m the nearest predecessor that has published its inclusive state.
-#pragma unroll
-                for (int k = 0; k < NQ; ++k) hreg[k] = 0.f;
-                float mult = 1.f;
-                int64_t qq = q - 1;                      // next predecessor to fold in
-                const int64_t qfirst = q - c.w;          // the chain's first window (always inclusive)
-                const uint64_t t0 = global_timer_ns();
-                while (ok && qq >= qfirst) {
-                    const int64_t mine = qq - lane;
-                    int f = 0;
-                    if (mine >= qfirst) f = ld_acquire(a.flags + mine);
-                    const unsigned incl_mask = __ballot_sync(0xffffffffu, f == 2);
-                    const unsigned none_mask = __ballot_sync(0xffffffffu, mine >= qfirst && f == 0);
-                    const int m = incl_mask ? (__ffs(incl_mask) - 1) : 32;     // nearest inclusive lane
-                    const unsigned need = (m >= 31) ? 0xffffffffu : ((2u << m) - 1u);
-                    if (none_mask & need) {
-                        // something up to the nearest inclusive state is not published yet: spin
-                        int verdict = 0;
-                        if (lane == 0) {
-                            if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) verdict = 2;
-                            else if (global_timer_ns() - t0 > kWaitLimitNs) {
-                                record_status(a.status, SSD_ERR_TIMEOUT);
-                                atomicCAS(a.status + 2, 0, 0x200);
-                                verdict = 2;
-                            }
-                        }
-                        if (__shfl_sync(0xffffffffu, verdict, 0) == 2) ok = false;
-                        continue;
-                    }
-                    __threadfence();   // the flags were seen set: order the state reads after them
-                    const int cnt = (m < 32) ? m + 1 : 32;
-                    float dec_l = 0.f;
-                    if (lane < cnt && (m == 32 || lane < m)) dec_l = __ldcg(a.decay + (qq - lane) * 2 + hrow);
-                    for (int j = 0; j < cnt; ++j) {
-                        const int64_t qj = qq - j;
-                        const bool is_incl = (j == m);
-                        const float* src = (is_incl ? a.incl : a.agg) + (qj * 128 + row) * N + nq0;
-#pragma unroll
-                        for (int k = 0; k < NQ; k += 4) {
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + k));
-                            hreg[k] = fmaf(mult, v.x, hreg[k]);
-                            hreg[k + 1] = fmaf(mult, v.y, hreg[k + 1]);
-                            hreg[k + 2] = fmaf(mult, v.z, hreg[k + 2]);
-                            hreg[k + 3] = fmaf(mult, v.w, hreg[k + 3]);
-                        }
-                        if (!is_incl) mult *= __shfl_sync(0xffffffffu, dec_l, j);
-                    }
-                    if (m < 32) break;
-                    qq -= 32;
-                }
-                if (!ok) break;
-                tc_fence_after_sync();
-                if (last_cont) {
-                    // inclusive = dec * h_in + aggregate (still in TMEM)
-                    const float dec = ex2(misc[kMiscTot0 + hrow]);
-                    float* dst = a.incl + (q * 128 + row) * N + nq0;
-                    float v[NQ];
-                    st_load(nq0, NQ, v);
-#pragma unroll
-                    for (int k = 0; k < NQ; k += 4) {
-                        const float4 o = make_float4(fmaf(dec, hreg[k], v[k]), fmaf(dec, hreg[k + 1], v[k + 1]),
-                                                     fmaf(dec, hreg[k + 2], v[k + 2]), fmaf(dec, hreg[k + 3], v[k + 3]));
-                        __stcg(reinterpret_cast<float4*>(dst + k), o);
-                    }
-                }
-                st_store(nq0, NQ, hreg);   // park h_in in this thread's TMEM state columns
-                tmem_wait_st();
-                tc_fence_before_sync();
-                math_bar();
-                if (last_cont && mt == 0) st_release(a.flags + q, 2);
-            } else {
-                // the window starts its chain: initial state (or zero) into this thread's state columns
-                const float* ip = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0 : nullptr;
+            // the entering state into this thread's state columns: the initial state (or zero) at a
+            // chain's start, else the scan's result
+            {
+                const float* src = c.w == 0
+                    ? (a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0 : nullptr)
+                    : a.incl + (c.q * 128 + row) * N + nq0;
                 float v[NQ];
 #pragma unroll
                 for (int k = 0; k < NQ; k += 4) {
-                    const float4 i4 = ip ? *reinterpret_cast<const float4*>(ip + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 i4 = src ? __ldcg(reinterpret_cast<const float4*>(src + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
                 }
                 st_store(nq0, NQ, v);
                 tmem_wait_st();
             }
-            if (!ok) break;
 
-            // ------------------------------------------------ pass 2 (diagonal blocks, left factors, state)
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int st = stage;
                 const int len = tile_len(c, t);
@@ -987,7 +1050,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 warp_arrive(sm, kBarST);
                 ok = wait_bar_warp(sm, kBarYD, ph, a);
                 if (!ok) break;
-                weight_x(std::integral_constant<int, 4>(), st, len, cs[len - 1], cs[128 + len - 1], mt);
+                weight_x(sm.x(st, 0), cs, len, cs[len - 1], cs[128 + len - 1]);
                 fence_proxy_async_smem();
                 warp_arrive(sm, kBarWX);
                 if (t + 1 < c.t1) {
@@ -1007,7 +1070,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 ++kt;
             }
             if (!ok) break;
-            // end of the window: the last S, then the final state at a chain end
+            // end of the window: the last S, then the final state at a chain end (each thread only
+            // touches its own state columns, so the next window may park its state right after)
             ok = wait_bar_warp(sm, kBarS, ph, a);
             if (!ok) break;
             tc_fence_after_sync();
@@ -1020,9 +1084,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     *reinterpret_cast<float4*>(fp + k) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
             }
             tc_fence_before_sync();
-            if (!ok) break;
-            // every warp is done with the piece before the next one's shared phases
-            math_bar();
         }
         if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
     }

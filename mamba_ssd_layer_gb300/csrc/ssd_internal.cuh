@@ -17,7 +17,8 @@ struct ChunkDesc {
 
 // Workspace layout (byte offsets, every section 256-byte aligned).
 //   header  : int32 status, int32 number of chunks (tiles) actually built, int32 location
-//             code of the first device-side timeout (0 = none), int32 spare
+//             code of the first device-side timeout (0 = none), int32 number of windows (packed
+//             batch, fused path), int32 grid-barrier arrival counter (fused path), int32 spare
 //   chunks  : ChunkDesc[max_chunks]  (chunks of `chunk` tokens; 128-token tiles on the fused path)
 //   seqoff  : int32[nseq + 1], first chunk of every sequence
 // three-kernel path:
@@ -59,7 +60,7 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
     else
         w.max_chunks = s.batch * ((s.seqlen + q - 1) / q);
     size_t off = 0;
-    w.header = off; off = align256(off + 16);
+    w.header = off; off = align256(off + 32);
     w.chunks = off; off = align256(off + sizeof(ChunkDesc) * (size_t)(w.max_chunks > 0 ? w.max_chunks : 1));
     w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
     if (w.fused) {
