@@ -195,6 +195,8 @@ __device__ __forceinline__ uint32_t bar_count(int i) {
 // arrival), an empty barrier (MMA commit) and a weights barrier (one arrival per math warp), plus
 // the aggregate barrier (MMA commit after a window's last tile).
 constexpr int kBarAFull0 = 0;   // + s: full, + 3 + s: empty, + 6 + s: weights, + 9: aggregate
+// Phase-A windows per CTA whose totals are precomputed together (more fall back to the producer)
+constexpr int kMaxWinA = 96;
 
 struct Smem;
 __device__ void init_bars_a(const Smem& sm);
@@ -220,6 +222,9 @@ struct Smem {
     __device__ float* csa(int s) const {
         return reinterpret_cast<float*>(N >= 128 ? hs() : ystage(0)) + s * 260;
     }
+    // phase A window totals (and their per-warp partial sums): behind the phase-A cumsums in the same
+    // unused area (32 KB for either state size)
+    __device__ float* tota() const { return csa(0) + 1024; }
     __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion); }
     // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
@@ -321,6 +326,35 @@ __device__ bool grid_sync(const Smem& sm, const FusedArgs& a, int k) {
         __threadfence();
     }
     __syncthreads();
+    return !*reinterpret_cast<volatile int*>(sm.abort_flag());
+}
+
+// The same among the 16 math warps only (named barrier 1 over their 512 threads): the producer and the
+// MMA warp are busy with phase C meanwhile.
+__device__ bool grid_sync_math(const Smem& sm, const FusedArgs& a, int k) {
+    asm volatile("bar.sync 1, %0;" :: "n"(kMathThreads) : "memory");
+    if (threadIdx.x == 64) {
+        int* ctr = a.status + 4;
+        __threadfence();
+        atomicAdd(ctr, 1);
+        volatile int* abort = sm.abort_flag();
+        if (!*abort) {
+            const int target = k * (int)gridDim.x;
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t it = 1; ld_acquire(ctr) < target; ++it) {
+                if ((it & 63u) != 0) continue;
+                if (*reinterpret_cast<volatile const int*>(a.status) != SSD_OK) { *abort = 1; break; }
+                if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    record_status(a.status, SSD_ERR_TIMEOUT);
+                    atomicCAS(a.status + 2, 0, 0x300 + k);
+                    *abort = 1;
+                    break;
+                }
+            }
+        }
+        __threadfence();
+    }
+    asm volatile("bar.sync 1, %0;" :: "n"(kMathThreads) : "memory");
     return !*reinterpret_cast<volatile int*>(sm.abort_flag());
 }
 
@@ -517,6 +551,53 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         }
     };
 
+    // Totals of dt*A (x log2 e) over this CTA's phase-A windows, by every thread at once: the weights of
+    // a window's tiles are decays to its end, so the producer needs them before its first tile. Each warp
+    // reduces its share, then one thread per window adds the warps' partial sums in a fixed order (the
+    // result must not depend on timing).
+    float* totA = sm.tota();
+    float* partA = totA + 2 * kMaxWinA;           // [window][warp][2]
+    const int64_t myA = nA > (int64_t)blockIdx.x ? (nA - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const bool totA_fits = myA <= kMaxWinA;
+    if (totA_fits) {
+        for (int64_t k = 0; k < myA; ++k) {
+            const Piece c = decode_piece(blockIdx.x + k * gridDim.x, a);
+            if (!c.valid || c.t1 >= c.nt) continue;
+            const int h0 = 2 * c.hp;
+            const int r0 = tile_row0(c, c.t0);
+            const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
+            float s0 = 0.f, s1 = 0.f;
+            for (int l = tid; l < ntok; l += blockDim.x) {
+                const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
+                s0 += d2.x;
+                s1 += d2.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+            }
+            if (lane == 0) {
+                partA[(k * (kThreads / 32) + warp) * 2] = s0;
+                partA[(k * (kThreads / 32) + warp) * 2 + 1] = s1;
+            }
+        }
+        __syncthreads();
+        if (tid < myA) {
+            const Piece c = decode_piece(blockIdx.x + (int64_t)tid * gridDim.x, a);
+            if (c.valid && c.t1 < c.nt) {
+                float s0 = 0.f, s1 = 0.f;
+                for (int w = 0; w < kThreads / 32; ++w) {
+                    s0 += partA[(tid * (kThreads / 32) + w) * 2];
+                    s1 += partA[(tid * (kThreads / 32) + w) * 2 + 1];
+                }
+                totA[2 * tid] = s0 * __ldg(a.A + 2 * c.hp) * kLog2e;
+                totA[2 * tid + 1] = s1 * __ldg(a.A + 2 * c.hp + 1) * kLog2e;
+            }
+        }
+        __syncthreads();
+    }
+
     // ==================================================================== phase A
     if (warp == 0) {
         // producer: per window its total dt*A first (the weights are decays to the window's end), then
@@ -529,21 +610,29 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (!c.valid) break;
             if (c.t1 >= c.nt) continue;
             const int h0 = 2 * c.hp;
-            const int r0 = tile_row0(c, c.t0);
-            const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
-            float s0 = 0.f, s1 = 0.f;
+            float tot0, tot1;
+            if (totA_fits) {
+                const int64_t k = (d - blockIdx.x) / gridDim.x;
+                tot0 = totA[2 * k];
+                tot1 = totA[2 * k + 1];
+            } else {
+                const int r0 = tile_row0(c, c.t0);
+                const int ntok = tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0;
+                float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
-            for (int l = lane; l < ntok; l += 32) {
-                const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
-                s0 += d2.x;
-                s1 += d2.y;
-            }
+                for (int l = lane; l < ntok; l += 32) {
+                    const float2 d2 = *reinterpret_cast<const float2*>(a.dt + (int64_t)(r0 + l) * a.H + h0);
+                    s0 += d2.x;
+                    s1 += d2.y;
+                }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                for (int o = 16; o > 0; o >>= 1) {
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                }
+                tot0 = s0 * __ldg(a.A + h0) * kLog2e;
+                tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
             }
-            const float tot0 = s0 * __ldg(a.A + h0) * kLog2e, tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
             float carry[2] = {0.f, 0.f};
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int row0 = tile_row0(c, t), len = tile_len(c, t);
@@ -641,45 +730,63 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 
     // ==================================================================== phase B
     bool run = grid_sync(sm, a, 1);
-    if (run) {
-        // chain ch = (sequence s, head pair hp) with windows q0 .. q0 + W - 1; thread item = 4 floats of
-        // the (head, channel) x state matrix: h(w + 1) = decay(w) h(w) + agg(w), h(0) = initial state
-        constexpr int per_chain = 32 * N;         // float4 units in 128 x N
-        const int64_t nch = (int64_t)a.nseq * a.npairs;
-        for (int64_t it = (int64_t)blockIdx.x * blockDim.x + tid; it < nch * per_chain;
-             it += (int64_t)gridDim.x * blockDim.x) {
-            const int64_t ch = it / per_chain;
-            const int e4 = (int)(it % per_chain);
-            const int s = (int)(ch / a.npairs), hp = (int)(ch % a.npairs);
-            int64_t q0;
-            int W;
-            if (a.dense) {
-                W = a.W_dense;
-                q0 = ch * W;
-            } else {
-                const int32_t w0 = a.woff[s];
-                W = a.woff[s + 1] - w0;
-                q0 = (int64_t)a.npairs * w0 + (int64_t)hp * W;
-            }
-            if (W <= 1) continue;
-            const int r = e4 / (N / 4), n = 4 * (e4 % (N / 4));
-            const int hr = r >> 6, pr = r & 63;
-            float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a.init) h = *reinterpret_cast<const float4*>(a.init + (((int64_t)s * a.H + 2 * hp + hr) * 64 + pr) * N + n);
-            for (int w = 0; w + 1 < W; ++w) {
-                const float dcy = __ldcg(a.decay + (q0 + w) * 2 + hr);
-                const float4 g = __ldcg(reinterpret_cast<const float4*>(a.agg + ((q0 + w) * 128 + r) * N + n));
-                h = make_float4(fmaf(dcy, h.x, g.x), fmaf(dcy, h.y, g.y), fmaf(dcy, h.z, g.z), fmaf(dcy, h.w, g.w));
-                __stcg(reinterpret_cast<float4*>(a.incl + ((q0 + w + 1) * 128 + r) * N + n), h);
-            }
-        }
-    }
-    run = grid_sync(sm, a, 2) && run;
+    // phase C's barriers now: the producer and the MMA warp start phase C right away (its inputs do not
+    // depend on phase B), while the math warps run the scan and a second grid-wide barrier of their own
     if (tid == 0) {
         init_bars_c(sm);
         fence_mbar_init();
     }
     __syncthreads();
+    if (warp >= 2) {
+        if (run) {
+            // chain ch = (sequence s, head pair hp) with windows q0 .. q0 + W - 1; item = 4 floats of the
+            // (head, channel) x state matrix: h(w + 1) = decay(w) h(w) + agg(w), h(0) = initial state
+            constexpr int per_chain = 32 * N;     // float4 units in 128 x N
+            const int64_t nch = (int64_t)a.nseq * a.npairs;
+            for (int64_t it = (int64_t)blockIdx.x * kMathThreads + mt; it < nch * per_chain;
+                 it += (int64_t)gridDim.x * kMathThreads) {
+                const int64_t ch = it / per_chain;
+                const int e4 = (int)(it % per_chain);
+                const int s = (int)(ch / a.npairs), hp = (int)(ch % a.npairs);
+                int64_t q0;
+                int W;
+                if (a.dense) {
+                    W = a.W_dense;
+                    q0 = ch * W;
+                } else {
+                    const int32_t w0 = a.woff[s];
+                    W = a.woff[s + 1] - w0;
+                    q0 = (int64_t)a.npairs * w0 + (int64_t)hp * W;
+                }
+                if (W <= 1) continue;
+                const int r = e4 / (N / 4), n = 4 * (e4 % (N / 4));
+                const int hr = r >> 6, pr = r & 63;
+                float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (a.init) h = *reinterpret_cast<const float4*>(a.init + (((int64_t)s * a.H + 2 * hp + hr) * 64 + pr) * N + n);
+                for (int w0 = 0; w0 + 1 < W; w0 += 8) {
+                    // eight windows' loads first, then the dependent updates
+                    float dcy[8];
+                    float4 g[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (w0 + j + 1 < W) {
+                            dcy[j] = __ldcg(a.decay + (q0 + w0 + j) * 2 + hr);
+                            g[j] = __ldcg(reinterpret_cast<const float4*>(a.agg + ((q0 + w0 + j) * 128 + r) * N + n));
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (w0 + j + 1 < W) {
+                            h = make_float4(fmaf(dcy[j], h.x, g[j].x), fmaf(dcy[j], h.y, g[j].y),
+                                            fmaf(dcy[j], h.z, g[j].z), fmaf(dcy[j], h.w, g[j].w));
+                            __stcg(reinterpret_cast<float4*>(a.incl + ((q0 + w0 + j + 1) * 128 + r) * N + n), h);
+                        }
+                    }
+                }
+            }
+        }
+        run = grid_sync_math(sm, a, 2) && run;
+    }
 
     // ==================================================================== phase C
     if (run && warp == 0) {
