@@ -634,10 +634,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
             }
             float carry[2] = {0.f, 0.f};
+            float vn[2][4];                               // dt of the next tile, loaded one tile ahead
+            load_dt(tile_row0(c, c.t0), tile_len(c, c.t0), h0, vn);
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int row0 = tile_row0(c, t), len = tile_len(c, t);
                 float v[2][4], cv[2][4];
-                load_dt(row0, len, h0, v);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) v[hh][k] = vn[hh][k];
+                if (t + 1 < c.t1) load_dt(tile_row0(c, t + 1), tile_len(c, t + 1), h0, vn);
                 if ((issued >> stage) & 1u) {
                     const bool w = wait_bar(sm, kBarAFull0 + 3 + stage, ph, a);   // the stage's empty barrier
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
