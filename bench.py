@@ -37,7 +37,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
                   "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh")
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 274485760 + 209124352, "stamp": "b47e893736c61106"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 383506944 + 184075008, "stamp": "43bf900d5b6835ca"},
 }
 
 
