@@ -1,33 +1,31 @@
-// ssd_fused.cu -- single-pass fused SSD forward for bf16 (tcgen05 + TMEM + TMA),
-// one persistent CTA per SM.
+// ssd_fused.cu -- fused SSD forward for bf16 (tcgen05 + TMEM + TMA), one persistent CTA per SM,
+// launched cooperatively.
 //
-// The chunked algorithm ("LLM(十一)——Mamba" §3.5) with every intermediate kept on
-// chip except one state per piece of work:
+// The chunked algorithm ("LLM(十一)——Mamba" §3.5) over 128-token tiles, with every intermediate kept on
+// chip except one state per window of tiles:
 //
-//   * Work list: "chains" (sequence s, head pair hp), each a run of 128-token tiles in
-//     time order; the list is chain-major and cut into equal pieces, handed out
-//     round-robin to the CTAs (balanced, deterministic, no atomics).
-//   * Inside a piece the state h (rows = 2 heads x 64 channels, columns = N) is
-//     carried in TMEM from tile to tile:  h_t = exp(sum dtA over tile t) h_{t-1} + S_t.
-//   * Across pieces: decoupled look-back. A piece whose last chain continues into the
-//     next piece first computes that segment's local end state (the "right factors",
-//     chunk states B^T X, from a zero start) and publishes it with the segment's decay;
-//     a piece whose first chain started earlier combines its predecessors' published
-//     states (the "center factors", a scalar 1-SS recurrence over pieces) until it
-//     reaches an inclusive state, then publishes its own inclusive state.
-//   * Per tile (M = 128 tokens):
+//   * Work: "chains" (sequence s, head pair hp), each a run of tiles in time order, cut into windows
+//     of K tiles; windows are dispatched window-rank-major (all chains' first windows, then the second
+//     ones, ...), round-robin over the CTAs.
+//   * Phase A (right factors): every window with a successor computes its aggregate, the state at its
+//     end from a zero start, sum_t decay(t -> end) (w o X_t)^T B_t, on the tensor core (M = 2 heads x
+//     64 channels, N = state size), and the decay over it.
+//   * Phase B (center factors): a scan over each chain's windows, h(w+1) = decay(w) h(w) + agg(w) from
+//     the initial state, gives the state entering every window.
+//   * Phase C: each window's tiles in time order, the state carried in TMEM from tile to tile:
 //       G  = C B^T                      tcgen05, A = C (K-major), B = B (K-major)
-//       LG = L o G (+ D_h on the diagonal), bf16, written back over G in TMEM
-//            L_ij = exp(cs_i - cs_j) on the two 64x64 diagonal blocks,
-//            exp(cs_i - cs_63) exp(cs_63 - cs_j) on the lower-left block (no
-//            subtraction of distant cumsums), 0 above the diagonal  -- §3.5.1, §3.5.4
+//       LG = L o G (+ D_h on the diagonal), bf16, written back over G in TMEM; L_ij = exp(cs_i - cs_j)
+//            on the diagonal 32-blocks, exp(cs_i - cs_p) exp(cs_p - cs_j) (p the last token of j's
+//            32-block, both factors <= 1) left of them, 0 above -- §3.5.1, §3.5.4
 //       Yd_h = LG_h X_h                 tcgen05, A from TMEM, B = x tile (MN-major)
 //       Yo   = C h_{t-1}^T              tcgen05, both heads at once (N = 128)     -- left factors
-//       S_t  = (w o X)^T B              tcgen05, M = 2 heads x 64, N = state size -- right factors
-//       y    = Yd + exp(cs_i) Yo       (the D skip rides on the LG diagonal)
+//       S_t  = (w o X)^T B              tcgen05, accumulated onto a_t h_{t-1}     -- right factors
+//       y    = Yd + exp(cs_i) Yo       (the D skip rides on the L o G diagonal)
+//     Two C B^T buffers in TMEM alternate between tiles (a tile's buffer later takes its Yo), so the
+//     next tile's C B^T and mask overlap this tile's MMAs.
 //
-// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
-// warps 2..9 = math (masks, state updates, weights, epilogue, look-back).
+// Roles (576 threads): warp 0 = TMA producer (and the dt cumsums), warp 1 = MMA issuer (and TMEM
+// owner), warps 2..17 = math (weights, masks, state steps, epilogue, aggregates, the scan).
 // Every wait is bounded; a timeout records SSD_ERR_TIMEOUT and the CTA winds down.
 #include <cuda.h>
 #include <cuda_runtime.h>
