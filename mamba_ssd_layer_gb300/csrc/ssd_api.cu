@@ -176,7 +176,12 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
         int64_t np = 0;
         fused_plan(p, &K, &np);
         if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;
-        e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.flags(), np, varlen ? p.woff() : nullptr, K));
+        if (varlen) {
+            e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, nullptr, 0, p.woff(), K));
+        } else {
+            // a dense batch needs no tables: only the header (status, diagnostics, barrier counter) at zero
+            e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, 32, p.stream));
+        }
         if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np));
     } else {
         e = note_cuda_error("prep launch", launch_prep(p, chunk, nullptr, 0));

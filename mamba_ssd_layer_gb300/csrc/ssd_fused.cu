@@ -438,7 +438,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     // sequences without tokens: the final state is the initial state (or zero)
     if (a.final_state) {
         for (int s = blockIdx.x; s < a.nseq; s += gridDim.x) {
-            if (a.seqoff[s + 1] != a.seqoff[s]) continue;
+            if (a.dense ? a.seqlen > 0 : a.seqoff[s + 1] != a.seqoff[s]) continue;
             const int64_t n = (int64_t)a.H * 64 * N;
             for (int64_t e = tid; e < n; e += blockDim.x)
                 a.final_state[(int64_t)s * n + e] = a.init ? a.init[(int64_t)s * n + e] : 0.f;
