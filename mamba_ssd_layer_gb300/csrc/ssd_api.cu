@@ -30,7 +30,7 @@ int check_shape(const ssd_shape* s, ssd_dtype dtype, int chunk, int nseq, bool v
     if (s->nheads > 65535) return SSD_ERR_UNSUPPORTED;
     if (dtype == SSD_F32) {
         if (s->headdim > 256 || s->dstate > 256) return SSD_ERR_UNSUPPORTED;
-    } else if (!bf16_path_supports(*s, chunk)) {
+    } else if (!use_fused_path(*s, dtype)) {
         return SSD_ERR_UNSUPPORTED;
     }
     return SSD_OK;
@@ -177,17 +177,20 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
         fused_plan(p, &K, &np);
         if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;
         if (varlen) {
-            e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, nullptr, 0, p.woff(), K));
+            e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.woff(), K));
         } else {
             // a dense batch needs no tables: only the header (status, diagnostics, barrier counter) at zero
             e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, 32, p.stream));
         }
-        if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np));
+        if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np, 0));
+        if (e == cudaSuccess && p.s.dstate > 128) {
+            // second half of the state columns: only the grid-barrier counter starts over
+            e = note_cuda_error("header reset", cudaMemsetAsync(p.status() + 4, 0, 8, p.stream));
+            if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np, 1));
+        }
     } else {
-        e = note_cuda_error("prep launch", launch_prep(p, chunk, nullptr, 0));
-        if (e == cudaSuccess)
-            e = note_cuda_error(dtype == SSD_F32 ? "fp32 launch" : "bf16 launch",
-                                (dtype == SSD_F32) ? launch_f32_path(p) : launch_bf16_path(p));
+        e = note_cuda_error("prep launch", launch_prep(p, chunk));
+        if (e == cudaSuccess) e = note_cuda_error("fp32 launch", launch_f32_path(p));
     }
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }

@@ -25,14 +25,12 @@ namespace ssd {
 __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ cu, int64_t nseq,
                                                     int64_t seqlen, int64_t rows, int Q,
                                                     int* header, ChunkDesc* chunks, int32_t* seqoff,
-                                                    int64_t max_chunks, int* flags, int64_t nflags,
-                                                    int32_t* woff, int K) {
+                                                    int64_t max_chunks, int32_t* woff, int K) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     __shared__ int bad;
     const int tid = threadIdx.x;
     if (tid == 0) { carry = 0; bad = 0; }
-    for (int64_t i = tid; i < nflags; i += blockDim.x) flags[i] = 0;
     __syncthreads();
     // pass 1: validate
     for (int64_t s = tid; s < nseq; s += blockDim.x) {
@@ -139,11 +137,10 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
     }
 }
 
-cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags, int32_t* woff, int K) {
+cudaError_t launch_prep(const Problem& p, int q, int32_t* woff, int K) {
     prof_launch();
     prep_kernel<<<1, 1024, 0, p.stream>>>(p.varlen ? p.cu_seqlens : nullptr, p.nseq, p.s.seqlen, p.rows,
-                                          q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks, flags, nflags,
-                                          woff, K);
+                                          q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks, woff, K);
     return cudaGetLastError();
 }
 

@@ -69,8 +69,7 @@ struct FusedArgs {
     const float* init;
     float* final_state;
     __nv_bfloat16* y;
-    int* flags;                 // per piece: 0 none, 1 aggregate, 2 inclusive
-    float* decay;               // per piece: [2] per-head decay of the published segment
+    float* decay;               // per piece: [2] per-head decay of the window
     float* agg;                 // per piece: [128][N]
     float* incl;                // per piece: [128][N]
     const int32_t* woff;        // packed batch: first window of each sequence
@@ -81,6 +80,10 @@ struct FusedArgs {
     int64_t seqlen;             // dense: tokens per sequence
     int nt_dense;               // dense: tiles per sequence
     int W_dense;                // dense: windows per sequence
+    // Split state: this launch covers state columns [n_off, n_off + N) of n_full (B, C, the initial
+    // and final states); with y_accum its y is added onto the y already there (the other columns'
+    // share), and D is left to the first launch.
+    int n_off, n_full, y_accum;
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -439,9 +442,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     if (a.final_state) {
         for (int s = blockIdx.x; s < a.nseq; s += gridDim.x) {
             if (a.dense ? a.seqlen > 0 : a.seqoff[s + 1] != a.seqoff[s]) continue;
-            const int64_t n = (int64_t)a.H * 64 * N;
-            for (int64_t e = tid; e < n; e += blockDim.x)
-                a.final_state[(int64_t)s * n + e] = a.init ? a.init[(int64_t)s * n + e] : 0.f;
+            const int64_t n = (int64_t)a.H * 64 * N;       // (head, channel) rows x this launch's columns
+            for (int64_t e = tid; e < n; e += blockDim.x) {
+                const int64_t g = ((int64_t)s * a.H * 64 + e / N) * a.n_full + a.n_off + e % N;
+                a.final_state[g] = a.init ? a.init[g] : 0.f;
+            }
         }
     }
     const int64_t np = a.npieces;
@@ -766,7 +771,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 const int r = e4 / (N / 4), n = 4 * (e4 % (N / 4));
                 const int hr = r >> 6, pr = r & 63;
                 float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (a.init) h = *reinterpret_cast<const float4*>(a.init + (((int64_t)s * a.H + 2 * hp + hr) * 64 + pr) * N + n);
+                if (a.init)
+                    h = *reinterpret_cast<const float4*>(a.init + (((int64_t)s * a.H + 2 * hp + hr) * 64 + pr) * a.n_full + a.n_off + n);
                 for (int w0 = 0; w0 + 1 < W; w0 += 8) {
                     // eight windows' loads first, then the dependent updates
                     float dcy[8];
@@ -1108,8 +1114,20 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             for (int pass = 0; pass < 4; ++pass) {
                 const int r = 32 * qd + 8 * pass + (lane >> 2);
                 if (r < len) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
-                    *reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl) = v;
+                    uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
+                    uint4* dst = reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl);
+                    if (a.y_accum) {
+                        // add onto the other state columns' share, in fp32
+                        const uint4 o = *dst;
+                        const uint32_t* ov = reinterpret_cast<const uint32_t*>(&o);
+                        uint32_t* nv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 f = __fadd2_rn(unpack_bf16x2(nv[m]), unpack_bf16x2(ov[m]));
+                            nv[m] = pack_bf16x2(f.x, f.y);
+                        }
+                    }
+                    *dst = v;
                 }
             }
             __syncwarp();
@@ -1132,7 +1150,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             // chain's start, else the scan's result
             {
                 const float* src = c.w == 0
-                    ? (a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0 : nullptr)
+                    ? (a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * a.n_full + a.n_off + nq0 : nullptr)
                     : a.incl + (c.q * 128 + row) * N + nq0;
                 float v[NQ];
 #pragma unroll
@@ -1187,7 +1205,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (!ok) break;
             tc_fence_after_sync();
             if (c.t1 == c.nt && a.final_state) {
-                float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * N + nq0;
+                float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * a.n_full + a.n_off + nq0;
                 float v[NQ];
                 st_load(nq0, NQ, v);
 #pragma unroll
@@ -1211,7 +1229,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64_t rows) {
+// 3-D view (inner, mid, rows) of a bf16 tensor whose mid and row strides are mid_stride and row_stride
+// elements (inner is contiguous), boxes of 64 x 1 x 128 with the 128-byte swizzle
+bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64_t rows, int64_t mid_stride,
+                    int64_t row_stride) {
     static EncodeTiledFn enc = nullptr;
     if (!enc) {
         void* fp = nullptr;
@@ -1222,7 +1243,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
         enc = reinterpret_cast<EncodeTiledFn>(fp);
     }
     cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)(rows > 0 ? rows : 1)};
-    cuuint64_t strides[2] = {(cuuint64_t)(inner * 2), (cuuint64_t)(inner * mid * 2)};
+    cuuint64_t strides[2] = {(cuuint64_t)(mid_stride * 2), (cuuint64_t)(row_stride * 2)};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -1292,12 +1313,16 @@ void fused_plan(const Problem& p, int* K_out, int64_t* np_out) {
     }
 }
 
-cudaError_t launch_fused(const Problem& p, int K, int64_t np) {
-    const int H = (int)p.s.nheads, N = (int)p.s.dstate, G = (int)p.s.ngroups;
+cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
+    const int H = (int)p.s.nheads, Nf = (int)p.s.dstate, G = (int)p.s.ngroups;
+    const int N = Nf > 128 ? 128 : Nf;            // state columns per launch
     const int64_t npairs = H / 2;
     FusedMaps maps;
-    if (!make_map_fused(&maps.x, p.x, 64, H, p.rows) || !make_map_fused(&maps.b, p.B, N, G, p.rows) ||
-        !make_map_fused(&maps.c, p.C, N, G, p.rows))
+    const __nv_bfloat16* Bp = static_cast<const __nv_bfloat16*>(p.B) + (int64_t)part * N;
+    const __nv_bfloat16* Cp = static_cast<const __nv_bfloat16*>(p.C) + (int64_t)part * N;
+    if (!make_map_fused(&maps.x, p.x, 64, H, p.rows, 64, (int64_t)64 * H) ||
+        !make_map_fused(&maps.b, Bp, N, G, p.rows, Nf, (int64_t)Nf * G) ||
+        !make_map_fused(&maps.c, Cp, N, G, p.rows, Nf, (int64_t)Nf * G))
         return note_cuda_error("fused tensor maps", cudaErrorInvalidValue);
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
     FusedArgs fa;
@@ -1308,11 +1333,10 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np) {
     fa.woff = p.varlen ? p.woff() : nullptr;
     fa.dt = p.dt;
     fa.A = p.A;
-    fa.D = p.D;
+    fa.D = part == 0 ? p.D : nullptr;
     fa.init = p.init;
     fa.final_state = p.final_state;
     fa.y = (__nv_bfloat16*)p.y;
-    fa.flags = p.flags();
     fa.decay = reinterpret_cast<float*>(p.ws + p.L.pdecay);
     fa.agg = reinterpret_cast<float*>(p.ws + p.L.agg);
     fa.incl = reinterpret_cast<float*>(p.ws + p.L.incl);
@@ -1326,6 +1350,9 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np) {
     fa.seqlen = p.s.seqlen;
     fa.nt_dense = (int)((p.s.seqlen + kFusedTile - 1) / kFusedTile);
     fa.W_dense = (fa.nt_dense + K - 1) / K;
+    fa.n_off = part * N;
+    fa.n_full = Nf;
+    fa.y_accum = part > 0 ? 1 : 0;
     cudaError_t e;
     prof_begin(p.stream, "ssd_fused_kernel");
     e = (N == 64) ? launch_fused_n<64>(p, fa, maps, grid) : launch_fused_n<128>(p, fa, maps, grid);

@@ -21,31 +21,34 @@ struct ChunkDesc {
 //             batch, fused path), int32 grid-barrier arrival counter (fused path), int32 spare
 //   chunks  : ChunkDesc[max_chunks]  (chunks of `chunk` tokens; 128-token tiles on the fused path)
 //   seqoff  : int32[nseq + 1], first chunk of every sequence
-// three-kernel path:
+// fp32 path (three kernels):
 //   decay   : float[max_chunks * H], exp(sum of dt*A over the chunk)
 //   states  : float[max_chunks * H * P * N]; the chunk-state kernel writes each chunk's
 //             local end state here and the state pass overwrites it in place with the
 //             true state entering the chunk
-// fused path (bf16, P = 64, N <= 128):
-//   flags   : int32[max_pieces]  0 = nothing published, 1 = aggregate, 2 = inclusive state
-//   pdecay  : float[max_pieces * 2], decay of each piece's published segment per head
-//   agg     : float[max_pieces * 128 * N], local end state of the piece's last segment
-//   incl    : float[max_pieces * 128 * N], true end state of that segment
+// fused path (bf16, P = 64, N in {64, 128, 256}; 128 state columns per launch):
+//   woff    : int32[nseq + 1], first window of every sequence (packed batch)
+//   pdecay  : float[max_pieces * 2], decay of each window over its tiles, per head of the pair
+//   agg     : float[max_pieces * 128 * Nl], the window's end state from a zero entering state
+//   incl    : float[max_pieces * 128 * Nl], the true state entering the window
+//   (Nl = min(N, 128), the state columns of one launch)
 constexpr int kFusedTile = 128;
 constexpr int kFusedMaxGrid = 256;
 constexpr int kFusedMinWindow = 4;    // tiles per piece, lower bound (bounds the workspace)
 constexpr int kFusedMaxWindow = 16;
 
 struct WsLayout {
-    size_t header, chunks, seqoff, woff, decay, states, flags, pdecay, agg, incl, total;
+    size_t header, chunks, seqoff, woff, decay, states, pdecay, agg, incl, total;
     int64_t max_chunks, nseq, max_pieces;
     bool fused;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// The fused kernel holds up to 128 state columns; N = 256 runs as two launches over the two column
+// halves (the state columns evolve independently and add up in y).
 inline bool use_fused_path(const ssd_shape& s, ssd_dtype dtype) {
-    return dtype == SSD_BF16 && s.headdim == 64 && (s.dstate == 64 || s.dstate == 128) &&
+    return dtype == SSD_BF16 && s.headdim == 64 && (s.dstate == 64 || s.dstate == 128 || s.dstate == 256) &&
            ((s.nheads / s.ngroups) % 2 == 0);
 }
 
@@ -68,11 +71,11 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
         const int64_t per_seq = varlen ? ((w.max_chunks - nseq_eff) + kFusedMinWindow - 1) / kFusedMinWindow + nseq_eff
                                        : s.batch * ((((s.seqlen + q - 1) / q) + kFusedMinWindow - 1) / kFusedMinWindow);
         w.max_pieces = (s.nheads / 2) * (per_seq > 0 ? per_seq : 1);
+        const int64_t ncol = s.dstate > 128 ? 128 : s.dstate;   // state columns of one launch
         w.woff = off;   off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
-        w.flags = off;  off = align256(off + sizeof(int32_t) * (size_t)w.max_pieces);
         w.pdecay = off; off = align256(off + sizeof(float) * 2 * (size_t)w.max_pieces);
-        w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * s.dstate));
-        w.incl = off;   off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * s.dstate));
+        w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
+        w.incl = off;   off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
     } else {
         w.decay = off;  off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads));
         w.states = off; off = align256(off + sizeof(float) * (size_t)(w.max_chunks * s.nheads * s.headdim * s.dstate));
@@ -110,7 +113,6 @@ struct Problem {
     int32_t* seqoff() const { return reinterpret_cast<int32_t*>(ws + L.seqoff); }
     float* decay() const { return reinterpret_cast<float*>(ws + L.decay); }
     float* states() const { return reinterpret_cast<float*>(ws + L.states); }
-    int* flags() const { return reinterpret_cast<int*>(ws + L.flags); }
     int32_t* woff() const { return reinterpret_cast<int32_t*>(ws + L.woff); }
 };
 
@@ -123,18 +125,16 @@ void prof_launch();
 void prof_begin(cudaStream_t s, const char* kernel);
 void prof_end(cudaStream_t s);
 
-// ssd_common.cu: chunk (tile) table of `q` tokens; zeroes `nflags` piece flags; with woff,
-// also the per-sequence offsets of windows of K chunks
-cudaError_t launch_prep(const Problem& p, int q, int* flags, int64_t nflags, int32_t* woff = nullptr, int K = 1);
+// ssd_common.cu: chunk (tile) table of `q` tokens; with woff, also the per-sequence offsets of
+// windows of K chunks
+cudaError_t launch_prep(const Problem& p, int q, int32_t* woff = nullptr, int K = 1);
 cudaError_t launch_state_pass(const Problem& p);
 // ssd_f32.cu
 cudaError_t launch_f32_path(const Problem& p);
-// ssd_tc.cu (three-kernel tcgen05 path)
-cudaError_t launch_bf16_path(const Problem& p);
-bool bf16_path_supports(const ssd_shape& s, int chunk);
 // ssd_fused.cu (single-pass tcgen05 path): the window size K (tiles per piece) and the number of
 // pieces (exact for a dense batch, an upper bound for a packed batch)
 void fused_plan(const Problem& p, int* K, int64_t* npieces);
-cudaError_t launch_fused(const Problem& p, int K, int64_t npieces);
+// part: which 128-column half of an N = 256 state (0 for N <= 128)
+cudaError_t launch_fused(const Problem& p, int K, int64_t npieces, int part);
 
 }  // namespace ssd

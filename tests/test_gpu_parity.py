@@ -69,32 +69,55 @@ def test_bf16_short_and_boundary_lengths(T):
     check(make_inputs(w), "bf16", 256)
 
 
-@pytest.mark.parametrize("T,H,batch", [(8192, 2, 1), (3000, 4, 3), (20000, 2, 1)])
-def test_bf16_long_chains_few_heads(T, H, batch):
-    # few head pairs and long sequences: many pieces per chain, deep look-back
-    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=T, nheads=H, batch=batch).with_(seed=99 + T)
+@pytest.mark.parametrize("T,H,batch,N", [(8192, 2, 1, 128), (3000, 4, 3, 128), (20000, 2, 1, 128),
+                                         (8192, 2, 1, 256), (3000, 4, 3, 64)])
+def test_bf16_long_chains_few_heads(T, H, batch, N):
+    # few head pairs and long sequences: many windows per chain, a deep cross-window scan
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=T, nheads=H, batch=batch).with_(dstate=N, seed=99 + T + N)
     check(make_inputs(w), "bf16", 256)
 
 
-def test_bf16_deterministic():
-    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=5000, nheads=4, batch=1).with_(seed=101)
+@pytest.mark.parametrize("N", [128, 256])
+def test_bf16_deterministic(N):
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=5000, nheads=4, batch=1).with_(dstate=N, seed=101)
     d = make_inputs(w)
     y1, f1 = run_gpu(d, "bf16", 256)
     y2, f2 = run_gpu(d, "bf16", 256)
     assert np.array_equal(y1, y2) and np.array_equal(f1, f2)
 
 
-def test_bf16_grouped_heads():
-    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=600, nheads=8, batch=1).with_(ngroups=2, seed=94)
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_bf16_grouped_heads(N):
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=600, nheads=8, batch=1).with_(ngroups=2, dstate=N, seed=94)
     check(make_inputs(w), "bf16", 128)
 
 
-def test_bf16_varlen_small():
+@pytest.mark.parametrize("N", [128, 256])
+def test_bf16_varlen_small(N):
     w = small_variant(WORKLOADS["varlen"], seqlen=3000, nheads=4).with_(seg_min=1, seg_max=700, seed=95,
-                                                                      init_state=True)
+                                                                      init_state=True, dstate=N)
     d = make_inputs(w)
     assert len(d["cu_seqlens"]) > 4
     check(d, "bf16", 256)
+
+
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_bf16_varlen_empty_segments(N):
+    # zero-length segments first, between others and last: their final state is their initial state
+    w = small_variant(WORKLOADS["varlen"], seqlen=2500, nheads=4).with_(seg_min=100, seg_max=900, seed=102,
+                                                                      dstate=N)
+    d = make_inputs(w)
+    cu = [int(v) for v in d["cu_seqlens"]]
+    cu = [0, 0] + cu[1:2] + cu[1:-1] + cu[-1:] + cu[-1:]
+    d["cu_seqlens"] = np.asarray(cu, dtype=np.int32)
+    nseq = len(cu) - 1
+    rng = np.random.Generator(np.random.PCG64(103 + N))
+    d["initial_state"] = rng.standard_normal((nseq, 4, 64, N), dtype=np.float32) * np.float32(0.1)
+    ey, ef = check(d, "bf16", 256)
+    _, f = run_gpu(d, "bf16", 256)
+    for s in range(nseq):
+        if cu[s + 1] == cu[s]:
+            assert np.array_equal(f[s], d["initial_state"][s].astype(np.float64))
 
 
 def test_fp32_varlen_small():
@@ -104,10 +127,11 @@ def test_fp32_varlen_small():
     check(make_inputs(w), "f32", 64)
 
 
-def test_empty_sequence():
+@pytest.mark.parametrize("N", [128, 256])
+def test_empty_sequence(N):
     import torch
     from mamba_ssd_layer_gb300 import ssd_forward
-    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=0, nheads=2, batch=2).with_(seed=97)
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=0, nheads=2, batch=2).with_(seed=97, dstate=N)
     d = make_inputs(w)
     from ssd_util import to_device
     t = to_device(d, "bf16")
