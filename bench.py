@@ -37,7 +37,9 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
                   "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh")
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 383506944 + 184075008, "stamp": "d96214211e3fd119"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 383702016 + 184512256, "stamp": "a5949564e981254b"},
+    # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 467646848 + 182264832, "stamp": "a5949564e981254b"},
 }
 
 
