@@ -13,6 +13,8 @@ Two independent formulations live here:
 * :func:`ssd_quadratic` (``quadratic.py``) -- the dual "attention" form
   ``Y = (L o C B^T) X + D X`` with the 1-semiseparable mask materialised as a
   T x T matrix, in numpy. It is used to pin the recurrence on tiny inputs.
+* :func:`ssd_decode_step` (``decode.py``) -- one token of the recurrence on a
+  batch of carried states (the recurrent inference step), in numpy fp64.
 
 The C file is compiled with the system ``gcc`` into ``oracle/_build`` the first
 time it is needed (or by ``__graft_entry__.build()``).
@@ -26,6 +28,7 @@ import threading
 
 import numpy as np
 
+from .decode import ssd_decode_step  # noqa: F401
 from .quadratic import ssd_quadratic  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
