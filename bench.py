@@ -28,26 +28,32 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "SSD fwd tokens/s and % of bf16 tensor/HBM roofline, T=2K–16K, N=128"
+DECODE_METRIC = "SSD recurrent step tokens/s (one token per carried state) and % of HBM roofline"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
 # workload, with a stamp of the kernel's sources at capture time. A stamp that no longer
 # matches the sources means the kernel changed since: the traffic is then reported as null.
-KERNEL_SOURCES = ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
-                  "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh")
+KERNEL_SOURCES = {
+    "ssd_fused_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
+                         "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh"),
+    "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
+}
 NCU_TRAFFIC = {
     "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 383702016 + 184512256, "stamp": "a5949564e981254b"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
     "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 467646848 + 182264832, "stamp": "a5949564e981254b"},
+    # recurrent step: part of the state's write-back is still in L2 when the launch ends
+    "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168504320 + 118605312, "stamp": "8b053c3cd6121ef8"},
 }
 
 
-def kernel_source_stamp() -> str:
+def kernel_source_stamp(kernel: str = "ssd_fused_kernel") -> str:
     """Hash of the kernel's code: comments and blank lines are left out, so that only a change of the
     code itself invalidates a recorded measurement."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             for line in f:
                 code = line.split("//", 1)[0].strip()
@@ -58,7 +64,7 @@ def kernel_source_stamp() -> str:
 
 def measured_traffic(workload: str, kernel: str):
     rec = NCU_TRAFFIC.get(workload)
-    if rec is None or rec["kernel"] != kernel or rec["stamp"] != kernel_source_stamp():
+    if rec is None or rec["kernel"] != kernel or rec["stamp"] != kernel_source_stamp(kernel):
         return None
     return rec["bytes"]
 
@@ -93,6 +99,14 @@ def algorithmic_bytes(w, batch_rows, nseq) -> int:
     by = 2 * T * H * P * e + 2 * T * G * N * e + 4 * T * H + 8 * H
     by += nseq * H * P * N * 4 * (2 if w.init_state else 1)
     return int(by)
+
+
+def decode_algorithmic_bytes(w) -> int:
+    """Bytes one recurrent step must move: the fp32 state in and out, x in and y out, B and C,
+    dt, A and D."""
+    b, H, P, N, G = w.batch, w.nheads, w.headdim, w.dstate, w.ngroups
+    e = 2 if w.dtype == "bf16" else 4
+    return int(2 * b * H * P * N * 4 + 2 * b * H * P * e + 2 * b * G * N * e + 4 * b * H + 8 * H)
 
 
 def algorithmic_flops(w, batch_rows) -> int:
@@ -172,12 +186,170 @@ def dist_setup():
     return world, rank, local
 
 
+def decode_sample(w, rows: int):
+    """The first `rows` carried states of a recurrent-step workload, as (state, x, dt, A, B, C, D)."""
+    from mamba_ssd_layer_gb300.inputs import make_inputs
+    d = make_inputs(w)
+    r = slice(0, min(rows, w.batch))
+    return (d["initial_state"][r], d["x"][r, 0], d["dt"][r, 0], d["A"], d["B"][r, 0], d["C"][r, 0], d["D"])
+
+
+def run_reference_decode(args, w):
+    """The oracle's recurrent step on the host, bounded: each step runs a sample of the carried states."""
+    import oracle
+    rows = max(1, min(w.batch, args.ref_tokens // 1024))
+    smp = decode_sample(w, rows)
+    oracle.ssd_decode_step(*smp)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.ssd_decode_step(*smp)
+        times.append(time.perf_counter() - t0)
+    tot = float(np.sum(times))
+    val = rows * args.steps / tot
+    sample = f"{rows} of {w.batch} carried states, all {w.nheads} heads, per step"
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": decode_config(w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def decode_config(w):
+    return {"workload": w.name, "batch": w.batch, "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
+            "ngroups": w.ngroups, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (two fp32 state buffers of ~168 MB each, read and written in turn)"}
+
+
+def decode_cpu_baseline(w, min_seconds: float = 10.0, max_runs: int = 5000):
+    """The oracle's recurrent step as it stands (numpy, one core), on 8 of the carried states,
+    repeated for about `min_seconds`."""
+    import oracle
+    rows = min(8, w.batch)
+    smp = decode_sample(w, rows)
+    runs, t0 = 0, time.perf_counter()
+    while runs < max_runs and (runs == 0 or time.perf_counter() - t0 < min_seconds):
+        oracle.ssd_decode_step(*smp)
+        runs += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows * runs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.batch} carried states (all {w.nheads} heads), {runs} runs in {dt:.1f} s"}
+
+
+def run_decode(args, w):
+    """Recurrent steps on the GPU: each step advances every carried state by one token."""
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from mamba_ssd_layer_gb300 import binding as bd
+    from mamba_ssd_layer_gb300 import ssd_decode_step, ssd_decode_step_host
+    from mamba_ssd_layer_gb300.inputs import make_inputs
+
+    d = make_inputs(w)
+    host = {"x": d["x"][:, 0], "dt": d["dt"][:, 0], "A": d["A"], "B": d["B"][:, 0], "C": d["C"][:, 0], "D": d["D"],
+            "state": d["initial_state"]}
+    t = {k: torch.from_numpy(np.ascontiguousarray(host[k])).to(dev, torch.bfloat16) for k in ("x", "B", "C")}
+    for k in ("dt", "A", "D"):
+        t[k] = torch.from_numpy(np.ascontiguousarray(host[k])).to(dev, torch.float32)
+    states = [torch.from_numpy(host["state"]).to(dev), torch.empty_like(torch.from_numpy(host["state"]), device=dev)]
+    y = torch.empty_like(t["x"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        ssd_decode_step(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], states[i % 2], states[(i + 1) % 2], y,
+                        stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    bd.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        wall0 = time.time()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.time()
+    bd.profile_enable(False)
+    kern_ms, kern_n = bd.profile_read()
+    launches = bd.profile_kernel_launches()
+    kernel = bd.profile_kernel_name()
+    ms = ev0.elapsed_time(ev1)
+    ms, value = reduce_over_ranks(ms, w.batch, args.steps, world, dev)
+    ms_per_step = ms / args.steps
+
+    # end to end through the host entry point: pinned inputs and state in, y and the state out
+    hx = {k: torch.from_numpy(np.ascontiguousarray(host[k])).to(torch.bfloat16).pin_memory() for k in ("x", "B", "C")}
+    hf = {k: torch.from_numpy(np.ascontiguousarray(host[k])).pin_memory() for k in ("dt", "A", "D", "state")}
+    hy = torch.empty_like(hx["x"]).pin_memory()
+    devbuf = torch.empty(int(bd.load_library().ssd_decode_host_buffer_size(
+        bd._shape(w.batch, 1, w.nheads, w.headdim, w.dstate, w.ngroups), bd.SSD_BF16)), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        ssd_decode_step_host(hx["x"], hf["dt"], hf["A"], hx["B"], hx["C"], hf["D"], hf["state"], hf["state"], hy,
+                             device_buffer=devbuf, stream=stream)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    h2d = sum(v.numel() * v.element_size() for v in list(hx.values()) + list(hf.values()))
+    d2h = hy.numel() * 2 + hf["state"].numel() * 4
+
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    alg_bytes = decode_algorithmic_bytes(w)
+    kern_avg_ms = kern_ms / max(kern_n, 1)
+    achieved = alg_bytes / (kern_avg_ms / 1e3) / 1e9 if kern_n else None
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": decode_config(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": measured_traffic(w.name, kernel), "peak_source": src, "kernel": kernel,
+                     "kernel_ms": kern_avg_ms, "alg_bytes_per_launch": alg_bytes, "launches_per_step": 1.0,
+                     "step_frac": alg_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
+        "e2e": {"value": world * w.batch * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(wall0, wall1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_reference(args, w):
     """The oracle on the host cores, bounded: each step runs a sample of the workload."""
     import oracle
     from mamba_ssd_layer_gb300.inputs import make_inputs, small_variant
     world, rank, _ = dist_setup()
     if rank != 0:
+        return
+    if w.seqlen == 1:
+        run_reference_decode(args, w)
         return
     # sample: every head, the first `tokens` tokens of the sequence (~several seconds per step)
     tokens = min(w.seqlen, args.ref_tokens)
@@ -245,6 +417,9 @@ def main():
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+        return
+    if w.seqlen == 1:
+        run_decode(args, w)
         return
 
     import torch

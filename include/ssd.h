@@ -147,6 +147,50 @@ int ssd_forward_noalloc(const ssd_shape *shape, ssd_dtype dtype,
                         void *stream);
 
 /*
+ * One token of the recurrence on a batch of carried states: the recurrent (autoregressive
+ * inference) step of the same layer ("Transformers是SSMs (一)" §2.1; "LLM(十一)——Mamba"
+ * §3.1.1-3.1.2, with its per-token cost in §3.5.3; "Mamba-2 状态空间对偶性理论" §1.2):
+ *
+ *   for every row b and head h (group g = h / (H/G)):
+ *     a = exp(dt[b,h] * A[h])
+ *     new_state[b,h] = a * state[b,h] + x[b,h,:] (outer) B[b,g,:]
+ *     y[b,h,:]       = new_state[b,h] . C[b,g,:] + D[h] * x[b,h,:]
+ *
+ * shape->seqlen must be 1 (one token per row); batch is the number of carried states.
+ *   x             (batch, 1, H, P)  dtype
+ *   dt            (batch, 1, H)     fp32
+ *   A             (H)               fp32
+ *   B, C          (batch, 1, G, N)  dtype
+ *   D             (H) fp32, or NULL for no skip term
+ *   state         (batch, H, P, N)  fp32, read
+ *   new_state     (batch, H, P, N)  fp32, written; it may be `state` itself (update in place) but
+ *                 must not overlap it otherwise
+ *   y             (batch, 1, H, P)  dtype, written
+ * All pointers are DEVICE pointers; state, new_state, B and C 16-byte aligned. Supported sizes:
+ * P <= 256, N <= 256 with N % 4 == 0, either dtype. No workspace; nothing is synchronised; the
+ * same error codes as ssd_forward (nothing is launched when a check fails). batch == 0 is a no-op.
+ */
+int ssd_decode_step(const ssd_shape *shape, ssd_dtype dtype,
+                    const void *x, const float *dt, const float *A,
+                    const void *B, const void *C, const float *D,
+                    const float *state, float *new_state, void *y,
+                    void *stream);
+
+/*
+ * The same step on HOST buffers: copies the inputs and the state into `device_buffer` (at least
+ * ssd_decode_host_buffer_size bytes, 256-byte aligned), runs ssd_decode_step there in place, copies
+ * y and the new state back and synchronises `stream`. new_state may be the host `state` buffer.
+ * ssd_decode_host_buffer_size returns 0 for invalid or unsupported shapes.
+ */
+size_t ssd_decode_host_buffer_size(const ssd_shape *shape, ssd_dtype dtype);
+int ssd_decode_step_host(const ssd_shape *shape, ssd_dtype dtype,
+                         const void *x, const float *dt, const float *A,
+                         const void *B, const void *C, const float *D,
+                         const float *state, float *new_state, void *y,
+                         void *device_buffer, size_t device_buffer_bytes,
+                         void *stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last ssd_forward that used it (SSD_OK or SSD_ERR_TIMEOUT),
  * or SSD_ERR_CUDA if the copy itself fails.

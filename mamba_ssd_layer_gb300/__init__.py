@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) SSD layer forward: C-ABI library + thin Python binding.
+"""GB300 (sm_103a) SSD layer forward and recurrent step: C-ABI library + thin Python binding.
 
 ``ssd_forward`` and friends are resolved lazily so that importing
 ``mamba_ssd_layer_gb300.inputs`` does not load the CUDA library.
@@ -6,7 +6,8 @@
 from __future__ import annotations
 
 __all__ = ["ssd_forward", "ssd_forward_host", "ssd_workspace_size", "ssd_status",
-           "ssd_status_string", "library_path", "SSDError", "profile_enable", "profile_read"]
+           "ssd_status_string", "library_path", "SSDError", "profile_enable", "profile_read",
+           "ssd_decode_step", "ssd_decode_step_host"]
 
 
 def __getattr__(name):

@@ -59,6 +59,13 @@ def load_library():
     lib.ssd_forward.restype = i32
     lib.ssd_forward_host.argtypes = fwd_args
     lib.ssd_forward_host.restype = i32
+    dec_args = [shp, i32, vp, fp, fp, vp, vp, fp, fp, fp, vp, vp]
+    lib.ssd_decode_step.argtypes = dec_args
+    lib.ssd_decode_step.restype = i32
+    lib.ssd_decode_host_buffer_size.argtypes = [shp, i32]
+    lib.ssd_decode_host_buffer_size.restype = sz
+    lib.ssd_decode_step_host.argtypes = dec_args[:-1] + [vp, sz, vp]
+    lib.ssd_decode_step_host.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
     lib.ssd_profile_enable.argtypes = [i32]
@@ -213,8 +220,86 @@ def ssd_forward_host(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=Non
     return y, (final_state if return_final_state else None)
 
 
+def _decode_shapes(x, B):
+    batch, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    return batch, H, P, G, N
+
+
+def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, stream=None):
+    """One recurrent step on CUDA tensors through ``ssd_decode_step``.
+
+    x (batch, H, P) and B, C (batch, G, N) in float32 or bfloat16 (the same); dt (batch, H),
+    A (H,), D (H,) or None, state (batch, H, P, N): float32. new_state defaults to ``state``
+    (updated in place); pass another tensor to keep ``state``. Returns (y, new_state); the work
+    is enqueued on `stream` (default: torch's current stream) and nothing is synchronised.
+    """
+    import torch
+    batch, H, P, G, N = _decode_shapes(x, B)
+    dev = x.device
+    code = _dtype_code(x)
+    _check(x, "x", (batch, H, P), x.dtype, dev)
+    _check(dt, "dt", (batch, H), torch.float32, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(B, "B", (batch, G, N), x.dtype, dev)
+    _check(C, "C", (batch, G, N), x.dtype, dev)
+    _check(D, "D", (H,), torch.float32, dev)
+    if state is None:
+        raise ValueError("state is required")
+    _check(state, "state", (batch, H, P, N), torch.float32, dev)
+    if new_state is None:
+        new_state = state
+    _check(new_state, "new_state", (batch, H, P, N), torch.float32, dev)
+    if y is None:
+        y = torch.empty_like(x)
+    _check(y, "y", (batch, H, P), x.dtype, dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = load_library().ssd_decode_step(ctypes.byref(_shape(batch, 1, H, P, N, G)), code, _ptr(x), _ptr(dt),
+                                        _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(new_state), _ptr(y),
+                                        ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_decode_step")
+    return y, new_state
+
+
+def ssd_decode_step_host(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, device_buffer=None,
+                         stream=None):
+    """The same step on HOST (CPU, ideally pinned) tensors through ``ssd_decode_step_host``: the
+    copies in, the kernel and the copies out all happen inside the C call, which synchronises."""
+    import torch
+    batch, H, P, G, N = _decode_shapes(x, B)
+    code = _dtype_code(x)
+    cpu = torch.device("cpu")
+    if state is None:
+        raise ValueError("state is required")
+    for t, name in ((x, "x"), (dt, "dt"), (A, "A"), (B, "B"), (C, "C"), (D, "D"), (state, "state")):
+        if t is not None and (t.device != cpu or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    if new_state is None:
+        new_state = state
+    if y is None:
+        y = torch.empty_like(x)
+    shape = _shape(batch, 1, H, P, N, G)
+    lib = load_library()
+    need = int(lib.ssd_decode_host_buffer_size(ctypes.byref(shape), code))
+    if need == 0:
+        raise SSDError(SSD_ERR_UNSUPPORTED, "ssd_decode_host_buffer_size")
+    if device_buffer is None or device_buffer.numel() < need:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(device_buffer.device)
+    rc = lib.ssd_decode_step_host(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                  _ptr(state), _ptr(new_state), _ptr(y), device_buffer.data_ptr(), need,
+                                  ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_decode_step_host")
+    return y, new_state
+
+
 def profile_enable(on: bool = True) -> None:
-    """Record CUDA events around the dominant kernel of every later ssd_forward on this thread."""
+    """Record CUDA events around the dominant kernel of every later ssd_forward or ssd_decode_step on
+    this thread."""
     load_library().ssd_profile_enable(1 if on else 0)
 
 

@@ -1,0 +1,282 @@
+// ssd_decode.cu -- the one-token recurrent step of the SSD layer on a batch of carried states:
+//
+//   for every row b and head h (group g = h / (H/G)):
+//     a       = exp(dt[b,h] * A[h])
+//     S[b,h]  = a * S[b,h] + x[b,h,:] (outer) B[b,g,:]          (P x N, fp32)
+//     y[b,h,:] = S[b,h] . C[b,g,:] + D[h] * x[b,h,:]
+//
+// This is the recurrent (autoregressive inference) mode of the selective SSM with a scalar A
+// ("Transformers是SSMs：通过结构化状态空间对偶性的广义模型和高效算法(一)" §2.1; "LLM(十一)——Mamba"
+// §3.1.1-3.1.2, and §3.5.3 for its per-token cost; "Mamba-2 状态空间对偶性理论" §1.2).
+//
+// The step moves the whole state in and out once and does 4 flops per state element, so it is
+// bound by HBM bandwidth. The kernel streams the state in 16-byte vectors: a row of the state
+// (N fp32) is spread over L lanes (L a power of two, the smallest that is >= N/4, at most 32),
+// each lane holding one or two float4 column groups, and a warp covers 32/L rows at a time.
+// Every thread loads its four rows before using any of them, so that enough loads are in flight.
+// The dot product with C is reduced across the row's L lanes with xor shuffles.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssd.h"
+#include "ssd_internal.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kDecRowsPerThread = 4;
+
+struct DecodeArgs {
+    const void* x;          // (batch, H, P) storage type
+    const float* dt;        // (batch, H)
+    const float* A;         // (H)
+    const void* B;          // (batch, G, N) storage type
+    const void* C;
+    const float* D;         // (H) or null
+    const float* state;     // (batch, H, P, N)
+    float* new_state;       // may alias state
+    void* y;                // (batch, H, P) storage type
+    int H, P, N, G;
+    int L;                  // lanes per state row
+    int rows_per_cta;       // kDecWarps * (32 / L) * kDecRowsPerThread
+    int row_blocks;         // ceil(P / rows_per_cta)
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// four consecutive elements of B or C starting at a multiple of 4, as fp32
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// CI: float4 column groups per lane (N/4 <= CI * L)
+template <typename T, int CI>
+__global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = a.L;
+    const int seg = lane / L, cl = lane % L;          // row slot within the warp, lane within the row
+    const int rows_per_pass = kDecWarps * (32 / L);
+    const int64_t unit = blockIdx.x;
+    const int rb = (int)(unit % a.row_blocks);
+    const int64_t bh = unit / a.row_blocks;           // b * H + h
+    const int h = (int)(bh % a.H);
+    const int64_t b = bh / a.H;
+    const int g = h / (a.H / a.G);
+    const int n4 = a.N >> 2;
+
+    const float decay = expf(a.dt[bh] * a.A[h]);
+    const float dskip = a.D ? a.D[h] : 0.f;
+
+    const T* Bp = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
+    const T* Cp = static_cast<const T*>(a.C) + (b * a.G + g) * a.N;
+    float4 bv[CI], cv[CI];
+#pragma unroll
+    for (int j = 0; j < CI; ++j) {
+        const int c = cl + j * L;
+        if (c < n4) {
+            bv[j] = load4<T>(Bp + 4 * c);
+            cv[j] = load4<T>(Cp + 4 * c);
+        } else {
+            bv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            cv[j] = bv[j];
+        }
+    }
+
+    const int64_t row_base = bh * a.P;                // first state row of (b, h)
+    const T* xp = static_cast<const T*>(a.x) + row_base;
+    int p[kDecRowsPerThread];
+    float xv[kDecRowsPerThread];
+    float4 s[kDecRowsPerThread][CI];
+#pragma unroll
+    for (int u = 0; u < kDecRowsPerThread; ++u) {
+        p[u] = rb * a.rows_per_cta + u * rows_per_pass + warp * (32 / L) + seg;
+        xv[u] = p[u] < a.P ? to_f32<T>(xp[p[u]]) : 0.f;
+#pragma unroll
+        for (int j = 0; j < CI; ++j) {
+            const int c = cl + j * L;
+            s[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p[u] < a.P && c < n4)
+                s[u][j] = __ldcs(reinterpret_cast<const float4*>(a.state + (row_base + p[u]) * a.N) + c);
+        }
+    }
+    T* yp = static_cast<T*>(a.y) + row_base;
+#pragma unroll
+    for (int u = 0; u < kDecRowsPerThread; ++u) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < CI; ++j) {
+            const int c = cl + j * L;
+            float4 v = s[u][j];
+            v.x = fmaf(decay, v.x, xv[u] * bv[j].x);
+            v.y = fmaf(decay, v.y, xv[u] * bv[j].y);
+            v.z = fmaf(decay, v.z, xv[u] * bv[j].z);
+            v.w = fmaf(decay, v.w, xv[u] * bv[j].w);
+            acc = fmaf(v.x, cv[j].x, acc);
+            acc = fmaf(v.y, cv[j].y, acc);
+            acc = fmaf(v.z, cv[j].z, acc);
+            acc = fmaf(v.w, cv[j].w, acc);
+            if (p[u] < a.P && c < n4)
+                __stcs(reinterpret_cast<float4*>(a.new_state + (row_base + p[u]) * a.N) + c, v);
+        }
+        for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (cl == 0 && p[u] < a.P) yp[p[u]] = from_f32<T>(fmaf(dskip, xv[u], acc));
+    }
+}
+
+template <typename T>
+cudaError_t launch_decode_t(const DecodeArgs& a, int64_t units, cudaStream_t st) {
+    const int ci = ((a.N >> 2) + a.L - 1) / a.L;
+    prof_launch();
+    prof_begin(st, "ssd_decode_kernel");
+    if (ci <= 1)
+        ssd_decode_kernel<T, 1><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+    else
+        ssd_decode_kernel<T, 2><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+    prof_end(st);
+    return cudaGetLastError();
+}
+
+bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
+int check_decode(const ssd_shape* s, ssd_dtype dtype) {
+    if (!s) return SSD_ERR_INVALID_ARG;
+    if (s->batch < 0 || s->seqlen != 1 || s->nheads <= 0 || s->headdim <= 0 || s->dstate <= 0 || s->ngroups <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (s->nheads % s->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (s->headdim > 256 || s->dstate > 256 || (s->dstate & 3) != 0) return SSD_ERR_UNSUPPORTED;
+    if (s->batch * s->nheads > (int64_t)INT32_MAX / 2) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+size_t decode_elt(ssd_dtype d) { return d == SSD_F32 ? 4 : 2; }
+
+}  // namespace
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                    const void* B, const void* C, const float* D, const float* state, float* new_state, void* y,
+                    void* stream) {
+    int rc = check_decode(s, dtype);
+    if (rc != SSD_OK) return rc;
+    if (s->batch == 0) return SSD_OK;
+    if (!x || !dt || !A || !B || !C || !state || !new_state || !y) return SSD_ERR_INVALID_ARG;
+    if (!aligned(state, 16) || !aligned(new_state, 16) || !aligned(B, 16) || !aligned(C, 16) ||
+        !aligned(x, decode_elt(dtype)) || !aligned(y, decode_elt(dtype)) || !aligned(dt, 4) || !aligned(A, 4) ||
+        (D && !aligned(D, 4)))
+        return SSD_ERR_INVALID_ARG;
+    // new_state either is state or does not overlap it
+    const size_t stb = (size_t)s->batch * s->nheads * s->headdim * s->dstate * sizeof(float);
+    const char* s0 = reinterpret_cast<const char*>(state);
+    const char* s1 = reinterpret_cast<const char*>(new_state);
+    if (s0 != s1 && s1 < s0 + stb && s0 < s1 + stb) return SSD_ERR_INVALID_ARG;
+    int dev = 0, major = 0, minor = 0;
+    if (note_cuda_error("cudaGetDevice", cudaGetDevice(&dev)) != cudaSuccess) return SSD_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (major != 10 || minor != 3) return SSD_ERR_UNSUPPORTED;
+
+    DecodeArgs a;
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D;
+    a.state = state; a.new_state = new_state; a.y = y;
+    a.H = (int)s->nheads; a.P = (int)s->headdim; a.N = (int)s->dstate; a.G = (int)s->ngroups;
+    const int n4 = a.N >> 2;
+    a.L = 1;
+    while (a.L < n4 && a.L < 32) a.L <<= 1;
+    a.rows_per_cta = kDecWarps * (32 / a.L) * kDecRowsPerThread;
+    a.row_blocks = (a.P + a.rows_per_cta - 1) / a.rows_per_cta;
+    const int64_t units = s->batch * s->nheads * a.row_blocks;
+    if (units > (int64_t)INT32_MAX) return SSD_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == SSD_F32 ? launch_decode_t<float>(a, units, st)
+                                           : launch_decode_t<__nv_bfloat16>(a, units, st);
+    return note_cuda_error("decode launch", e) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
+    if (check_decode(s, dtype) != SSD_OK) return 0;
+    const size_t e = decode_elt(dtype);
+    const size_t rows = (size_t)s->batch * s->nheads;
+    size_t tot = 0;
+    tot += align256(rows * s->headdim * e) * 2;                    // x, y
+    tot += align256(rows * 4);                                     // dt
+    tot += align256((size_t)s->nheads * 4) * 2;                    // A, D
+    tot += align256((size_t)s->batch * s->ngroups * s->dstate * e) * 2;   // B, C
+    tot += align256(rows * s->headdim * s->dstate * 4);            // state (updated in place)
+    return tot > 0 ? tot : 256;
+}
+
+int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                         const void* B, const void* C, const float* D, const float* state, float* new_state,
+                         void* y, void* device_buffer, size_t device_buffer_bytes, void* stream) {
+    int rc = check_decode(s, dtype);
+    if (rc != SSD_OK) return rc;
+    const size_t need = ssd_decode_host_buffer_size(s, dtype);
+    if (!device_buffer || !aligned(device_buffer, 256) || device_buffer_bytes < need) return SSD_ERR_WORKSPACE;
+    if (s->batch == 0) return SSD_OK;
+    if (!x || !dt || !A || !B || !C || !state || !new_state || !y) return SSD_ERR_INVALID_ARG;
+    const size_t e = decode_elt(dtype);
+    const size_t rows = (size_t)s->batch * s->nheads;
+    const size_t xb = rows * s->headdim * e, dtb = rows * 4, hb = (size_t)s->nheads * 4;
+    const size_t bcb = (size_t)s->batch * s->ngroups * s->dstate * e, stb = rows * s->headdim * s->dstate * 4;
+    char* base = static_cast<char*>(device_buffer);
+    size_t off = 0;
+    auto carve = [&](size_t bytes) { char* p = base + off; off += align256(bytes); return p; };
+    char* dx = carve(xb);
+    char* dy = carve(xb);
+    char* ddt = carve(dtb);
+    char* dA = carve(hb);
+    char* dD = carve(hb);
+    char* dB = carve(bcb);
+    char* dC = carve(bcb);
+    char* dS = carve(stb);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaSuccess;
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && src && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+    };
+    h2d(dx, x, xb);
+    h2d(ddt, dt, dtb);
+    h2d(dA, A, hb);
+    h2d(dD, D, hb);
+    h2d(dB, B, bcb);
+    h2d(dC, C, bcb);
+    h2d(dS, state, stb);
+    if (note_cuda_error("decode host copy in", err) != cudaSuccess) return SSD_ERR_CUDA;
+    rc = ssd_decode_step(s, dtype, dx, (const float*)ddt, (const float*)dA, dB, dC, D ? (const float*)dD : nullptr,
+                         (const float*)dS, (float*)dS, dy, stream);
+    if (rc != SSD_OK) return rc;
+    err = cudaMemcpyAsync(y, dy, xb, cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(new_state, dS, stb, cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    return note_cuda_error("decode host copy out", err) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -41,8 +41,8 @@ class Workload:
         return replace(self, **kw)
 
 
-# The five workloads: tiny fp32, Mamba-2-130M-shaped, Mamba-2-2.7B-shaped,
-# long sequence with a state-size sweep, and a variable-length packed batch.
+# The forward workloads: tiny fp32, Mamba-2-130M-shaped, Mamba-2-2.7B-shaped, long sequence with
+# a state-size sweep, and a variable-length packed batch; and one recurrent-step workload.
 WORKLOADS = {
     "fp32_tiny": Workload("fp32_tiny", 1, 256, 2, 16, 16, 1, 64, "f32", 1000),
     "m2_130m": Workload("m2_130m", 8, 2048, 24, 64, 128, 1, 256, "bf16", 1001),
@@ -51,6 +51,9 @@ WORKLOADS = {
     "long_n128": Workload("long_n128", 1, 16384, 80, 64, 128, 1, 256, "bf16", 1003 + 128),
     "long_n256": Workload("long_n256", 1, 16384, 80, 64, 256, 1, 256, "bf16", 1003 + 256),
     "varlen": Workload("varlen", 1, 32768, 32, 64, 128, 1, 256, "bf16", 1004, varlen_total=32768),
+    # one recurrent step for 64 carried states of a Mamba-2-2.7B-shaped layer (seqlen 1; the
+    # initial state is the carried state)
+    "decode_2p7b": Workload("decode_2p7b", 64, 1, 80, 64, 128, 1, 256, "bf16", 1005, init_state=True),
 }
 
 

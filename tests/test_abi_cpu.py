@@ -95,3 +95,28 @@ def test_no_gpu_reports_cuda_or_unsupported(lib):
     s = shape()
     rc = call(lib, s)
     assert rc in (bd.SSD_ERR_CUDA, bd.SSD_ERR_UNSUPPORTED)
+
+
+def dcall(lib, s, dtype=bd.SSD_BF16, x=FAKE, state=FAKE, new_state=FAKE, B=FAKE):
+    return lib.ssd_decode_step(ctypes.byref(s), dtype, x, FAKE, FAKE, B, FAKE, None, state, new_state, FAKE, None)
+
+
+def test_decode_argument_errors_before_any_device_work(lib):
+    s = shape(batch=4, T=1)
+    assert dcall(lib, shape(batch=4, T=2)) == bd.SSD_ERR_INVALID_ARG          # one token per row
+    assert dcall(lib, shape(batch=4, T=1, H=3, G=2)) == bd.SSD_ERR_INVALID_ARG   # H % G
+    assert dcall(lib, shape(batch=4, T=1, N=18)) == bd.SSD_ERR_UNSUPPORTED    # N % 4
+    assert dcall(lib, shape(batch=4, T=1, N=260)) == bd.SSD_ERR_UNSUPPORTED
+    assert dcall(lib, shape(batch=4, T=1, P=300)) == bd.SSD_ERR_UNSUPPORTED
+    assert dcall(lib, s, x=None) == bd.SSD_ERR_INVALID_ARG
+    assert dcall(lib, s, state=FAKE + 8) == bd.SSD_ERR_INVALID_ARG            # state not 16-byte aligned
+    assert dcall(lib, s, B=FAKE + 8) == bd.SSD_ERR_INVALID_ARG
+    assert dcall(lib, s, new_state=FAKE + 16) == bd.SSD_ERR_INVALID_ARG       # partial overlap with state
+    assert dcall(lib, s, dtype=7) == bd.SSD_ERR_INVALID_ARG
+    assert dcall(lib, shape(batch=0, T=1)) == bd.SSD_OK                       # nothing to do
+    assert lib.ssd_decode_host_buffer_size(ctypes.byref(shape(batch=4, T=1, N=18)), bd.SSD_BF16) == 0
+    need = lib.ssd_decode_host_buffer_size(ctypes.byref(s), bd.SSD_BF16)
+    assert need >= 4 * 4 * 64 * 128 * 4                                        # holds the state
+    rc = lib.ssd_decode_step_host(ctypes.byref(s), bd.SSD_BF16, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
+                                  FAKE, FAKE, 16, None)
+    assert rc == bd.SSD_ERR_WORKSPACE
