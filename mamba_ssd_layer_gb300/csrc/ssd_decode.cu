@@ -13,7 +13,8 @@
 // bound by HBM bandwidth. The kernel streams the state in 16-byte vectors: a row of the state
 // (N fp32) is spread over L lanes (L a power of two, the smallest that is >= N/4, at most 32),
 // each lane holding one or two float4 column groups, and a warp covers 32/L rows at a time.
-// Every thread loads its four rows before using any of them, so that enough loads are in flight.
+// Every thread loads its four rows before using any of them, so that enough loads are in flight;
+// CTAs are small (two warps), so that many are resident per SM and a CTA's set-up is cheap.
 // The dot product with C is reduced across the row's L lanes with xor shuffles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -24,7 +25,7 @@
 namespace ssd {
 namespace {
 
-constexpr int kDecThreads = 256;
+constexpr int kDecThreads = 64;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kDecRowsPerThread = 4;
 

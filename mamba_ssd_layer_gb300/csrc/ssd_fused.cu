@@ -70,8 +70,11 @@ struct FusedArgs {
     float* final_state;
     __nv_bfloat16* y;
     float* decay;               // per piece: [2] per-head decay of the window
-    float* agg;                 // per piece: [128][N]
-    float* incl;                // per piece: [128][N]
+    // Per piece, 128 x N fp32 in column-chunk-major order: the float4 holding row r, columns
+    // 4c .. 4c + 3 is unit c * 128 + r, so that a warp (32 consecutive rows) reads or writes 512
+    // contiguous bytes per column chunk.
+    float* agg;                 // the window's end state from a zero entering state
+    float* incl;                // the state entering the window
     const int32_t* woff;        // packed batch: first window of each sequence
     int H, G, nseq, npairs;
     int64_t npieces;            // pieces to dispatch (exact for a dense batch, a bound for a packed one)
@@ -93,7 +96,6 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -103,28 +105,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
-    uint32_t a[16], b[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) { a[k] = __float_as_uint(v[k]); b[k] = __float_as_uint(v[16 + k]); }
-    tmem_st16(taddr, a);
-    tmem_st16(taddr + 16, b);
-}
-
 // TMEM -> registers without waiting; pair with tmem_wait_ld() before using the values
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, float* v) {
-    uint32_t* r = reinterpret_cast<uint32_t*>(v);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float* v) {
     uint32_t* r = reinterpret_cast<uint32_t*>(v);
     asm volatile(
@@ -164,10 +145,6 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void st_release(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 
 // Barrier slots in shared memory
@@ -230,7 +207,6 @@ struct Smem {
     // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
     // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * 260; }
-    __device__ float* stage_misc(int s) const { return cs(s) + 256; }
     // exp(cs_p - cs_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
     __device__ float* vt() const { return cs(0) + 520; }
     __device__ float* misc() const { return cs(0) + 520 + 192; }                                     // [8]
@@ -727,10 +703,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tc_fence_after_sync();
             float v[NQ];
             st_load(nq0, NQ, v);
-            float* dst = a.agg + (c.q * 128 + row) * N + nq0;
+            float4* dst = reinterpret_cast<float4*>(a.agg + c.q * 128 * N) + (nq0 / 4) * 128 + row;
 #pragma unroll
-            for (int k = 0; k < NQ; k += 4)
-                __stcg(reinterpret_cast<float4*>(dst + k), make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]));
+            for (int k = 0; k < NQ; k += 4) __stcg(dst + (k / 4) * 128, make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]));
             if (mt < 2) a.decay[c.q * 2 + mt] = ex2(mt ? tot1 : tot0);
             tc_fence_before_sync();
         }
@@ -768,7 +743,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     q0 = (int64_t)a.npairs * w0 + (int64_t)hp * W;
                 }
                 if (W <= 1) continue;
-                const int r = e4 / (N / 4), n = 4 * (e4 % (N / 4));
+                const int r = e4 & 127, n = 4 * (e4 >> 7);     // column-chunk-major unit e4
                 const int hr = r >> 6, pr = r & 63;
                 float4 h = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (a.init)
@@ -781,7 +756,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     for (int j = 0; j < 8; ++j) {
                         if (w0 + j + 1 < W) {
                             dcy[j] = __ldcg(a.decay + (q0 + w0 + j) * 2 + hr);
-                            g[j] = __ldcg(reinterpret_cast<const float4*>(a.agg + ((q0 + w0 + j) * 128 + r) * N + n));
+                            g[j] = __ldcg(reinterpret_cast<const float4*>(a.agg + (q0 + w0 + j) * 128 * N) + e4);
                         }
                     }
 #pragma unroll
@@ -789,7 +764,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         if (w0 + j + 1 < W) {
                             h = make_float4(fmaf(dcy[j], h.x, g[j].x), fmaf(dcy[j], h.y, g[j].y),
                                             fmaf(dcy[j], h.z, g[j].z), fmaf(dcy[j], h.w, g[j].w));
-                            __stcg(reinterpret_cast<float4*>(a.incl + ((q0 + w0 + j + 1) * 128 + r) * N + n), h);
+                            __stcg(reinterpret_cast<float4*>(a.incl + (q0 + w0 + j + 1) * 128 * N) + e4, h);
                         }
                     }
                 }
@@ -951,103 +926,102 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         int stage = 0;
         uint32_t kt = 0;                         // tiles done (selects the C B^T buffer)
         bool ok = true;
-        // One 32-column block kb of L o G (+ D on the diagonal) of stage st, in place over C B^T in the
-        // TMEM buffer gcol. This thread: row i, columns j = 32 kb .. 32 kb + 31, written as packed bf16
-        // (per 16 tokens: 8 columns of head 0, then 8 of head 1). A block above the diagonal is zero; a
-        // block strictly below takes exp(cs_i - cs_p) exp(cs_p - cs_j) with p the block's last token (both
-        // factors <= 1, no subtraction of distant cumsums); the diagonal block takes exp(cs_i - cs_j).
-        auto lg_block = [&](int st, int len, int kb, uint32_t gcol, float D0, float D1) {
-            const float* cs = sm.cs(st);
-            const int i = row;
-            const bool rv = i < len;
-            const uint32_t col = lane_base + gcol + 32 * kb;
-            if (kb > qd || !__any_sync(0xffffffffu, rv)) {
-                uint32_t z[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) z[e] = 0u;
-                tmem_st16(col, z);
-                tmem_st16(col + 16, z);
-                return;
-            }
-            float g[32];
-            tmem_ld16_nowait(col, g);
-            tmem_ld16_nowait(col + 16, g + 16);
-            const float ci0 = cs[i], ci1 = cs[128 + i];
-            if (kb < qd) {
-                const float u0 = ex2(ci0 - cs[32 * kb + 31]), u1 = ex2(ci1 - cs[128 + 32 * kb + 31]);
+        // L o G (+ D on the diagonal) of stage st, in place over C B^T in the TMEM buffer gcol, by groups
+        // of 16 columns. This thread: row i; group g holds columns j = 16 g .. 16 g + 15 and is written as
+        // packed bf16 (8 columns of head 0, then 8 of head 1). A group above the diagonal block of the
+        // thread's row quadrant is zero; a group left of it takes exp(cs_i - cs_p) exp(cs_p - cs_j) with p
+        // the last token of the 32-token block the group lies in (both factors <= 1, no subtraction of
+        // distant cumsums); the two groups of the diagonal block take exp(cs_i - cs_j) directly.
+        // The causal work grows with the row quadrant, and a quadrant's rows can only be reached from the
+        // warps of its own SM sub-partition. Each of those four warps takes groups kq and 7 - kq, so that
+        // the two costly diagonal groups of a quadrant go to different warps.
+        auto lg_group = [&](const float* cs, int g, const float* gv, bool rv, float ci0, float ci1, uint32_t col,
+                            float D0, float D1) {
+            uint32_t p0[8], p1[8];
+            if (g < 2 * qd) {
+                const int p = 32 * (g >> 1) + 31;
+                const float u0 = ex2(ci0 - cs[p]), u1 = ex2(ci1 - cs[128 + p]);
                 const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
-                const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 32 * kb);
-                const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 32 * kb);
-                tmem_wait_ld();
+                const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 16 * g);
+                const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 16 * g);
 #pragma unroll
-                for (int gg = 0; gg < 2; ++gg) {
-                    uint32_t p0[8], p1[8];
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 a4 = v0[k4], b4 = v1[k4];
+                    const int e = 4 * k4;
+                    const float2 g0 = make_float2(gv[e], gv[e + 1]), g1 = make_float2(gv[e + 2], gv[e + 3]);
+                    const float2 ra = __fmul2_rn(g0, __fmul2_rn(uu0, make_float2(a4.x, a4.y)));
+                    const float2 rb = __fmul2_rn(g1, __fmul2_rn(uu0, make_float2(a4.z, a4.w)));
+                    const float2 rc = __fmul2_rn(g0, __fmul2_rn(uu1, make_float2(b4.x, b4.y)));
+                    const float2 rd = __fmul2_rn(g1, __fmul2_rn(uu1, make_float2(b4.z, b4.w)));
+                    p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
+                    p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
+                    p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
+                    p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
+                }
+            } else if (g <= 2 * qd + 1) {
+                const float4* c0p = reinterpret_cast<const float4*>(cs + 16 * g);
+                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 16 * g);
+                const float2 cc0 = make_float2(ci0, ci0), cc1 = make_float2(ci1, ci1), m1 = make_float2(-1.f, -1.f);
+                const int jb0 = 16 * (g - 2 * qd);      // first column relative to the diagonal block
 #pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const float4 a4 = v0[4 * gg + k4], b4 = v1[4 * gg + k4];
-                        const int e = 16 * gg + 4 * k4;
-                        const float2 g0 = make_float2(g[e], g[e + 1]), g1 = make_float2(g[e + 2], g[e + 3]);
-                        const float2 ra = __fmul2_rn(g0, __fmul2_rn(uu0, make_float2(a4.x, a4.y)));
-                        const float2 rb = __fmul2_rn(g1, __fmul2_rn(uu0, make_float2(a4.z, a4.w)));
-                        const float2 rc = __fmul2_rn(g0, __fmul2_rn(uu1, make_float2(b4.x, b4.y)));
-                        const float2 rd = __fmul2_rn(g1, __fmul2_rn(uu1, make_float2(b4.z, b4.w)));
-                        p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
-                        p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
-                        p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
-                        p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
-                    }
-                    if (!rv) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
-                    }
-                    tmem_st8(col + 16 * gg, p0);
-                    tmem_st8(col + 16 * gg + 8, p1);
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 a4 = c0p[k4], b4 = c1p[k4];
+                    const int e = 4 * k4;
+                    const int jl = jb0 + e;               // row within the diagonal block = lane
+                    const float2 da = __ffma2_rn(make_float2(a4.x, a4.y), m1, cc0);
+                    const float2 db = __ffma2_rn(make_float2(a4.z, a4.w), m1, cc0);
+                    const float2 dc = __ffma2_rn(make_float2(b4.x, b4.y), m1, cc1);
+                    const float2 dd = __ffma2_rn(make_float2(b4.z, b4.w), m1, cc1);
+                    float2 ra = __fmul2_rn(make_float2(gv[e], gv[e + 1]), make_float2(ex2(da.x), ex2(da.y)));
+                    float2 rb = __fmul2_rn(make_float2(gv[e + 2], gv[e + 3]), make_float2(ex2(db.x), ex2(db.y)));
+                    float2 rc = __fmul2_rn(make_float2(gv[e], gv[e + 1]), make_float2(ex2(dc.x), ex2(dc.y)));
+                    float2 rd = __fmul2_rn(make_float2(gv[e + 2], gv[e + 3]), make_float2(ex2(dd.x), ex2(dd.y)));
+                    if (jl > lane) { ra.x = 0.f; rc.x = 0.f; }
+                    if (jl + 1 > lane) { ra.y = 0.f; rc.y = 0.f; }
+                    if (jl + 2 > lane) { rb.x = 0.f; rd.x = 0.f; }
+                    if (jl + 3 > lane) { rb.y = 0.f; rd.y = 0.f; }
+                    if (jl == lane) { ra.x += D0; rc.x += D1; }
+                    if (jl + 1 == lane) { ra.y += D0; rc.y += D1; }
+                    if (jl + 2 == lane) { rb.x += D0; rd.x += D1; }
+                    if (jl + 3 == lane) { rb.y += D0; rd.y += D1; }
+                    p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
+                    p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
+                    p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
+                    p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
                 }
             } else {
-                const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * kb);
-                const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * kb);
-                const float2 cc0 = make_float2(ci0, ci0), cc1 = make_float2(ci1, ci1), m1 = make_float2(-1.f, -1.f);
-                tmem_wait_ld();
 #pragma unroll
-                for (int gg = 0; gg < 2; ++gg) {
-                    uint32_t p0[8], p1[8];
-#pragma unroll
-                    for (int k4 = 0; k4 < 4; ++k4) {
-                        const float4 a4 = c0p[4 * gg + k4], b4 = c1p[4 * gg + k4];
-                        const int jl = 16 * gg + 4 * k4;     // column within the block; row within it = lane
-                        const float2 da = __ffma2_rn(make_float2(a4.x, a4.y), m1, cc0);
-                        const float2 db = __ffma2_rn(make_float2(a4.z, a4.w), m1, cc0);
-                        const float2 dc = __ffma2_rn(make_float2(b4.x, b4.y), m1, cc1);
-                        const float2 dd = __ffma2_rn(make_float2(b4.z, b4.w), m1, cc1);
-                        float2 ra = __fmul2_rn(make_float2(g[jl], g[jl + 1]), make_float2(ex2(da.x), ex2(da.y)));
-                        float2 rb = __fmul2_rn(make_float2(g[jl + 2], g[jl + 3]), make_float2(ex2(db.x), ex2(db.y)));
-                        float2 rc = __fmul2_rn(make_float2(g[jl], g[jl + 1]), make_float2(ex2(dc.x), ex2(dc.y)));
-                        float2 rd = __fmul2_rn(make_float2(g[jl + 2], g[jl + 3]), make_float2(ex2(dd.x), ex2(dd.y)));
-                        if (jl > lane) { ra.x = 0.f; rc.x = 0.f; }
-                        if (jl + 1 > lane) { ra.y = 0.f; rc.y = 0.f; }
-                        if (jl + 2 > lane) { rb.x = 0.f; rd.x = 0.f; }
-                        if (jl + 3 > lane) { rb.y = 0.f; rd.y = 0.f; }
-                        if (jl == lane) { ra.x += D0; rc.x += D1; }
-                        if (jl + 1 == lane) { ra.y += D0; rc.y += D1; }
-                        if (jl + 2 == lane) { rb.x += D0; rd.x += D1; }
-                        if (jl + 3 == lane) { rb.y += D0; rd.y += D1; }
-                        p0[2 * k4] = pack_bf16x2(ra.x, ra.y);
-                        p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y);
-                        p1[2 * k4] = pack_bf16x2(rc.x, rc.y);
-                        p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y);
-                    }
-                    if (!rv) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
-                    }
-                    tmem_st8(col + 16 * gg, p0);
-                    tmem_st8(col + 16 * gg + 8, p1);
-                }
+                for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
             }
+            if (!rv) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
+            }
+            tmem_st8(col, p0);
+            tmem_st8(col + 8, p1);
         };
-        // this warp's column block of L o G for stage st into buffer gcol
+        // this warp's two column groups of L o G for stage st into buffer gcol
         auto lg_tile = [&](int st, int len, uint32_t gcol, float D0, float D1) {
-            lg_block(st, len, kq, gcol, D0, D1);
+            const float* cs = sm.cs(st);
+            const bool rv = row < len;
+            const uint32_t ca = lane_base + gcol + 16 * kq, cb = lane_base + gcol + 16 * (7 - kq);
+            if (!__any_sync(0xffffffffu, rv)) {
+                uint32_t z[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) z[e] = 0u;
+                tmem_st8(ca, z);
+                tmem_st8(ca + 8, z);
+                tmem_st8(cb, z);
+                tmem_st8(cb + 8, z);
+            } else {
+                float gv[32];
+                tmem_ld16_nowait(ca, gv);
+                tmem_ld16_nowait(cb, gv + 16);
+                const float ci0 = cs[row], ci1 = cs[128 + row];
+                tmem_wait_ld();
+                lg_group(cs, kq, gv, rv, ci0, ci1, ca, D0, D1);
+                lg_group(cs, 7 - kq, gv + 16, rv, ci0, ci1, cb, D0, D1);
+            }
             tmem_wait_st();
             tc_fence_before_sync();
             warp_arrive(sm, kBarLG);
@@ -1149,13 +1123,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             // the entering state into this thread's state columns: the initial state (or zero) at a
             // chain's start, else the scan's result
             {
+                // the initial state is (row, column) row-major; the scan's result is column-chunk-major
                 const float* src = c.w == 0
                     ? (a.init ? a.init + (((int64_t)c.s * a.H + h0 + hrow) * 64 + prow) * a.n_full + a.n_off + nq0 : nullptr)
-                    : a.incl + (c.q * 128 + row) * N + nq0;
+                    : a.incl + c.q * 128 * N;
+                const int step = c.w == 0 ? 4 : 512;
+                const float* s0 = c.w == 0 ? src : src + ((nq0 / 4) * 128 + row) * 4;
                 float v[NQ];
 #pragma unroll
                 for (int k = 0; k < NQ; k += 4) {
-                    const float4 i4 = src ? __ldcg(reinterpret_cast<const float4*>(src + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 i4 = src ? __ldcg(reinterpret_cast<const float4*>(s0 + (k / 4) * step)) : make_float4(0.f, 0.f, 0.f, 0.f);
                     v[k] = i4.x; v[k + 1] = i4.y; v[k + 2] = i4.z; v[k + 3] = i4.w;
                 }
                 st_store(nq0, NQ, v);
