@@ -508,10 +508,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     };
     // producer: tile-local inclusive cumsum of dt*A (x log2 e) plus `carry`, written to cs[2][128];
     // cv gets this lane's four values per head, carry advances by the tile's total
-    auto cumsum = [&](const float (&v)[2][4], int h0, float* cs, float (&carry)[2], float (&cv)[2][4]) {
+    auto cumsum = [&](const float (&v)[2][4], const float (&Al)[2], float* cs, float (&carry)[2], float (&cv)[2][4]) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const float A2 = __ldg(a.A + h0 + hh) * kLog2e;
+            const float A2 = Al[hh];
             float p[4];
             p[0] = v[hh][0] * A2;
 #pragma unroll
@@ -612,17 +612,20 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tot0 = s0 * __ldg(a.A + h0) * kLog2e;
                 tot1 = s1 * __ldg(a.A + h0 + 1) * kLog2e;
             }
+            const float Al[2] = {__ldg(a.A + h0) * kLog2e, __ldg(a.A + h0 + 1) * kLog2e};
             float carry[2] = {0.f, 0.f};
-            float vn[2][4];                               // dt of the next tile, loaded one tile ahead
+            // dt of the next two tiles, loaded two tiles ahead (a load takes longer than a tile here)
+            float vn[2][4], vn2[2][4];
             load_dt(tile_row0(c, c.t0), tile_len(c, c.t0), h0, vn);
+            if (c.t0 + 1 < c.t1) load_dt(tile_row0(c, c.t0 + 1), tile_len(c, c.t0 + 1), h0, vn2);
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int row0 = tile_row0(c, t), len = tile_len(c, t);
                 float v[2][4], cv[2][4];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) v[hh][k] = vn[hh][k];
-                if (t + 1 < c.t1) load_dt(tile_row0(c, t + 1), tile_len(c, t + 1), h0, vn);
+                    for (int k = 0; k < 4; ++k) { v[hh][k] = vn[hh][k]; vn[hh][k] = vn2[hh][k]; }
+                if (t + 2 < c.t1) load_dt(tile_row0(c, t + 2), tile_len(c, t + 2), h0, vn2);
                 if ((issued >> stage) & 1u) {
                     const bool w = wait_bar(sm, kBarAFull0 + 3 + stage, ph, a);   // the stage's empty barrier
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -638,7 +641,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         tma_load_3d(sm.ba(stage) + k * kRegion, &maps.b, full, 64 * k, g, row0);
                 }
                 float* cs = sm.csa(stage);
-                cumsum(v, h0, cs, carry, cv);
+                cumsum(v, Al, cs, carry, cv);
                 if (lane == 0) { cs[256] = tot0; cs[257] = tot1; }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full);
@@ -786,6 +789,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const Piece c = decode_piece(d, a);
             if (!c.valid) break;
             const int h0 = 2 * c.hp;
+            const float Al[2] = {__ldg(a.A + h0) * kLog2e, __ldg(a.A + h0 + 1) * kLog2e};
             for (int t = c.t0; t < c.t1 && ok; ++t) {
                 const int row0 = tile_row0(c, t), len = tile_len(c, t);
                 float v[2][4], cv[2][4];
@@ -809,7 +813,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
                 }
                 float carry[2] = {0.f, 0.f};
-                cumsum(v, h0, sm.cs(stage), carry, cv);
+                cumsum(v, Al, sm.cs(stage), carry, cv);
                 if (p2 > 0) {
                     const bool w = wait_bar(sm, kBarLG, ph, a);
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
