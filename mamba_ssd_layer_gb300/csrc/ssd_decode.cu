@@ -40,6 +40,7 @@ struct DecodeArgs {
     float* new_state;       // may alias state
     void* y;                // (batch, H, P) storage type
     int H, P, N, G;
+    int heads_per_group;    // H / G
     int L;                  // lanes per state row
     int rows_per_cta;       // kDecWarps * (32 / L) * kDecRowsPerThread
     int row_blocks;         // ceil(P / rows_per_cta)
@@ -79,12 +80,13 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
     const int L = a.L;
     const int seg = lane / L, cl = lane % L;          // row slot within the warp, lane within the row
     const int rows_per_pass = kDecWarps * (32 / L);
-    const int64_t unit = blockIdx.x;
-    const int rb = (int)(unit % a.row_blocks);
-    const int64_t bh = unit / a.row_blocks;           // b * H + h
-    const int h = (int)(bh % a.H);
-    const int64_t b = bh / a.H;
-    const int g = h / (a.H / a.G);
+    const uint32_t unit = blockIdx.x;                 // < 2^31 (checked at launch): 32-bit index math
+    const int rb = (int)(unit % (uint32_t)a.row_blocks);
+    const uint32_t bh32 = unit / (uint32_t)a.row_blocks;
+    const int h = (int)(bh32 % (uint32_t)a.H);
+    const int64_t bh = bh32;                          // b * H + h
+    const int64_t b = bh32 / (uint32_t)a.H;
+    const int g = h / a.heads_per_group;
     const int n4 = a.N >> 2;
 
     const float decay = expf(a.dt[bh] * a.A[h]);
@@ -208,6 +210,7 @@ int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const fl
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D;
     a.state = state; a.new_state = new_state; a.y = y;
     a.H = (int)s->nheads; a.P = (int)s->headdim; a.N = (int)s->dstate; a.G = (int)s->ngroups;
+    a.heads_per_group = a.H / a.G;
     const int n4 = a.N >> 2;
     a.L = 1;
     while (a.L < n4 && a.L < 32) a.L <<= 1;
