@@ -102,11 +102,12 @@ def algorithmic_bytes(w, batch_rows, nseq) -> int:
 
 
 def decode_algorithmic_bytes(w) -> int:
-    """Bytes one recurrent step must move: the fp32 state in and out, x in and y out, B and C,
-    dt, A and D."""
+    """Bytes one recurrent step must move: the state in and out (fp32 or bf16), x in and y out, B and
+    C, dt, A and D."""
     b, H, P, N, G = w.batch, w.nheads, w.headdim, w.dstate, w.ngroups
     e = 2 if w.dtype == "bf16" else 4
-    return int(2 * b * H * P * N * 4 + 2 * b * H * P * e + 2 * b * G * N * e + 4 * b * H + 8 * H)
+    es = 2 if w.state_dtype == "bf16" else 4
+    return int(2 * b * H * P * N * es + 2 * b * H * P * e + 2 * b * G * N * e + 4 * b * H + 8 * H)
 
 
 def algorithmic_flops(w, batch_rows) -> int:
@@ -218,9 +219,11 @@ def run_reference_decode(args, w):
 
 
 def decode_config(w):
+    sb = w.batch * w.nheads * w.headdim * w.dstate * (2 if w.state_dtype == "bf16" else 4)
     return {"workload": w.name, "batch": w.batch, "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate,
-            "ngroups": w.ngroups, "parallelism": "replicas",
-            "l2": "inputs larger than L2 (two fp32 state buffers of ~168 MB each, read and written in turn)"}
+            "ngroups": w.ngroups, "state_dtype": w.state_dtype, "parallelism": "replicas",
+            "l2": f"inputs larger than L2 (two {w.state_dtype} state buffers of ~{sb / 1e6:.0f} MB each, "
+                  "read and written in turn)"}
 
 
 def decode_cpu_baseline(w, min_seconds: float = 10.0, max_runs: int = 5000):
@@ -260,7 +263,8 @@ def run_decode(args, w):
     t = {k: torch.from_numpy(np.ascontiguousarray(host[k])).to(dev, torch.bfloat16) for k in ("x", "B", "C")}
     for k in ("dt", "A", "D"):
         t[k] = torch.from_numpy(np.ascontiguousarray(host[k])).to(dev, torch.float32)
-    states = [torch.from_numpy(host["state"]).to(dev), torch.empty_like(torch.from_numpy(host["state"]), device=dev)]
+    sdt = torch.bfloat16 if w.state_dtype == "bf16" else torch.float32
+    states = [torch.from_numpy(host["state"]).to(dev, sdt), torch.empty(host["state"].shape, dtype=sdt, device=dev)]
     y = torch.empty_like(t["x"])
     stream = torch.cuda.current_stream(dev)
 
@@ -295,7 +299,8 @@ def run_decode(args, w):
 
     # end to end through the host entry point: pinned inputs and state in, y and the state out
     hx = {k: torch.from_numpy(np.ascontiguousarray(host[k])).to(torch.bfloat16).pin_memory() for k in ("x", "B", "C")}
-    hf = {k: torch.from_numpy(np.ascontiguousarray(host[k])).pin_memory() for k in ("dt", "A", "D", "state")}
+    hf = {k: torch.from_numpy(np.ascontiguousarray(host[k])).pin_memory() for k in ("dt", "A", "D")}
+    hf["state"] = torch.from_numpy(np.ascontiguousarray(host["state"])).to(sdt).pin_memory()
     hy = torch.empty_like(hx["x"]).pin_memory()
     devbuf = torch.empty(int(bd.load_library().ssd_decode_host_buffer_size(
         bd._shape(w.batch, 1, w.nheads, w.headdim, w.dstate, w.ngroups), bd.SSD_BF16)), dtype=torch.uint8, device=dev)
@@ -312,7 +317,7 @@ def run_decode(args, w):
         e2e_step()
     e2e_s = time.perf_counter() - t0
     h2d = sum(v.numel() * v.element_size() for v in list(hx.values()) + list(hf.values()))
-    d2h = hy.numel() * 2 + hf["state"].numel() * 4
+    d2h = hy.numel() * 2 + hf["state"].numel() * hf["state"].element_size()
 
     peaks, src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))

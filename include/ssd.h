@@ -177,6 +177,19 @@ int ssd_decode_step(const ssd_shape *shape, ssd_dtype dtype,
                     void *stream);
 
 /*
+ * ssd_decode_step with the carried state stored as `state_dtype`: SSD_F32 (as above) or SSD_BF16,
+ * which halves the bytes the step moves. With a bf16 state the update is computed in fp32 from the
+ * stored values, y is taken from the unrounded new state, and only the stored new state is rounded
+ * (to nearest even). state and new_state are then (batch, H, P, N) bf16 and N must be a multiple of
+ * 8. Everything else is as for ssd_decode_step.
+ */
+int ssd_decode_step_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype,
+                       const void *x, const float *dt, const float *A,
+                       const void *B, const void *C, const float *D,
+                       const void *state, void *new_state, void *y,
+                       void *stream);
+
+/*
  * The same step on HOST buffers: copies the inputs and the state into `device_buffer` (at least
  * ssd_decode_host_buffer_size bytes, 256-byte aligned), runs ssd_decode_step there in place, copies
  * y and the new state back and synchronises `stream`. new_state may be the host `state` buffer.
@@ -189,6 +202,14 @@ int ssd_decode_step_host(const ssd_shape *shape, ssd_dtype dtype,
                          const float *state, float *new_state, void *y,
                          void *device_buffer, size_t device_buffer_bytes,
                          void *stream);
+/* The host-buffer step with the state stored as `state_dtype` (see ssd_decode_step_ex); the buffer
+ * size from ssd_decode_host_buffer_size is enough for either state type. */
+int ssd_decode_step_host_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype,
+                            const void *x, const float *dt, const float *A,
+                            const void *B, const void *C, const float *D,
+                            const void *state, void *new_state, void *y,
+                            void *device_buffer, size_t device_buffer_bytes,
+                            void *stream);
 
 /*
  * Synchronises `stream`, then returns the device-side status recorded in the

@@ -62,10 +62,14 @@ def load_library():
     dec_args = [shp, i32, vp, fp, fp, vp, vp, fp, fp, fp, vp, vp]
     lib.ssd_decode_step.argtypes = dec_args
     lib.ssd_decode_step.restype = i32
+    lib.ssd_decode_step_ex.argtypes = [shp, i32, i32, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp]
+    lib.ssd_decode_step_ex.restype = i32
     lib.ssd_decode_host_buffer_size.argtypes = [shp, i32]
     lib.ssd_decode_host_buffer_size.restype = sz
     lib.ssd_decode_step_host.argtypes = dec_args[:-1] + [vp, sz, vp]
     lib.ssd_decode_step_host.restype = i32
+    lib.ssd_decode_step_host_ex.argtypes = [shp, i32, i32, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_decode_step_host_ex.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
     lib.ssd_profile_enable.argtypes = [i32]
@@ -230,9 +234,10 @@ def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, 
     """One recurrent step on CUDA tensors through ``ssd_decode_step``.
 
     x (batch, H, P) and B, C (batch, G, N) in float32 or bfloat16 (the same); dt (batch, H),
-    A (H,), D (H,) or None, state (batch, H, P, N): float32. new_state defaults to ``state``
-    (updated in place); pass another tensor to keep ``state``. Returns (y, new_state); the work
-    is enqueued on `stream` (default: torch's current stream) and nothing is synchronised.
+    A (H,), D (H,) or None: float32; state (batch, H, P, N) float32, or bfloat16 for a state stored
+    in bf16 (``ssd_decode_step_ex``). new_state defaults to ``state`` (updated in place); pass
+    another tensor of the state's dtype to keep ``state``. Returns (y, new_state); the work is
+    enqueued on `stream` (default: torch's current stream) and nothing is synchronised.
     """
     import torch
     batch, H, P, G, N = _decode_shapes(x, B)
@@ -246,20 +251,21 @@ def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, 
     _check(D, "D", (H,), torch.float32, dev)
     if state is None:
         raise ValueError("state is required")
-    _check(state, "state", (batch, H, P, N), torch.float32, dev)
+    state_code = _dtype_code(state)
+    _check(state, "state", (batch, H, P, N), state.dtype, dev)
     if new_state is None:
         new_state = state
-    _check(new_state, "new_state", (batch, H, P, N), torch.float32, dev)
+    _check(new_state, "new_state", (batch, H, P, N), state.dtype, dev)
     if y is None:
         y = torch.empty_like(x)
     _check(y, "y", (batch, H, P), x.dtype, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    rc = load_library().ssd_decode_step(ctypes.byref(_shape(batch, 1, H, P, N, G)), code, _ptr(x), _ptr(dt),
-                                        _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(new_state), _ptr(y),
-                                        ctypes.c_void_p(stream.cuda_stream))
+    rc = load_library().ssd_decode_step_ex(ctypes.byref(_shape(batch, 1, H, P, N, G)), code, state_code, _ptr(x),
+                                           _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state),
+                                           _ptr(new_state), _ptr(y), ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
-        raise SSDError(rc, "ssd_decode_step")
+        raise SSDError(rc, "ssd_decode_step_ex")
     return y, new_state
 
 
@@ -289,11 +295,11 @@ def ssd_decode_step_host(x, dt, A, B, C, D=None, state=None, new_state=None, y=N
         device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
     if stream is None:
         stream = torch.cuda.current_stream(device_buffer.device)
-    rc = lib.ssd_decode_step_host(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                                  _ptr(state), _ptr(new_state), _ptr(y), device_buffer.data_ptr(), need,
-                                  ctypes.c_void_p(stream.cuda_stream))
+    rc = lib.ssd_decode_step_host_ex(ctypes.byref(shape), code, _dtype_code(state), _ptr(x), _ptr(dt), _ptr(A),
+                                     _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(new_state), _ptr(y),
+                                     device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
-        raise SSDError(rc, "ssd_decode_step_host")
+        raise SSDError(rc, "ssd_decode_step_host_ex")
     return y, new_state
 
 

@@ -11,8 +11,11 @@
 //
 // The step moves the whole state in and out once and does 4 flops per state element, so it is
 // bound by HBM bandwidth. The kernel streams the state in 16-byte vectors: a row of the state
-// (N fp32) is spread over L lanes (L a power of two, the smallest that is >= N/4, at most 32),
-// each lane holding one or two float4 column groups, and a warp covers 32/L rows at a time.
+// (N / E chunks of E = 16 bytes / element size) is spread over L lanes (L a power of two, the
+// smallest that is >= N / E, at most 32), each lane holding one or two chunks, and a warp covers
+// 32/L rows at a time.
+// The state may be stored as fp32 or as bf16 (then a 16-byte chunk holds 8 elements; the update is
+// computed in fp32, y from the unrounded new state, and only the stored state is rounded).
 // Every thread loads its four rows before using any of them, so that enough loads are in flight;
 // CTAs are small (two warps), so that many are resident per SM and a CTA's set-up is cheap.
 // The dot product with C is reduced across the row's L lanes with xor shuffles.
@@ -36,8 +39,8 @@ struct DecodeArgs {
     const void* B;          // (batch, G, N) storage type
     const void* C;
     const float* D;         // (H) or null
-    const float* state;     // (batch, H, P, N)
-    float* new_state;       // may alias state
+    const void* state;      // (batch, H, P, N) state type
+    void* new_state;        // may alias state
     void* y;                // (batch, H, P) storage type
     int H, P, N, G;
     int heads_per_group;    // H / G
@@ -60,22 +63,68 @@ __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// four consecutive elements of B or C starting at a multiple of 4, as fp32
-template <typename T>
-__device__ __forceinline__ float4 load4(const T* p);
-template <>
-__device__ __forceinline__ float4 load4<float>(const float* p) { return *reinterpret_cast<const float4*>(p); }
-template <>
-__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    return make_float4(lo.x, lo.y, hi.x, hi.y);
+// E consecutive elements (4 or 8, starting at a multiple of E) as fp32
+template <typename T, int E>
+__device__ __forceinline__ void load_vec(const T* p, float (&v)[E]) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int k = 0; k < E; k += 4) {
+            const float4 f = *reinterpret_cast<const float4*>(p + k);
+            v[k] = f.x; v[k + 1] = f.y; v[k + 2] = f.z; v[k + 3] = f.w;
+        }
+    } else if constexpr (E == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            v[2 * k] = f.x; v[2 * k + 1] = f.y;
+        }
+    }
 }
 
-// CI: float4 column groups per lane (N/4 <= CI * L)
-template <typename T, int CI>
+// one 16-byte chunk of a state row (E = 4 fp32 or 8 bf16) as fp32, from its raw bytes (the chunks
+// are loaded raw, streamed, and unpacked only when their row is computed: fewer live registers)
+template <typename TS, int E>
+__device__ __forceinline__ void unpack_state(const uint4 u, float (&v)[E]) {
+    if constexpr (sizeof(TS) == 4) {
+        v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y); v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+    } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+            v[2 * k] = f.x; v[2 * k + 1] = f.y;
+        }
+    }
+}
+template <typename TS, int E>
+__device__ __forceinline__ void store_state(TS* p, const float (&v)[E]) {
+    uint4 u;
+    if constexpr (sizeof(TS) == 4) {
+        u = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+            w[k] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        u = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __stcs(reinterpret_cast<uint4*>(p), u);
+}
+
+// T: storage type of x, B, C, y; TS: storage type of the state; CI: 16-byte column chunks per lane
+// (N / E <= CI * L, E = 16 / sizeof(TS) state elements per chunk)
+template <typename T, typename TS, int CI>
 __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArgs a) {
+    constexpr int E = 16 / (int)sizeof(TS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int L = a.L;
     const int seg = lane / L, cl = lane % L;          // row slot within the warp, lane within the row
@@ -87,31 +136,33 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
     const int64_t bh = bh32;                          // b * H + h
     const int64_t b = bh32 / (uint32_t)a.H;
     const int g = h / a.heads_per_group;
-    const int n4 = a.N >> 2;
+    const int nch = a.N / E;                          // 16-byte chunks per state row
 
     const float decay = expf(a.dt[bh] * a.A[h]);
     const float dskip = a.D ? a.D[h] : 0.f;
 
     const T* Bp = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
     const T* Cp = static_cast<const T*>(a.C) + (b * a.G + g) * a.N;
-    float4 bv[CI], cv[CI];
+    float bv[CI][E], cv[CI][E];
 #pragma unroll
     for (int j = 0; j < CI; ++j) {
         const int c = cl + j * L;
-        if (c < n4) {
-            bv[j] = load4<T>(Bp + 4 * c);
-            cv[j] = load4<T>(Cp + 4 * c);
+        if (c < nch) {
+            load_vec<T, E>(Bp + E * c, bv[j]);
+            load_vec<T, E>(Cp + E * c, cv[j]);
         } else {
-            bv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            cv[j] = bv[j];
+#pragma unroll
+            for (int e = 0; e < E; ++e) { bv[j][e] = 0.f; cv[j][e] = 0.f; }
         }
     }
 
     const int64_t row_base = bh * a.P;                // first state row of (b, h)
     const T* xp = static_cast<const T*>(a.x) + row_base;
+    const TS* sp = static_cast<const TS*>(a.state);
+    TS* np = static_cast<TS*>(a.new_state);
     int p[kDecRowsPerThread];
     float xv[kDecRowsPerThread];
-    float4 s[kDecRowsPerThread][CI];
+    uint4 sraw[kDecRowsPerThread][CI];
 #pragma unroll
     for (int u = 0; u < kDecRowsPerThread; ++u) {
         p[u] = rb * a.rows_per_cta + u * rows_per_pass + warp * (32 / L) + seg;
@@ -119,44 +170,48 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
 #pragma unroll
         for (int j = 0; j < CI; ++j) {
             const int c = cl + j * L;
-            s[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (p[u] < a.P && c < n4)
-                s[u][j] = __ldcs(reinterpret_cast<const float4*>(a.state + (row_base + p[u]) * a.N) + c);
+            sraw[u][j] = make_uint4(0u, 0u, 0u, 0u);
+            if (p[u] < a.P && c < nch)
+                sraw[u][j] = __ldcs(reinterpret_cast<const uint4*>(sp + (row_base + p[u]) * a.N + E * c));
         }
     }
     T* yp = static_cast<T*>(a.y) + row_base;
+    const float2 dd = make_float2(decay, decay);
 #pragma unroll
     for (int u = 0; u < kDecRowsPerThread; ++u) {
-        float acc = 0.f;
+        const float2 xx = make_float2(xv[u], xv[u]);
+        float2 acc2 = make_float2(0.f, 0.f);              // packed fp32 pairs: half the FP instructions
 #pragma unroll
         for (int j = 0; j < CI; ++j) {
             const int c = cl + j * L;
-            float4 v = s[u][j];
-            v.x = fmaf(decay, v.x, xv[u] * bv[j].x);
-            v.y = fmaf(decay, v.y, xv[u] * bv[j].y);
-            v.z = fmaf(decay, v.z, xv[u] * bv[j].z);
-            v.w = fmaf(decay, v.w, xv[u] * bv[j].w);
-            acc = fmaf(v.x, cv[j].x, acc);
-            acc = fmaf(v.y, cv[j].y, acc);
-            acc = fmaf(v.z, cv[j].z, acc);
-            acc = fmaf(v.w, cv[j].w, acc);
-            if (p[u] < a.P && c < n4)
-                __stcs(reinterpret_cast<float4*>(a.new_state + (row_base + p[u]) * a.N) + c, v);
+            float sv[E], v[E];
+            unpack_state<TS, E>(sraw[u][j], sv);
+#pragma unroll
+            for (int e = 0; e < E; e += 2) {
+                const float2 nv = __ffma2_rn(dd, make_float2(sv[e], sv[e + 1]),
+                                             __fmul2_rn(xx, make_float2(bv[j][e], bv[j][e + 1])));
+                acc2 = __ffma2_rn(nv, make_float2(cv[j][e], cv[j][e + 1]), acc2);
+                v[e] = nv.x;
+                v[e + 1] = nv.y;
+            }
+            if (p[u] < a.P && c < nch) store_state<TS, E>(np + (row_base + p[u]) * a.N + E * c, v);
         }
+        float acc = acc2.x + acc2.y;
         for (int off = L >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (cl == 0 && p[u] < a.P) yp[p[u]] = from_f32<T>(fmaf(dskip, xv[u], acc));
     }
 }
 
-template <typename T>
+template <typename T, typename TS>
 cudaError_t launch_decode_t(const DecodeArgs& a, int64_t units, cudaStream_t st) {
-    const int ci = ((a.N >> 2) + a.L - 1) / a.L;
+    constexpr int E = 16 / (int)sizeof(TS);
+    const int ci = (a.N / E + a.L - 1) / a.L;
     prof_launch();
     prof_begin(st, "ssd_decode_kernel");
     if (ci <= 1)
-        ssd_decode_kernel<T, 1><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+        ssd_decode_kernel<T, TS, 1><<<(unsigned)units, kDecThreads, 0, st>>>(a);
     else
-        ssd_decode_kernel<T, 2><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+        ssd_decode_kernel<T, TS, 2><<<(unsigned)units, kDecThreads, 0, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -183,11 +238,13 @@ using namespace ssd;
 
 extern "C" {
 
-int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
-                    const void* B, const void* C, const float* D, const float* state, float* new_state, void* y,
-                    void* stream) {
+int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, const void* x, const float* dt,
+                       const float* A, const void* B, const void* C, const float* D, const void* state,
+                       void* new_state, void* y, void* stream) {
     int rc = check_decode(s, dtype);
     if (rc != SSD_OK) return rc;
+    if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    if (state_dtype == SSD_BF16 && (s->dstate & 7) != 0) return SSD_ERR_UNSUPPORTED;
     if (s->batch == 0) return SSD_OK;
     if (!x || !dt || !A || !B || !C || !state || !new_state || !y) return SSD_ERR_INVALID_ARG;
     if (!aligned(state, 16) || !aligned(new_state, 16) || !aligned(B, 16) || !aligned(C, 16) ||
@@ -195,9 +252,9 @@ int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const fl
         (D && !aligned(D, 4)))
         return SSD_ERR_INVALID_ARG;
     // new_state either is state or does not overlap it
-    const size_t stb = (size_t)s->batch * s->nheads * s->headdim * s->dstate * sizeof(float);
-    const char* s0 = reinterpret_cast<const char*>(state);
-    const char* s1 = reinterpret_cast<const char*>(new_state);
+    const size_t stb = (size_t)s->batch * s->nheads * s->headdim * s->dstate * decode_elt(state_dtype);
+    const char* s0 = static_cast<const char*>(state);
+    const char* s1 = static_cast<const char*>(new_state);
     if (s0 != s1 && s1 < s0 + stb && s0 < s1 + stb) return SSD_ERR_INVALID_ARG;
     int dev = 0, major = 0, minor = 0;
     if (note_cuda_error("cudaGetDevice", cudaGetDevice(&dev)) != cudaSuccess) return SSD_ERR_CUDA;
@@ -211,17 +268,28 @@ int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const fl
     a.state = state; a.new_state = new_state; a.y = y;
     a.H = (int)s->nheads; a.P = (int)s->headdim; a.N = (int)s->dstate; a.G = (int)s->ngroups;
     a.heads_per_group = a.H / a.G;
-    const int n4 = a.N >> 2;
+    const int nch = a.N / (state_dtype == SSD_F32 ? 4 : 8);   // 16-byte chunks per state row
     a.L = 1;
-    while (a.L < n4 && a.L < 32) a.L <<= 1;
+    while (a.L < nch && a.L < 32) a.L <<= 1;
     a.rows_per_cta = kDecWarps * (32 / a.L) * kDecRowsPerThread;
     a.row_blocks = (a.P + a.rows_per_cta - 1) / a.rows_per_cta;
     const int64_t units = s->batch * s->nheads * a.row_blocks;
     if (units > (int64_t)INT32_MAX) return SSD_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = dtype == SSD_F32 ? launch_decode_t<float>(a, units, st)
-                                           : launch_decode_t<__nv_bfloat16>(a, units, st);
+    cudaError_t e;
+    if (state_dtype == SSD_F32)
+        e = dtype == SSD_F32 ? launch_decode_t<float, float>(a, units, st)
+                             : launch_decode_t<__nv_bfloat16, float>(a, units, st);
+    else
+        e = dtype == SSD_F32 ? launch_decode_t<float, __nv_bfloat16>(a, units, st)
+                             : launch_decode_t<__nv_bfloat16, __nv_bfloat16>(a, units, st);
     return note_cuda_error("decode launch", e) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                    const void* B, const void* C, const float* D, const float* state, float* new_state, void* y,
+                    void* stream) {
+    return ssd_decode_step_ex(s, dtype, SSD_F32, x, dt, A, B, C, D, state, new_state, y, stream);
 }
 
 size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
@@ -237,11 +305,13 @@ size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
     return tot > 0 ? tot : 256;
 }
 
-int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
-                         const void* B, const void* C, const float* D, const float* state, float* new_state,
-                         void* y, void* device_buffer, size_t device_buffer_bytes, void* stream) {
+int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, const void* x,
+                            const float* dt, const float* A, const void* B, const void* C, const float* D,
+                            const void* state, void* new_state, void* y, void* device_buffer,
+                            size_t device_buffer_bytes, void* stream) {
     int rc = check_decode(s, dtype);
     if (rc != SSD_OK) return rc;
+    if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     const size_t need = ssd_decode_host_buffer_size(s, dtype);
     if (!device_buffer || !aligned(device_buffer, 256) || device_buffer_bytes < need) return SSD_ERR_WORKSPACE;
     if (s->batch == 0) return SSD_OK;
@@ -249,7 +319,8 @@ int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, con
     const size_t e = decode_elt(dtype);
     const size_t rows = (size_t)s->batch * s->nheads;
     const size_t xb = rows * s->headdim * e, dtb = rows * 4, hb = (size_t)s->nheads * 4;
-    const size_t bcb = (size_t)s->batch * s->ngroups * s->dstate * e, stb = rows * s->headdim * s->dstate * 4;
+    const size_t bcb = (size_t)s->batch * s->ngroups * s->dstate * e;
+    const size_t stb = rows * s->headdim * s->dstate * decode_elt(state_dtype);
     char* base = static_cast<char*>(device_buffer);
     size_t off = 0;
     auto carve = [&](size_t bytes) { char* p = base + off; off += align256(bytes); return p; };
@@ -274,13 +345,20 @@ int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, con
     h2d(dC, C, bcb);
     h2d(dS, state, stb);
     if (note_cuda_error("decode host copy in", err) != cudaSuccess) return SSD_ERR_CUDA;
-    rc = ssd_decode_step(s, dtype, dx, (const float*)ddt, (const float*)dA, dB, dC, D ? (const float*)dD : nullptr,
-                         (const float*)dS, (float*)dS, dy, stream);
+    rc = ssd_decode_step_ex(s, dtype, state_dtype, dx, (const float*)ddt, (const float*)dA, dB, dC,
+                            D ? (const float*)dD : nullptr, dS, dS, dy, stream);
     if (rc != SSD_OK) return rc;
     err = cudaMemcpyAsync(y, dy, xb, cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaMemcpyAsync(new_state, dS, stb, cudaMemcpyDeviceToHost, st);
     if (err == cudaSuccess) err = cudaStreamSynchronize(st);
     return note_cuda_error("decode host copy out", err) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                         const void* B, const void* C, const float* D, const float* state, float* new_state,
+                         void* y, void* device_buffer, size_t device_buffer_bytes, void* stream) {
+    return ssd_decode_step_host_ex(s, dtype, SSD_F32, x, dt, A, B, C, D, state, new_state, y, device_buffer,
+                                   device_buffer_bytes, stream);
 }
 
 }  // extern "C"

@@ -35,6 +35,7 @@ class Workload:
     varlen_total: int = 0     # >0: one packed row of this many tokens, split into segments
     seg_min: int = 64
     seg_max: int = 4096
+    state_dtype: str = "f32"  # recurrent-step workloads: storage type of the carried state
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -54,6 +55,9 @@ WORKLOADS = {
     # one recurrent step for 64 carried states of a Mamba-2-2.7B-shaped layer (seqlen 1; the
     # initial state is the carried state)
     "decode_2p7b": Workload("decode_2p7b", 64, 1, 80, 64, 128, 1, 256, "bf16", 1005, init_state=True),
+    # the same step with the carried state stored in bf16 (the state is rounded to bf16 once on the host)
+    "decode_2p7b_bf16state": Workload("decode_2p7b_bf16state", 64, 1, 80, 64, 128, 1, 256, "bf16", 1005,
+                                      init_state=True, state_dtype="bf16"),
 }
 
 
@@ -113,6 +117,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
         init = (rng.standard_normal((nseq, H, P, N), dtype=np.float32) * np.float32(0.1)).astype(np.float32)
     if w.dtype == "bf16":
         x, B, C = bf16_round(x), bf16_round(B), bf16_round(C)
+    if init is not None and w.state_dtype == "bf16":
+        init = bf16_round(init)
     return dict(x=x, dt=dt, A=A, B=B, C=C, D=D, initial_state=init, cu_seqlens=cu)
 
 

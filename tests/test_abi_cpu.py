@@ -120,3 +120,15 @@ def test_decode_argument_errors_before_any_device_work(lib):
     rc = lib.ssd_decode_step_host(ctypes.byref(s), bd.SSD_BF16, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE,
                                   FAKE, FAKE, 16, None)
     assert rc == bd.SSD_ERR_WORKSPACE
+
+
+def test_decode_state_dtype_errors(lib):
+    s = shape(batch=4, T=1)
+    call = lambda sh, sd: lib.ssd_decode_step_ex(ctypes.byref(sh), bd.SSD_BF16, sd, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                  None, FAKE, FAKE, FAKE, None)
+    assert call(s, 7) == bd.SSD_ERR_INVALID_ARG                                # unknown state type
+    assert call(shape(batch=4, T=1, N=20), bd.SSD_BF16) == bd.SSD_ERR_UNSUPPORTED   # bf16 state: N % 8
+    assert call(shape(batch=0, T=1), bd.SSD_BF16) == bd.SSD_OK
+    rc = lib.ssd_decode_step_host_ex(ctypes.byref(s), bd.SSD_BF16, 7, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                     FAKE, FAKE, FAKE, 1 << 40, None)
+    assert rc == bd.SSD_ERR_INVALID_ARG
