@@ -150,20 +150,17 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 // Barrier slots in shared memory
 enum {
     kBarFullX0 = 0, kBarFullX1, kBarFullBC0, kBarFullBC1, kBarEmpty0, kBarEmpty1,
-    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarWX1a, kBarWX1b, kBarS, kBarYFree, kBarAgg, kBarMath,
+    kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarS, kBarYFree,
     kNumBars
 };
 
-// Pass-1 weights use one barrier per stage (kBarWX1a + stage): the math warps may weight the
-// next stage's tile before the MMA warp has consumed this one, and a second arrival on the same
-// barrier before the first was waited for would make the waiter miss a phase.
 // Expected arrivals per phase: the x barrier = producer's expect_tx + its "cumsum written"
 // arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16); MMA
 // commits 1.
 __device__ __forceinline__ uint32_t bar_count(int i) {
     switch (i) {
         case kBarFullX0: case kBarFullX1: return 2;
-        case kBarLG: case kBarST: case kBarWX: case kBarYFree: case kBarWX1a: case kBarWX1b: case kBarMath:
+        case kBarLG: case kBarST: case kBarWX: case kBarYFree:
             return 16;
         default: return 1;
     }
@@ -173,6 +170,7 @@ __device__ __forceinline__ uint32_t bar_count(int i) {
 // arrival), an empty barrier (MMA commit) and a weights barrier (one arrival per math warp), plus
 // the aggregate barrier (MMA commit after a window's last tile).
 constexpr int kBarAFull0 = 0;   // + s: full, + 3 + s: empty, + 6 + s: weights, + 9: aggregate
+static_assert(kBarAFull0 + 10 <= kNumBars, "phase A reuses the first ten barrier slots");
 // Phase-A windows per CTA whose totals are precomputed together (more fall back to the producer)
 constexpr int kMaxWinA = 96;
 
@@ -204,13 +202,12 @@ struct Smem {
     // unused area (32 KB for either state size)
     __device__ float* tota() const { return csa(0) + 1024; }
     __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion); }
-    // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128] (pass 1: relative to
-    // the segment start) and 4 floats of per-tile values (pass 1: the segment totals)
+    // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128], and 4 floats after it
+    // (phase A keeps the window's two totals there, in its own copy of these tables)
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * 260; }
     // exp(cs_p - cs_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
     __device__ float* vt() const { return cs(0) + 520; }
-    __device__ float* misc() const { return cs(0) + 520 + 192; }                                     // [8]
-    __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(misc() + 8); }           // [kNumBars]
+    __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(vt() + 192); }           // [kNumBars]
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
 };
@@ -234,8 +231,6 @@ __device__ void init_bars_c(const Smem& sm) {
 // may go on.
 __device__ bool grid_sync(const Smem& sm, const FusedArgs& a, int k);
 
-// misc[] layout
-enum { kMiscA0 = 0, kMiscA1, kMiscTot0, kMiscTot1, kMiscCarry0, kMiscCarry1, kMiscD0, kMiscD1 };
 
 // Bounded mbarrier wait that also gives up once the CTA is aborting.
 // `phases` holds one parity bit per barrier (bit idx), kept in a register.
@@ -1235,7 +1230,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 template <int N>
 size_t fused_smem_bytes() {
     const size_t stage = 2 * kRegion + 2 * (N / 64) * kRegion;
-    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (520 + 192 + 8) * 4 + kNumBars * 8 + 16;
+    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (520 + 192) * 4 + kNumBars * 8 + 16;
 }
 
 template <int N>
