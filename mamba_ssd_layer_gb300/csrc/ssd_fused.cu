@@ -56,6 +56,7 @@ constexpr uint32_t kColGB = 256;   // two 128-column buffers, alternating per ti
 
 struct FusedMaps {
     CUtensorMap x, b, c;
+    CUtensorMap y;              // y as (64, H, rows), 64 x 1 x 32 boxes: one row quadrant of one head
 };
 
 struct FusedArgs {
@@ -151,13 +152,15 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 enum {
     kBarFullX0 = 0, kBarFullX1, kBarFullBC0, kBarFullBC1, kBarEmpty0, kBarEmpty1,
     kBarG, kBarLG, kBarYD, kBarST, kBarYO, kBarWX, kBarS, kBarYFree,
-    kNumBars
+    kBarPair0,                       // + qd + 4 * (kq / 2): the two warps that stage one head of a row quadrant
+    kNumBars = kBarPair0 + 8
 };
 
 // Expected arrivals per phase: the x barrier = producer's expect_tx + its "cumsum written"
 // arrival; the B/C barrier = the expect_tx alone; math-warp signals one per math warp (16); MMA
-// commits 1.
+// commits 1; a warp-pair barrier one per warp.
 __device__ __forceinline__ uint32_t bar_count(int i) {
+    if (i >= kBarPair0) return 2;
     switch (i) {
         case kBarFullX0: case kBarFullX1: return 2;
         case kBarLG: case kBarST: case kBarWX: case kBarYFree:
@@ -1027,7 +1030,22 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         };
         // state step of stage st: h_{t-1} (this thread's state columns) to bf16 in the staging area for
         // Yo, and a_t h_{t-1} back into TMEM for S(t) to accumulate onto
+        // The two warps (kq = 2 hh, 2 hh + 1) of a row quadrant that stage head hh's rows meet on their
+        // own barrier (bounded like every wait, so an aborting partner cannot leave the other stuck).
+        // Both take every meeting point in the same order, so its phases stay in step.
+        auto pair_sync = [&]() {
+            const int idx = kBarPair0 + qd + 4 * (kq >> 1);
+            warp_arrive(sm, idx);
+            return wait_bar_warp(sm, idx, ph, a);
+        };
+        // the staging bytes of this warp pair's last bulk store may be overwritten once the store has
+        // read them: the issuing lane waits for that, then the pair meets
+        auto ystage_release = [&]() {
+            if ((kq & 1) == 0 && lane == 0) bulk_wait_read_all();
+            return pair_sync();
+        };
         auto state_step = [&](int st, int len) {
+            if (!ystage_release()) return false;
             const float* cs = sm.cs(st);
             const float at = ex2(cs[hrow * 128 + len - 1]);
             const float2 aa = make_float2(at, at);
@@ -1051,13 +1069,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             st_store(nq0, NQ, v);
             tmem_wait_st();
+            return true;
         };
         // y = Yd + e Yo for row i, head kq / 2, channels 32 (kq % 2) .. + 31, with e = exp(cs_i) (read
         // from the stage before it was released: the stage may be refilled by now) and Yo in buffer gcol.
-        // The warp stages its 32 rows x 64 bytes (x layout) and writes them back four lanes per row, so
-        // that each store instruction covers eight whole 64-byte row pieces. For N = 128 the staging bytes
-        // are exactly those this warp's state step writes (state columns kq N/4 .. = head kq / 2's region,
-        // chunks 4 (kq % 2) ..), which it overwrites only after this read-back.
+        // The warp stages its 32 rows x 64 bytes (x layout). A row quadrant that lies wholly inside the
+        // sequence goes out as one bulk tensor store per head; otherwise (and when adding onto y) the
+        // warp writes its rows back four lanes per row, so that each store instruction covers eight
+        // whole 64-byte row pieces. For N = 128 the staging bytes are exactly those this warp's state
+        // step writes (state columns kq N/4 .. = head kq / 2's region, chunks 4 (kq % 2) ..); the state
+        // step first waits until the bulk store has read them (ystage_release).
         auto epilogue = [&](float e, int len, int row0, int h0, uint32_t gcol) {
             const int hh = kq >> 1, c0 = 32 * (kq & 1);
             const int i = row;
@@ -1080,6 +1101,17 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     vu[m] = pack_bf16x2(r.x, r.y);
                 }
                 *reinterpret_cast<uint4*>(stg + sw128_offset(i, (c0 + k) / 8)) = v;
+            }
+            if (!a.y_accum && 32 * qd + 32 <= len) {
+                // the quadrant's 32 rows all belong to the sequence: the two warps holding its two halves
+                // of the head's 64 channels meet, and one bulk tensor store writes the 4 KB
+                fence_proxy_async_smem();
+                if (!pair_sync()) return false;
+                if ((kq & 1) == 0 && lane == 0) {
+                    tma_store_3d(&maps.y, stg + 32 * qd * 128, 0, h0 + hh, row0 + 32 * qd);
+                    bulk_commit_group();
+                }
+                return true;
             }
             __syncwarp();
             const int cl = (c0 >> 3) + (lane & 3);          // 16-byte chunk of the row this lane writes
@@ -1104,6 +1136,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
             }
             __syncwarp();
+            return true;
         };
 
         for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
@@ -1149,7 +1182,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 tc_fence_after_sync();
                 const float e_row = ex2(cs[(kq >> 1) * 128 + row]);   // for this tile's epilogue
-                state_step(st, len);
+                ok = state_step(st, len);
+                if (!ok) break;
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(sm, kBarST);
@@ -1167,7 +1201,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 ok = wait_bar_warp(sm, kBarYO, ph, a);
                 if (!ok) break;
                 tc_fence_after_sync();
-                epilogue(e_row, len, row0, h0, kColGB + 128 * (kt & 1));
+                ok = epilogue(e_row, len, row0, h0, kColGB + 128 * (kt & 1));
+                if (!ok) break;
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(sm, kBarYFree);
@@ -1190,6 +1225,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             tc_fence_before_sync();
         }
+        // the bulk stores of y issued by this lane complete before the CTA's shared memory goes away
+        if ((kq & 1) == 0 && lane == 0) bulk_wait_all();
         if (!ok) *reinterpret_cast<volatile int*>(sm.abort_flag()) = 1;
     }
 
@@ -1206,9 +1243,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // 3-D view (inner, mid, rows) of a bf16 tensor whose mid and row strides are mid_stride and row_stride
-// elements (inner is contiguous), boxes of 64 x 1 x 128 with the 128-byte swizzle
+// elements (inner is contiguous), boxes of 64 x 1 x box_rows with the 128-byte swizzle
 bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64_t rows, int64_t mid_stride,
-                    int64_t row_stride) {
+                    int64_t row_stride, int box_rows = kTile) {
     static EncodeTiledFn enc = nullptr;
     if (!enc) {
         void* fp = nullptr;
@@ -1220,7 +1257,7 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
     }
     cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)(rows > 0 ? rows : 1)};
     cuuint64_t strides[2] = {(cuuint64_t)(mid_stride * 2), (cuuint64_t)(row_stride * 2)};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTile};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1298,7 +1335,8 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     const __nv_bfloat16* Cp = static_cast<const __nv_bfloat16*>(p.C) + (int64_t)part * N;
     if (!make_map_fused(&maps.x, p.x, 64, H, p.rows, 64, (int64_t)64 * H) ||
         !make_map_fused(&maps.b, Bp, N, G, p.rows, Nf, (int64_t)Nf * G) ||
-        !make_map_fused(&maps.c, Cp, N, G, p.rows, Nf, (int64_t)Nf * G))
+        !make_map_fused(&maps.c, Cp, N, G, p.rows, Nf, (int64_t)Nf * G) ||
+        !make_map_fused(&maps.y, p.y, 64, H, p.rows, 64, (int64_t)64 * H, 32))
         return note_cuda_error("fused tensor maps", cudaErrorInvalidValue);
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
     FusedArgs fa;
