@@ -425,6 +425,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     }
     const int64_t np = a.npieces;
     if (np == 0 || (a.dense && a.nt_dense == 0)) return;
+    // phase C visits this CTA's windows in the reverse of phase A's order: its first tiles are then the
+    // ones it aggregated last, whose x and B may still be in L2
+    const int64_t pc_count = np > (int64_t)blockIdx.x ? (np - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     // phase A visits the windows with a successor: for a dense batch the first W - 1 window ranks of
     // every chain (the dispatch order puts them first), for a packed batch every window, skipping ends
     const int64_t nA = a.dense ? (int64_t)a.nseq * a.npairs * (a.W_dense - 1) : np;
@@ -783,9 +786,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         uint32_t ph = 0, issued = 0, p2 = 0;
         int stage = 0;
         bool ok = true;
-        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+        for (int64_t kd = pc_count - 1; kd >= 0 && ok; --kd) {
+            const int64_t d = blockIdx.x + kd * gridDim.x;
             const Piece c = decode_piece(d, a);
-            if (!c.valid) break;
+            if (!c.valid) continue;
             const int h0 = 2 * c.hp;
             const float Al[2] = {__ldg(a.A + h0) * kLog2e, __ldg(a.A + h0 + 1) * kLog2e};
             for (int t = c.t0; t < c.t1 && ok; ++t) {
@@ -852,9 +856,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 mma_commit(sm.bars() + kBarG);
             };
-            for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+            for (int64_t kd = pc_count - 1; kd >= 0 && ok; --kd) {
+                const int64_t d = blockIdx.x + kd * gridDim.x;
                 const Piece c = decode_piece(d, a);
-                if (!c.valid) break;
+                if (!c.valid) continue;
                 // per tile t (tcgen05.mma runs in issue order, so a later MMA never overtakes an earlier
                 // one's reads of the same TMEM). The tile's C B^T buffer gb holds C B^T, then L o C B^T,
                 // then Yo; the other buffer gn takes C B^T of the next tile.
@@ -1139,9 +1144,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             return true;
         };
 
-        for (int64_t d = blockIdx.x; d < np && ok; d += gridDim.x) {
+        for (int64_t kd = pc_count - 1; kd >= 0 && ok; --kd) {
+            const int64_t d = blockIdx.x + kd * gridDim.x;
             const Piece c = decode_piece(d, a);
-            if (!c.valid) break;
+            if (!c.valid) continue;
             const int h0 = 2 * c.hp;
             const float Dlg0 = a.D ? __ldg(a.D + h0) : 0.f;
             const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
