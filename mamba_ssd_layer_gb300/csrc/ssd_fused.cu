@@ -452,7 +452,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 
     // math-warp geometry (warps 2..17): four per TMEM lane quadrant qd (the rows 32 qd .. 32 qd + 31
     // a warp may access); kq (0..3) picks the warp's share of the columns in every phase:
-    //   L o G       column block 32 kq .. 32 kq + 31 (both heads)
+    //   L o G       16-column groups kq and 7 - kq (both heads)
     //   state       state columns kq N/4 .. (kq + 1) N/4
     //   epilogue    head kq / 2, channels 32 (kq % 2) .. + 31
     const int mt = tid - 64;                 // 0..511
