@@ -1050,12 +1050,15 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             return pair_sync();
         };
         auto state_step = [&](int st, int len) {
-            if (!ystage_release()) return false;
+            // the state's TMEM load is in flight while the warp pair meets (it touches no shared memory)
+            float v[NQ];
+            for (int k = 0; k < NQ; k += 16) tmem_ld16_nowait(lane_base + kColST + nq0 + k, v + k);
+            const bool released = ystage_release();
+            tmem_wait_ld();
+            if (!released) return false;
             const float* cs = sm.cs(st);
             const float at = ex2(cs[hrow * 128 + len - 1]);
             const float2 aa = make_float2(at, at);
-            float v[NQ];
-            st_load(nq0, NQ, v);
 #pragma unroll
             for (int cc = 0; cc < NQ; cc += 8) {
                 const int n = nq0 + cc;
