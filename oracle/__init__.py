@@ -64,6 +64,11 @@ def _load():
                                            ctypes.POINTER(ctypes.c_int32), i64,
                                            dp, dp, ctypes.c_int]
             lib.ssd_oracle_f64.restype = ctypes.c_int
+            lib.ssd_oracle_f64_ex.argtypes = [i64, i64, i64, i64, i64, i64,
+                                              dp, dp, dp, dp, dp, dp, dp,
+                                              ctypes.POINTER(ctypes.c_int32), i64,
+                                              dp, dp, ctypes.c_int, ctypes.c_int]
+            lib.ssd_oracle_f64_ex.restype = ctypes.c_int
             lib.ssd_oracle_default_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -82,7 +87,7 @@ def _ptr(a, ctype=ctypes.c_double):
 
 
 def ssd_recurrence(x, dt, A, B, C, D=None, initial_state=None, cu_seqlens=None,
-                   nthreads: int = 0, return_final: bool = True):
+                   nthreads: int = 0, return_final: bool = True, scale_x_by_dt: bool = False):
     """fp64 recurrence. Shapes follow the library's call:
 
     x (batch, T, H, P); dt (batch, T, H); A (H,); B, C (batch, T, G, N); D (H,) or None;
@@ -90,7 +95,8 @@ def ssd_recurrence(x, dt, A, B, C, D=None, initial_state=None, cu_seqlens=None,
     is required and the row is split into sequences at those offsets).
 
     Returns ``(y, final_state)`` as float64 arrays; ``y`` has x's shape and
-    ``final_state`` is (nseq, H, P, N), nseq = batch for a dense call.
+    ``final_state`` is (nseq, H, P, N), nseq = batch for a dense call. With ``scale_x_by_dt`` the
+    input term is ``dt_t x_t (outer) B_t`` (the skip term keeps ``D x_t``).
     """
     x, dt, A, B, C, D, init = (_f64(v) for v in (x, dt, A, B, C, D, initial_state))
     batch, T, H, P = x.shape
@@ -107,9 +113,10 @@ def ssd_recurrence(x, dt, A, B, C, D=None, initial_state=None, cu_seqlens=None,
         assert init.shape == (nseq, H, P, N)
     y = np.empty_like(x)
     final = np.empty((nseq, H, P, N), dtype=np.float64) if return_final else None
-    rc = _load().ssd_oracle_f64(batch, T, H, P, N, G,
-                                _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
-                                _ptr(cu, ctypes.c_int32), nseq, _ptr(y), _ptr(final), int(nthreads))
+    rc = _load().ssd_oracle_f64_ex(batch, T, H, P, N, G,
+                                   _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(init),
+                                   _ptr(cu, ctypes.c_int32), nseq, _ptr(y), _ptr(final), 1 if scale_x_by_dt else 0,
+                                   int(nthreads))
     if rc != 0:
         raise RuntimeError(f"ssd_oracle_f64 failed with code {rc}")
     return y, final

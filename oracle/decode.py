@@ -21,12 +21,13 @@ from __future__ import annotations
 import numpy as np
 
 
-def ssd_decode_step(state, x, dt, A, B, C, D=None):
+def ssd_decode_step(state, x, dt, A, B, C, D=None, scale_x_by_dt=False):
     """One recurrent step.
 
     state (batch, H, P, N); x (batch, H, P); dt (batch, H); A (H,); B, C (batch, G, N);
     D (H,) or None. Returns ``(y, new_state)`` as float64 arrays of shapes (batch, H, P)
-    and (batch, H, P, N); the inputs are not modified.
+    and (batch, H, P, N); the inputs are not modified. With ``scale_x_by_dt`` the input term
+    is ``dt x (outer) B`` and the skip term keeps ``D x``.
     """
     S = np.array(state, dtype=np.float64, copy=True)
     x = np.asarray(x, dtype=np.float64)
@@ -43,7 +44,8 @@ def ssd_decode_step(state, x, dt, A, B, C, D=None):
         for h in range(H):
             g = h // (H // G)
             a = np.exp(dt[b, h] * A[h])
-            S[b, h] = a * S[b, h] + np.outer(x[b, h], B[b, g])
+            xin = x[b, h] * dt[b, h] if scale_x_by_dt else x[b, h]
+            S[b, h] = a * S[b, h] + np.outer(xin, B[b, g])
             y[b, h] = S[b, h] @ C[b, g]
             if D is not None:
                 y[b, h] += float(D[h]) * x[b, h]

@@ -34,6 +34,11 @@
  *     starts from its own initial state (zero when none is given).
  *   - grouped B, C (a group of H/G consecutive heads shares B_t, C_t):
  *     "LLM(十一)——Mamba", §3.6 (multi-input / grouped-value head patterns).
+ *   - optional input scaling by dt (ssd_oracle_f64_ex with scale_x_by_dt): the input term becomes
+ *     dt_t * x_t (outer) B_t while the skip term keeps D_h * x_t. This is the discretization the
+ *     full model keeps from Mamba ("LLM(十一)——Mamba" §3.5.4: the parameters are transformed
+ *     before they enter the SSD code; "Transformers是SSMs (一)" §2.1, Remark 1), read as
+ *     B-bar = dt * B; the pages do not print the formula itself.
  *
  * Layouts (all row-major, contiguous, fp64):
  *   x, y        (rows, H, P)   rows = batch*seqlen (dense) or total tokens
@@ -54,6 +59,7 @@
 
 typedef struct {
     int64_t H, P, N, G;
+    int scale_x_by_dt;
     const double *x, *dt, *A, *B, *C, *D, *init;
     const int64_t *seq_start, *seq_len;
     int64_t nseq;
@@ -76,7 +82,9 @@ static void run_unit(oracle_job *j, int64_t s, int64_t h, double *S)
         memset(S, 0, sizeof(double) * P * N);
 
     for (int64_t t = j->seq_start[s]; t < j->seq_start[s] + j->seq_len[s]; ++t) {
-        const double a = exp(j->dt[t * H + h] * A_h);
+        const double dt_th = j->dt[t * H + h];
+        const double a = exp(dt_th * A_h);
+        const double in_scale = j->scale_x_by_dt ? dt_th : 1.0;
         const double *xt = j->x + (t * H + h) * P;
         const double *Bt = j->B + (t * G + g) * N;
         const double *Ct = j->C + (t * G + g) * N;
@@ -84,9 +92,10 @@ static void run_unit(oracle_job *j, int64_t s, int64_t h, double *S)
         for (int64_t p = 0; p < P; ++p) {
             double *Sp = S + p * N;
             const double xp = xt[p];
+            const double xin = in_scale * xp;
             double acc = 0.0;
             for (int64_t n = 0; n < N; ++n) {
-                Sp[n] = a * Sp[n] + xp * Bt[n];
+                Sp[n] = a * Sp[n] + xin * Bt[n];
                 acc += Sp[n] * Ct[n];
             }
             yt[p] = acc + D_h * xp;
@@ -121,13 +130,13 @@ int ssd_oracle_default_threads(void)
 
 /*
  * Returns 0 on success, 1 on bad arguments, 2 on allocation failure.
- * nthreads <= 0 uses every online core.
+ * nthreads <= 0 uses every online core. scale_x_by_dt != 0 selects the dt-scaled input term.
  */
-int ssd_oracle_f64(int64_t batch, int64_t seqlen, int64_t H, int64_t P, int64_t N, int64_t G,
-                   const double *x, const double *dt, const double *A,
-                   const double *B, const double *C, const double *D,
-                   const double *init, const int32_t *cu_seqlens, int64_t nseq,
-                   double *y, double *final_state, int nthreads)
+int ssd_oracle_f64_ex(int64_t batch, int64_t seqlen, int64_t H, int64_t P, int64_t N, int64_t G,
+                      const double *x, const double *dt, const double *A,
+                      const double *B, const double *C, const double *D,
+                      const double *init, const int32_t *cu_seqlens, int64_t nseq,
+                      double *y, double *final_state, int scale_x_by_dt, int nthreads)
 {
     if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) return 1;
     if (!x || !dt || !A || !B || !C || !y) return 1;
@@ -152,6 +161,7 @@ int ssd_oracle_f64(int64_t batch, int64_t seqlen, int64_t H, int64_t P, int64_t 
 
     oracle_job j;
     j.H = H; j.P = P; j.N = N; j.G = G;
+    j.scale_x_by_dt = scale_x_by_dt;
     j.x = x; j.dt = dt; j.A = A; j.B = B; j.C = C; j.D = D; j.init = init;
     j.seq_start = start; j.seq_len = len; j.nseq = nseq;
     j.y = y; j.final_state = final_state;
@@ -179,4 +189,15 @@ int ssd_oracle_f64(int64_t batch, int64_t seqlen, int64_t H, int64_t P, int64_t 
     free(start);
     free(len);
     return rc;
+}
+
+/* The recurrence without input scaling. */
+int ssd_oracle_f64(int64_t batch, int64_t seqlen, int64_t H, int64_t P, int64_t N, int64_t G,
+                   const double *x, const double *dt, const double *A,
+                   const double *B, const double *C, const double *D,
+                   const double *init, const int32_t *cu_seqlens, int64_t nseq,
+                   double *y, double *final_state, int nthreads)
+{
+    return ssd_oracle_f64_ex(batch, seqlen, H, P, N, G, x, dt, A, B, C, D, init, cu_seqlens, nseq, y,
+                             final_state, 0, nthreads);
 }

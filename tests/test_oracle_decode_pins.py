@@ -104,3 +104,29 @@ def test_inputs_are_not_modified():
     keep = S.copy()
     oracle.ssd_decode_step(S, x, dt, A, B, C, D)
     assert np.array_equal(S, keep)
+
+
+def test_dt_scaled_step_closed_form_and_chain():
+    rng = np.random.default_rng(27)
+    S, x, dt, A, B, C, D = rand_step(rng, G=1)
+    y, S1 = oracle.ssd_decode_step(S, x, dt, A, B, C, D, scale_x_by_dt=True)
+    for b in range(S.shape[0]):
+        for h in range(S.shape[1]):
+            a = np.exp(dt[b, h] * A[h])
+            Sr = a * S[b, h] + dt[b, h] * np.outer(x[b, h], B[b, 0])
+            assert rel(S1[b, h], Sr) < 1e-15
+            assert rel(y[b, h], Sr @ C[b, 0] + D[h] * x[b, h]) < 1e-14
+    # chained steps equal the pinned recurrence with the same option
+    T, batch, H, P, N = 7, 2, 3, 4, 5
+    xs = rng.standard_normal((batch, T, H, P))
+    dts = np.logaddexp(0, rng.standard_normal((batch, T, H)) - 1.0)
+    Bs = rng.standard_normal((batch, T, 1, N)) / np.sqrt(N)
+    Cs = rng.standard_normal((batch, T, 1, N)) / np.sqrt(N)
+    A3, D3 = -np.exp(rng.uniform(0, np.log(16), H)), rng.standard_normal(H)
+    h0 = 0.1 * rng.standard_normal((batch, H, P, N))
+    yr, fr = oracle.ssd_recurrence(xs, dts, A3, Bs, Cs, D3, h0, scale_x_by_dt=True)
+    St = h0
+    for t in range(T):
+        yt, St = oracle.ssd_decode_step(St, xs[:, t], dts[:, t], A3, Bs[:, t], Cs[:, t], D3, scale_x_by_dt=True)
+        assert rel(yt, yr[:, t]) < 1e-12
+    assert rel(St, fr) < 1e-12

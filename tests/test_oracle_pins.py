@@ -196,3 +196,44 @@ def test_workload_inputs_follow_recipe():
     cu = v["cu_seqlens"]
     assert cu[0] == 0 and cu[-1] == 9000 and (np.diff(cu) > 0).all()
     assert (np.diff(cu)[:-1] >= 64).all() and (np.diff(cu) <= 4096).all()
+
+
+# ---------------------------------------------------------------- dt-scaled input term
+@pytest.mark.parametrize("T,G", [(1, 1), (23, 1), (48, 2)])
+def test_dt_scaled_input_against_quadratic_form(T, G):
+    # dt x as the input term equals the dense quadratic form on dt o x, with the skip on the unscaled x
+    x, dt, A, B, C, D, h0 = rand_problem(np.random.default_rng(70 + T + G), T=T, G=G, H=4)
+    y_s, f_s = oracle.ssd_recurrence(x, dt, A, B, C, D, h0, scale_x_by_dt=True)
+    xs = x * dt[..., None]
+    y_q, f_q = ssd_quadratic(xs, dt, A, B, C, None, h0)
+    assert rel(y_s, y_q + D[None, None, :, None] * x) < 1e-12
+    assert rel(f_s, f_q) < 1e-12
+
+
+def test_dt_scaled_input_one_token_closed_form():
+    rng = np.random.default_rng(73)
+    x, dt, A, B, C, D, h0 = rand_problem(rng, batch=1, T=1, H=2, P=3, N=4, G=1)
+    y, f = oracle.ssd_recurrence(x, dt, A, B, C, D, h0, scale_x_by_dt=True)
+    for h in range(2):
+        a = np.exp(dt[0, 0, h] * A[h])
+        S = a * h0[0, h] + dt[0, 0, h] * np.outer(x[0, 0, h], B[0, 0, 0])
+        assert rel(f[0, h], S) < 1e-15
+        assert rel(y[0, 0, h], S @ C[0, 0, 0] + D[h] * x[0, 0, h]) < 1e-14
+
+
+def test_dt_scaled_input_packed_and_unit_dt():
+    # with dt = 1 the option changes nothing; packed sequences still reset at every boundary
+    rng = np.random.default_rng(74)
+    x, dt, A, B, C, D, _ = rand_problem(rng, batch=1, T=60, H=2, G=1, init=False)
+    one = np.ones_like(dt)
+    y1, f1 = oracle.ssd_recurrence(x, one, A, B, C, D, None, scale_x_by_dt=True)
+    y0, f0 = oracle.ssd_recurrence(x, one, A, B, C, D, None)
+    assert np.array_equal(y1, y0) and np.array_equal(f1, f0)
+    cu = np.array([0, 17, 17, 60], dtype=np.int32)
+    yp, fp = oracle.ssd_recurrence(x, dt, A, B, C, D, None, cu_seqlens=cu, scale_x_by_dt=True)
+    for s in range(3):
+        a, b = cu[s], cu[s + 1]
+        ys, fs = oracle.ssd_recurrence(x[:, a:b], dt[:, a:b], A, B[:, a:b], C[:, a:b], D, None,
+                                       scale_x_by_dt=True)
+        assert rel(yp[:, a:b], ys) < 1e-13 if b > a else True
+        assert rel(fp[s], fs[0]) < 1e-13 if b > a else np.array_equal(fp[s], np.zeros_like(fp[s]))
