@@ -370,7 +370,7 @@ def run_reference(args, w):
     for _ in range(args.steps):
         t0 = time.perf_counter()
         oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
-                              d["cu_seqlens"], nthreads=threads)
+                              d["cu_seqlens"], nthreads=threads, scale_x_by_dt=w.scale_x_by_dt)
         times.append(time.perf_counter() - t0)
     tot = float(np.sum(times))
     val = tokens * args.steps / tot
@@ -386,7 +386,8 @@ def run_reference(args, w):
 
 def config_dict(w):
     return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
-            "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk, "parallelism": "replicas",
+            "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk, "scale_x_by_dt": w.scale_x_by_dt,
+            "parallelism": "replicas",
             "l2": "inputs larger than L2 (2 rotating input sets of ~350 MB each)"}
 
 
@@ -401,7 +402,7 @@ def cpu_baseline(w, budget_tokens: int, min_seconds: float = 10.0, max_runs: int
     runs, t0 = 0, time.perf_counter()
     while runs < max_runs and (runs == 0 or time.perf_counter() - t0 < min_seconds):
         oracle.ssd_recurrence(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["initial_state"],
-                              d["cu_seqlens"], nthreads=threads)
+                              d["cu_seqlens"], nthreads=threads, scale_x_by_dt=w.scale_x_by_dt)
         runs += 1
     dt = time.perf_counter() - t0
     return {"value": tokens * runs / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -469,7 +470,8 @@ def main():
     def step(i):
         t = sets[i % 2]
         ssd_forward(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], chunk=w.chunk, initial_state=t["init"],
-                    cu_seqlens=t["cu"], y=t["y"], final_state=t["final"], workspace=workspace, stream=stream)
+                    cu_seqlens=t["cu"], y=t["y"], final_state=t["final"], workspace=workspace, stream=stream,
+                    scale_x_by_dt=w.scale_x_by_dt)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -517,7 +519,7 @@ def main():
         nonlocal devbuf
         _, _ = ssd_forward_host(hx["x"], hf["dt"], hf["A"], hx["B"], hx["C"], hf["D"], chunk=w.chunk,
                                 initial_state=hinit, cu_seqlens=hcu, y=hy, final_state=hfin,
-                                device_buffer=devbuf, stream=stream)
+                                device_buffer=devbuf, stream=stream, scale_x_by_dt=w.scale_x_by_dt)
 
     import ctypes
     shp = bd._shape(1 if hcu is not None else d["x"].shape[0], d["x"].shape[1], w.nheads, w.headdim, w.dstate,

@@ -103,6 +103,31 @@ int ssd_forward(const ssd_shape *shape, ssd_dtype dtype,
                 void *stream);
 
 /*
+ * Flags of ssd_forward_ex / ssd_forward_host_ex / ssd_decode_step_ex.
+ *
+ * SSD_SCALE_X_BY_DT: the input term of the recurrence is dt_t * x_t (outer) B_t instead of
+ *   x_t (outer) B_t -- the discretization the full model keeps from Mamba, with the input matrix
+ *   taken as dt * B ("LLM(十一)——Mamba" §3.5.4: the continuous parameters are transformed before they
+ *   enter the SSD code; "Transformers是SSMs (一)" §2.1, Remark 1). The skip term stays D * x_t, and
+ *   the decay stays exp(dt_t * A). dt must then be >= 0 (its logarithm is taken on the bf16 path).
+ *   Fusing it saves the caller a pass that scales x.
+ */
+#define SSD_SCALE_X_BY_DT 1u
+
+/*
+ * ssd_forward with option flags (0 or SSD_SCALE_X_BY_DT); other bits give SSD_ERR_INVALID_ARG.
+ * Everything else is as for ssd_forward.
+ */
+int ssd_forward_ex(const ssd_shape *shape, ssd_dtype dtype, unsigned flags,
+                   const void *x, const float *dt, const float *A,
+                   const void *B, const void *C, const float *D,
+                   int chunk, const float *initial_state,
+                   const int32_t *cu_seqlens, int nseq,
+                   void *y, float *final_state,
+                   void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
  * The same forward pass on HOST buffers: copies the inputs to device memory
  * carved out of `device_buffer`, runs ssd_forward, copies y and final_state back,
  * and synchronises `stream`. Host buffers should be pinned for full copy speed.
@@ -118,6 +143,15 @@ int ssd_forward_host(const ssd_shape *shape, ssd_dtype dtype,
                      void *y, float *final_state,
                      void *device_buffer, size_t device_buffer_bytes,
                      void *stream);
+/* ssd_forward_host with option flags (see ssd_forward_ex). */
+int ssd_forward_host_ex(const ssd_shape *shape, ssd_dtype dtype, unsigned flags,
+                        const void *x, const float *dt, const float *A,
+                        const void *B, const void *C, const float *D,
+                        int chunk, const float *initial_state,
+                        const int32_t *cu_seqlens, int nseq,
+                        void *y, float *final_state,
+                        void *device_buffer, size_t device_buffer_bytes,
+                        void *stream);
 
 /*
  * ssd_forward for callers that cannot allocate device memory (for example code that runs
@@ -181,9 +215,9 @@ int ssd_decode_step(const ssd_shape *shape, ssd_dtype dtype,
  * which halves the bytes the step moves. With a bf16 state the update is computed in fp32 from the
  * stored values, y is taken from the unrounded new state, and only the stored new state is rounded
  * (to nearest even). state and new_state are then (batch, H, P, N) bf16 and N must be a multiple of
- * 8. Everything else is as for ssd_decode_step.
+ * 8. flags: 0 or SSD_SCALE_X_BY_DT (defined above). Everything else is as for ssd_decode_step.
  */
-int ssd_decode_step_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype,
+int ssd_decode_step_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags,
                        const void *x, const float *dt, const float *A,
                        const void *B, const void *C, const float *D,
                        const void *state, void *new_state, void *y,
@@ -204,7 +238,7 @@ int ssd_decode_step_host(const ssd_shape *shape, ssd_dtype dtype,
                          void *stream);
 /* The host-buffer step with the state stored as `state_dtype` (see ssd_decode_step_ex); the buffer
  * size from ssd_decode_host_buffer_size is enough for either state type. */
-int ssd_decode_step_host_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype,
+int ssd_decode_step_host_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags,
                             const void *x, const float *dt, const float *A,
                             const void *B, const void *C, const float *D,
                             const void *state, void *new_state, void *y,

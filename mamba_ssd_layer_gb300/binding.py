@@ -14,6 +14,7 @@ from . import build as _build
 
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_WORKSPACE = range(6)
 SSD_F32, SSD_BF16 = 0, 1
+SSD_SCALE_X_BY_DT = 1
 
 _lib = None
 
@@ -59,16 +60,22 @@ def load_library():
     lib.ssd_forward.restype = i32
     lib.ssd_forward_host.argtypes = fwd_args
     lib.ssd_forward_host.restype = i32
+    fwd_ex_args = fwd_args[:2] + [ctypes.c_uint] + fwd_args[2:]
+    lib.ssd_forward_ex.argtypes = fwd_ex_args
+    lib.ssd_forward_ex.restype = i32
+    lib.ssd_forward_host_ex.argtypes = fwd_ex_args
+    lib.ssd_forward_host_ex.restype = i32
     dec_args = [shp, i32, vp, fp, fp, vp, vp, fp, fp, fp, vp, vp]
     lib.ssd_decode_step.argtypes = dec_args
     lib.ssd_decode_step.restype = i32
-    lib.ssd_decode_step_ex.argtypes = [shp, i32, i32, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp]
+    lib.ssd_decode_step_ex.argtypes = [shp, i32, i32, ctypes.c_uint, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp]
     lib.ssd_decode_step_ex.restype = i32
     lib.ssd_decode_host_buffer_size.argtypes = [shp, i32]
     lib.ssd_decode_host_buffer_size.restype = sz
     lib.ssd_decode_step_host.argtypes = dec_args[:-1] + [vp, sz, vp]
     lib.ssd_decode_step_host.restype = i32
-    lib.ssd_decode_step_host_ex.argtypes = [shp, i32, i32, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp, sz, vp]
+    lib.ssd_decode_step_host_ex.argtypes = [shp, i32, i32, ctypes.c_uint, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp, sz,
+                                            vp]
     lib.ssd_decode_step_host_ex.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
@@ -128,14 +135,16 @@ def _check(t, name, shape, dtype, device):
 
 
 def ssd_forward(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu_seqlens=None,
-                return_final_state: bool = True, y=None, final_state=None, workspace=None, stream=None):
-    """SSD forward through the C ABI on CUDA tensors.
+                return_final_state: bool = True, y=None, final_state=None, workspace=None, stream=None,
+                scale_x_by_dt: bool = False):
+    """SSD forward through the C ABI on CUDA tensors (``ssd_forward_ex``).
 
     x (batch, T, H, P) and B, C (batch, T, G, N) in float32 or bfloat16 (the same);
     dt (batch, T, H), A (H,), D (H,) or None, initial_state (nseq, H, P, N) or None: float32.
     cu_seqlens: int32 (nseq + 1,) on the device, batch must be 1. Returns (y, final_state),
     final_state None when return_final_state is False. The work is enqueued on `stream`
-    (default: torch's current stream); nothing is synchronised.
+    (default: torch's current stream); nothing is synchronised. ``scale_x_by_dt`` makes the input
+    term dt x B^T (the skip term keeps D x).
     """
     import torch
     batch, T, H, P = x.shape
@@ -168,12 +177,13 @@ def ssd_forward(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    rc = lib.ssd_forward(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                         int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
-                         _ptr(final_state) if return_final_state else None,
-                         workspace.data_ptr(), ws_bytes, ctypes.c_void_p(stream.cuda_stream))
+    flags = SSD_SCALE_X_BY_DT if scale_x_by_dt else 0
+    rc = lib.ssd_forward_ex(ctypes.byref(shape), code, flags, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                            int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
+                            _ptr(final_state) if return_final_state else None,
+                            workspace.data_ptr(), ws_bytes, ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
-        raise SSDError(rc, "ssd_forward")
+        raise SSDError(rc, "ssd_forward_ex")
     return y, (final_state if return_final_state else None)
 
 
@@ -187,7 +197,7 @@ def ssd_status(workspace, stream=None) -> int:
 
 def ssd_forward_host(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu_seqlens=None,
                      return_final_state: bool = True, y=None, final_state=None, device_buffer=None,
-                     stream=None):
+                     stream=None, scale_x_by_dt: bool = False):
     """The same forward pass on HOST (CPU, ideally pinned) tensors through ``ssd_forward_host``:
     host->device copies, the kernels and the device->host copies all happen inside the C call,
     which synchronises the stream before returning."""
@@ -215,12 +225,13 @@ def ssd_forward_host(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=Non
         device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
     if stream is None:
         stream = torch.cuda.current_stream(device_buffer.device)
-    rc = lib.ssd_forward_host(ctypes.byref(shape), code, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
-                              int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
-                              _ptr(final_state) if return_final_state else None,
-                              device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
+    flags = SSD_SCALE_X_BY_DT if scale_x_by_dt else 0
+    rc = lib.ssd_forward_host_ex(ctypes.byref(shape), code, flags, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                 _ptr(D), int(chunk), _ptr(initial_state), _ptr(cu_seqlens), int(nseq), _ptr(y),
+                                 _ptr(final_state) if return_final_state else None,
+                                 device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
-        raise SSDError(rc, "ssd_forward_host")
+        raise SSDError(rc, "ssd_forward_host_ex")
     return y, (final_state if return_final_state else None)
 
 
@@ -230,7 +241,8 @@ def _decode_shapes(x, B):
     return batch, H, P, G, N
 
 
-def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, stream=None):
+def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, stream=None,
+                    scale_x_by_dt: bool = False):
     """One recurrent step on CUDA tensors through ``ssd_decode_step``.
 
     x (batch, H, P) and B, C (batch, G, N) in float32 or bfloat16 (the same); dt (batch, H),
@@ -261,7 +273,8 @@ def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, 
     _check(y, "y", (batch, H, P), x.dtype, dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    rc = load_library().ssd_decode_step_ex(ctypes.byref(_shape(batch, 1, H, P, N, G)), code, state_code, _ptr(x),
+    flags = SSD_SCALE_X_BY_DT if scale_x_by_dt else 0
+    rc = load_library().ssd_decode_step_ex(ctypes.byref(_shape(batch, 1, H, P, N, G)), code, state_code, flags, _ptr(x),
                                            _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state),
                                            _ptr(new_state), _ptr(y), ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
@@ -270,7 +283,7 @@ def ssd_decode_step(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, 
 
 
 def ssd_decode_step_host(x, dt, A, B, C, D=None, state=None, new_state=None, y=None, device_buffer=None,
-                         stream=None):
+                         stream=None, scale_x_by_dt: bool = False):
     """The same step on HOST (CPU, ideally pinned) tensors through ``ssd_decode_step_host``: the
     copies in, the kernel and the copies out all happen inside the C call, which synchronises."""
     import torch
@@ -295,7 +308,8 @@ def ssd_decode_step_host(x, dt, A, B, C, D=None, state=None, new_state=None, y=N
         device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
     if stream is None:
         stream = torch.cuda.current_stream(device_buffer.device)
-    rc = lib.ssd_decode_step_host_ex(ctypes.byref(shape), code, _dtype_code(state), _ptr(x), _ptr(dt), _ptr(A),
+    flags = SSD_SCALE_X_BY_DT if scale_x_by_dt else 0
+    rc = lib.ssd_decode_step_host_ex(ctypes.byref(shape), code, _dtype_code(state), flags, _ptr(x), _ptr(dt), _ptr(A),
                                      _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(new_state), _ptr(y),
                                      device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:

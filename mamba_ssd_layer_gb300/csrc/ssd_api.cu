@@ -130,11 +130,12 @@ size_t ssd_workspace_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int ns
     return ws_layout(*s, dtype, chunk, varlen ? nseq : s->batch, varlen).total;
 }
 
-int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
-                const void* B, const void* C, const float* D, int chunk, const float* initial_state,
-                const int32_t* cu_seqlens, int nseq, void* y, float* final_state, void* workspace,
-                size_t workspace_bytes, void* stream) {
+int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const void* x, const float* dt,
+                   const float* A, const void* B, const void* C, const float* D, int chunk,
+                   const float* initial_state, const int32_t* cu_seqlens, int nseq, void* y, float* final_state,
+                   void* workspace, size_t workspace_bytes, void* stream) {
     const bool varlen = cu_seqlens != nullptr;
+    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
     int rc = check_shape(s, dtype, chunk, nseq, varlen);
     if (rc != SSD_OK) return rc;
     const int64_t rows = s->batch * s->seqlen;
@@ -158,6 +159,7 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
     p.dtype = dtype;
     p.chunk = chunk;
     p.varlen = varlen;
+    p.scale_x_by_dt = (flags & SSD_SCALE_X_BY_DT) != 0;
     p.nseq = nseq_eff;
     p.rows = rows;
     p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D;
@@ -195,6 +197,14 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
     return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                const void* B, const void* C, const float* D, int chunk, const float* initial_state,
+                const int32_t* cu_seqlens, int nseq, void* y, float* final_state, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    return ssd_forward_ex(s, dtype, 0u, x, dt, A, B, C, D, chunk, initial_state, cu_seqlens, nseq, y, final_state,
+                          workspace, workspace_bytes, stream);
+}
+
 size_t ssd_host_buffer_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int nseq) {
     const size_t ws = ssd_workspace_size(s, dtype, chunk, nseq);
     if (!ws) return 0;
@@ -211,11 +221,12 @@ size_t ssd_host_buffer_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int 
     return tot;
 }
 
-int ssd_forward_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
-                     const void* B, const void* C, const float* D, int chunk, const float* initial_state,
-                     const int32_t* cu_seqlens, int nseq, void* y, float* final_state, void* device_buffer,
-                     size_t device_buffer_bytes, void* stream) {
+int ssd_forward_host_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const void* x, const float* dt,
+                        const float* A, const void* B, const void* C, const float* D, int chunk,
+                        const float* initial_state, const int32_t* cu_seqlens, int nseq, void* y, float* final_state,
+                        void* device_buffer, size_t device_buffer_bytes, void* stream) {
     const bool varlen = cu_seqlens != nullptr;
+    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
     int rc = check_shape(s, dtype, chunk, nseq, varlen);
     if (rc != SSD_OK) return rc;
     if (varlen && nseq <= 0) return SSD_ERR_INVALID_ARG;
@@ -260,16 +271,24 @@ int ssd_forward_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const f
     h2d(dinit, initial_state, stb);
     h2d(dcu, cu_seqlens, (nseq_eff + 1) * 4);
     if (err != cudaSuccess) return SSD_ERR_CUDA;
-    rc = ssd_forward(s, dtype, dx, (const float*)ddt, (const float*)dA, dB, dC, D ? (const float*)dD : nullptr,
-                     chunk, initial_state ? (const float*)dinit : nullptr,
-                     varlen ? (const int32_t*)dcu : nullptr, nseq, dy,
-                     final_state ? (float*)dfinal : nullptr, ws, ws_bytes, stream);
+    rc = ssd_forward_ex(s, dtype, flags, dx, (const float*)ddt, (const float*)dA, dB, dC,
+                        D ? (const float*)dD : nullptr, chunk, initial_state ? (const float*)dinit : nullptr,
+                        varlen ? (const int32_t*)dcu : nullptr, nseq, dy, final_state ? (float*)dfinal : nullptr, ws,
+                        ws_bytes, stream);
     if (rc != SSD_OK) return rc;
     if (cudaMemcpyAsync(y, dy, xb, cudaMemcpyDeviceToHost, st) != cudaSuccess) return SSD_ERR_CUDA;
     if (final_state && cudaMemcpyAsync(final_state, dfinal, stb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return SSD_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return SSD_ERR_CUDA;
     return ssd_status(ws, stream);
+}
+
+int ssd_forward_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
+                     const void* B, const void* C, const float* D, int chunk, const float* initial_state,
+                     const int32_t* cu_seqlens, int nseq, void* y, float* final_state, void* device_buffer,
+                     size_t device_buffer_bytes, void* stream) {
+    return ssd_forward_host_ex(s, dtype, 0u, x, dt, A, B, C, D, chunk, initial_state, cu_seqlens, nseq, y,
+                               final_state, device_buffer, device_buffer_bytes, stream);
 }
 
 int ssd_status(const void* workspace, void* stream) {

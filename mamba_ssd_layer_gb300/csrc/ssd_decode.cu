@@ -44,6 +44,7 @@ struct DecodeArgs {
     void* y;                // (batch, H, P) storage type
     int H, P, N, G;
     int heads_per_group;    // H / G
+    int scale_x_by_dt;      // the input term is dt x B^T
     int L;                  // lanes per state row
     int rows_per_cta;       // kDecWarps * (32 / L) * kDecRowsPerThread
     int row_blocks;         // ceil(P / rows_per_cta)
@@ -138,7 +139,9 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
     const int g = h / a.heads_per_group;
     const int nch = a.N / E;                          // 16-byte chunks per state row
 
-    const float decay = expf(a.dt[bh] * a.A[h]);
+    const float dtv = a.dt[bh];
+    const float decay = expf(dtv * a.A[h]);
+    const float in_scale = a.scale_x_by_dt ? dtv : 1.f;   // the skip term keeps the unscaled x
     const float dskip = a.D ? a.D[h] : 0.f;
 
     const T* Bp = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
     const float2 dd = make_float2(decay, decay);
 #pragma unroll
     for (int u = 0; u < kDecRowsPerThread; ++u) {
-        const float2 xx = make_float2(xv[u], xv[u]);
+        const float2 xx = make_float2(in_scale * xv[u], in_scale * xv[u]);
         float2 acc2 = make_float2(0.f, 0.f);              // packed fp32 pairs: half the FP instructions
 #pragma unroll
         for (int j = 0; j < CI; ++j) {
@@ -238,11 +241,12 @@ using namespace ssd;
 
 extern "C" {
 
-int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, const void* x, const float* dt,
-                       const float* A, const void* B, const void* C, const float* D, const void* state,
-                       void* new_state, void* y, void* stream) {
+int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags, const void* x,
+                       const float* dt, const float* A, const void* B, const void* C, const float* D,
+                       const void* state, void* new_state, void* y, void* stream) {
     int rc = check_decode(s, dtype);
     if (rc != SSD_OK) return rc;
+    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
     if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     if (state_dtype == SSD_BF16 && (s->dstate & 7) != 0) return SSD_ERR_UNSUPPORTED;
     if (s->batch == 0) return SSD_OK;
@@ -268,6 +272,7 @@ int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtyp
     a.state = state; a.new_state = new_state; a.y = y;
     a.H = (int)s->nheads; a.P = (int)s->headdim; a.N = (int)s->dstate; a.G = (int)s->ngroups;
     a.heads_per_group = a.H / a.G;
+    a.scale_x_by_dt = (flags & SSD_SCALE_X_BY_DT) ? 1 : 0;
     const int nch = a.N / (state_dtype == SSD_F32 ? 4 : 8);   // 16-byte chunks per state row
     a.L = 1;
     while (a.L < nch && a.L < 32) a.L <<= 1;
@@ -289,7 +294,7 @@ int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtyp
 int ssd_decode_step(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
                     const void* B, const void* C, const float* D, const float* state, float* new_state, void* y,
                     void* stream) {
-    return ssd_decode_step_ex(s, dtype, SSD_F32, x, dt, A, B, C, D, state, new_state, y, stream);
+    return ssd_decode_step_ex(s, dtype, SSD_F32, 0u, x, dt, A, B, C, D, state, new_state, y, stream);
 }
 
 size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
@@ -305,12 +310,13 @@ size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
     return tot > 0 ? tot : 256;
 }
 
-int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, const void* x,
-                            const float* dt, const float* A, const void* B, const void* C, const float* D,
-                            const void* state, void* new_state, void* y, void* device_buffer,
+int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags,
+                            const void* x, const float* dt, const float* A, const void* B, const void* C,
+                            const float* D, const void* state, void* new_state, void* y, void* device_buffer,
                             size_t device_buffer_bytes, void* stream) {
     int rc = check_decode(s, dtype);
     if (rc != SSD_OK) return rc;
+    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
     if (state_dtype != SSD_F32 && state_dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
     const size_t need = ssd_decode_host_buffer_size(s, dtype);
     if (!device_buffer || !aligned(device_buffer, 256) || device_buffer_bytes < need) return SSD_ERR_WORKSPACE;
@@ -345,7 +351,7 @@ int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state
     h2d(dC, C, bcb);
     h2d(dS, state, stb);
     if (note_cuda_error("decode host copy in", err) != cudaSuccess) return SSD_ERR_CUDA;
-    rc = ssd_decode_step_ex(s, dtype, state_dtype, dx, (const float*)ddt, (const float*)dA, dB, dC,
+    rc = ssd_decode_step_ex(s, dtype, state_dtype, flags, dx, (const float*)ddt, (const float*)dA, dB, dC,
                             D ? (const float*)dD : nullptr, dS, dS, dy, stream);
     if (rc != SSD_OK) return rc;
     err = cudaMemcpyAsync(y, dy, xb, cudaMemcpyDeviceToHost, st);
@@ -357,7 +363,7 @@ int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state
 int ssd_decode_step_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const float* dt, const float* A,
                          const void* B, const void* C, const float* D, const float* state, float* new_state,
                          void* y, void* device_buffer, size_t device_buffer_bytes, void* stream) {
-    return ssd_decode_step_host_ex(s, dtype, SSD_F32, x, dt, A, B, C, D, state, new_state, y, device_buffer,
+    return ssd_decode_step_host_ex(s, dtype, SSD_F32, 0u, x, dt, A, B, C, D, state, new_state, y, device_buffer,
                                    device_buffer_bytes, stream);
 }
 

@@ -10,6 +10,8 @@
 //   chunk_out_f32:   y_i = sum_{j<=i} exp(cs_i - cs_j) (C_i . B_j) x_j      (diagonal block, §3.5.1)
 //                        + exp(cs_i) C_i . h_in                              (left factors, §3.5.2)
 //                        + D x_i.
+// With the dt-scaled input term every x_j that enters a state or a diagonal block is dt_j x_j; the
+// skip term keeps D x_i.
 // Cumulative sums are accumulated in fp64 so that differences of large sums do not
 // lose digits (the stability concern of §3.5.4); exponentials are fp32.
 #include "ssd_internal.cuh"
@@ -38,7 +40,7 @@ __global__ void __launch_bounds__(256) chunk_state_f32(const int* __restrict__ h
                                                        const float* __restrict__ x, const float* __restrict__ dt,
                                                        const float* __restrict__ A, const float* __restrict__ B,
                                                        float* __restrict__ decay, float* __restrict__ states,
-                                                       int H, int P, int N, int G) {
+                                                       int H, int P, int N, int G, int scale_x_by_dt) {
     __shared__ double cs[kMaxQ];
     __shared__ float w[kMaxQ];
     if (header[0] != SSD_OK || (int)blockIdx.x >= header[1]) return;
@@ -47,7 +49,8 @@ __global__ void __launch_bounds__(256) chunk_state_f32(const int* __restrict__ h
     const int g = h / (H / G);
     chunk_cumsum_f64(dt, A, h, H, d.row0, d.len, cs);
     const double last = d.len > 0 ? cs[d.len - 1] : 0.0;
-    for (int l = threadIdx.x; l < d.len; l += blockDim.x) w[l] = (float)exp(last - cs[l]);
+    for (int l = threadIdx.x; l < d.len; l += blockDim.x)
+        w[l] = (float)exp(last - cs[l]) * (scale_x_by_dt ? dt[(int64_t)(d.row0 + l) * H + h] : 1.f);
     if (threadIdx.x == 0) decay[(int64_t)blockIdx.x * H + h] = (float)exp(last);
     __syncthreads();
     float* S = states + ((int64_t)blockIdx.x * H + h) * P * N;
@@ -74,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) chunk_out_f32(const int* __restrict_
                                                           const float* __restrict__ A, const float* __restrict__ B,
                                                           const float* __restrict__ C, const float* __restrict__ D,
                                                           const float* __restrict__ states, float* __restrict__ y,
-                                                          int H, int P, int N, int G) {
+                                                          int H, int P, int N, int G, int scale_x_by_dt) {
     __shared__ double cs[kMaxQ];
     __shared__ float coef[kTile][kTile + 1];
     if (header[0] != SSD_OK || (int)blockIdx.x >= header[1]) return;
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) chunk_out_f32(const int* __restrict_
                     float dot = 0.f;
                     for (int n = 0; n < N; ++n) dot = fmaf(Ci[n], Bj[n], dot);
                     v = dot * (float)exp(cs[ia] - cs[jb]);
+                    if (scale_x_by_dt) v *= dt[((int64_t)d.row0 + jb) * H + h];
                 }
                 coef[a][b] = v;
             }
@@ -152,7 +156,8 @@ cudaError_t launch_f32_path(const Problem& p) {
     dim3 grid((unsigned)p.L.max_chunks, (unsigned)H);
     prof_launch();
     chunk_state_f32<<<grid, 256, 0, p.stream>>>(p.status(), p.chunks(), (const float*)p.x, p.dt, p.A,
-                                                (const float*)p.B, p.decay(), p.states(), H, P, N, G);
+                                                (const float*)p.B, p.decay(), p.states(), H, P, N, G,
+                                                p.scale_x_by_dt ? 1 : 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = launch_state_pass(p);
@@ -161,7 +166,7 @@ cudaError_t launch_f32_path(const Problem& p) {
     prof_begin(p.stream, "chunk_out_f32");
     chunk_out_f32<<<grid, kThreads, 0, p.stream>>>(p.status(), p.chunks(), (const float*)p.x, p.dt, p.A,
                                                    (const float*)p.B, (const float*)p.C, p.D, p.states(),
-                                                   (float*)p.y, H, P, N, G);
+                                                   (float*)p.y, H, P, N, G, p.scale_x_by_dt ? 1 : 0);
     prof_end(p.stream);
     return cudaGetLastError();
 }

@@ -176,6 +176,10 @@ constexpr int kBarAFull0 = 0;   // + s: full, + 3 + s: empty, + 6 + s: weights, 
 static_assert(kBarAFull0 + 10 <= kNumBars, "phase A reuses the first ten barrier slots");
 // Phase-A windows per CTA whose totals are precomputed together (more fall back to the producer)
 constexpr int kMaxWinA = 96;
+// phase-C cumsum table per stage: [2][128] plus 8 row-side values
+constexpr int kCsStride = 264;
+// floor of dt in log2(dt): dt = 0 contributes exp(-99.7) ~ 0 instead of an infinity
+constexpr float kMinDt = 1e-30f;
 
 struct Smem;
 __device__ void init_bars_a(const Smem& sm);
@@ -205,11 +209,13 @@ struct Smem {
     // unused area (32 KB for either state size)
     __device__ float* tota() const { return csa(0) + 1024; }
     __device__ uint8_t* small() const { return hs() + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion); }
-    // per stage: tile-local cumsum of dt*A (x log2 e) for both heads [2][128], and 4 floats after it
-    // (phase A keeps the window's two totals there, in its own copy of these tables)
-    __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * 260; }
-    // exp(cs_p - cs_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
-    __device__ float* vt() const { return cs(0) + 520; }
+    // per stage: the tile-local cumsum of dt*A (x log2 e) as seen from a column (token j), [2][128]:
+    // cs_j, minus log2(dt_j) when the input term is dt x (exp(cs_i - table_j) is then L_ij dt_j);
+    // then 8 floats per stage: per head (4 h + k) the plain cumsum at the last tokens of the first three
+    // 32-token blocks (k = 0..2) and at the tile's last token (k = 3)
+    __device__ float* cs(int s) const { return reinterpret_cast<float*>(small()) + s * kCsStride; }
+    // exp(cs_p - table_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
+    __device__ float* vt() const { return cs(0) + 2 * kCsStride; }
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(vt() + 192); }           // [kNumBars]
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(bars() + kNumBars); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(tmem_slot() + 1); }
@@ -399,7 +405,8 @@ __device__ __forceinline__ int tile_len(const Piece& c, int t) {
 //      every window (starting from the initial state);
 //   C  the window's tiles in time order from its entering state: diagonal blocks, left factors, the
 //      state carried on chip from tile to tile, y.
-template <int N>
+// kScaleX: the input term is dt x B^T (a separate instantiation, so that the plain one carries none of it).
+template <int N, bool kScaleX>
 __global__ void __launch_bounds__(kThreads)
 ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -507,8 +514,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 v[hh][k] = (l < len) ? __ldg(a.dt + (int64_t)(row0 + l) * a.H + h0 + hh) : 0.f;
             }
     };
-    // producer: tile-local inclusive cumsum of dt*A (x log2 e) plus `carry`, written to cs[2][128];
-    // cv gets this lane's four values per head, carry advances by the tile's total
+    // producer: tile-local inclusive cumsum of dt*A (x log2 e) plus `carry`; cv gets this lane's four
+    // values per head, carry advances by the tile's total, and cs[2][128] gets the column-side table
+    // (minus log2(dt) when the input term is dt x)
     auto cumsum = [&](const float (&v)[2][4], const float (&Al)[2], float* cs, float (&carry)[2], float (&cv)[2][4]) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -526,7 +534,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const float base = sc - p[3] + carry[hh];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cv[hh][k] = base + p[k];
-            *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
+            float4 col = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
+            if constexpr (kScaleX) {
+                col.x -= __log2f(fmaxf(v[hh][0], kMinDt));
+                col.y -= __log2f(fmaxf(v[hh][1], kMinDt));
+                col.z -= __log2f(fmaxf(v[hh][2], kMinDt));
+                col.w -= __log2f(fmaxf(v[hh][3], kMinDt));
+            }
+            *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = col;
             carry[hh] += __shfl_sync(0xffffffffu, sc, 31);
         }
     };
@@ -815,7 +830,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     tma_load_3d(sm.x(stage, 1), &maps.x, fullx, 0, h0 + 1, row0);
                 }
                 float carry[2] = {0.f, 0.f};
-                cumsum(v, Al, sm.cs(stage), carry, cv);
+                float* cst = sm.cs(stage);
+                cumsum(v, Al, cst, carry, cv);
+                // row-side values: the cumsum at tokens 31, 63, 95 and at the tile's last token (the
+                // plain table already holds them)
+#pragma unroll
+                for (int hh = 0; hh < 2 && kScaleX; ++hh) {
+                    if (lane == 7 || lane == 15 || lane == 23) cst[256 + 4 * hh + (lane >> 3)] = cv[hh][3];
+                    if (lane == ((len - 1) >> 2)) {
+                        const int k = (len - 1) & 3;
+                        cst[256 + 4 * hh + 3] = k == 0 ? cv[hh][0] : k == 1 ? cv[hh][1] : k == 2 ? cv[hh][2] : cv[hh][3];
+                    }
+                }
                 if (p2 > 0) {
                     const bool w = wait_bar(sm, kBarLG, ph, a);
                     if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -825,10 +851,16 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const float piv = __shfl_sync(0xffffffffu, cv[hh][3], lane | 7);
+                    float4 col = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
+                    if constexpr (kScaleX) {    // the same column-side values as the table
+                        col.x -= __log2f(fmaxf(v[hh][0], kMinDt));
+                        col.y -= __log2f(fmaxf(v[hh][1], kMinDt));
+                        col.z -= __log2f(fmaxf(v[hh][2], kMinDt));
+                        col.w -= __log2f(fmaxf(v[hh][3], kMinDt));
+                    }
                     if (lane < 24)
                         *reinterpret_cast<float4*>(vt + hh * 96 + 4 * lane) =
-                            make_float4(ex2(piv - cv[hh][0]), ex2(piv - cv[hh][1]), ex2(piv - cv[hh][2]),
-                                        ex2(piv - cv[hh][3]));
+                            make_float4(ex2(piv - col.x), ex2(piv - col.y), ex2(piv - col.z), ex2(piv - col.w));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(fullx);
@@ -946,8 +978,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                             float D0, float D1) {
             uint32_t p0[8], p1[8];
             if (g < 2 * qd) {
+                // the row-side cumsum at p = 32 (g / 2) + 31
                 const int p = 32 * (g >> 1) + 31;
-                const float u0 = ex2(ci0 - cs[p]), u1 = ex2(ci1 - cs[128 + p]);
+                const float cp0 = kScaleX ? cs[256 + (g >> 1)] : cs[p], cp1 = kScaleX ? cs[256 + 4 + (g >> 1)] : cs[128 + p];
+                const float u0 = ex2(ci0 - cp0), u1 = ex2(ci1 - cp1);
                 const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
                 const float4* v0 = reinterpret_cast<const float4*>(sm.vt() + 16 * g);
                 const float4* v1 = reinterpret_cast<const float4*>(sm.vt() + 96 + 16 * g);
@@ -1008,9 +1042,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_st8(col + 8, p1);
         };
         // this warp's two column groups of L o G for stage st into buffer gcol
-        auto lg_tile = [&](int st, int len, uint32_t gcol, float D0, float D1) {
+        // lgd: log2(dt) of this thread's row per head when the input term is dt x (else 0), turning the
+        // column-side table entry of the row into its row-side cumsum. Returns exp(cs_i) of the row for
+        // head kq / 2, which the tile's epilogue needs.
+        auto lg_tile = [&](int st, int len, uint32_t gcol, float D0, float D1, const float (&lgd)[2]) {
             const float* cs = sm.cs(st);
             const bool rv = row < len;
+            float ci0 = 0.f, ci1 = 0.f, e_out = 0.f;
+            if constexpr (kScaleX) {
+                ci0 = cs[row] + lgd[0];
+                ci1 = cs[128 + row] + lgd[1];
+                e_out = ex2((kq >> 1) ? ci1 : ci0);
+            }
             const uint32_t ca = lane_base + gcol + 16 * kq, cb = lane_base + gcol + 16 * (7 - kq);
             if (!__any_sync(0xffffffffu, rv)) {
                 uint32_t z[8];
@@ -1024,7 +1067,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 float gv[32];
                 tmem_ld16_nowait(ca, gv);
                 tmem_ld16_nowait(cb, gv + 16);
-                const float ci0 = cs[row], ci1 = cs[128 + row];
+                if constexpr (!kScaleX) {
+                    ci0 = cs[row];
+                    ci1 = cs[128 + row];
+                }
                 tmem_wait_ld();
                 lg_group(cs, kq, gv, rv, ci0, ci1, ca, D0, D1);
                 lg_group(cs, 7 - kq, gv + 16, rv, ci0, ci1, cb, D0, D1);
@@ -1032,6 +1078,20 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_wait_st();
             tc_fence_before_sync();
             warp_arrive(sm, kBarLG);
+            return e_out;
+        };
+        // dt of this thread's row of a tile, per head (only needed when the input term is dt x)
+        auto load_row_dt = [&](int row0, int len, int h0, float (&d)[2]) {
+            d[0] = d[1] = 1.f;
+            if (kScaleX && row < len) {
+                const float2 v = *reinterpret_cast<const float2*>(a.dt + (int64_t)(row0 + row) * a.H + h0);
+                d[0] = v.x;
+                d[1] = v.y;
+            }
+        };
+        auto log2_row_dt = [&](const float (&d)[2], float (&lgd)[2]) {
+            lgd[0] = kScaleX ? __log2f(fmaxf(d[0], kMinDt)) : 0.f;
+            lgd[1] = kScaleX ? __log2f(fmaxf(d[1], kMinDt)) : 0.f;
         };
         // state step of stage st: h_{t-1} (this thread's state columns) to bf16 in the staging area for
         // Yo, and a_t h_{t-1} back into TMEM for S(t) to accumulate onto
@@ -1057,7 +1117,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_wait_ld();
             if (!released) return false;
             const float* cs = sm.cs(st);
-            const float at = ex2(cs[hrow * 128 + len - 1]);
+            // the tile's decay (row-side cumsum at its last token)
+            const float at = ex2(kScaleX ? cs[256 + 4 * hrow + 3] : cs[hrow * 128 + len - 1]);
             const float2 aa = make_float2(at, at);
 #pragma unroll
             for (int cc = 0; cc < NQ; cc += 8) {
@@ -1156,10 +1217,13 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const float Dlg1 = a.D ? __ldg(a.D + h0 + 1) : 0.f;
 
             // L o G of the window's first tile (it does not need the entering state)
+            float dnext[2], lgd[2];
+            load_row_dt(tile_row0(c, c.t0), tile_len(c, c.t0), h0, dnext);
             ok = wait_bar_warp(sm, kBarFullX0 + stage, ph, a) && wait_bar_warp(sm, kBarG, ph, a);
             if (!ok) break;
             tc_fence_after_sync();
-            lg_tile(stage, tile_len(c, c.t0), kColGB + 128 * (kt & 1), Dlg0, Dlg1);
+            log2_row_dt(dnext, lgd);
+            float e_next = lg_tile(stage, tile_len(c, c.t0), kColGB + 128 * (kt & 1), Dlg0, Dlg1, lgd);
 
             // the entering state into this thread's state columns: the initial state (or zero) at a
             // chain's start, else the scan's result
@@ -1190,7 +1254,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     if (!ok) break;
                 }
                 tc_fence_after_sync();
-                const float e_row = ex2(cs[(kq >> 1) * 128 + row]);   // for this tile's epilogue
+                // exp(cs_i) for this tile's epilogue (read before the stage can be refilled)
+                const float e_row = kScaleX ? e_next : ex2(cs[(kq >> 1) * 128 + row]);
+                if (kScaleX && t + 1 < c.t1) load_row_dt(tile_row0(c, t + 1), tile_len(c, t + 1), h0, dnext);
                 ok = state_step(st, len);
                 if (!ok) break;
                 fence_proxy_async_smem();
@@ -1198,14 +1264,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 warp_arrive(sm, kBarST);
                 ok = wait_bar_warp(sm, kBarYD, ph, a);
                 if (!ok) break;
-                weight_x(sm.x(st, 0), cs, len, cs[len - 1], cs[128 + len - 1]);
+                if constexpr (kScaleX)
+                    weight_x(sm.x(st, 0), cs, len, cs[256 + 3], cs[256 + 7]);
+                else
+                    weight_x(sm.x(st, 0), cs, len, cs[len - 1], cs[128 + len - 1]);
                 fence_proxy_async_smem();
                 warp_arrive(sm, kBarWX);
                 if (t + 1 < c.t1) {
                     ok = wait_bar_warp(sm, kBarFullX0 + (st ^ 1), ph, a) && wait_bar_warp(sm, kBarG, ph, a);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    lg_tile(st ^ 1, tile_len(c, t + 1), kColGB + 128 * ((kt + 1) & 1), Dlg0, Dlg1);
+                    log2_row_dt(dnext, lgd);
+                    e_next = lg_tile(st ^ 1, tile_len(c, t + 1), kColGB + 128 * ((kt + 1) & 1), Dlg0, Dlg1, lgd);
                 }
                 ok = wait_bar_warp(sm, kBarYO, ph, a);
                 if (!ok) break;
@@ -1276,18 +1346,18 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 template <int N>
 size_t fused_smem_bytes() {
     const size_t stage = 2 * kRegion + 2 * (N / 64) * kRegion;
-    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (520 + 192) * 4 + kNumBars * 8 + 16;
+    return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (2 * kCsStride + 192) * 4 + kNumBars * 8 + 16;
 }
 
-template <int N>
+template <int N, bool kScaleX>
 cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMaps& maps, int grid) {
     const size_t smem = fused_smem_bytes<N>();
     cudaError_t e = note_cuda_error("fused smem attribute",
-        cudaFuncSetAttribute(ssd_fused_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        cudaFuncSetAttribute(ssd_fused_kernel<N, kScaleX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = note_cuda_error("fused occupancy",
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N>, kThreads, smem));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N, kScaleX>, kThreads, smem));
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return note_cuda_error("fused occupancy is zero", cudaErrorLaunchOutOfResources);
     cudaLaunchConfig_t cfg = {};
@@ -1301,7 +1371,7 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_launch();
-    return note_cuda_error("fused cooperative launch", cudaLaunchKernelEx(&cfg, ssd_fused_kernel<N>, maps, fa));
+    return note_cuda_error("fused cooperative launch", cudaLaunchKernelEx(&cfg, ssd_fused_kernel<N, kScaleX>, maps, fa));
 }
 
 }  // namespace
@@ -1378,7 +1448,10 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     fa.y_accum = part > 0 ? 1 : 0;
     cudaError_t e;
     prof_begin(p.stream, "ssd_fused_kernel");
-    e = (N == 64) ? launch_fused_n<64>(p, fa, maps, grid) : launch_fused_n<128>(p, fa, maps, grid);
+    if (p.scale_x_by_dt)
+        e = (N == 64) ? launch_fused_n<64, true>(p, fa, maps, grid) : launch_fused_n<128, true>(p, fa, maps, grid);
+    else
+        e = (N == 64) ? launch_fused_n<64, false>(p, fa, maps, grid) : launch_fused_n<128, false>(p, fa, maps, grid);
     prof_end(p.stream);
     return e;
 }

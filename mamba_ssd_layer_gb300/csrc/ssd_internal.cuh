@@ -90,6 +90,7 @@ struct Problem {
     ssd_dtype dtype;
     int chunk;
     bool varlen;
+    bool scale_x_by_dt;    // the input term is dt x B^T (SSD_SCALE_X_BY_DT)
     int64_t nseq;          // sequences: batch (dense) or segments (varlen)
     int64_t rows;          // packed rows = batch * seqlen
     const void* x;

@@ -36,6 +36,7 @@ class Workload:
     seg_min: int = 64
     seg_max: int = 4096
     state_dtype: str = "f32"  # recurrent-step workloads: storage type of the carried state
+    scale_x_by_dt: bool = False  # the input term is dt x B^T (the layer's option, not an input draw)
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -51,6 +52,9 @@ WORKLOADS = {
     "long_n64": Workload("long_n64", 1, 16384, 80, 64, 64, 1, 256, "bf16", 1003 + 64),
     "long_n128": Workload("long_n128", 1, 16384, 80, 64, 128, 1, 256, "bf16", 1003 + 128),
     "long_n256": Workload("long_n256", 1, 16384, 80, 64, 256, 1, 256, "bf16", 1003 + 256),
+    # the long-sequence layer with the dt-scaled input term (same draws as long_n128)
+    "long_n128_dtscaled": Workload("long_n128_dtscaled", 1, 16384, 80, 64, 128, 1, 256, "bf16", 1003 + 128,
+                                   scale_x_by_dt=True),
     "varlen": Workload("varlen", 1, 32768, 32, 64, 128, 1, 256, "bf16", 1004, varlen_total=32768),
     # one recurrent step for 64 carried states of a Mamba-2-2.7B-shaped layer (seqlen 1; the
     # initial state is the carried state)

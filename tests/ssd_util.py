@@ -34,7 +34,7 @@ def to_device(d: dict, dtype: str, device="cuda"):
     return t
 
 
-def run_gpu(d: dict, dtype: str, chunk: int, use_D=True, return_final=True):
+def run_gpu(d: dict, dtype: str, chunk: int, use_D=True, return_final=True, scale_x_by_dt=False):
     import torch
     from mamba_ssd_layer_gb300 import binding as bd
     from mamba_ssd_layer_gb300 import ssd_forward
@@ -46,7 +46,7 @@ def run_gpu(d: dict, dtype: str, chunk: int, use_D=True, return_final=True):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=x.device)
     y, f = ssd_forward(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"] if use_D else None, chunk=chunk,
                        initial_state=t["initial_state"], cu_seqlens=t["cu_seqlens"],
-                       return_final_state=return_final, workspace=ws)
+                       return_final_state=return_final, workspace=ws, scale_x_by_dt=scale_x_by_dt)
     torch.cuda.synchronize()
     st = bd.ssd_status(ws)
     if st != bd.SSD_OK:
@@ -56,7 +56,7 @@ def run_gpu(d: dict, dtype: str, chunk: int, use_D=True, return_final=True):
             None if f is None else f.cpu().numpy().astype(np.float64))
 
 
-def run_oracle(d: dict, heads=None, use_D=True):
+def run_oracle(d: dict, heads=None, use_D=True, scale_x_by_dt=False):
     x, dt, A, B, C, D, init = d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d.get("initial_state")
     if heads is not None:
         heads = np.asarray(heads)
@@ -67,4 +67,5 @@ def run_oracle(d: dict, heads=None, use_D=True):
         if init is not None:
             init = init[:, heads]
         del H
-    return oracle.ssd_recurrence(x, dt, A, B, C, D if use_D else None, init, d.get("cu_seqlens"))
+    return oracle.ssd_recurrence(x, dt, A, B, C, D if use_D else None, init, d.get("cu_seqlens"),
+                                 scale_x_by_dt=scale_x_by_dt)

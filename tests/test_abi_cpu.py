@@ -124,11 +124,23 @@ def test_decode_argument_errors_before_any_device_work(lib):
 
 def test_decode_state_dtype_errors(lib):
     s = shape(batch=4, T=1)
-    call = lambda sh, sd: lib.ssd_decode_step_ex(ctypes.byref(sh), bd.SSD_BF16, sd, FAKE, FAKE, FAKE, FAKE, FAKE,
-                                                  None, FAKE, FAKE, FAKE, None)
+    call = lambda sh, sd, fl=0: lib.ssd_decode_step_ex(ctypes.byref(sh), bd.SSD_BF16, sd, fl, FAKE, FAKE, FAKE, FAKE,
+                                                        FAKE, None, FAKE, FAKE, FAKE, None)
     assert call(s, 7) == bd.SSD_ERR_INVALID_ARG                                # unknown state type
     assert call(shape(batch=4, T=1, N=20), bd.SSD_BF16) == bd.SSD_ERR_UNSUPPORTED   # bf16 state: N % 8
     assert call(shape(batch=0, T=1), bd.SSD_BF16) == bd.SSD_OK
-    rc = lib.ssd_decode_step_host_ex(ctypes.byref(s), bd.SSD_BF16, 7, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+    assert call(s, bd.SSD_F32, 6) == bd.SSD_ERR_INVALID_ARG                    # unknown flag bits
+    rc = lib.ssd_decode_step_host_ex(ctypes.byref(s), bd.SSD_BF16, 7, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
                                      FAKE, FAKE, FAKE, 1 << 40, None)
+    assert rc == bd.SSD_ERR_INVALID_ARG
+
+
+def test_forward_flag_errors(lib):
+    s = shape()
+    ex = lambda fl: lib.ssd_forward_ex(ctypes.byref(s), bd.SSD_BF16, fl, FAKE, FAKE, FAKE, FAKE, FAKE, None, 256,
+                                       None, None, 0, FAKE, None, FAKE, 1 << 40, None)
+    assert ex(2) == bd.SSD_ERR_INVALID_ARG
+    assert ex(0x80000000) == bd.SSD_ERR_INVALID_ARG
+    rc = lib.ssd_forward_host_ex(ctypes.byref(s), bd.SSD_BF16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, 256, None,
+                                 None, 0, FAKE, None, FAKE, 1 << 40, None)
     assert rc == bd.SSD_ERR_INVALID_ARG

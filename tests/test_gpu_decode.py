@@ -28,12 +28,13 @@ def to_dev(d, dtype):
     return t
 
 
-def gpu_step(d, dtype, use_D=True, in_place=False):
+def gpu_step(d, dtype, use_D=True, in_place=False, scale_x_by_dt=False):
     import torch
     from mamba_ssd_layer_gb300 import ssd_decode_step
     t = to_dev(d, dtype)
     new = t["state"] if in_place else torch.empty_like(t["state"])
-    y, s = ssd_decode_step(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"] if use_D else None, t["state"], new)
+    y, s = ssd_decode_step(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"] if use_D else None, t["state"], new,
+                           scale_x_by_dt=scale_x_by_dt)
     torch.cuda.synchronize()
     return y.float().cpu().numpy().astype(np.float64), s.cpu().numpy().astype(np.float64)
 
@@ -178,3 +179,11 @@ def test_decode_bf16_state_in_place_and_host_entry():
     y, s = ssd_decode_step_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["state"], new)
     assert np.array_equal(y.float().numpy().astype(np.float64), y1)
     assert np.array_equal(s.float().numpy().astype(np.float64), s1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_dt_scaled_input(dtype):
+    d = decode_inputs(3, 4, 64, 128, 2, dtype, seed=440)
+    y, s = gpu_step(d, dtype, scale_x_by_dt=True)
+    yr, sr = oracle.ssd_decode_step(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], scale_x_by_dt=True)
+    assert normwise(y, yr) <= TOL[dtype] and normwise(s, sr) <= 1e-5

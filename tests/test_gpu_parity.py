@@ -10,9 +10,9 @@ from ssd_util import TOL, normwise, run_gpu, run_oracle
 pytestmark = pytest.mark.gpu
 
 
-def check(d, dtype, chunk, heads=None, use_D=True):
-    y, f = run_gpu(d, dtype, chunk, use_D=use_D)
-    yr, fr = run_oracle(d, heads=heads, use_D=use_D)
+def check(d, dtype, chunk, heads=None, use_D=True, scale_x_by_dt=False):
+    y, f = run_gpu(d, dtype, chunk, use_D=use_D, scale_x_by_dt=scale_x_by_dt)
+    yr, fr = run_oracle(d, heads=heads, use_D=use_D, scale_x_by_dt=scale_x_by_dt)
     if heads is not None:
         y, f = y[:, :, heads], f[:, heads]
     ey, ef = normwise(y, yr), normwise(f, fr)
@@ -166,3 +166,38 @@ def test_full_workload_sampled_heads(name, heads):
     w = WORKLOADS[name]
     d = make_inputs(w)
     check(d, "bf16", w.chunk, heads=heads)
+
+
+# ---------------------------------------------------------------- dt-scaled input term (dt x B^T)
+@pytest.mark.parametrize("N", [64, 128, 256])
+def test_bf16_dt_scaled_input_ragged(N):
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=1000, nheads=4, batch=2).with_(dstate=N, seed=500 + N)
+    check(make_inputs(w), "bf16", 256, scale_x_by_dt=True)
+
+
+def test_bf16_dt_scaled_input_long_chain_and_packed():
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=8192, nheads=2, batch=1).with_(seed=510)
+    check(make_inputs(w), "bf16", 256, scale_x_by_dt=True)
+    wv = small_variant(WORKLOADS["varlen"], seqlen=3000, nheads=4).with_(seg_min=1, seg_max=700, seed=511,
+                                                                       init_state=True)
+    check(make_inputs(wv), "bf16", 256, scale_x_by_dt=True)
+
+
+def test_bf16_dt_scaled_input_tiny_dt():
+    # dt down to zero: the kernel floors log2(dt); the contribution of such a token is ~0 either way
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=700, nheads=2, batch=1).with_(seed=512)
+    d = make_inputs(w)
+    d["dt"] = d["dt"].copy()
+    d["dt"][0, ::7, :] = 0.0
+    d["dt"][0, 3::11, :] = 1e-12
+    check(d, "bf16", 256, scale_x_by_dt=True)
+
+
+def test_fp32_dt_scaled_input():
+    w = WORKLOADS["fp32_tiny"].with_(batch=2, seqlen=300, nheads=4, init_state=True, seed=513)
+    check(make_inputs(w), "f32", 64, scale_x_by_dt=True)
+
+
+def test_dt_scaled_full_workload_sampled_heads():
+    w = WORKLOADS["long_n128"]
+    check(make_inputs(w), "bf16", w.chunk, heads=[0, 79], scale_x_by_dt=True)
