@@ -1381,17 +1381,19 @@ void fused_plan(const Problem& p, int* K_out, int64_t* np_out) {
     const int64_t npairs = p.s.nheads / 2;
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
     if (!p.varlen) {
-        // dense: pick the window K (tiles per piece) that balances the rounds best; a piece costs
-        // its K tiles plus about one tile of fixed work (look-back, pass-1 set-up)
+        // dense: pick the window K (tiles per piece) with the lowest estimated time, in units of one
+        // tile of phase C (measured on GB300): the busiest CTA's phase-C windows, K tiles plus about
+        // one tile of fixed work each; its phase-A windows at about 0.27 of a tile per tile; and the
+        // scan over all windows with a successor, about 0.008 of a tile per window
         const int64_t nt = (p.s.seqlen + kFusedTile - 1) / kFusedTile;
         const int64_t nchains = p.s.batch * npairs;
         int bestK = kFusedMinWindow;
         double best = 1e300;
         for (int K = kFusedMinWindow; K <= kFusedMaxWindow; ++K) {
             const int64_t W = (nt + K - 1) / K;
-            const int64_t np = nchains * W;
-            const int64_t rounds = (np + grid - 1) / grid;
-            const double cost = (double)rounds * (K + 1.0);
+            const int64_t np = nchains * W, nA = nchains * (W - 1);
+            const int64_t rounds = (np + grid - 1) / grid, rounds_a = (nA + grid - 1) / grid;
+            const double cost = (double)rounds * (K + 1.0) + 0.27 * (double)rounds_a * K + 0.008 * (double)nA;
             if (cost < best - 1e-9) { best = cost; bestK = K; }
         }
         *K_out = bestK;
