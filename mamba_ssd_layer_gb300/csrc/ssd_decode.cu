@@ -44,7 +44,6 @@ struct DecodeArgs {
     void* y;                // (batch, H, P) storage type
     int H, P, N, G;
     int heads_per_group;    // H / G
-    int scale_x_by_dt;      // the input term is dt x B^T
     int L;                  // lanes per state row
     int rows_per_cta;       // kDecWarps * (32 / L) * kDecRowsPerThread
     int row_blocks;         // ceil(P / rows_per_cta)
@@ -122,8 +121,8 @@ __device__ __forceinline__ void store_state(TS* p, const float (&v)[E]) {
 }
 
 // T: storage type of x, B, C, y; TS: storage type of the state; CI: 16-byte column chunks per lane
-// (N / E <= CI * L, E = 16 / sizeof(TS) state elements per chunk)
-template <typename T, typename TS, int CI>
+// (N / E <= CI * L, E = 16 / sizeof(TS) state elements per chunk); kScaleX: the input term is dt x
+template <typename T, typename TS, int CI, bool kScaleX>
 __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArgs a) {
     constexpr int E = 16 / (int)sizeof(TS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -141,7 +140,7 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
 
     const float dtv = a.dt[bh];
     const float decay = expf(dtv * a.A[h]);
-    const float in_scale = a.scale_x_by_dt ? dtv : 1.f;   // the skip term keeps the unscaled x
+    const float in_scale = kScaleX ? dtv : 1.f;           // the skip term keeps the unscaled x
     const float dskip = a.D ? a.D[h] : 0.f;
 
     const T* Bp = static_cast<const T*>(a.B) + (b * a.G + g) * a.N;
@@ -206,15 +205,19 @@ __global__ void __launch_bounds__(kDecThreads) ssd_decode_kernel(const DecodeArg
 }
 
 template <typename T, typename TS>
-cudaError_t launch_decode_t(const DecodeArgs& a, int64_t units, cudaStream_t st) {
+cudaError_t launch_decode_t(const DecodeArgs& a, int64_t units, bool scale_x, cudaStream_t st) {
     constexpr int E = 16 / (int)sizeof(TS);
     const int ci = (a.N / E + a.L - 1) / a.L;
     prof_launch();
     prof_begin(st, "ssd_decode_kernel");
-    if (ci <= 1)
-        ssd_decode_kernel<T, TS, 1><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+    if (ci <= 1 && !scale_x)
+        ssd_decode_kernel<T, TS, 1, false><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+    else if (ci <= 1)
+        ssd_decode_kernel<T, TS, 1, true><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+    else if (!scale_x)
+        ssd_decode_kernel<T, TS, 2, false><<<(unsigned)units, kDecThreads, 0, st>>>(a);
     else
-        ssd_decode_kernel<T, TS, 2><<<(unsigned)units, kDecThreads, 0, st>>>(a);
+        ssd_decode_kernel<T, TS, 2, true><<<(unsigned)units, kDecThreads, 0, st>>>(a);
     prof_end(st);
     return cudaGetLastError();
 }
@@ -272,7 +275,6 @@ int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtyp
     a.state = state; a.new_state = new_state; a.y = y;
     a.H = (int)s->nheads; a.P = (int)s->headdim; a.N = (int)s->dstate; a.G = (int)s->ngroups;
     a.heads_per_group = a.H / a.G;
-    a.scale_x_by_dt = (flags & SSD_SCALE_X_BY_DT) ? 1 : 0;
     const int nch = a.N / (state_dtype == SSD_F32 ? 4 : 8);   // 16-byte chunks per state row
     a.L = 1;
     while (a.L < nch && a.L < 32) a.L <<= 1;
@@ -282,12 +284,13 @@ int ssd_decode_step_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtyp
     if (units > (int64_t)INT32_MAX) return SSD_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
+    const bool sx = (flags & SSD_SCALE_X_BY_DT) != 0;
     if (state_dtype == SSD_F32)
-        e = dtype == SSD_F32 ? launch_decode_t<float, float>(a, units, st)
-                             : launch_decode_t<__nv_bfloat16, float>(a, units, st);
+        e = dtype == SSD_F32 ? launch_decode_t<float, float>(a, units, sx, st)
+                             : launch_decode_t<__nv_bfloat16, float>(a, units, sx, st);
     else
-        e = dtype == SSD_F32 ? launch_decode_t<float, __nv_bfloat16>(a, units, st)
-                             : launch_decode_t<__nv_bfloat16, __nv_bfloat16>(a, units, st);
+        e = dtype == SSD_F32 ? launch_decode_t<float, __nv_bfloat16>(a, units, sx, st)
+                             : launch_decode_t<__nv_bfloat16, __nv_bfloat16>(a, units, sx, st);
     return note_cuda_error("decode launch", e) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
