@@ -41,13 +41,14 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 375721728 + 183118080, "stamp": "61d1ef56bae08437"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 375032832 + 182451968, "stamp": "b304a874f6c90e01"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 458770560 + 182162816, "stamp": "61d1ef56bae08437"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 457998336 + 182124544, "stamp": "b304a874f6c90e01"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 375395328 + 182318848, "stamp": "b304a874f6c90e01"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
-    "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168496896 + 117427200, "stamp": "06c566e69a4338e5"},
-    "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609536 + 34459136,
-                              "stamp": "06c566e69a4338e5"},
+    "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168495104 + 117637120, "stamp": "154fb82720b02848"},
+    "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609280 + 34404352,
+                              "stamp": "154fb82720b02848"},
 }
 
 
