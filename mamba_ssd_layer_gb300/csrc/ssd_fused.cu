@@ -406,7 +406,8 @@ __device__ __forceinline__ int tile_len(const Piece& c, int t) {
 //   C  the window's tiles in time order from its entering state: diagonal blocks, left factors, the
 //      state carried on chip from tile to tile, y.
 // kScaleX: the input term is dt x B^T (a separate instantiation, so that the plain one carries none of it).
-template <int N, bool kScaleX>
+// kAccum: y is added onto the y already in memory (the second state-column half of N = 256).
+template <int N, bool kScaleX, bool kAccum>
 __global__ void __launch_bounds__(kThreads)
 ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1171,37 +1172,74 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 *reinterpret_cast<uint4*>(stg + sw128_offset(i, (c0 + k) / 8)) = v;
             }
-            if (!a.y_accum && 32 * qd + 32 <= len) {
+            if (kAccum ? 32 * qd + 32 <= len : (!a.y_accum && 32 * qd + 32 <= len)) {
                 // the quadrant's 32 rows all belong to the sequence: the two warps holding its two halves
-                // of the head's 64 channels meet, and one bulk tensor store writes the 4 KB
+                // of the head's 64 channels meet, and one bulk tensor store writes the 4 KB (with kAccum
+                // a bulk reduction adds them onto the y in memory: the bf16 sum of two bf16 values, as
+                // in the loop below)
                 fence_proxy_async_smem();
                 if (!pair_sync()) return false;
                 if ((kq & 1) == 0 && lane == 0) {
-                    tma_store_3d(&maps.y, stg + 32 * qd * 128, 0, h0 + hh, row0 + 32 * qd);
+                    if constexpr (kAccum)
+                        tma_reduce_add_3d(&maps.y, stg + 32 * qd * 128, 0, h0 + hh, row0 + 32 * qd);
+                    else
+                        tma_store_3d(&maps.y, stg + 32 * qd * 128, 0, h0 + hh, row0 + 32 * qd);
                     bulk_commit_group();
                 }
                 return true;
             }
             __syncwarp();
             const int cl = (c0 >> 3) + (lane & 3);          // 16-byte chunk of the row this lane writes
+            if constexpr (kAccum) {
+                // add onto the other state columns' share, in fp32; the four old pieces are loaded
+                // before any store (as far as the compiler knows a store could alias a later load,
+                // which would serialise the loads)
+                uint4 old[4];
 #pragma unroll
-            for (int pass = 0; pass < 4; ++pass) {
-                const int r = 32 * qd + 8 * pass + (lane >> 2);
-                if (r < len) {
-                    uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
-                    uint4* dst = reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl);
-                    if (a.y_accum) {
-                        // add onto the other state columns' share, in fp32
-                        const uint4 o = *dst;
-                        const uint32_t* ov = reinterpret_cast<const uint32_t*>(&o);
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int r = 32 * qd + 8 * pass + (lane >> 2);
+                    old[pass] = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < len)
+                        old[pass] = __ldcs(reinterpret_cast<const uint4*>(
+                            a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl));
+                }
+#pragma unroll
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int r = 32 * qd + 8 * pass + (lane >> 2);
+                    if (r < len) {
+                        uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
+                        const uint32_t* ov = reinterpret_cast<const uint32_t*>(&old[pass]);
                         uint32_t* nv = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const float2 f = __fadd2_rn(unpack_bf16x2(nv[m]), unpack_bf16x2(ov[m]));
                             nv[m] = pack_bf16x2(f.x, f.y);
                         }
+                        *reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl) = v;
                     }
-                    *dst = v;
+                }
+            } else {
+                // the general loop: it also handles a.y_accum, although the accumulating launches take
+                // the kAccum instantiation (this text keeps the plain instantiations' code unchanged)
+#pragma unroll
+                for (int pass = 0; pass < 4; ++pass) {
+                    const int r = 32 * qd + 8 * pass + (lane >> 2);
+                    if (r < len) {
+                        uint4 v = *reinterpret_cast<const uint4*>(stg + sw128_offset(r, cl));
+                        uint4* dst = reinterpret_cast<uint4*>(a.y + ((int64_t)(row0 + r) * a.H + h0 + hh) * 64 + 8 * cl);
+                        if (a.y_accum) {
+                            // add onto the other state columns' share, in fp32
+                            const uint4 o = *dst;
+                            const uint32_t* ov = reinterpret_cast<const uint32_t*>(&o);
+                            uint32_t* nv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const float2 f = __fadd2_rn(unpack_bf16x2(nv[m]), unpack_bf16x2(ov[m]));
+                                nv[m] = pack_bf16x2(f.x, f.y);
+                            }
+                        }
+                        *dst = v;
+                    }
                 }
             }
             __syncwarp();
@@ -1349,15 +1387,15 @@ size_t fused_smem_bytes() {
     return 2 * stage + (N / 64) * kRegion + (N >= 128 ? 0 : 2 * kRegion) + (2 * kCsStride + 192) * 4 + kNumBars * 8 + 16;
 }
 
-template <int N, bool kScaleX>
+template <int N, bool kScaleX, bool kAccum>
 cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMaps& maps, int grid) {
     const size_t smem = fused_smem_bytes<N>();
     cudaError_t e = note_cuda_error("fused smem attribute",
-        cudaFuncSetAttribute(ssd_fused_kernel<N, kScaleX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        cudaFuncSetAttribute(ssd_fused_kernel<N, kScaleX, kAccum>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     e = note_cuda_error("fused occupancy",
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N, kScaleX>, kThreads, smem));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ssd_fused_kernel<N, kScaleX, kAccum>, kThreads, smem));
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return note_cuda_error("fused occupancy is zero", cudaErrorLaunchOutOfResources);
     cudaLaunchConfig_t cfg = {};
@@ -1371,7 +1409,7 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_launch();
-    return note_cuda_error("fused cooperative launch", cudaLaunchKernelEx(&cfg, ssd_fused_kernel<N, kScaleX>, maps, fa));
+    return note_cuda_error("fused cooperative launch", cudaLaunchKernelEx(&cfg, ssd_fused_kernel<N, kScaleX, kAccum>, maps, fa));
 }
 
 }  // namespace
@@ -1450,10 +1488,13 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     fa.y_accum = part > 0 ? 1 : 0;
     cudaError_t e;
     prof_begin(p.stream, "ssd_fused_kernel");
-    if (p.scale_x_by_dt)
-        e = (N == 64) ? launch_fused_n<64, true>(p, fa, maps, grid) : launch_fused_n<128, true>(p, fa, maps, grid);
+    if (fa.y_accum)      // only the second half of N = 256, which runs the N = 128 kernel
+        e = p.scale_x_by_dt ? launch_fused_n<128, true, true>(p, fa, maps, grid)
+                            : launch_fused_n<128, false, true>(p, fa, maps, grid);
+    else if (p.scale_x_by_dt)
+        e = (N == 64) ? launch_fused_n<64, true, false>(p, fa, maps, grid) : launch_fused_n<128, true, false>(p, fa, maps, grid);
     else
-        e = (N == 64) ? launch_fused_n<64, false>(p, fa, maps, grid) : launch_fused_n<128, false>(p, fa, maps, grid);
+        e = (N == 64) ? launch_fused_n<64, false, false>(p, fa, maps, grid) : launch_fused_n<128, false, false>(p, fa, maps, grid);
     prof_end(p.stream);
     return e;
 }
