@@ -41,10 +41,10 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 375032832 + 182451968, "stamp": "b304a874f6c90e01"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 376092928 + 182684160, "stamp": "532861e9adad5c2b"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 457998336 + 182124544, "stamp": "b304a874f6c90e01"},
-    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 375395328 + 182318848, "stamp": "b304a874f6c90e01"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 457100800 + 177253760, "stamp": "532861e9adad5c2b"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 375994112 + 182185472, "stamp": "532861e9adad5c2b"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
     "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168495104 + 117637120, "stamp": "154fb82720b02848"},
     "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609280 + 34404352,
