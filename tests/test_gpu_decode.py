@@ -43,6 +43,7 @@ CASES = [  # batch, H, P, N, G, dtype
     (3, 4, 64, 128, 1, "bf16"), (5, 6, 64, 256, 2, "bf16"), (2, 4, 64, 64, 1, "bf16"),
     (3, 2, 16, 16, 1, "f32"), (2, 6, 12, 20, 3, "f32"), (1, 2, 256, 256, 1, "f32"),
     (7, 3, 33, 36, 3, "f32"), (2, 2, 5, 132, 1, "f32"), (4, 8, 64, 128, 4, "bf16"), (1, 1, 1, 4, 1, "f32"),
+    (2, 3, 200, 128, 1, "f32"),   # several row blocks per head, the last one partial
 ]
 
 
@@ -103,6 +104,18 @@ def test_decode_full_workload():
     assert ey <= TOL["bf16"] and es <= 1e-5
 
 
+def test_decode_bf16_state_full_workload():
+    from mamba_ssd_layer_gb300.inputs import bf16_round
+    w = WORKLOADS["decode_2p7b_bf16state"]
+    d = decode_inputs(w.batch, w.nheads, w.headdim, w.dstate, w.ngroups, w.dtype, seed=w.seed)
+    d["state"] = bf16_round(d["state"])
+    y, s = bf16_state_step(d, w.dtype, in_place=True)
+    yr, sr = oracle.ssd_decode_step(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"])
+    ey, es = normwise(y, yr), normwise(s, sr)
+    print(f"[decode parity] decode_2p7b_bf16state y_err={ey:.3e} state_err={es:.3e}")
+    assert ey <= TOL["bf16"] and es <= TOL["bf16"]
+
+
 def test_decode_host_entry_matches_device_entry():
     import torch
     from mamba_ssd_layer_gb300 import ssd_decode_step_host
@@ -132,7 +145,8 @@ def test_decode_empty_batch():
 
 # ---------------------------------------------------------------- state stored in bf16
 BF16S_CASES = [(3, 4, 64, 128, 1, "bf16"), (2, 6, 64, 256, 2, "bf16"), (2, 4, 64, 64, 1, "bf16"),
-               (2, 4, 16, 8, 1, "f32"), (1, 2, 33, 24, 1, "f32"), (3, 3, 7, 136, 3, "f32")]
+               (2, 4, 16, 8, 1, "f32"), (1, 2, 33, 24, 1, "f32"), (3, 3, 7, 136, 3, "f32"),
+               (3, 2, 100, 128, 1, "bf16")]   # two row blocks per head, the second partial
 
 
 def bf16_state_step(d, dtype, in_place=False):
