@@ -115,7 +115,19 @@ int ssd_forward(const ssd_shape *shape, ssd_dtype dtype,
 #define SSD_SCALE_X_BY_DT 1u
 
 /*
- * ssd_forward with option flags (0 or SSD_SCALE_X_BY_DT); other bits give SSD_ERR_INVALID_ARG.
+ * SSD_DEBUG_FORCE_TIMEOUT: a failure-detection test hook of the bf16 (tcgen05) path, not for normal
+ *   use. Every wait of a CTA for a window state published by another CTA (the look-back of the
+ *   inter-chunk pass) waits for a value that is never written, with a limit of about one millisecond
+ *   instead of two seconds. The call then ends with SSD_ERR_TIMEOUT in the workspace (ssd_status
+ *   returns it, and the workspace's third int32 holds the location code 0x300), every kernel returns,
+ *   and y is only partly written. Nothing is left running on the GPU: copies and tensor-core work
+ *   already issued are waited for before each CTA exits. The fp32 path ignores the flag.
+ */
+#define SSD_DEBUG_FORCE_TIMEOUT 0x80000000u
+
+/*
+ * ssd_forward with option flags (0, SSD_SCALE_X_BY_DT, SSD_DEBUG_FORCE_TIMEOUT); other bits give
+ * SSD_ERR_INVALID_ARG.
  * Everything else is as for ssd_forward.
  */
 int ssd_forward_ex(const ssd_shape *shape, ssd_dtype dtype, unsigned flags,
@@ -166,11 +178,15 @@ int ssd_forward_host_ex(const ssd_shape *shape, ssd_dtype dtype, unsigned flags,
  * Nothing in the array has to start at zero: the first kernel of every call clears the
  * status word, counters and look-back flags that the later kernels read.
  *
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * and caches it; make that first call before any stream capture on that device.
+ * Every call looks up the array's device address in the current context (cudaGetSymbolAddress, which
+ * does not synchronise). The first call in a process may also load the library's device code; make it
+ * before any stream capture.
  * Every call shares the one array: calls whose work overlaps on the GPU (different
  * streams, or host threads without ordering) race and corrupt each other's results.
- * Device-side status (a bounded wait that timed out) is not readable for these calls.
+ * Errors found on the device are not readable for these calls, because the caller cannot reach the
+ * array: a bounded wait that timed out, or malformed cu_seqlens (not starting at 0, decreasing, or not
+ * ending at seqlen), which the device-side table builder rejects and which leaves y unwritten. Callers
+ * must therefore pass checked segment offsets.
  */
 int ssd_forward_noalloc(const ssd_shape *shape, ssd_dtype dtype,
                         const void *x, const float *dt, const float *A,
@@ -247,8 +263,9 @@ int ssd_decode_step_host_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype s
 
 /*
  * Synchronises `stream`, then returns the device-side status recorded in the
- * workspace by the last ssd_forward that used it (SSD_OK or SSD_ERR_TIMEOUT),
- * or SSD_ERR_CUDA if the copy itself fails.
+ * workspace by the last ssd_forward that used it: SSD_OK, SSD_ERR_TIMEOUT (a bounded wait gave up),
+ * SSD_ERR_INVALID_ARG (malformed cu_seqlens, found by the device-side table builder; y is then not
+ * written), or SSD_ERR_CUDA if the copy itself fails.
  */
 int ssd_status(const void *workspace, void *stream);
 

@@ -15,6 +15,8 @@ from . import build as _build
 SSD_OK, SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED, SSD_ERR_CUDA, SSD_ERR_TIMEOUT, SSD_ERR_WORKSPACE = range(6)
 SSD_F32, SSD_BF16 = 0, 1
 SSD_SCALE_X_BY_DT = 1
+# failure-detection test hook (include/ssd.h): cross-CTA waits of the bf16 path are made to run out
+SSD_DEBUG_FORCE_TIMEOUT = 0x80000000
 
 _lib = None
 

@@ -135,7 +135,7 @@ int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const vo
                    const float* initial_state, const int32_t* cu_seqlens, int nseq, void* y, float* final_state,
                    void* workspace, size_t workspace_bytes, void* stream) {
     const bool varlen = cu_seqlens != nullptr;
-    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
+    if (flags & ~(SSD_SCALE_X_BY_DT | SSD_DEBUG_FORCE_TIMEOUT)) return SSD_ERR_INVALID_ARG;
     int rc = check_shape(s, dtype, chunk, nseq, varlen);
     if (rc != SSD_OK) return rc;
     const int64_t rows = s->batch * s->seqlen;
@@ -160,6 +160,7 @@ int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const vo
     p.chunk = chunk;
     p.varlen = varlen;
     p.scale_x_by_dt = (flags & SSD_SCALE_X_BY_DT) != 0;
+    p.force_timeout = (flags & SSD_DEBUG_FORCE_TIMEOUT) != 0;
     p.nseq = nseq_eff;
     p.rows = rows;
     p.x = x; p.dt = dt; p.A = A; p.B = B; p.C = C; p.D = D;
@@ -178,16 +179,15 @@ int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const vo
         int64_t np = 0;
         fused_plan(p, &K, &np);
         if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;
-        if (varlen) {
-            e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.woff(), K));
-        } else {
-            // a dense batch needs no tables: only the header (status, diagnostics, barrier counter) at zero
-            e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, 32, p.stream));
-        }
+        // the header (status, diagnostics) and the window flags start at zero
+        e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, L.clear_bytes, p.stream));
+        // a packed batch needs its tile and window tables; a dense batch decodes windows arithmetically
+        if (e == cudaSuccess && varlen) e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.woff(), K));
         if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np, 0));
         if (e == cudaSuccess && p.s.dstate > 128) {
-            // second half of the state columns: only the grid-barrier counter starts over
-            e = note_cuda_error("header reset", cudaMemsetAsync(p.status() + 4, 0, 8, p.stream));
+            // second half of the state columns: the window flags start over (an error recorded by the
+            // first launch stays in the status word)
+            e = note_cuda_error("flag reset", cudaMemsetAsync(p.flags(), 0, L.clear_bytes - L.flags, p.stream));
             if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np, 1));
         }
     } else {
@@ -226,7 +226,7 @@ int ssd_forward_host_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, con
                         const float* initial_state, const int32_t* cu_seqlens, int nseq, void* y, float* final_state,
                         void* device_buffer, size_t device_buffer_bytes, void* stream) {
     const bool varlen = cu_seqlens != nullptr;
-    if (flags & ~SSD_SCALE_X_BY_DT) return SSD_ERR_INVALID_ARG;
+    if (flags & ~(SSD_SCALE_X_BY_DT | SSD_DEBUG_FORCE_TIMEOUT)) return SSD_ERR_INVALID_ARG;
     int rc = check_shape(s, dtype, chunk, nseq, varlen);
     if (rc != SSD_OK) return rc;
     if (varlen && nseq <= 0) return SSD_ERR_INVALID_ARG;

@@ -15,10 +15,13 @@ struct ChunkDesc {
     int32_t row0, len, seq, ci;
 };
 
-// Workspace layout (byte offsets, every section 256-byte aligned).
+// Workspace layout (byte offsets, every section 256-byte aligned except the flags, which follow the
+// header directly so that one memset clears both).
 //   header  : int32 status, int32 number of chunks (tiles) actually built, int32 location
 //             code of the first device-side timeout (0 = none), int32 number of windows (packed
-//             batch, fused path), int32 grid-barrier arrival counter (fused path), int32 spare
+//             batch, fused path), int32 spare x 4
+//   flags   : (fused path) int32[max_pieces * 4], per window and TMEM lane quadrant: 1 = the window's
+//             aggregate is published, 2 = the state at its end is published, 0 = neither yet
 //   chunks  : ChunkDesc[max_chunks]  (chunks of `chunk` tokens; 128-token tiles on the fused path)
 //   seqoff  : int32[nseq + 1], first chunk of every sequence
 // fp32 path (three kernels):
@@ -28,9 +31,10 @@ struct ChunkDesc {
 //             true state entering the chunk
 // fused path (bf16, P = 64, N in {64, 128, 256}; 128 state columns per launch):
 //   woff    : int32[nseq + 1], first window of every sequence (packed batch)
-//   pdecay  : float[max_pieces * 2], decay of each window over its tiles, per head of the pair
+//   pdecay  : float[max_pieces * 4], decay of each window over its tiles, per lane quadrant (the
+//             head of quadrants 0, 1 is the pair's first head, of quadrants 2, 3 its second)
 //   agg     : float[max_pieces * 128 * Nl], the window's end state from a zero entering state
-//   incl    : float[max_pieces * 128 * Nl], the true state entering the window
+//   incl    : float[max_pieces * 128 * Nl], the true state at the window's end
 //   (Nl = min(N, 128), the state columns of one launch)
 constexpr int kFusedTile = 128;
 constexpr int kFusedMaxGrid = 256;
@@ -38,7 +42,8 @@ constexpr int kFusedMinWindow = 4;    // tiles per piece, lower bound (bounds th
 constexpr int kFusedMaxWindow = 16;
 
 struct WsLayout {
-    size_t header, chunks, seqoff, woff, decay, states, pdecay, agg, incl, total;
+    size_t header, flags, chunks, seqoff, woff, decay, states, pdecay, agg, incl, total;
+    size_t clear_bytes;          // bytes from the header on that every call clears before its kernels
     int64_t max_chunks, nseq, max_pieces;
     bool fused;
 };
@@ -63,17 +68,22 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
     else
         w.max_chunks = s.batch * ((s.seqlen + q - 1) / q);
     size_t off = 0;
-    w.header = off; off = align256(off + 32);
-    w.chunks = off; off = align256(off + sizeof(ChunkDesc) * (size_t)(w.max_chunks > 0 ? w.max_chunks : 1));
-    w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
+    w.header = off; off += 32;
     if (w.fused) {
         // pieces are windows of >= kFusedMinWindow tiles of one (sequence, head pair)
         const int64_t per_seq = varlen ? ((w.max_chunks - nseq_eff) + kFusedMinWindow - 1) / kFusedMinWindow + nseq_eff
                                        : s.batch * ((((s.seqlen + q - 1) / q) + kFusedMinWindow - 1) / kFusedMinWindow);
         w.max_pieces = (s.nheads / 2) * (per_seq > 0 ? per_seq : 1);
+        w.flags = off; off += sizeof(int32_t) * 4 * (size_t)w.max_pieces;
+    }
+    w.clear_bytes = off;
+    off = align256(off);
+    w.chunks = off; off = align256(off + sizeof(ChunkDesc) * (size_t)(w.max_chunks > 0 ? w.max_chunks : 1));
+    w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
+    if (w.fused) {
         const int64_t ncol = s.dstate > 128 ? 128 : s.dstate;   // state columns of one launch
         w.woff = off;   off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
-        w.pdecay = off; off = align256(off + sizeof(float) * 2 * (size_t)w.max_pieces);
+        w.pdecay = off; off = align256(off + sizeof(float) * 4 * (size_t)w.max_pieces);
         w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
         w.incl = off;   off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
     } else {
@@ -91,6 +101,8 @@ struct Problem {
     int chunk;
     bool varlen;
     bool scale_x_by_dt;    // the input term is dt x B^T (SSD_SCALE_X_BY_DT)
+    bool force_timeout;    // SSD_DEBUG_FORCE_TIMEOUT: every cross-CTA wait of the fused kernel is made to
+                           // run out after about a millisecond (failure-detection tests)
     int64_t nseq;          // sequences: batch (dense) or segments (varlen)
     int64_t rows;          // packed rows = batch * seqlen
     const void* x;
@@ -115,6 +127,7 @@ struct Problem {
     float* decay() const { return reinterpret_cast<float*>(ws + L.decay); }
     float* states() const { return reinterpret_cast<float*>(ws + L.states); }
     int32_t* woff() const { return reinterpret_cast<int32_t*>(ws + L.woff); }
+    int32_t* flags() const { return reinterpret_cast<int32_t*>(ws + L.flags); }
 };
 
 // ssd_api.cu: records the failing step of an SSD_ERR_CUDA for ssd_last_error_detail

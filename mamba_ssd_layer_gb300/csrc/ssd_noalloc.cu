@@ -5,9 +5,9 @@
 // The scratch that ssd_forward takes from the caller's workspace lives here instead, in a
 // file-scope device array of fixed size. Every GPU that loads this library holds that array
 // until the process exits. Host code cannot use the array's name as a device address, so
-// the address is looked up once per device with cudaGetSymbolAddress and passed on.
+// the address is looked up with cudaGetSymbolAddress (in the current context, on every call) and
+// passed on.
 #include <cstdio>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -21,23 +21,14 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_lock;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up on first use.
+// Device address of the scratch array in the current context. Looked up on every call: the lookup does
+// not synchronise, and a context that was reset (cudaDeviceReset) and created again may place the
+// array elsewhere, so a cached address could point at memory the array no longer occupies.
 int scratch_address(void** out) {
-    int dev = 0;
-    if (ssd::note_cuda_error("cudaGetDevice", cudaGetDevice(&dev)) != cudaSuccess) return SSD_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return SSD_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> guard(g_noalloc_lock);
-    if (!g_noalloc_ptr[dev]) {
-        void* p = nullptr;
-        if (ssd::note_cuda_error("cudaGetSymbolAddress", cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
-            return SSD_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void* p = nullptr;
+    if (ssd::note_cuda_error("cudaGetSymbolAddress", cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    *out = p;
     return SSD_OK;
 }
 

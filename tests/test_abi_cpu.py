@@ -140,7 +140,9 @@ def test_forward_flag_errors(lib):
     ex = lambda fl: lib.ssd_forward_ex(ctypes.byref(s), bd.SSD_BF16, fl, FAKE, FAKE, FAKE, FAKE, FAKE, None, 256,
                                        None, None, 0, FAKE, None, FAKE, 1 << 40, None)
     assert ex(2) == bd.SSD_ERR_INVALID_ARG
-    assert ex(0x80000000) == bd.SSD_ERR_INVALID_ARG
+    assert ex(0x40000000) == bd.SSD_ERR_INVALID_ARG
+    # the failure-detection test hook is a known flag: the call gets past the flag check
+    assert ex(bd.SSD_DEBUG_FORCE_TIMEOUT) != bd.SSD_ERR_INVALID_ARG
     rc = lib.ssd_forward_host_ex(ctypes.byref(s), bd.SSD_BF16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, 256, None,
                                  None, 0, FAKE, None, FAKE, 1 << 40, None)
     assert rc == bd.SSD_ERR_INVALID_ARG

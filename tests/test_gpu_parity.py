@@ -49,13 +49,28 @@ def test_bf16_chunk_sizes_ragged(chunk, N):
     check(make_inputs(w), "bf16", chunk)
 
 
-def test_bf16_chunk_invariance():
+def test_bf16_chunk_does_not_change_the_result():
+    """On the bf16 path the kernel's tile is 128 tokens whatever `chunk` says (the decomposition is exact
+    for any block length, "LLM(十一)——Mamba" §3.5), so the three values give bit-identical outputs; the
+    oracle check of each is in test_bf16_chunk_sizes_ragged."""
     w = small_variant(WORKLOADS["m2_2p7b"], seqlen=777, nheads=2, batch=1).with_(seed=91)
     d = make_inputs(w)
     outs = [run_gpu(d, "bf16", q) for q in (64, 128, 256)]
     for (y, f) in outs[1:]:
-        assert normwise(y, outs[0][0]) <= TOL["bf16"]
-        assert normwise(f, outs[0][1]) <= TOL["bf16"]
+        assert np.array_equal(y, outs[0][0]) and np.array_equal(f, outs[0][1])
+
+
+def test_bf16_skip_term_in_fp32():
+    """With C = 0 the layer reduces to its skip term: y = D x exactly. D is fp32, so y must be the
+    bf16 rounding (to nearest even) of the fp32 product D x, element by element."""
+    import torch
+    w = small_variant(WORKLOADS["m2_2p7b"], seqlen=700, nheads=4, batch=2).with_(seed=103)
+    d = dict(make_inputs(w))
+    d["C"] = np.zeros_like(d["C"])
+    y, _ = run_gpu(d, "bf16", 256)
+    prod = d["D"].astype(np.float32)[None, None, :, None] * d["x"].astype(np.float32)
+    want = torch.from_numpy(prod).to(torch.bfloat16).float().numpy()
+    assert np.array_equal(y.astype(np.float32), want)
 
 
 def test_bf16_no_skip_no_init():

@@ -1,7 +1,8 @@
 """ssd_forward_noalloc: the same forward pass with scratch in a static device array, for
 callers that cannot allocate device memory. Checked through the C ABI against ssd_forward
-on the same inputs, on two calls in a row (the array is shared and keeps the previous call's
-contents, so the second call also checks that stale scratch does not leak into results).
+on the same inputs, on two calls in a row. The array is shared and keeps the previous call's
+contents, so a call on other inputs runs between the two compared calls: the second compared call
+then starts from another problem's scratch, which must not leak into its results.
 
 This file is named to run last: if it fails, a run that stops at the first failure has
 already run every other test."""
@@ -51,16 +52,25 @@ def test_noalloc_matches_workspace_entry_point(dtype, w):
     shape = bd._shape(x.shape[0], x.shape[1], x.shape[2], x.shape[3], t["B"].shape[3], t["B"].shape[2])
     code = bd.SSD_F32 if dtype == "f32" else bd.SSD_BF16
     stream = torch.cuda.current_stream()
-    for _ in range(2):
+    def call(tt, y, f):
+        return fn(ctypes.byref(shape), code, _ptr(tt["x"]), _ptr(tt["dt"]), _ptr(tt["A"]), _ptr(tt["B"]),
+                  _ptr(tt["C"]), _ptr(tt["D"]), w.chunk, _ptr(tt["initial_state"]), _ptr(cu), nseq, _ptr(y),
+                  _ptr(f), ctypes.c_void_p(stream.cuda_stream))
+
+    other = to_device(make_inputs(w.with_(seed=w.seed + 1000)), dtype)
+    for k in range(2):
         y = torch.full_like(x, float("nan"))
         f = torch.full_like(f_ref, float("nan"))
-        rc = fn(ctypes.byref(shape), code, _ptr(x), _ptr(t["dt"]), _ptr(t["A"]), _ptr(t["B"]), _ptr(t["C"]),
-                _ptr(t["D"]), w.chunk, _ptr(t["initial_state"]), _ptr(cu), nseq, _ptr(y), _ptr(f),
-                ctypes.c_void_p(stream.cuda_stream))
+        rc = call(t, y, f)
         assert rc == bd.SSD_OK, bd.ssd_status_string(rc)
         torch.cuda.synchronize()
         assert normwise(y.float().cpu().numpy(), y_ref.float().cpu().numpy()) <= TOL[dtype]
         assert normwise(f.cpu().numpy(), f_ref.cpu().numpy()) <= TOL[dtype]
+        if k == 0:
+            # another problem of the same shape in between: it leaves its own scratch behind
+            rc = call(other, torch.empty_like(x), torch.empty_like(f_ref))
+            assert rc == bd.SSD_OK, bd.ssd_status_string(rc)
+            torch.cuda.synchronize()
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
