@@ -178,7 +178,8 @@ int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const vo
         int K = 0;
         int64_t np = 0;
         fused_plan(p, &K, &np);
-        if (np > L.max_pieces) return SSD_ERR_UNSUPPORTED;
+        // window slots are indexed with 32-bit arithmetic on the device
+        if (np > L.max_pieces || np >= (int64_t(1) << 28)) return SSD_ERR_UNSUPPORTED;
         // the header (status, diagnostics) and the window flags start at zero
         e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, L.clear_bytes, p.stream));
         // a packed batch needs its tile and window tables; a dense batch decodes windows arithmetically

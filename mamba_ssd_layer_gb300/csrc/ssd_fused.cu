@@ -80,7 +80,7 @@ enum : int {
     kFullBC = 0,     // [2] B (and C) of the stage landed (TMA bytes)
     kFullX = 2,      // [2] x of the stage landed (TMA bytes)
     kTblC = 4,       // [2] the stage's tables written, for a tile
-    kTblA = 6,       // [2] the stage's tables written, for an aggregate tile
+    kTblAny = 6,     // [2] the stage's tables and tile record written (every tile, and the end record)
     kBCFree = 8,     // [2] MMA done with the stage's B and C
     kXFreeC = 10,    // [2] a tile's y (staged in the stage's x) stored: 8 epilogue warps
     kXFreeA = 12,    // [2] MMA done with an aggregate tile's x
@@ -102,6 +102,9 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
          : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree || i == kSTFree) ? 4u
          : 1u;
 }
+
+// tile record flags: an aggregate tile; the end of this CTA's stream (no tile)
+constexpr int kRecAgg = 1, kRecEnd = 2;
 
 // Timeout location codes (workspace header word 2): 0x100 + barrier for an mbarrier wait, 0x300 for a
 // look-back wait on another CTA's published state.
@@ -131,10 +134,10 @@ struct FusedArgs {
     float* agg;                 // the window's end state from a zero entering state
     float* incl;                // the window's true end state
     int H, G, nseq, npairs;
-    int64_t npieces;            // windows to dispatch (exact for a dense batch, a bound for a packed one)
+    int npieces;                // windows to dispatch (exact for a dense batch, a bound for a packed one)
     int K;                      // tiles per window
     int dense;                  // 1: batch of equal sequences (windows decoded arithmetically)
-    int64_t seqlen;             // dense: tokens per sequence
+    int seqlen;                 // dense: tokens per sequence
     int nt_dense;               // dense: tiles per sequence
     int W_dense;                // dense: windows per sequence
     // Split state: this launch covers state columns [n_off, n_off + N) of n_full (B, C, the initial
@@ -177,6 +180,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -192,6 +201,14 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
+// Per-warpgroup register budgets (setmaxnreg): the launch gives every thread kLaunchRegs; the
+// producer / MMA / tables warpgroup and the mask warpgroup hand some back and the two epilogue
+// warpgroups take them. 128 (56 + 88 + 96) + 256 * 120 = 640 * 96.
+constexpr uint32_t kLaunchRegs = 96, kRegsWG0 = 56, kRegsMask = 88, kRegsEpi = 120;
+static_assert(128 * (kRegsWG0 + kRegsMask + kLaunchRegs) + 256 * kRegsEpi <= 640 * kLaunchRegs, "register split");
+template <uint32_t R> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(R)); }
+template <uint32_t R> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(R)); }
+
 // ---------------------------------------------------------------- shared memory layout
 template <int N>
 struct Lay {
@@ -200,7 +217,8 @@ struct Lay {
     static constexpr uint32_t kHS = 2 * kStage;                        // h_{t-1} in bf16 for Yo
     static constexpr uint32_t kCs = kHS + NB * kRegion;                // [2][kCsStride] floats
     static constexpr uint32_t kVt = kCs + 2 * kCsStride * 4;           // [2][kVtCols] halves
-    static constexpr uint32_t kBars = kVt + 2 * kVtCols * 2;           // [kNumBars] u64
+    static constexpr uint32_t kRec = kVt + 2 * kVtCols * 2;            // [2] tile records (int4)
+    static constexpr uint32_t kBars = kRec + 2 * 16;                   // [kNumBars] u64
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
     static constexpr uint32_t kTotal = kMisc + 16;
     static_assert(kBars % 8 == 0, "barriers are 8-byte aligned");
@@ -221,6 +239,8 @@ struct Smem {
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(base + Lay<N>::kCs) + s * kCsStride; }
     // exp(cs_p - table_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
     __device__ __half* vt() const { return reinterpret_cast<__half*>(base + Lay<N>::kVt); }
+    // per stage: the tile record {first row, tokens, first head, flags} (flags: kRecAgg, kRecEnd)
+    __device__ int4* rec(int s) const { return reinterpret_cast<int4*>(base + Lay<N>::kRec) + s; }
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(base + Lay<N>::kBars); }
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + Lay<N>::kMisc); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(base + Lay<N>::kMisc + 4); }
@@ -235,13 +255,17 @@ struct Waiter {
 
 // Bounded wait for the phase of `idx` whose parity is bit idx of `ph` (then flipped). Gives up when
 // the CTA is aborting (honor_abort) or after the limit; returns false then.
-__device__ __forceinline__ bool wait_par(const Waiter& w, int idx, uint32_t par, bool honor_abort = true) {
-    uint64_t* bar = w.bars + idx;
-    if (mbar_try_wait(bar, par)) return true;
+// The loop of a wait that did not complete at once.
+__device__ __forceinline__ bool wait_par_slow(uint64_t* bars, volatile int* abort, int* status, int idx, uint32_t par,
+                                              bool honor_abort) {
+    const Waiter w{bars, abort, status};
+    uint64_t* bar = bars + idx;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, par)) return true;   // may block for a short, hardware-chosen time
-        if ((it & 63u) != 0) continue;
+        // the thread sleeps until the phase completes or about 20 us pass, so that waiting warps leave
+        // the issue slots to the warps that work
+        if (mbar_try_wait_sleep(bar, par, 20000u)) return true;
+        if ((it & 7u) != 0) continue;
         if (honor_abort && *w.abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             record_status(w.status, SSD_ERR_TIMEOUT);
@@ -250,6 +274,11 @@ __device__ __forceinline__ bool wait_par(const Waiter& w, int idx, uint32_t par,
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool wait_par(const Waiter& w, int idx, uint32_t par, bool honor_abort = true) {
+    if (mbar_try_wait(w.bars + idx, par)) return true;
+    return wait_par_slow(w.bars, w.abort, w.status, idx, par, honor_abort);
 }
 
 __device__ __forceinline__ bool wait_bar(const Waiter& w, int idx, uint32_t& ph) {
@@ -283,43 +312,44 @@ __device__ __forceinline__ void warp_arrive(const Waiter& w, int idx) {
 // A piece is one window of K consecutive 128-token tiles of one chain (sequence s, head pair hp).
 // q: its slot for published states (chain-major); d: its place in the dispatch order.
 struct Piece {
-    int64_t q, d;
+    int q, d;
     int s, hp, w, W;           // sequence, head pair, window, windows of the chain
     int t0, t1, nt;            // tiles [t0, t1) of the sequence's nt tiles
     int32_t seq_row0, seq_len; // first packed row and length of the sequence
     bool valid;
 };
 
-__device__ __forceinline__ Piece decode_piece(int64_t d, const FusedArgs& a) {
+// Window counts fit in 32 bits (the launcher checks), so the decoding divides 32-bit integers.
+__device__ __forceinline__ Piece decode_piece(int d, const FusedArgs& a) {
     Piece p;
     p.valid = true;
     p.d = d;
     if (a.dense) {
-        const int64_t nchains = (int64_t)a.nseq * a.npairs;
-        const int64_t w = d / nchains, c = d % nchains;
-        p.w = (int)w;
+        const int nchains = a.nseq * a.npairs;
+        const int w = d / nchains, c = d - w * nchains;
+        p.w = w;
         p.W = a.W_dense;
-        p.s = (int)(c / a.npairs);
-        p.hp = (int)(c % a.npairs);
+        p.s = c / a.npairs;
+        p.hp = c - p.s * a.npairs;
         p.q = c * a.W_dense + w;
         p.nt = a.nt_dense;
         p.seq_row0 = (int32_t)(p.s * a.seqlen);
         p.seq_len = (int32_t)a.seqlen;
     } else {
-        const int64_t total = (int64_t)a.status[3] * a.npairs;
+        const int total = a.status[3] * a.npairs;
         if (d >= total) { p.valid = false; return p; }
         int lo = 0, hi = a.nseq - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)a.npairs * a.woff[mid] <= d) lo = mid; else hi = mid - 1;
+            if (a.npairs * a.woff[mid] <= d) lo = mid; else hi = mid - 1;
         }
         const int32_t w0 = a.woff[lo], w1 = a.woff[lo + 1];
-        const int64_t local = d - (int64_t)a.npairs * w0;
+        const int local = d - a.npairs * w0;
         const int Ws = w1 - w0;
         p.s = lo;
         p.W = Ws;
-        p.hp = (int)(local / Ws);
-        p.w = (int)(local % Ws);
+        p.hp = local / Ws;
+        p.w = local - p.hp * Ws;
         p.q = d;
         const int32_t f0 = a.seqoff[lo], f1 = a.seqoff[lo + 1];
         p.nt = f1 - f0;
@@ -339,19 +369,15 @@ __device__ __forceinline__ int tile_len(const Piece& c, int t) {
 }
 
 // dispatch index of the next / previous window of the same chain
-__device__ __forceinline__ int64_t succ_d(int64_t d, const FusedArgs& a) {
-    return a.dense ? d + (int64_t)a.nseq * a.npairs : d + 1;
-}
-__device__ __forceinline__ int64_t pred_d(int64_t d, const FusedArgs& a) {
-    return a.dense ? d - (int64_t)a.nseq * a.npairs : d - 1;
-}
+__device__ __forceinline__ int succ_d(int d, const FusedArgs& a) { return a.dense ? d + a.nseq * a.npairs : d + 1; }
+__device__ __forceinline__ int pred_d(int d, const FusedArgs& a) { return a.dense ? d - a.nseq * a.npairs : d - 1; }
 // the window publishes its aggregate: its successor runs in the same iteration
 __device__ __forceinline__ bool needs_agg(const Piece& c, const FusedArgs& a) {
-    return c.w + 1 < c.W && succ_d(c.d, a) / gridDim.x == c.d / gridDim.x;
+    return c.w + 1 < c.W && (unsigned)succ_d(c.d, a) / gridDim.x == (unsigned)c.d / gridDim.x;
 }
 // the window publishes its end state: its successor runs in a later iteration
 __device__ __forceinline__ bool needs_end(const Piece& c, const FusedArgs& a) {
-    return c.w + 1 < c.W && succ_d(c.d, a) / gridDim.x != c.d / gridDim.x;
+    return c.w + 1 < c.W && (unsigned)succ_d(c.d, a) / gridDim.x != (unsigned)c.d / gridDim.x;
 }
 
 // The tile stream of this CTA, walked identically by every role: for each of its windows, the
@@ -364,7 +390,7 @@ struct Stream {
     int32_t row0, len;    // first packed row and length of the sequence
     bool agg;             // an aggregate tile
     bool valid;
-    __device__ int64_t d() const { return (int64_t)blockIdx.x + (int64_t)kd * gridDim.x; }
+    __device__ int d() const { return (int)blockIdx.x + kd * (int)gridDim.x; }
     __device__ int tile_row0() const { return row0 + kTile * t; }
     __device__ int tile_len() const {
         const int rem = len - kTile * t;
@@ -386,7 +412,7 @@ struct Stream {
     }
     __device__ void start(const FusedArgs& a) {
         kd = 0;
-        nwin = a.npieces > (int64_t)blockIdx.x ? (int)((a.npieces - blockIdx.x + gridDim.x - 1) / gridDim.x) : 0;
+        nwin = a.npieces > (int)blockIdx.x ? (a.npieces - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
         load(a);
     }
     __device__ void next(const FusedArgs& a) {
@@ -395,15 +421,11 @@ struct Stream {
         ++kd;
         load(a);
     }
-    __device__ void next_window(const FusedArgs& a) {
-        ++kd;
-        load(a);
-    }
 };
 
 // Sum of dt*A (x log2 e) over a window's tokens [r0, r0 + ntok), per head h0, h0 + 1, by one warp in a
 // fixed order (the same code everywhere it is needed, so every caller gets the same bits).
-__device__ __noinline__ float2 window_total(const float* __restrict__ dt, const float* __restrict__ A, int H,
+__device__ __forceinline__ float2 window_total(const float* __restrict__ dt, const float* __restrict__ A, int H,
                                             int h0, int r0, int ntok, int lane) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll 8
@@ -423,6 +445,47 @@ __device__ __forceinline__ float2 window_total(const FusedArgs& a, const Stream&
     const int r0 = st.row0 + kTile * st.t0;
     const int end = st.row0 + (kTile * st.t1 < st.len ? kTile * st.t1 : st.len);
     return window_total(a.dt, a.A, a.H, 2 * st.hp, r0, end - r0, lane);
+}
+
+// ---------------------------------------------------------------- epilogue helpers (cold paths kept out
+// of line so that they do not add to the registers of the per-tile path)
+// 16-byte chunk ch of a 128-byte row of a swizzled region (row pointer, row & 7)
+__device__ __forceinline__ uint8_t* chunk_ptr(uint8_t* rowp, int ix, int ch) { return rowp + ((ch ^ ix) << 4); }
+
+// an aggregate tile's x row (64 bf16 channels) times w in place, in fp32, rounded once
+__device__ __noinline__ void weight_row(uint8_t* rowp, int ix, float w) {
+    const float2 ww = make_float2(w, w);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(rowp, ix, ch));
+        uint4 v = *pv;
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float2 f = __fmul2_rn(unpack_bf16x2(u[m]), ww);
+            u[m] = pack_bf16x2(f.x, f.y);
+        }
+        *pv = v;
+    }
+}
+
+// one staged y row (64 bf16 channels) to global memory; with `accum` added in fp32 onto the y there
+__device__ __noinline__ void store_row(uint8_t* rowp, int ix, __nv_bfloat16* yrow, bool accum) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint4 v = *reinterpret_cast<const uint4*>(chunk_ptr(rowp, ix, ch));
+        if (accum) {
+            const uint4 o = *reinterpret_cast<const uint4*>(yrow + 8 * ch);
+            const uint32_t* ov = reinterpret_cast<const uint32_t*>(&o);
+            uint32_t* nv = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float2 f = __fadd2_rn(unpack_bf16x2(nv[m]), unpack_bf16x2(ov[m]));
+                nv[m] = pack_bf16x2(f.x, f.y);
+            }
+        }
+        *reinterpret_cast<uint4*>(yrow + 8 * ch) = v;
+    }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -478,6 +541,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         // Stage s = p & 1 of stream position p holds x (both heads), B and, for a tile, C. A stage is
         // reloaded once the MMA warp is done with its B and C and its x is free: for a tile, once its
         // y (staged there) has been stored; for an aggregate tile, once the MMA warp has read it.
+        regs_dec<kRegsWG0>();
         if (lane == 0) {
             uint32_t ph = 0;
             bool ok = true;
@@ -513,6 +577,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         }
     } else if (warp == kWarpMMA) {
         // ============================================================ MMA issuer (lane 0)
+        regs_dec<kRegsWG0>();
         if (lane == 0) {
             uint32_t ph = 0;
             bool ok = true, any = false;
@@ -524,6 +589,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const uint32_t id_yd = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t id_s = idesc_bf16_f32(128, N, 1, 1);
             auto issue_g = [&](int st, int buf) {
+#pragma unroll 1
                 for (int ks = 0; ks < N / 16; ++ks) {
                     const int k = ks / 4, off = (ks % 4) * 32;
                     const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + k * kRegion + off), 0, 1024);
@@ -534,6 +600,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             };
             // S += (w o X)^T B over the stage (M = 2 heads x 64 channels, N = state columns)
             auto issue_s = [&](int st, bool acc) {
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
                     const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
@@ -573,6 +640,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t gb = kColGB + 128 * buf;
+#pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -581,10 +649,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                 }
                 mma_commit(sm.bars() + kYDFull);
-                // C B^T of the next tile as soon as its B and C are there and its buffer is free
-                Stream nx = it;
-                nx.next(a);
-                const bool next_tile = nx.valid && !nx.agg;
+                // C B^T of the window's next tile as soon as its B and C are there and its buffer is free
+                const bool next_tile = it.t + 1 < it.t1;
                 bool bc_ok = false, gb_ok = false;
                 if (next_tile) {
                     bc_ok = test_bar(wt, kFullBC + (s ^ 1), ph);
@@ -600,6 +666,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (!ok) break;
                 tc_fence_after_sync();
                 issue_s(s, true);
+#pragma unroll 1
                 for (int ks = 0; ks < N / 16; ++ks) {
                     const int kk = ks / 4, off = (ks % 4) * 32;
                     const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(s) + kk * kRegion + off), 0, 1024);
@@ -627,19 +694,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         }
     } else if (warp == kWarpTables) {
         // ============================================================ tables (whole warp)
-        // Per stream position: dt of the tile for both heads of the pair (prefetched two positions
+        // Per stream position: dt of the tile for both heads of the pair (prefetched one position
         // ahead), the cumsum of dt*A (x log2 e) -- window-relative for an aggregate tile, tile-local
         // for a tile -- and, for a tile, the factored-mask column table (once the mask warps are done
         // with the previous one).
+        regs_dec<kRegsWG0>();
         uint32_t ph = 0;
         bool ok = true;
         bool prev_agg[2] = {false, false};
         bool vt_used = false;
         float carry[2] = {0.f, 0.f};
         float2 tot = make_float2(0.f, 0.f);
-        Stream it, ahead;
+        Stream it;
         it.start(a);
-        ahead = it;
         auto load_dt = [&](const Stream& st, float (&v)[2][4]) {
             if (!st.valid) return;
             const int row0 = st.tile_row0(), len = st.tile_len(), h0 = 2 * st.hp;
@@ -652,30 +719,30 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 v[1][k] = d2.y;
             }
         };
-        float vn1[2][4] = {}, vn2[2][4] = {};
-        load_dt(ahead, vn1);
-        if (ahead.valid) ahead.next(a);
-        load_dt(ahead, vn2);
-        if (ahead.valid) ahead.next(a);
-        for (int p = 0; it.valid && ok; it.next(a), ++p) {
+        float vn[2][4] = {};
+        int np_done = 0;
+        load_dt(it, vn);
+        for (int p = 0; it.valid && ok; ++p) {
             const int s = p & 1;
+            // this tile's dt (loaded one tile ahead) and place in the stream; then the next tile's dt
             float v[2][4];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) { v[hh][k] = vn1[hh][k]; vn1[hh][k] = vn2[hh][k]; }
-            load_dt(ahead, vn2);
-            if (ahead.valid) ahead.next(a);
-            if (it.agg && it.t == it.t0) {
+                for (int k = 0; k < 4; ++k) v[hh][k] = vn[hh][k];
+            const bool agg = it.agg, first_agg = it.agg && it.t == it.t0;
+            const int h0 = 2 * it.hp, len = it.tile_len(), row0 = it.tile_row0();
+            if (first_agg) {
                 tot = window_total(a, it, lane);
                 carry[0] = carry[1] = 0.f;
             }
-            if (!it.agg) carry[0] = carry[1] = 0.f;
+            it.next(a);
+            load_dt(it, vn);
+            if (!agg) carry[0] = carry[1] = 0.f;
             if (p >= 2) {
                 ok = __all_sync(0xffffffffu, wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph));
                 if (!ok) break;
             }
-            const int h0 = 2 * it.hp, len = it.tile_len();
             float* cs = sm.cs(s);
             float cv[2][4];
 #pragma unroll
@@ -705,14 +772,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 carry[hh] += __shfl_sync(0xffffffffu, sc, 31);
                 // row-side values: the plain cumsum at tokens 31, 63, 95, and the last value
                 if (lane == 7 || lane == 15 || lane == 23) cs[256 + 4 * hh + (lane >> 3)] = cv[hh][3];
-                if (it.agg) {
+                if (agg) {
                     if (lane == 0) cs[256 + 4 * hh + 3] = hh ? tot.y : tot.x;
                 } else if (lane == ((len - 1) >> 2)) {
                     const int k = (len - 1) & 3;
                     cs[256 + 4 * hh + 3] = k == 0 ? cv[hh][0] : k == 1 ? cv[hh][1] : k == 2 ? cv[hh][2] : cv[hh][3];
                 }
             }
-            if (!it.agg) {
+            if (!agg) {
                 // v_j = exp(cs_p - table_j), p the last token of j's 32-token block (j < 96)
                 if (vt_used) {
                     ok = __all_sync(0xffffffffu, wait_bar(wt, kVTFree, ph));
@@ -739,11 +806,27 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                 }
             }
+            if (lane == 0) *sm.rec(s) = make_int4(row0, len, h0, agg ? kRecAgg : 0);
             __syncwarp();
-            if (lane == 0) mbar_arrive(sm.bars() + (it.agg ? kTblA : kTblC) + s);
-            prev_agg[s] = it.agg;
+            if (lane == 0) {
+                mbar_arrive(sm.bars() + kTblAny + s);
+                if (!agg) mbar_arrive(sm.bars() + kTblC + s);
+            }
+            prev_agg[s] = agg;
+            np_done = p + 1;
+        }
+        // the end record after the last tile, once its stage is free
+        if (ok) {
+            const int s = np_done & 1;
+            if (np_done >= 2) ok = __all_sync(0xffffffffu, wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph));
+            if (ok && lane == 0) {
+                *sm.rec(s) = make_int4(0, 0, 0, kRecEnd);
+                mbar_arrive(sm.bars() + kTblAny + s);
+            }
         }
         if (!ok) set_abort();
+    } else if (warp == 3) {
+        regs_dec<kRegsWG0>();          // no role; its share of the registers goes to the epilogue
     } else if (warp >= kWarpMask && warp < kWarpMask + 4) {
         // ============================================================ L o G (one warp per lane quadrant)
         // Row i = 32 q + lane of the tile; 16-column group g holds tokens j = 16 g .. 16 g + 15 and is
@@ -751,6 +834,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         //   b < q   exp(cs_i - cs_p) exp(cs_p - cs_j), p the block's last token (both factors <= 1)
         //   b = q   exp(cs_i - cs_j), zero where j > i
         //   b > q   zero
+        regs_dec<kRegsMask>();
         const int q = warp & 3, i = 32 * q + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t ph = 0;
@@ -788,7 +872,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
                 for (int g = 0; g < 8; ++g) { tmem_st8(gcol + 16 * g, zero); tmem_st8(gcol + 16 * g + 8, zero); }
             } else {
-#pragma unroll
+#pragma unroll 1
                 for (int b = 0; b < 4; ++b) {
                     if (b > q) {
                         tmem_st8(gcol + 32 * b, zero);
@@ -809,59 +893,51 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
 #pragma unroll
                     for (int gg = 0; gg < 2; ++gg) {     // the block's two 16-column groups
-                        uint32_t p0[8], p1[8];           // packed bf16: head 0 / head 1
-                        if (b < q) {
-                            const uint4* v0 = reinterpret_cast<const uint4*>(vt + 32 * b + 16 * gg);
-                            const uint4* v1 = reinterpret_cast<const uint4*>(vt + kVtCols + 32 * b + 16 * gg);
 #pragma unroll
-                            for (int k8 = 0; k8 < 2; ++k8) {
-                                const uint4 a8 = v0[k8], b8 = v1[k8];
-                                const __half2* ah = reinterpret_cast<const __half2*>(&a8);
-                                const __half2* bh = reinterpret_cast<const __half2*>(&b8);
+                        for (int hh = 0; hh < 2; ++hh) {  // head 0's 8 packed columns, then head 1's
+                            uint32_t pk[8];
+                            const float ci = hh ? ci1 : ci0;
+                            if (b < q) {
+                                const float2 uu = hh ? uu1 : uu0;
+                                const uint4* vp = reinterpret_cast<const uint4*>(vt + hh * kVtCols + 32 * b + 16 * gg);
 #pragma unroll
-                                for (int m = 0; m < 4; ++m) {
-                                    const int e = 16 * gg + 8 * k8 + 2 * m;
-                                    const float2 g2 = make_float2(__uint_as_float(gr[e]), __uint_as_float(gr[e + 1]));
-                                    const float2 r0 = fmul2(g2, fmul2(uu0, __half22float2(ah[m])));
-                                    const float2 r1 = fmul2(g2, fmul2(uu1, __half22float2(bh[m])));
-                                    p0[4 * k8 + m] = pack_bf16x2(r0.x, r0.y);
-                                    p1[4 * k8 + m] = pack_bf16x2(r1.x, r1.y);
+                                for (int k8 = 0; k8 < 2; ++k8) {
+                                    const uint4 a8 = vp[k8];
+                                    const __half2* ah = reinterpret_cast<const __half2*>(&a8);
+#pragma unroll
+                                    for (int m = 0; m < 4; ++m) {
+                                        const int e = 16 * gg + 8 * k8 + 2 * m;
+                                        const float2 g2 = make_float2(__uint_as_float(gr[e]), __uint_as_float(gr[e + 1]));
+                                        const float2 r = fmul2(g2, fmul2(uu, __half22float2(ah[m])));
+                                        pk[4 * k8 + m] = pack_bf16x2(r.x, r.y);
+                                    }
+                                }
+                            } else {
+                                const float4* cp = reinterpret_cast<const float4*>(cs + hh * 128 + 32 * b + 16 * gg);
+                                const float2 cc = make_float2(ci, ci), m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+                                for (int k4 = 0; k4 < 4; ++k4) {
+                                    const float4 a4 = cp[k4];
+                                    const float2 da = __ffma2_rn(make_float2(a4.x, a4.y), m1, cc);
+                                    const float2 db = __ffma2_rn(make_float2(a4.z, a4.w), m1, cc);
+                                    const int e = 16 * gg + 4 * k4;      // column within the block
+                                    const float2 ra = fmul2(make_float2(__uint_as_float(gr[e]), __uint_as_float(gr[e + 1])),
+                                                            make_float2(ex2(da.x), ex2(da.y)));
+                                    const float2 rb = fmul2(make_float2(__uint_as_float(gr[e + 2]), __uint_as_float(gr[e + 3])),
+                                                            make_float2(ex2(db.x), ex2(db.y)));
+                                    // columns e .. e + 3 of the block against row `lane` of it: keep j <= i
+                                    const uint32_t m01 = (e + 1 <= lane) ? 0xffffffffu : (e <= lane ? 0x0000ffffu : 0u);
+                                    const uint32_t m23 = (e + 3 <= lane) ? 0xffffffffu : (e + 2 <= lane ? 0x0000ffffu : 0u);
+                                    pk[2 * k4] = pack_bf16x2(ra.x, ra.y) & m01;
+                                    pk[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y) & m23;
                                 }
                             }
-                        } else {
-                            const float4* c0p = reinterpret_cast<const float4*>(cs + 32 * b + 16 * gg);
-                            const float4* c1p = reinterpret_cast<const float4*>(cs + 128 + 32 * b + 16 * gg);
-                            const float2 cc0 = make_float2(ci0, ci0), cc1 = make_float2(ci1, ci1), m1 = make_float2(-1.f, -1.f);
+                            if (!rv) {
 #pragma unroll
-                            for (int k4 = 0; k4 < 4; ++k4) {
-                                const float4 a4 = c0p[k4], b4 = c1p[k4];
-                                const float2 da = __ffma2_rn(make_float2(a4.x, a4.y), m1, cc0);
-                                const float2 db = __ffma2_rn(make_float2(a4.z, a4.w), m1, cc0);
-                                const float2 dc = __ffma2_rn(make_float2(b4.x, b4.y), m1, cc1);
-                                const float2 dd = __ffma2_rn(make_float2(b4.z, b4.w), m1, cc1);
-                                const int e = 16 * gg + 4 * k4;      // column within the block
-                                const float2 g01 = make_float2(__uint_as_float(gr[e]), __uint_as_float(gr[e + 1]));
-                                const float2 g23 = make_float2(__uint_as_float(gr[e + 2]), __uint_as_float(gr[e + 3]));
-                                const float2 ra = fmul2(g01, make_float2(ex2(da.x), ex2(da.y)));
-                                const float2 rb = fmul2(g23, make_float2(ex2(db.x), ex2(db.y)));
-                                const float2 rc = fmul2(g01, make_float2(ex2(dc.x), ex2(dc.y)));
-                                const float2 rd = fmul2(g23, make_float2(ex2(dd.x), ex2(dd.y)));
-                                // columns e .. e + 3 of the block against row `lane` of it: keep j <= i
-                                const uint32_t m01 = (e + 1 <= lane) ? 0xffffffffu : (e <= lane ? 0x0000ffffu : 0u);
-                                const uint32_t m23 = (e + 3 <= lane) ? 0xffffffffu : (e + 2 <= lane ? 0x0000ffffu : 0u);
-                                p0[2 * k4] = pack_bf16x2(ra.x, ra.y) & m01;
-                                p0[2 * k4 + 1] = pack_bf16x2(rb.x, rb.y) & m23;
-                                p1[2 * k4] = pack_bf16x2(rc.x, rc.y) & m01;
-                                p1[2 * k4 + 1] = pack_bf16x2(rd.x, rd.y) & m23;
+                                for (int e = 0; e < 8; ++e) pk[e] = 0u;
                             }
+                            tmem_st8(gcol + 32 * b + 16 * gg + 8 * hh, pk);
                         }
-                        if (!rv) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) { p0[e] = 0u; p1[e] = 0u; }
-                        }
-                        // group 2 b + gg: head 0's 8 packed columns, then head 1's
-                        tmem_st8(gcol + 32 * b + 16 * gg, p0);
-                        tmem_st8(gcol + 32 * b + 16 * gg + 8, p1);
                     }
                 }
             }
@@ -883,44 +959,39 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         //          combine -- y = z + exp(cs_i) Yo, rounded once to bf16, staged in the x region of the
         //          stage (free once S and Yo are done), and stored: a row quadrant wholly inside the
         //          sequence as one bulk tensor store (kAccum: a bulk reduce-add), otherwise row by row
-        const int hh = (warp - kWarpEpi) >> 2, q = warp & 3, i = 32 * q + lane;
+        regs_inc<kRegsEpi>();
+        const int hh = (warp - kWarpEpi) >> 2, q = warp & 3, i = 32 * q + lane, ix = i & 7;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t ph = 0;
-        bool ok = true, stored = false;
+        bool ok = true;
         int cC = 0;
         int prev_a = -1;      // stage of the aggregate tile this warp signalled last, until it is taken
-        Stream it;
-        it.start(a);
-        for (int p = 0; it.valid && ok; it.next(a), ++p) {
+        for (int p = 0; ok; ++p) {
             const int s = p & 1;
-            const int len = it.tile_len(), row0 = it.tile_row0(), h0 = 2 * it.hp;
+            // the tile record tells what the stage holds (or that the stream has ended)
+            ok = wait_warp(wt, kTblAny + s, ph);
+            if (!ok) break;
+            const int4 rc = *sm.rec(s);
+            if (rc.w & kRecEnd) break;
+            const bool is_agg = (rc.w & kRecAgg) != 0;
+            const int row0 = rc.x, len = rc.y, h0 = rc.z;
             float lgd = 0.f;
             if constexpr (kScaleX) {
-                if (!it.agg) {
+                if (!is_agg) {
                     float dti = 1.f;
                     if (i < len) dti = __ldg(a.dt + (int64_t)(row0 + i) * a.H + h0 + hh);
                     lgd = __log2f(fmaxf(dti, kMinDt));
                 }
             }
-            ok = wait_warp(wt, kFullX + s, ph) && wait_warp(wt, (it.agg ? kTblA : kTblC) + s, ph);
+            ok = wait_warp(wt, kFullX + s, ph);
             if (!ok) break;
             const float* cs = sm.cs(s);
             const float tab = cs[hh * 128 + i], last = cs[256 + 4 * hh + 3];
             const float w = (i < len) ? ex2(last - tab) : 0.f;
-            uint8_t* xr = sm.x(s, hh);
-            if (it.agg) {
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4* pv = reinterpret_cast<uint4*>(xr + sw128_offset(i, ch));
-                    uint4 v = *pv;
-                    uint32_t* u = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float2 f = fmul2(unpack_bf16x2(u[m]), make_float2(w, w));
-                        u[m] = pack_bf16x2(f.x, f.y);
-                    }
-                    *pv = v;
-                }
+            uint8_t* const xr = sm.x(s, hh);
+            uint8_t* const xrow = xr + i * 128;
+            if (is_agg) {
+                weight_row(xrow, ix, w);
                 fence_proxy_async_smem();
                 // the eight warps are not in step: before a warp signals this tile, the MMA warp must have
                 // taken the previous aggregate tile (whose phase needs all eight warps), or an early
@@ -941,21 +1012,24 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tmem_ld32_nowait(lane_base + kColYD + 64 * hh, reinterpret_cast<uint32_t*>(z));
             tmem_ld32_nowait(lane_base + kColYD + 64 * hh + 32, reinterpret_cast<uint32_t*>(z + 32));
             tmem_wait_ld();
+            {
+                const float2 dd = make_float2(Dh, Dh), ww = make_float2(w, w);
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint4* pv = reinterpret_cast<uint4*>(xr + sw128_offset(i, ch));
-                uint4 v = *pv;
-                uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, ch));
+                    uint4 v = *pv;
+                    uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float2 xf = unpack_bf16x2(u[m]);
-                    const float2 zz = __ffma2_rn(make_float2(Dh, Dh), xf, make_float2(z[8 * ch + 2 * m], z[8 * ch + 2 * m + 1]));
-                    z[8 * ch + 2 * m] = zz.x;
-                    z[8 * ch + 2 * m + 1] = zz.y;
-                    const float2 f = fmul2(xf, make_float2(w, w));
-                    u[m] = pack_bf16x2(f.x, f.y);
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 xf = unpack_bf16x2(u[m]);
+                        const float2 zz = __ffma2_rn(dd, xf, make_float2(z[8 * ch + 2 * m], z[8 * ch + 2 * m + 1]));
+                        z[8 * ch + 2 * m] = zz.x;
+                        z[8 * ch + 2 * m + 1] = zz.y;
+                        const float2 f = fmul2(xf, ww);
+                        u[m] = pack_bf16x2(f.x, f.y);
+                    }
+                    *pv = v;
                 }
-                *pv = v;
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -968,24 +1042,23 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             ok = wait_warp(wt, kSO, ph);
             if (!ok) break;
             tc_fence_after_sync();
-            const float2 ee = make_float2(e_row, e_row);
+            {
+                const float2 ee = make_float2(e_row, e_row);
+                const uint32_t yo_col = lane_base + kColGB + 128 * buf + 64 * hh;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t yo[16];
-                tmem_ld16_nowait(lane_base + kColGB + 128 * buf + 64 * hh + 16 * k, yo);
-                tmem_wait_ld();
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
+                for (int k = 0; k < 8; ++k) {
+                    uint32_t yo[8];
+                    tmem_ld8_nowait(yo_col + 8 * k, yo);
+                    tmem_wait_ld();
                     uint4 v;
                     uint32_t* vu = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        const int e = 8 * kk + 2 * m;
-                        const float2 r = __ffma2_rn(ee, make_float2(__uint_as_float(yo[e]), __uint_as_float(yo[e + 1])),
-                                                    make_float2(z[16 * k + e], z[16 * k + e + 1]));
+                        const float2 r = __ffma2_rn(ee, make_float2(__uint_as_float(yo[2 * m]), __uint_as_float(yo[2 * m + 1])),
+                                                    make_float2(z[8 * k + 2 * m], z[8 * k + 2 * m + 1]));
                         vu[m] = pack_bf16x2(r.x, r.y);
                     }
-                    *reinterpret_cast<uint4*>(xr + sw128_offset(i, 2 * k + kk)) = v;
+                    *reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, k)) = v;
                 }
             }
             tc_fence_before_sync();
@@ -1000,34 +1073,18 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         tma_store_3d(&maps.y, xr + 32 * q * 128, 0, h0 + hh, row0 + 32 * q);
                     bulk_commit_group();
                     bulk_wait_read_all();
-                    stored = true;
                 }
             } else if (i < len) {
                 // a partial quadrant: each row from the staging (added in fp32 onto the other state
                 // columns' share when accumulating)
-                __nv_bfloat16* yrow = a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 v = *reinterpret_cast<const uint4*>(xr + sw128_offset(i, ch));
-                    if (kAccum || a.y_accum) {
-                        const uint4 o = *reinterpret_cast<const uint4*>(yrow + 8 * ch);
-                        const uint32_t* ov = reinterpret_cast<const uint32_t*>(&o);
-                        uint32_t* nv = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float2 f = __fadd2_rn(unpack_bf16x2(nv[m]), unpack_bf16x2(ov[m]));
-                            nv[m] = pack_bf16x2(f.x, f.y);
-                        }
-                    }
-                    *reinterpret_cast<uint4*>(yrow + 8 * ch) = v;
-                }
+                store_row(xrow, ix, a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64, kAccum || a.y_accum);
             }
             warp_arrive(wt, kXFreeC + s);
             ++cC;
         }
         if (!ok) set_abort();
         // the bulk stores issued by this lane complete before the CTA's shared memory goes away
-        if (lane == 0 && stored) bulk_wait_all();
+        if (lane == 0) bulk_wait_all();
     } else if (warp >= kWarpState && warp < kWarpState + 4) {
         // ============================================================ state (one warp per lane quadrant)
         // TMEM row r = 32 q + lane of the state: head hr of the pair, channel pr; N state columns.
@@ -1037,13 +1094,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t ph = 0;
         bool ok = true;
-        int n_agg = 0;
-        constexpr int NC = N / 32;                 // 32-column chunks of the state
-        auto pub_ptr = [&](float* base, int64_t slot, int chunk) {
+        auto pub_ptr = [&](float* base, int slot, int chunk) {
             // the 4 float4 units of row r, columns 16 chunk .. + 15 (column-chunk-major)
-            return reinterpret_cast<float4*>(base + slot * 128 * N) + (4 * chunk) * 128 + r;
+            return reinterpret_cast<float4*>(base + (int64_t)slot * (128 * N)) + (4 * chunk) * 128 + r;
         };
-        auto publish = [&](float* base, int64_t slot, int flag, float dec) {
+        auto publish = [&](float* base, int slot, int flag, float dec) {
+#pragma unroll 1
             for (int k = 0; k < N / 16; ++k) {
                 uint32_t v[16];
                 tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
@@ -1062,7 +1118,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (lane == 0) st_release_gpu(a.flags + slot * 4 + q, flag);
         };
         // bounded wait of lane 0 for a quadrant flag of another window; false on timeout or abort
-        auto wait_flag = [&](int64_t slot, int want) {
+        auto wait_flag = [&](int slot, int want) {
             bool good = true;
             if (lane == 0) {
                 const int* fp = a.flags + slot * 4 + q;
@@ -1088,20 +1144,21 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (good) (void)ld_acquire_gpu(a.flags + slot * 4 + q);
             return good;
         };
-        Stream it;
-        it.start(a);
+        const int nwin = a.npieces > (int)blockIdx.x ? (a.npieces - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
         int p = 0;       // stream position of the window's first tile
-        for (; it.valid && ok; it.next_window(a)) {
-            const Piece c = decode_piece(it.d(), a);
+        for (int kd = 0; kd < nwin && ok; ++kd) {
+            const Piece c = decode_piece((int)blockIdx.x + kd * (int)gridDim.x, a);
+            if (!c.valid) break;       // a packed batch's bound overshoots; later windows are past the end too
             const int h0 = 2 * c.hp;
-            const int nagg_tiles = it.agg ? c.t1 - c.t0 : 0;
+            const bool has_agg = needs_agg(c, a);
+            const int nagg_tiles = has_agg ? c.t1 - c.t0 : 0;
             // ---- the aggregate out
-            if (it.agg) {
-                const float2 tot = window_total(a, it, lane);
+            if (has_agg) {
+                const int r0 = tile_row0(c, c.t0);
+                const float2 tot = window_total(a.dt, a.A, a.H, h0, r0, tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0, lane);
                 ok = wait_warp(wt, kAggDone, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                ++n_agg;
                 publish(a.agg, c.q, 1, ex2(hr ? tot.y : tot.x));
             }
             // ---- the entering state into TMEM: the initial state (or zero) at a chain's start, else
@@ -1109,16 +1166,17 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             // iteration (or the initial state), then h = decay(w') h + agg(w') over the predecessors
             // in this iteration, oldest first
             {
-                const int64_t iter = c.d / gridDim.x;
+                const unsigned iter = (unsigned)c.d / gridDim.x;
                 int m = 0;
-                int64_t dd = c.d;
-                while (c.w - m - 1 >= 0 && pred_d(dd, a) / gridDim.x == iter) { dd = pred_d(dd, a); ++m; }
+                int dd = c.d;
+                while (c.w - m - 1 >= 0 && (unsigned)pred_d(dd, a) / gridDim.x == iter) { dd = pred_d(dd, a); ++m; }
                 const bool from_end = c.w - m - 1 >= 0;
                 for (int j = 1; j <= m && ok; ++j) ok = wait_flag(c.q - j, 1);
                 if (ok && from_end) ok = wait_flag(c.q - m - 1, 2);
                 if (!ok) break;
                 const float* init_row = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off
                                                : nullptr;
+#pragma unroll 1
                 for (int k = 0; k < N / 16; ++k) {
                     float4 h[4];
                     if (from_end) {
@@ -1192,6 +1250,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tc_fence_after_sync();
             if (c.t1 == c.nt && a.final_state) {
                 float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off;
+#pragma unroll 1
                 for (int k = 0; k < N / 16; ++k) {
                     uint32_t v[16];
                     tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
@@ -1207,7 +1266,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tc_fence_before_sync();
             warp_arrive(wt, kSTFree);
         }
-        (void)n_agg;
         if (!ok) set_abort();
     }
 
@@ -1349,10 +1407,10 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     fa.G = G;
     fa.nseq = (int)p.nseq;
     fa.npairs = (int)npairs;
-    fa.npieces = np;
+    fa.npieces = (int)np;
     fa.K = K;
     fa.dense = p.varlen ? 0 : 1;
-    fa.seqlen = p.s.seqlen;
+    fa.seqlen = (int)p.s.seqlen;
     fa.nt_dense = (int)((p.s.seqlen + kFusedTile - 1) / kFusedTile);
     fa.W_dense = (fa.nt_dense + K - 1) / K;
     fa.n_off = part * N;
