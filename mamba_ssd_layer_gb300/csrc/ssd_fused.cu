@@ -54,6 +54,8 @@ namespace {
 constexpr int kTile = kFusedTile;
 constexpr int kRegion = kTile * 128;          // one 128-row x 128-byte swizzled box (16 KB)
 constexpr int kThreads = 640;                 // 20 warps (warp 3 has no role)
+// stream positions ahead of the loads whose x the producer requests into L2
+constexpr int kPrefetch = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 // floor of dt in log2(dt): dt = 0 contributes exp(-99.7) ~ 0 instead of an infinity
 constexpr float kMinDt = 1e-30f;
@@ -87,18 +89,19 @@ enum : int {
     kGFull = 14,     // [2] C B^T in the buffer
     kLGFull = 16,    // [2] L o G in the buffer: 4 mask warps
     kGBFree = 18,    // [2] the buffer's Yo read: 8 epilogue warps
-    kYDFull = 20,    // Yd in TMEM
-    kDrained = 21,   // Yd read and x weighted (or, for an aggregate tile, x weighted): 8 epilogue warps
-    kState = 22,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM: 4 state warps
-    kSO = 23,        // S(t) and Yo(t) done
-    kVTFree = 24,    // the factored-mask table read: 4 mask warps
-    kAggDone = 25,   // a window's aggregate complete (and the MMA warp's final drain)
-    kSTFree = 26,    // the state read at a window's end: 4 state warps
-    kNumBars = 27
+    kDrained = 20,   // [2] the stage's x weighted (and, for a tile, Yd read): 8 epilogue warps
+    kYDFull = 22,    // Yd in TMEM
+    kState = 23,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM: 4 state warps
+    kSO = 24,        // S(t) and Yo(t) done
+    kVTFree = 25,    // the factored-mask table read: 4 mask warps
+    kAggDone = 26,   // a window's aggregate complete (and the MMA warp's final drain)
+    kSTFree = 27,    // the state read at a window's end: 4 state warps
+    kNumBars = 28
 };
 
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-    return ((i >= kXFreeC && i < kXFreeC + 2) || (i >= kGBFree && i < kGBFree + 2) || i == kDrained) ? 8u
+    return ((i >= kXFreeC && i < kXFreeC + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
+               ? 8u
          : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree || i == kSTFree) ? 4u
          : 1u;
 }
@@ -219,7 +222,7 @@ struct Lay {
     static constexpr uint32_t kVt = kCs + 2 * kCsStride * 4;           // [2][kVtCols] halves
     static constexpr uint32_t kRec = kVt + 2 * kVtCols * 2;            // [2] tile records (int4)
     static constexpr uint32_t kBars = kRec + 2 * 16;                   // [kNumBars] u64
-    static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag
+    static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag, window total
     static constexpr uint32_t kTotal = kMisc + 16;
     static_assert(kBars % 8 == 0, "barriers are 8-byte aligned");
     static_assert(kTotal <= 232448, "shared memory per CTA");
@@ -244,6 +247,8 @@ struct Smem {
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(base + Lay<N>::kBars); }
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + Lay<N>::kMisc); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(base + Lay<N>::kMisc + 4); }
+    // the last window's total of dt*A (x log2 e), per head of the pair
+    __device__ float* wtotal() const { return reinterpret_cast<float*>(base + Lay<N>::kMisc + 8); }
 };
 
 // ---------------------------------------------------------------- bounded waits
@@ -285,6 +290,35 @@ __device__ __forceinline__ bool wait_bar(const Waiter& w, int idx, uint32_t& ph)
     const uint32_t par = (ph >> idx) & 1u;
     ph ^= 1u << idx;
     return wait_par(w, idx, par);
+}
+
+// Bounded wait like wait_bar that, while the phase is pending, keeps calling `side` (which returns true
+// once it has nothing left to do) between short sleeps; the single-thread MMA issuer uses it to issue
+// independent work as soon as that work's inputs are there.
+template <class F>
+__device__ __forceinline__ bool poll_bar(const Waiter& w, int idx, uint32_t& ph, F&& side) {
+    const uint32_t par = (ph >> idx) & 1u;
+    uint64_t* bar = w.bars + idx;
+    if (!mbar_try_wait(bar, par)) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (side()) {
+                if (!wait_par_slow(w.bars, w.abort, w.status, idx, par, true)) return false;
+                break;
+            }
+            if (mbar_try_wait_sleep(bar, par, 200u)) break;
+            if ((it & 7u) != 0) continue;
+            if (*w.abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                record_status(w.status, SSD_ERR_TIMEOUT);
+                atomicCAS(w.status + 2, 0, 0x100 + idx);
+                *w.abort = 1;
+                return false;
+            }
+        }
+    }
+    ph ^= 1u << idx;
+    return true;
 }
 
 // Every lane waits, then the warp agrees on the outcome, so later warp-collective instructions
@@ -362,11 +396,6 @@ __device__ __forceinline__ Piece decode_piece(int d, const FusedArgs& a) {
     return p;
 }
 
-__device__ __forceinline__ int tile_row0(const Piece& c, int t) { return c.seq_row0 + kTile * t; }
-__device__ __forceinline__ int tile_len(const Piece& c, int t) {
-    const int rem = c.seq_len - kTile * t;
-    return rem < kTile ? rem : kTile;
-}
 
 // dispatch index of the next / previous window of the same chain
 __device__ __forceinline__ int succ_d(int d, const FusedArgs& a) { return a.dense ? d + a.nseq * a.npairs : d + 1; }
@@ -381,7 +410,8 @@ __device__ __forceinline__ bool needs_end(const Piece& c, const FusedArgs& a) {
 }
 
 // The tile stream of this CTA, walked identically by every role: for each of its windows, the
-// aggregate tiles (when the window publishes an aggregate) and then the tiles. It keeps only what every
+// aggregate tiles from the last back to the first (when the window publishes an aggregate; in that
+// order each one's decay to the window's end is a running sum) and then the tiles in time order. It keeps only what every
 // role needs per tile; decode_piece(d()) gives the rest of the window.
 struct Stream {
     int kd, nwin;         // window ordinal on this CTA, windows dispatched to it
@@ -404,7 +434,7 @@ struct Stream {
         agg = needs_agg(c, a);
         t0 = c.t0;
         t1 = c.t1;
-        t = c.t0;
+        t = agg ? c.t1 - 1 : c.t0;
         hp = c.hp;
         row0 = c.seq_row0;
         len = c.seq_len;
@@ -416,36 +446,16 @@ struct Stream {
         load(a);
     }
     __device__ void next(const FusedArgs& a) {
+        if (agg) {
+            if (t > t0) { --t; return; }
+            agg = false;
+            return;              // t == t0: the window's tiles follow
+        }
         if (++t < t1) return;
-        if (agg) { agg = false; t = t0; return; }
         ++kd;
         load(a);
     }
 };
-
-// Sum of dt*A (x log2 e) over a window's tokens [r0, r0 + ntok), per head h0, h0 + 1, by one warp in a
-// fixed order (the same code everywhere it is needed, so every caller gets the same bits).
-__device__ __forceinline__ float2 window_total(const float* __restrict__ dt, const float* __restrict__ A, int H,
-                                            int h0, int r0, int ntok, int lane) {
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-    for (int l = lane; l < ntok; l += 32) {
-        const float2 d2 = __ldg(reinterpret_cast<const float2*>(dt + (int64_t)(r0 + l) * H + h0));
-        s0 += d2.x;
-        s1 += d2.y;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-    }
-    return make_float2(s0 * (__ldg(A + h0) * kLog2e), s1 * (__ldg(A + h0 + 1) * kLog2e));
-}
-__device__ __forceinline__ float2 window_total(const FusedArgs& a, const Stream& st, int lane) {
-    const int r0 = st.row0 + kTile * st.t0;
-    const int end = st.row0 + (kTile * st.t1 < st.len ? kTile * st.t1 : st.len);
-    return window_total(a.dt, a.A, a.H, 2 * st.hp, r0, end - r0, lane);
-}
 
 // ---------------------------------------------------------------- epilogue helpers (cold paths kept out
 // of line so that they do not add to the registers of the per-tile path)
@@ -549,10 +559,28 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             bool prev_agg[2] = {false, false};
             Stream it;
             it.start(a);
+            // x of the positions kPrefetch ahead is requested into L2 (the ring holds two positions,
+            // too few loads in flight to cover the memory latency); a window's tiles re-read the x
+            // its aggregate tiles brought in, so only first reads are prefetched
+            Stream pf;
+            pf.start(a);
+            int pfp = 0, pf_kd = -1;
+            bool pf_win_agg = false;       // the window of position pfp has aggregate tiles
+            auto prefetch_to = [&](int upto) {
+                for (; pf.valid && pfp < upto; pf.next(a), ++pfp) {
+                    if (pf.kd != pf_kd) { pf_kd = pf.kd; pf_win_agg = pf.agg; }
+                    if (pfp < 2 || !(pf.agg || !pf_win_agg)) continue;
+                    const int pr = pf.tile_row0();
+                    tma_prefetch_3d(&maps.x, 0, 2 * pf.hp, pr);
+                    tma_prefetch_3d(&maps.x, 0, 2 * pf.hp + 1, pr);
+                }
+            };
+            prefetch_to(kPrefetch);
             for (int p = 0; it.valid && ok; it.next(a), ++p) {
                 const int s = p & 1;
                 const int h0 = 2 * it.hp, g = h0 / (a.H / a.G);
                 const int row0 = it.tile_row0();
+                prefetch_to(p + kPrefetch + 1);
                 if (p >= 2 && !(ok = wait_bar(wt, kBCFree + s, ph))) break;
                 uint64_t* fbc = sm.bars() + kFullBC + s;
                 mbar_arrive_expect_tx(fbc, (uint32_t)((it.agg ? NB : 2 * NB) * kRegion));
@@ -615,15 +643,15 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 if (it.agg) {
                     // the window's first aggregate tile overwrites the state columns: the previous
                     // window's end state must have been read (the state warps arrive once per window)
-                    if (it.t == it.t0 && it.kd > 0 &&
+                    if (it.t == it.t1 - 1 && it.kd > 0 &&
                         !(ok = wait_par(wt, kSTFree, (uint32_t)(it.kd - 1) & 1u))) break;
-                    ok = wait_bar(wt, kFullBC + s, ph) && wait_bar(wt, kFullX + s, ph) && wait_bar(wt, kDrained, ph);
+                    ok = wait_bar(wt, kFullBC + s, ph) && wait_bar(wt, kFullX + s, ph) && wait_bar(wt, kDrained + s, ph);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    issue_s(s, it.t > it.t0);
+                    issue_s(s, it.t < it.t1 - 1);
                     mma_commit(sm.bars() + kBCFree + s);
                     mma_commit(sm.bars() + kXFreeA + s);
-                    if (it.t + 1 == it.t1) { mma_commit(sm.bars() + kAggDone); ++n_agg_commits; }
+                    if (it.t == it.t0) { mma_commit(sm.bars() + kAggDone); ++n_agg_commits; }
                     continue;
                 }
                 const int buf = cC & 1;
@@ -634,9 +662,23 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     issue_g(s, buf);
                 }
                 g_next = false;
+                // C B^T of the window's next tile goes out as soon as its B and C are there and its buffer
+                // is free, also while this tile waits for its L o G, so that the mask warps can go on
+                const bool next_tile = it.t + 1 < it.t1;
+                bool bc_ok = false, gb_ok = false;
+                auto try_g_next = [&]() -> bool {
+                    if (!next_tile || g_next) return true;
+                    if (!bc_ok) bc_ok = test_bar(wt, kFullBC + (s ^ 1), ph);
+                    if (bc_ok && !gb_ok) gb_ok = (cC + 1 < 2) || test_bar(wt, kGBFree + (buf ^ 1), ph);
+                    if (!(bc_ok && gb_ok)) return false;
+                    tc_fence_after_sync();
+                    issue_g(s ^ 1, buf ^ 1);
+                    g_next = true;
+                    return true;
+                };
                 // Yd(t), both heads interleaved: needs L o G(t) and x(t); the previous tile's Yd has been
                 // drained (its Drained phase was waited for before its S)
-                ok = wait_bar(wt, kLGFull + buf, ph) && wait_bar(wt, kFullX + s, ph);
+                ok = poll_bar(wt, kLGFull + buf, ph, try_g_next) && wait_bar(wt, kFullX + s, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t gb = kColGB + 128 * buf;
@@ -649,20 +691,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                 }
                 mma_commit(sm.bars() + kYDFull);
-                // C B^T of the window's next tile as soon as its B and C are there and its buffer is free
-                const bool next_tile = it.t + 1 < it.t1;
-                bool bc_ok = false, gb_ok = false;
-                if (next_tile) {
-                    bc_ok = test_bar(wt, kFullBC + (s ^ 1), ph);
-                    if (bc_ok) gb_ok = (cC + 1 < 2) || test_bar(wt, kGBFree + (buf ^ 1), ph);
-                    if (bc_ok && gb_ok) {
-                        tc_fence_after_sync();
-                        issue_g(s ^ 1, buf ^ 1);
-                        g_next = true;
-                    }
-                }
                 // S(t) onto a_t h_{t-1}, then Yo(t) into the buffer that held L o G(t)
-                ok = wait_bar(wt, kDrained, ph) && wait_bar(wt, kState, ph);
+                ok = poll_bar(wt, kDrained + s, ph, try_g_next) && wait_bar(wt, kState, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
                 issue_s(s, true);
@@ -704,7 +734,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         bool prev_agg[2] = {false, false};
         bool vt_used = false;
         float carry[2] = {0.f, 0.f};
-        float2 tot = make_float2(0.f, 0.f);
+        float suffix[2] = {0.f, 0.f};    // aggregate tiles: the decay of the window's later tiles
         Stream it;
         it.start(a);
         auto load_dt = [&](const Stream& st, float (&v)[2][4]) {
@@ -730,15 +760,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[hh][k] = vn[hh][k];
-            const bool agg = it.agg, first_agg = it.agg && it.t == it.t0;
+            const bool agg = it.agg, agg_last = it.agg && it.t == it.t1 - 1, agg_first = it.agg && it.t == it.t0;
             const int h0 = 2 * it.hp, len = it.tile_len(), row0 = it.tile_row0();
-            if (first_agg) {
-                tot = window_total(a, it, lane);
-                carry[0] = carry[1] = 0.f;
-            }
+            if (agg_last) suffix[0] = suffix[1] = 0.f;
             it.next(a);
             load_dt(it, vn);
-            if (!agg) carry[0] = carry[1] = 0.f;
+            carry[0] = carry[1] = 0.f;
             if (p >= 2) {
                 ok = __all_sync(0xffffffffu, wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph));
                 if (!ok) break;
@@ -773,20 +800,21 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 // row-side values: the plain cumsum at tokens 31, 63, 95, and the last value
                 if (lane == 7 || lane == 15 || lane == 23) cs[256 + 4 * hh + (lane >> 3)] = cv[hh][3];
                 if (agg) {
-                    if (lane == 0) cs[256 + 4 * hh + 3] = hh ? tot.y : tot.x;
+                    // the decay to the window's end: this tile's total (the cumsum at its last token; dt
+                    // is zero past the sequence) plus the later tiles'
+                    const float ttot = __shfl_sync(0xffffffffu, cv[hh][3], 31);
+                    if (lane == 0) cs[256 + 4 * hh + 3] = ttot + suffix[hh];
+                    suffix[hh] += ttot;
+                    if (agg_first && lane == 0) sm.wtotal()[hh] = suffix[hh];
                 } else if (lane == ((len - 1) >> 2)) {
                     const int k = (len - 1) & 3;
                     cs[256 + 4 * hh + 3] = k == 0 ? cv[hh][0] : k == 1 ? cv[hh][1] : k == 2 ? cv[hh][2] : cv[hh][3];
                 }
             }
             if (!agg) {
-                // v_j = exp(cs_p - table_j), p the last token of j's 32-token block (j < 96)
-                if (vt_used) {
-                    ok = __all_sync(0xffffffffu, wait_bar(wt, kVTFree, ph));
-                    if (!ok) break;
-                }
-                vt_used = true;
-                __half* vt = sm.vt();
+                // v_j = exp(cs_p - table_j), p the last token of j's 32-token block (j < 96), computed before
+                // the mask warps release the table so that only the stores follow the release
+                __half2 vv[2][2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const float piv = __shfl_sync(0xffffffffu, cv[hh][3], lane | 7);
@@ -797,12 +825,20 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         col.z -= __log2f(fmaxf(v[hh][2], kMinDt));
                         col.w -= __log2f(fmaxf(v[hh][3], kMinDt));
                     }
-                    if (lane < 24) {
-                        const __half2 lo = __floats2half2_rn(ex2(piv - col.x), ex2(piv - col.y));
-                        const __half2 hi = __floats2half2_rn(ex2(piv - col.z), ex2(piv - col.w));
-                        __half2* dst = reinterpret_cast<__half2*>(vt + hh * kVtCols + 4 * lane);
-                        dst[0] = lo;
-                        dst[1] = hi;
+                    vv[hh][0] = __floats2half2_rn(ex2(piv - col.x), ex2(piv - col.y));
+                    vv[hh][1] = __floats2half2_rn(ex2(piv - col.z), ex2(piv - col.w));
+                }
+                if (vt_used) {
+                    ok = __all_sync(0xffffffffu, wait_bar(wt, kVTFree, ph));
+                    if (!ok) break;
+                }
+                vt_used = true;
+                if (lane < 24) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        __half2* dst = reinterpret_cast<__half2*>(sm.vt() + hh * kVtCols + 4 * lane);
+                        dst[0] = vv[hh][0];
+                        dst[1] = vv[hh][1];
                     }
                 }
             }
@@ -965,7 +1001,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         uint32_t ph = 0;
         bool ok = true;
         int cC = 0;
-        int prev_a = -1;      // stage of the aggregate tile this warp signalled last, until it is taken
         for (int p = 0; ok; ++p) {
             const int s = p & 1;
             // the tile record tells what the stage holds (or that the stream has ended)
@@ -993,12 +1028,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (is_agg) {
                 weight_row(xrow, ix, w);
                 fence_proxy_async_smem();
-                // the eight warps are not in step: before a warp signals this tile, the MMA warp must have
-                // taken the previous aggregate tile (whose phase needs all eight warps), or an early
-                // arrival would complete that phase for a warp still weighting it
-                if (prev_a >= 0 && !(ok = wait_warp(wt, kXFreeA + prev_a, ph))) break;
-                warp_arrive(wt, kDrained);
-                prev_a = s;
+                // one Drained barrier per stage: a warp ahead of the others signals the other stage's
+                // barrier, and it cannot get two positions ahead (the stage is reloaded only once all
+                // eight warps have signalled it)
+                warp_arrive(wt, kDrained + s);
                 continue;
             }
             const float e_row = ex2(tab + lgd);
@@ -1033,11 +1066,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             fence_proxy_async_smem();
             tc_fence_before_sync();
-            // (Yd of this tile was issued after the MMA warp took the last aggregate tile, so the wait is
-            // already satisfied; it keeps this warp's phase count of the barrier)
-            if (prev_a >= 0 && !(ok = wait_warp(wt, kXFreeA + prev_a, ph))) break;
-            prev_a = -1;
-            warp_arrive(wt, kDrained);
+            warp_arrive(wt, kDrained + s);
             // ---- combine
             ok = wait_warp(wt, kSO, ph);
             if (!ok) break;
@@ -1154,12 +1183,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const int nagg_tiles = has_agg ? c.t1 - c.t0 : 0;
             // ---- the aggregate out
             if (has_agg) {
-                const int r0 = tile_row0(c, c.t0);
-                const float2 tot = window_total(a.dt, a.A, a.H, h0, r0, tile_row0(c, c.t1 - 1) + tile_len(c, c.t1 - 1) - r0, lane);
                 ok = wait_warp(wt, kAggDone, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                publish(a.agg, c.q, 1, ex2(hr ? tot.y : tot.x));
+                // the window's total decay, left by the table warp with its last aggregate tile (ordered
+                // before the aggregate's completion through the barriers in between)
+                publish(a.agg, c.q, 1, ex2(sm.wtotal()[hr]));
             }
             // ---- the entering state into TMEM: the initial state (or zero) at a chain's start, else
             // the look-back: base = the end state of the last predecessor that ran in an earlier
