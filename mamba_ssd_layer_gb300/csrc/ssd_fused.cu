@@ -8,14 +8,16 @@
 //     of K tiles. A CTA takes windows d = blockIdx.x, blockIdx.x + grid, ... of the dispatch order
 //     (window-rank-major for a dense batch: every chain's first window, then the second ones, ...);
 //     "iteration" d / grid is the round in which a window runs.
-//   * Right factors: a window whose successor runs in the same iteration first computes its
-//     aggregate, the state at its end from a zero start, sum_t decay(t -> end) (w o X_t)^T B_t (tcgen05,
-//     M = 2 heads x 64 channels, N = state columns), and publishes it. The same CTA then reads the
-//     window's x again for its tiles, while it is still in L2.
+//   * Right factors: a window with a successor first computes its aggregate, the state at its end from a
+//     zero start, sum_t decay(t -> end) (w o X_t)^T B_t (tcgen05, M = 2 heads x 64 channels, N = state
+//     columns), and publishes it. The same CTA then reads the window's x again for its tiles, while it
+//     is still in L2.
 //   * Center factors (look-back): the state entering a window is the published end state of the last
 //     predecessor that ran in an earlier iteration (or the initial state), carried through the
-//     aggregates of the predecessors in this iteration: h = decay(w') h + agg(w'). The order of that
-//     sum is fixed by the dispatch alone, so results do not depend on timing.
+//     aggregates of the predecessors in this iteration: h = decay(w') h + agg(w'). A window whose
+//     successor runs in a later iteration publishes its end state as the same fold, decay(w) h_in +
+//     agg(w), as soon as it has h_in, long before its last tile. The order of every sum is fixed by the
+//     dispatch alone, so results do not depend on timing.
 //   * Tiles, in time order from the entering state, the state carried in TMEM:
 //       G  = C B^T                      tcgen05, A = C (K-major), B = B (K-major)
 //       LG = L o G, bf16, written back over G in TMEM; L_ij = exp(cs_i - cs_j) on the diagonal
@@ -81,8 +83,8 @@ constexpr uint32_t kColGB = 256;   // two 128-column buffers, alternating per ti
 enum : int {
     kFullBC = 0,     // [2] B (and C) of the stage landed (TMA bytes)
     kFullX = 2,      // [2] x of the stage landed (TMA bytes)
-    kTblC = 4,       // [2] the stage's tables written, for a tile
-    kTblAny = 6,     // [2] the stage's tables and tile record written (every tile, and the end record)
+    kTblRead = 4,    // [2] the stage's tables and record read: 8 epilogue, 4 mask and 4 state warps
+    kTblAny = 6,     // [2] the stage's tables and tile record written (every position, and the end record)
     kBCFree = 8,     // [2] MMA done with the stage's B and C
     kXFreeC = 10,    // [2] a tile's y (staged in the stage's x) stored: 8 epilogue warps
     kXFreeA = 12,    // [2] MMA done with an aggregate tile's x
@@ -102,6 +104,7 @@ enum : int {
 __host__ __device__ constexpr uint32_t bar_count(int i) {
     return ((i >= kXFreeC && i < kXFreeC + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
                ? 8u
+         : (i >= kTblRead && i < kTblRead + 2) ? 16u
          : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree || i == kSTFree) ? 4u
          : 1u;
 }
@@ -400,11 +403,11 @@ __device__ __forceinline__ Piece decode_piece(int d, const FusedArgs& a) {
 // dispatch index of the next / previous window of the same chain
 __device__ __forceinline__ int succ_d(int d, const FusedArgs& a) { return a.dense ? d + a.nseq * a.npairs : d + 1; }
 __device__ __forceinline__ int pred_d(int d, const FusedArgs& a) { return a.dense ? d - a.nseq * a.npairs : d - 1; }
-// the window publishes its aggregate: its successor runs in the same iteration
-__device__ __forceinline__ bool needs_agg(const Piece& c, const FusedArgs& a) {
-    return c.w + 1 < c.W && (unsigned)succ_d(c.d, a) / gridDim.x == (unsigned)c.d / gridDim.x;
-}
-// the window publishes its end state: its successor runs in a later iteration
+// the window publishes its aggregate: it has a successor (a successor in the same iteration folds the
+// aggregate in; for one in a later iteration the aggregate gives the end state early, see needs_end)
+__device__ __forceinline__ bool needs_agg(const Piece& c, const FusedArgs&) { return c.w + 1 < c.W; }
+// the window publishes its end state (decay(w) h_in + agg(w), as soon as its entering state is known):
+// its successor runs in a later iteration
 __device__ __forceinline__ bool needs_end(const Piece& c, const FusedArgs& a) {
     return c.w + 1 < c.W && (unsigned)succ_d(c.d, a) / gridDim.x != (unsigned)c.d / gridDim.x;
 }
@@ -731,7 +734,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         regs_dec<kRegsWG0>();
         uint32_t ph = 0;
         bool ok = true;
-        bool prev_agg[2] = {false, false};
         bool vt_used = false;
         float carry[2] = {0.f, 0.f};
         float suffix[2] = {0.f, 0.f};    // aggregate tiles: the decay of the window's later tiles
@@ -767,7 +769,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             load_dt(it, vn);
             carry[0] = carry[1] = 0.f;
             if (p >= 2) {
-                ok = __all_sync(0xffffffffu, wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph));
+                // every role has read the tables this stage held two positions ago
+                ok = __all_sync(0xffffffffu, wait_bar(wt, kTblRead + s, ph));
                 if (!ok) break;
             }
             float* cs = sm.cs(s);
@@ -846,15 +849,13 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(sm.bars() + kTblAny + s);
-                if (!agg) mbar_arrive(sm.bars() + kTblC + s);
             }
-            prev_agg[s] = agg;
             np_done = p + 1;
         }
         // the end record after the last tile, once its stage is free
         if (ok) {
             const int s = np_done & 1;
-            if (np_done >= 2) ok = __all_sync(0xffffffffu, wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph));
+            if (np_done >= 2) ok = __all_sync(0xffffffffu, wait_bar(wt, kTblRead + s, ph));
             if (ok && lane == 0) {
                 *sm.rec(s) = make_int4(0, 0, 0, kRecEnd);
                 mbar_arrive(sm.bars() + kTblAny + s);
@@ -882,7 +883,13 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         Stream it;
         it.start(a);
         for (int p = 0; it.valid && ok; it.next(a), ++p) {
-            if (it.agg) continue;
+            if (it.agg) {
+                // nothing to do for an aggregate tile but to take part in the release of its tables
+                const int s = p & 1;
+                ok = wait_warp(wt, kTblAny + s, ph);
+                if (ok) warp_arrive(wt, kTblRead + s);
+                continue;
+            }
             const int s = p & 1, buf = cC & 1;
             const int len = it.tile_len();
             if constexpr (kScaleX) {
@@ -893,7 +900,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 lgd[0] = __log2f(fmaxf(d2.x, kMinDt));
                 lgd[1] = __log2f(fmaxf(d2.y, kMinDt));
             }
-            ok = wait_warp(wt, kGFull + buf, ph) && wait_warp(wt, kTblC + s, ph);
+            ok = wait_warp(wt, kGFull + buf, ph) && wait_warp(wt, kTblAny + s, ph);
             if (!ok) break;
             tc_fence_after_sync();
             const float* cs = sm.cs(s);
@@ -983,6 +990,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (lane == 0) {
                 mbar_arrive(sm.bars() + kLGFull + buf);
                 mbar_arrive(sm.bars() + kVTFree);
+                mbar_arrive(sm.bars() + kTblRead + s);
             }
             ++cC;
         }
@@ -1010,6 +1018,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (rc.w & kRecEnd) break;
             const bool is_agg = (rc.w & kRecAgg) != 0;
             const int row0 = rc.x, len = rc.y, h0 = rc.z;
+            const float tab = sm.cs(s)[hh * 128 + i], last = sm.cs(s)[256 + 4 * hh + 3];
+            warp_arrive(wt, kTblRead + s);
             float lgd = 0.f;
             if constexpr (kScaleX) {
                 if (!is_agg) {
@@ -1020,8 +1030,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             ok = wait_warp(wt, kFullX + s, ph);
             if (!ok) break;
-            const float* cs = sm.cs(s);
-            const float tab = cs[hh * 128 + i], last = cs[256 + 4 * hh + 3];
             const float w = (i < len) ? ex2(last - tab) : 0.f;
             uint8_t* const xr = sm.x(s, hh);
             uint8_t* const xrow = xr + i * 128;
@@ -1074,20 +1082,26 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             {
                 const float2 ee = make_float2(e_row, e_row);
                 const uint32_t yo_col = lane_base + kColGB + 128 * buf + 64 * hh;
+                // two 32-column loads (one TMEM round trip each) against the 64 z values in registers
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    uint32_t yo[8];
-                    tmem_ld8_nowait(yo_col + 8 * k, yo);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t yo[32];
+                    tmem_ld32_nowait(yo_col + 32 * half, yo);
                     tmem_wait_ld();
-                    uint4 v;
-                    uint32_t* vu = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float2 r = __ffma2_rn(ee, make_float2(__uint_as_float(yo[2 * m]), __uint_as_float(yo[2 * m + 1])),
-                                                    make_float2(z[8 * k + 2 * m], z[8 * k + 2 * m + 1]));
-                        vu[m] = pack_bf16x2(r.x, r.y);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k = 4 * half + kk;
+                        uint4 v;
+                        uint32_t* vu = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 r = __ffma2_rn(
+                                ee, make_float2(__uint_as_float(yo[8 * kk + 2 * m]), __uint_as_float(yo[8 * kk + 2 * m + 1])),
+                                make_float2(z[8 * k + 2 * m], z[8 * k + 2 * m + 1]));
+                            vu[m] = pack_bf16x2(r.x, r.y);
+                        }
+                        *reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, k)) = v;
                     }
-                    *reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, k)) = v;
                 }
             }
             tc_fence_before_sync();
@@ -1152,9 +1166,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (lane == 0) {
                 const int* fp = a.flags + slot * 4 + q;
                 const int target = a.force_timeout ? 3 : want;
-                if (ld_acquire_gpu(fp) != target) {
+                if (ld_acquire_gpu(fp) < target) {
                     const uint64_t t0 = global_timer_ns();
-                    for (uint32_t it2 = 1; ld_acquire_gpu(fp) != target; ++it2) {
+                    for (uint32_t it2 = 1; ld_acquire_gpu(fp) < target; ++it2) {
                         if ((it2 & 31u) != 0) continue;
                         if (*reinterpret_cast<volatile int*>(sm.abort_flag()) ||
                             *reinterpret_cast<volatile const int*>(a.status) != SSD_OK) { good = false; break; }
@@ -1179,8 +1193,15 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             const Piece c = decode_piece((int)blockIdx.x + kd * (int)gridDim.x, a);
             if (!c.valid) break;       // a packed batch's bound overshoots; later windows are past the end too
             const int h0 = 2 * c.hp;
-            const bool has_agg = needs_agg(c, a);
+            const bool has_agg = needs_agg(c, a), early_end = needs_end(c, a);
+            float wdec = 0.f;     // the window's total decay
             const int nagg_tiles = has_agg ? c.t1 - c.t0 : 0;
+            // the aggregate tiles' tables are not read here, but every role takes part in their release
+            for (int j = 0; j < nagg_tiles && ok; ++j) {
+                ok = wait_warp(wt, kTblAny + ((p + j) & 1), ph);
+                if (ok) warp_arrive(wt, kTblRead + ((p + j) & 1));
+            }
+            if (!ok) break;
             // ---- the aggregate out
             if (has_agg) {
                 ok = wait_warp(wt, kAggDone, ph);
@@ -1188,7 +1209,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 tc_fence_after_sync();
                 // the window's total decay, left by the table warp with its last aggregate tile (ordered
                 // before the aggregate's completion through the barriers in between)
-                publish(a.agg, c.q, 1, ex2(sm.wtotal()[hr]));
+                wdec = ex2(sm.wtotal()[hr]);
+                publish(a.agg, c.q, 1, wdec);
             }
             // ---- the entering state into TMEM: the initial state (or zero) at a chain's start, else
             // the look-back: base = the end state of the last predecessor that ran in an earlier
@@ -1231,17 +1253,37 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                                                fmaf(dcy, h[j].z, g[j].z), fmaf(dcy, h[j].w, g[j].w));
                     }
                     tmem_st16(lane_base + kColST + 16 * k, reinterpret_cast<const uint32_t*>(h));
+                    if (early_end) {
+                        // this window's end state, decay(w) h_in + agg(w), for a successor in a later
+                        // iteration (the aggregate rows are this thread's own stores)
+                        const float4* ag = pub_ptr(a.agg, c.q, k);
+                        float4* dst = pub_ptr(a.incl, c.q, k);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 g = __ldcg(ag + j * 128);
+                            __stcg(dst + j * 128, make_float4(fmaf(wdec, h[j].x, g.x), fmaf(wdec, h[j].y, g.y),
+                                                              fmaf(wdec, h[j].z, g.z), fmaf(wdec, h[j].w, g.w)));
+                        }
+                    }
                 }
                 tmem_wait_st();
+                if (early_end) {
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) st_release_gpu(a.flags + c.q * 4 + q, 2);
+                }
             }
             p += nagg_tiles;
             // ---- the tiles: h_{t-1} to bf16 for Yo, a_t h_{t-1} back for S(t) to accumulate onto
             for (int t = c.t0; t < c.t1 && ok; ++t, ++p) {
                 const int s = p & 1;
-                ok = wait_warp(wt, kTblC + s, ph) && (t == c.t0 || wait_warp(wt, kSO, ph));
+                ok = wait_warp(wt, kTblAny + s, ph);
+                if (!ok) break;
+                const float at = ex2(sm.cs(s)[256 + 4 * hr + 3]);
+                warp_arrive(wt, kTblRead + s);
+                ok = t == c.t0 || wait_warp(wt, kSO, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const float at = ex2(sm.cs(s)[256 + 4 * hr + 3]);
                 const float2 aa = make_float2(at, at);
 #pragma unroll 1
                 for (int k = 0; k < N / 16; ++k) {
@@ -1291,7 +1333,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                 }
             }
-            if (needs_end(c, a)) publish(a.incl, c.q, 2, 0.f);
             tc_fence_before_sync();
             warp_arrive(wt, kSTFree);
         }
@@ -1373,7 +1414,7 @@ static double dense_plan_cost(int64_t nt, int64_t nchains, int grid, int K) {
             const int64_t w = d / nchains;
             const int64_t tiles = (w + 1 < W) ? K : nt - (W - 1) * K;
             t += tiles + kWindowCost;
-            if (w + 1 < W && (d + nchains) / grid == d / grid) t += kAggCost * tiles;
+            if (w + 1 < W) t += kAggCost * tiles;
         }
         if (t > worst) worst = t;
     }
