@@ -262,8 +262,38 @@ int ssd_decode_step_host_ex(const ssd_shape *shape, ssd_dtype dtype, ssd_dtype s
                             void *stream);
 
 /*
+ * Sequence-parallel hand-off ("LLM(十一)——Mamba" §3.7.2 Sequence Parallelism: a worker passes its final
+ * state to the next). A sequence cut into consecutive slices runs every slice with ssd_forward from a
+ * zero state (on one device each, or one after another); that gives the slice's local y and local
+ * final state. With h_in the true state entering a slice and cs_l the sum of dt*A from the slice's
+ * first token through token l, linearity gives ("LLM(十一)——Mamba" §3.5.2, center and left factors)
+ *     true final = local final + decay * h_in,   decay = exp(cs_last)      (the next slice's h_in)
+ *     true y_l   = local y_l   + exp(cs_l) * C_l . h_in^T
+ * The caller moves h_in between devices (a copy into local memory; see the Python package's
+ * context_parallel module); these calls are the device-side pieces. Dense batches only: each of the
+ * `batch` rows of `shape` is a slice of its own sequence (no cu_seqlens).
+ *
+ * ssd_slice_workspace_size: scratch bytes of either call for `shape` (a 256-byte header whose first
+ *   word is read by ssd_status, then per-tile sums of dt and the decays).
+ * ssd_slice_decay: decay (batch, H) fp32 = exp(A[h] * sum over the row of dt[., h]); 1 for an empty
+ *   slice. Works for both storage types (it reads dt and A only).
+ * ssd_slice_correct: y (bf16, (batch, seqlen, H, P), the slice's local outputs) += exp(cs_l) C_l h_in^T,
+ *   accumulated in fp32 and rounded to bf16 once more; and, when final_state is not NULL,
+ *   final_state (batch, H, P, N) += decay * h_in. h_in: (batch, H, P, N) fp32, read-only (staged as bf16
+ *   for the tensor cores, like the chunk states of the forward). bf16 only, with the forward's bf16
+ *   shape rules (P = 64, N in {64, 128, 256}, H/G even); C as in ssd_forward.
+ * Errors as ssd_forward (argument checks before any launch; SSD_ERR_TIMEOUT through ssd_status).
+ */
+size_t ssd_slice_workspace_size(const ssd_shape *shape);
+int ssd_slice_decay(const ssd_shape *shape, const float *dt, const float *A, float *decay,
+                    void *workspace, size_t workspace_bytes, void *stream);
+int ssd_slice_correct(const ssd_shape *shape, ssd_dtype dtype, const float *dt, const float *A,
+                      const void *C, const float *h_in, void *y, float *final_state,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status recorded in the
- * workspace by the last ssd_forward that used it: SSD_OK, SSD_ERR_TIMEOUT (a bounded wait gave up),
+ * workspace by the last ssd_forward (or ssd_slice_* call) that used it: SSD_OK, SSD_ERR_TIMEOUT (a bounded wait gave up),
  * SSD_ERR_INVALID_ARG (malformed cu_seqlens, found by the device-side table builder; y is then not
  * written), or SSD_ERR_CUDA if the copy itself fails.
  */

@@ -79,6 +79,12 @@ def load_library():
     lib.ssd_decode_step_host_ex.argtypes = [shp, i32, i32, ctypes.c_uint, vp, fp, fp, vp, vp, fp, vp, vp, vp, vp, sz,
                                             vp]
     lib.ssd_decode_step_host_ex.restype = i32
+    lib.ssd_slice_workspace_size.argtypes = [shp]
+    lib.ssd_slice_workspace_size.restype = sz
+    lib.ssd_slice_decay.argtypes = [shp, fp, fp, fp, vp, sz, vp]
+    lib.ssd_slice_decay.restype = i32
+    lib.ssd_slice_correct.argtypes = [shp, i32, fp, fp, vp, fp, vp, fp, vp, sz, vp]
+    lib.ssd_slice_correct.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
     lib.ssd_profile_enable.argtypes = [i32]
@@ -187,6 +193,66 @@ def ssd_forward(x, dt, A, B, C, D=None, chunk: int = 256, initial_state=None, cu
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_forward_ex")
     return y, (final_state if return_final_state else None)
+
+
+def _slice_workspace(shape, dev, workspace):
+    import torch
+    lib = load_library()
+    ws_bytes = int(lib.ssd_slice_workspace_size(ctypes.byref(shape)))
+    if ws_bytes == 0:
+        raise SSDError(SSD_ERR_INVALID_ARG, "ssd_slice_workspace_size")
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    return lib, workspace, ws_bytes
+
+
+def ssd_slice_decay(dt, A, decay=None, workspace=None, stream=None):
+    """exp(A[h] * sum_t dt[b, t, h]) per batch row and head (``ssd_slice_decay``): the decay a slice
+    of a sequence applies to the state entering it. dt (batch, T, H), A (H,) float32 on the device.
+    Returns decay (batch, H) float32."""
+    import torch
+    batch, T, H = dt.shape
+    dev = dt.device
+    _check(dt, "dt", (batch, T, H), torch.float32, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    if decay is None:
+        decay = torch.empty((batch, H), dtype=torch.float32, device=dev)
+    _check(decay, "decay", (batch, H), torch.float32, dev)
+    shape = _shape(batch, T, H, 1, 1, 1)
+    lib, workspace, ws_bytes = _slice_workspace(shape, dev, workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ssd_slice_decay(ctypes.byref(shape), _ptr(dt), _ptr(A), _ptr(decay), workspace.data_ptr(), ws_bytes,
+                             ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_slice_decay")
+    return decay
+
+
+def ssd_slice_correct(dt, A, C, h_in, y, final_state=None, workspace=None, stream=None):
+    """Turn a slice's zero-state outputs into the true ones given the state h_in entering it
+    (``ssd_slice_correct``): y += exp(cs_l) C_l h_in^T in place (bf16), and final_state += decay h_in
+    when given. dt (batch, T, H), A (H,), h_in and final_state (batch, H, P, N) float32; C (batch, T, G, N)
+    and y (batch, T, H, P) bfloat16. Returns (y, final_state)."""
+    import torch
+    batch, T, H, P = y.shape
+    G, N = C.shape[2], C.shape[3]
+    dev = y.device
+    _check(y, "y", (batch, T, H, P), torch.bfloat16, dev)
+    _check(dt, "dt", (batch, T, H), torch.float32, dev)
+    _check(A, "A", (H,), torch.float32, dev)
+    _check(C, "C", (batch, T, G, N), torch.bfloat16, dev)
+    _check(h_in, "h_in", (batch, H, P, N), torch.float32, dev)
+    _check(final_state, "final_state", (batch, H, P, N), torch.float32, dev)
+    shape = _shape(batch, T, H, P, N, G)
+    lib, workspace, ws_bytes = _slice_workspace(shape, dev, workspace)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ssd_slice_correct(ctypes.byref(shape), SSD_BF16, _ptr(dt), _ptr(A), _ptr(C), _ptr(h_in), _ptr(y),
+                               _ptr(final_state), workspace.data_ptr(), ws_bytes, ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_slice_correct")
+    return y, final_state
 
 
 def ssd_status(workspace, stream=None) -> int:

@@ -292,6 +292,57 @@ int ssd_forward_host(const ssd_shape* s, ssd_dtype dtype, const void* x, const f
                                final_state, device_buffer, device_buffer_bytes, stream);
 }
 
+size_t ssd_slice_workspace_size(const ssd_shape* s) {
+    if (!s || s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0 || s->dstate <= 0 ||
+        s->ngroups <= 0 || s->nheads % s->ngroups != 0)
+        return 0;
+    return slice_ws_bytes(*s);
+}
+
+namespace {
+int check_slice(const ssd_shape* s, const void* workspace, size_t workspace_bytes, int* num_sms) {
+    if (!ssd_slice_workspace_size(s)) return SSD_ERR_INVALID_ARG;
+    if (s->batch * s->seqlen > (int64_t)INT32_MAX / 2 || s->nheads > 65535) return SSD_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < slice_ws_bytes(*s))
+        return SSD_ERR_WORKSPACE;
+    g_err_detail[0] = '\0';
+    return check_device(num_sms);
+}
+}  // namespace
+
+int ssd_slice_decay(const ssd_shape* s, const float* dt, const float* A, float* decay, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    if (!s) return SSD_ERR_INVALID_ARG;
+    if ((s->batch * s->seqlen > 0 && !dt) || !A || !decay) return SSD_ERR_INVALID_ARG;
+    if ((dt && !aligned16(dt)) || !aligned16(A) || !aligned16(decay)) return SSD_ERR_INVALID_ARG;
+    int num_sms = 0;
+    const int rc = check_slice(s, workspace, workspace_bytes, &num_sms);
+    if (rc != SSD_OK) return rc;
+    const cudaError_t e = launch_slice_decay(*s, dt, A, decay, static_cast<char*>(workspace),
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+int ssd_slice_correct(const ssd_shape* s, ssd_dtype dtype, const float* dt, const float* A, const void* C,
+                      const float* h_in, void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (!s) return SSD_ERR_INVALID_ARG;
+    if (dtype != SSD_F32 && dtype != SSD_BF16) return SSD_ERR_INVALID_ARG;
+    const bool any = s->batch * s->seqlen > 0;
+    if ((any && (!dt || !C || !y)) || !A || !h_in) return SSD_ERR_INVALID_ARG;
+    const void* ptrs[] = {dt, A, C, h_in, y, final_state};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+    if (!ssd_slice_workspace_size(s)) return SSD_ERR_INVALID_ARG;
+    if (!use_fused_path(*s, dtype)) return SSD_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    const int rc = check_slice(s, workspace, workspace_bytes, &num_sms);
+    if (rc != SSD_OK) return rc;
+    const cudaError_t e = launch_slice_correct(*s, dt, A, C, h_in, y, final_state, static_cast<char*>(workspace),
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 int ssd_status(const void* workspace, void* stream) {
     if (!workspace) return SSD_ERR_WORKSPACE;
     int v = SSD_ERR_CUDA;

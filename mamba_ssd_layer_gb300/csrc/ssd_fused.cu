@@ -1347,6 +1347,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     }
 }
 
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -1354,7 +1356,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 // 3-D view (inner, mid, rows) of a bf16 tensor whose mid and row strides are mid_stride and row_stride
 // elements (inner is contiguous), boxes of 64 x 1 x box_rows with the 128-byte swizzle
 bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64_t rows, int64_t mid_stride,
-                    int64_t row_stride, int box_rows = kTile) {
+                    int64_t row_stride, int box_rows) {
     static EncodeTiledFn enc = nullptr;
     if (!enc) {
         void* fp = nullptr;
@@ -1372,6 +1374,8 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int N, bool kScaleX, bool kAccum>
 cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMaps& maps, int grid) {

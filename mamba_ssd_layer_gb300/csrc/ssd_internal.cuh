@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ssd.h"
@@ -150,5 +151,17 @@ cudaError_t launch_f32_path(const Problem& p);
 void fused_plan(const Problem& p, int* K, int64_t* npieces);
 // part: which 128-column half of an N = 256 state (0 for N <= 128)
 cudaError_t launch_fused(const Problem& p, int K, int64_t npieces, int part);
+
+// A TMA map of a 3-D view (inner, mid, rows) of a bf16 tensor whose mid and row strides are mid_stride
+// and row_stride elements (inner contiguous): boxes of 64 x 1 x box_rows with the 128-byte swizzle.
+bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid, int64_t rows, int64_t mid_stride,
+                    int64_t row_stride, int box_rows = kFusedTile);
+
+// The sequence-slice hand-off (ssd_handoff.cu).
+size_t slice_ws_bytes(const ssd_shape& s);
+cudaError_t launch_slice_decay(const ssd_shape& s, const float* dt, const float* A, float* decay, char* ws,
+                               cudaStream_t st);
+cudaError_t launch_slice_correct(const ssd_shape& s, const float* dt, const float* A, const void* C,
+                                 const float* h_in, void* y, float* final_state, char* ws, cudaStream_t st);
 
 }  // namespace ssd

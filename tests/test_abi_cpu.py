@@ -146,3 +146,23 @@ def test_forward_flag_errors(lib):
     rc = lib.ssd_forward_host_ex(ctypes.byref(s), bd.SSD_BF16, 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, 256, None,
                                  None, 0, FAKE, None, FAKE, 1 << 40, None)
     assert rc == bd.SSD_ERR_INVALID_ARG
+
+
+def test_slice_handoff_argument_errors_before_any_device_work(lib):
+    s = shape(batch=2, T=300, H=4, P=64, N=128)
+    ws = lib.ssd_slice_workspace_size(ctypes.byref(s))
+    assert ws >= 256 + 2 * 3 * 4 * 4 + 2 * 4 * 4        # header, tile sums, decays
+    assert lib.ssd_slice_workspace_size(ctypes.byref(shape(H=3, G=2))) == 0
+    dec = lambda sh, A=FAKE, out=FAKE, w=FAKE, wb=1 << 30: lib.ssd_slice_decay(ctypes.byref(sh), FAKE, A, out, w, wb,
+                                                                             None)
+    assert dec(s, A=None) == bd.SSD_ERR_INVALID_ARG
+    assert dec(s, out=FAKE + 4) == bd.SSD_ERR_INVALID_ARG
+    assert dec(s, w=FAKE + 16) == bd.SSD_ERR_WORKSPACE
+    assert dec(s, wb=16) == bd.SSD_ERR_WORKSPACE
+    cor = lambda sh, dtype=bd.SSD_BF16, h=FAKE, y=FAKE: lib.ssd_slice_correct(ctypes.byref(sh), dtype, FAKE, FAKE,
+                                                                              FAKE, h, y, None, FAKE, 1 << 30, None)
+    assert cor(s, dtype=bd.SSD_F32) == bd.SSD_ERR_UNSUPPORTED
+    assert cor(shape(batch=2, T=300, H=4, P=32, N=128)) == bd.SSD_ERR_UNSUPPORTED
+    assert cor(s, dtype=7) == bd.SSD_ERR_INVALID_ARG
+    assert cor(s, h=None) == bd.SSD_ERR_INVALID_ARG
+    assert cor(s, y=FAKE + 2) == bd.SSD_ERR_INVALID_ARG
