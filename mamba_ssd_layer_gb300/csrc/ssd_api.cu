@@ -183,7 +183,7 @@ int ssd_forward_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const vo
         // the header (status, diagnostics) and the window flags start at zero
         e = note_cuda_error("header reset", cudaMemsetAsync(p.status(), 0, L.clear_bytes, p.stream));
         // a packed batch needs its tile and window tables; a dense batch decodes windows arithmetically
-        if (e == cudaSuccess && varlen) e = note_cuda_error("prep launch", launch_prep(p, kFusedTile, p.woff(), K));
+        if (e == cudaSuccess && varlen) e = note_cuda_error("prep launch", launch_prep(p, kFusedTile));
         if (e == cudaSuccess) e = note_cuda_error("fused launch", launch_fused(p, K, np, 0));
         if (e == cudaSuccess && p.s.dstate > 128) {
             // second half of the state columns: the window flags start over (an error recorded by the

@@ -19,13 +19,11 @@ namespace ssd {
 // start (the last one may be shorter). Sequence s is [cu[s], cu[s+1]) when
 // cu != nullptr, else [s*seqlen, (s+1)*seqlen). Invalid offsets (decreasing, or
 // past the row) record SSD_ERR_INVALID_ARG and build an empty table.
-//
-// With woff != nullptr it also numbers "windows" of K chunks per sequence: woff[s] is the
-// exclusive prefix of ceil(chunks(s) / K) and header[3] their total.
+
 __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ cu, int64_t nseq,
                                                     int64_t seqlen, int64_t rows, int Q,
                                                     int* header, ChunkDesc* chunks, int32_t* seqoff,
-                                                    int64_t max_chunks, int32_t* woff, int K) {
+                                                    int64_t max_chunks) {
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     __shared__ int bad;
@@ -44,44 +42,6 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
         if (tid == 0) { header[0] = SSD_ERR_INVALID_ARG; header[1] = 0; seqoff[0] = 0; }
         for (int64_t s = tid; s < nseq; s += blockDim.x) seqoff[s + 1] = 0;
         return;
-    }
-    // pass 2 (only with woff): exclusive scan of window counts
-    __shared__ int32_t wcarry;
-    if (woff) {
-        if (tid == 0) wcarry = 0;
-        __syncthreads();
-        for (int64_t base = 0; base < nseq; base += blockDim.x) {
-            const int64_t s = base + tid;
-            int32_t n = 0;
-            if (s < nseq) {
-                const int64_t len = cu ? (int64_t)cu[s + 1] - cu[s] : seqlen;
-                const int64_t nt = (len + Q - 1) / Q;
-                n = (int32_t)((nt + K - 1) / K);
-            }
-            int32_t v = n;
-            const int lane = tid & 31, warp = tid >> 5;
-            for (int o = 1; o < 32; o <<= 1) {
-                int32_t t = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += t;
-            }
-            if (lane == 31) warp_tot[warp] = v;
-            __syncthreads();
-            if (warp == 0) {
-                int32_t w = (lane < (int)(blockDim.x >> 5)) ? warp_tot[lane] : 0;
-                for (int o = 1; o < 32; o <<= 1) {
-                    int32_t t = __shfl_up_sync(0xffffffffu, w, o);
-                    if (lane >= o) w += t;
-                }
-                warp_tot[lane] = w;
-            }
-            __syncthreads();
-            if (s < nseq) woff[s] = wcarry + (warp > 0 ? warp_tot[warp - 1] : 0) + v - n;
-            __syncthreads();
-            if (tid == 0) wcarry += warp_tot[(blockDim.x >> 5) - 1];
-            __syncthreads();
-        }
-        if (tid == 0) { woff[nseq] = wcarry; header[3] = wcarry; }
-        __syncthreads();
     }
     // pass 3: exclusive scan of chunk counts, block-wide, in tiles of blockDim
     for (int64_t base = 0; base < nseq; base += blockDim.x) {
@@ -131,16 +91,16 @@ __global__ void __launch_bounds__(1024) prep_kernel(const int32_t* __restrict__ 
         header[0] = SSD_OK;
         header[1] = carry;
         header[2] = 0;   // first device-side timeout location (diagnostic), 0 = none
-        if (!woff) header[3] = 0;
+        header[3] = 0;
         header[4] = 0;   // arrival counter of the fused kernel's grid-wide barriers
         header[5] = 0;
     }
 }
 
-cudaError_t launch_prep(const Problem& p, int q, int32_t* woff, int K) {
+cudaError_t launch_prep(const Problem& p, int q) {
     prof_launch();
     prep_kernel<<<1, 1024, 0, p.stream>>>(p.varlen ? p.cu_seqlens : nullptr, p.nseq, p.s.seqlen, p.rows,
-                                          q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks, woff, K);
+                                          q, p.status(), p.chunks(), p.seqoff(), p.L.max_chunks);
     return cudaGetLastError();
 }
 

@@ -56,8 +56,6 @@ namespace {
 constexpr int kTile = kFusedTile;
 constexpr int kRegion = kTile * 128;          // one 128-row x 128-byte swizzled box (16 KB)
 constexpr int kThreads = 640;                 // 20 warps (warp 3 has no role)
-// stream positions ahead of the loads whose x the producer requests into L2
-constexpr int kPrefetch = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 // floor of dt in log2(dt): dt = 0 contributes exp(-99.7) ~ 0 instead of an infinity
 constexpr float kMinDt = 1e-30f;
@@ -96,16 +94,15 @@ enum : int {
     kState = 23,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM: 4 state warps
     kSO = 24,        // S(t) and Yo(t) done
     kVTFree = 25,    // the factored-mask table read: 4 mask warps
-    kAggDone = 26,   // a window's aggregate complete (and the MMA warp's final drain)
-    kSTFree = 27,    // the state read at a window's end: 4 state warps
-    kNumBars = 28
+    kAggDone = 26,   // the aggregate complete (and the MMA warp's final drain)
+    kNumBars = 27
 };
 
 __host__ __device__ constexpr uint32_t bar_count(int i) {
     return ((i >= kXFreeC && i < kXFreeC + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
                ? 8u
          : (i >= kTblRead && i < kTblRead + 2) ? 16u
-         : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree || i == kSTFree) ? 4u
+         : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree) ? 4u
          : 1u;
 }
 
@@ -125,27 +122,24 @@ struct FusedArgs {
     int* status;                // workspace header: [0] status word, [2] first timeout location
     const ChunkDesc* tiles;     // tile table (packed batch)
     const int32_t* seqoff;      // first tile of each sequence (packed batch)
-    const int32_t* woff;        // first window of each sequence (packed batch)
     const float* dt;
     const float* A;
     const float* D;
     const float* init;
     float* final_state;
     __nv_bfloat16* y;
-    int* flags;                 // per window slot and lane quadrant: 1 aggregate, 2 end state published
-    float* decay;               // per window slot and lane quadrant: decay over the window
-    // Per window slot, 128 x N fp32 in column-chunk-major order: the float4 holding row r, columns
+    // Published states of a CTA's last window when it ends inside its chain (slot = the CTA):
+    int* flags;                 // per slot and lane quadrant: 1 aggregate, 2 end state published
+    float* decay;               // per slot and lane quadrant: decay over the window
+    // Per slot, 128 x N fp32 in column-chunk-major order: the float4 holding row r, columns
     // 4c .. 4c + 3 is unit c * 128 + r, so that a warp (32 consecutive rows) reads or writes 512
     // contiguous bytes per column chunk.
     float* agg;                 // the window's end state from a zero entering state
     float* incl;                // the window's true end state
     int H, G, nseq, npairs;
-    int npieces;                // windows to dispatch (exact for a dense batch, a bound for a packed one)
-    int K;                      // tiles per window
-    int dense;                  // 1: batch of equal sequences (windows decoded arithmetically)
+    int dense;                  // 1: batch of equal sequences (chains decoded arithmetically)
     int seqlen;                 // dense: tokens per sequence
     int nt_dense;               // dense: tiles per sequence
-    int W_dense;                // dense: windows per sequence
     // Split state: this launch covers state columns [n_off, n_off + N) of n_full (B, C, the initial
     // and final states); with y_accum its y is added onto the y already there (the other columns'
     // share), and D is left to the first launch.
@@ -346,117 +340,118 @@ __device__ __forceinline__ void warp_arrive(const Waiter& w, int idx) {
 }
 
 // ---------------------------------------------------------------- work decomposition
-// A piece is one window of K consecutive 128-token tiles of one chain (sequence s, head pair hp).
-// q: its slot for published states (chain-major); d: its place in the dispatch order.
-struct Piece {
-    int q, d;
-    int s, hp, w, W;           // sequence, head pair, window, windows of the chain
-    int t0, t1, nt;            // tiles [t0, t1) of the sequence's nt tiles
-    int32_t seq_row0, seq_len; // first packed row and length of the sequence
-    bool valid;
+// Chains (sequence s, head pair hp) are laid end to end, chain-major (sequence major, head pair minor),
+// as one run of 128-token tiles; CTA b takes the contiguous range [range_start(b), range_start(b + 1))
+// of it. The range is cut at chain boundaries into windows: the first may start inside a chain (it
+// looks back at the CTAs before it for its entering state), the last may end inside one (its successor,
+// on the next CTA, needs its aggregate), the ones between are whole chains.
+
+// total tiles of all chains: dense, arithmetic; packed, from the tile table the prep kernel built
+__device__ __forceinline__ int total_tiles(const FusedArgs& a) {
+    return a.dense ? a.nseq * a.npairs * a.nt_dense : a.npairs * a.status[1];
+}
+__device__ __forceinline__ int range_start(int b, const FusedArgs& a) {
+    return (int)(((long long)b * total_tiles(a)) / (long long)gridDim.x);
+}
+// The published-state slot of CTA b: b itself, or, when there are fewer tiles than CTAs, the run
+// index of its first tile (distinct for every CTA that has tiles), so that min(grid, tiles) slots do.
+__device__ __forceinline__ int slot_of(int b, const FusedArgs& a) {
+    const int r = range_start(b, a);
+    return r < b ? r : b;
+}
+
+// The chain holding global tile g, and g's tile index in it.
+struct ChainPos {
+    int s, hp, t, nt;           // sequence, head pair, tile in the chain, tiles of the chain
+    int32_t seq_row0, seq_len;  // first packed row and length of the sequence
 };
 
-// Window counts fit in 32 bits (the launcher checks), so the decoding divides 32-bit integers.
-__device__ __forceinline__ Piece decode_piece(int d, const FusedArgs& a) {
-    Piece p;
-    p.valid = true;
-    p.d = d;
+__device__ __forceinline__ ChainPos decode_at(int g, const FusedArgs& a) {
+    ChainPos c;
     if (a.dense) {
-        const int nchains = a.nseq * a.npairs;
-        const int w = d / nchains, c = d - w * nchains;
-        p.w = w;
-        p.W = a.W_dense;
-        p.s = c / a.npairs;
-        p.hp = c - p.s * a.npairs;
-        p.q = c * a.W_dense + w;
-        p.nt = a.nt_dense;
-        p.seq_row0 = (int32_t)(p.s * a.seqlen);
-        p.seq_len = (int32_t)a.seqlen;
+        const int ch = g / a.nt_dense;
+        c.t = g - ch * a.nt_dense;
+        c.nt = a.nt_dense;
+        c.s = ch / a.npairs;
+        c.hp = ch - c.s * a.npairs;
+        c.seq_row0 = (int32_t)(c.s * a.seqlen);
+        c.seq_len = (int32_t)a.seqlen;
     } else {
-        const int total = a.status[3] * a.npairs;
-        if (d >= total) { p.valid = false; return p; }
+        // the last sequence whose first chain starts at or before g (an empty sequence is never it)
         int lo = 0, hi = a.nseq - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (a.npairs * a.woff[mid] <= d) lo = mid; else hi = mid - 1;
+            if (a.npairs * a.seqoff[mid] <= g) lo = mid; else hi = mid - 1;
         }
-        const int32_t w0 = a.woff[lo], w1 = a.woff[lo + 1];
-        const int local = d - a.npairs * w0;
-        const int Ws = w1 - w0;
-        p.s = lo;
-        p.W = Ws;
-        p.hp = local / Ws;
-        p.w = local - p.hp * Ws;
-        p.q = d;
         const int32_t f0 = a.seqoff[lo], f1 = a.seqoff[lo + 1];
-        p.nt = f1 - f0;
+        c.s = lo;
+        c.nt = f1 - f0;
+        const int local = g - a.npairs * f0;
+        c.hp = local / c.nt;
+        c.t = local - c.hp * c.nt;
         const ChunkDesc first = a.tiles[f0], last = a.tiles[f1 - 1];
-        p.seq_row0 = first.row0;
-        p.seq_len = last.row0 + last.len - first.row0;
+        c.seq_row0 = first.row0;
+        c.seq_len = last.row0 + last.len - first.row0;
     }
-    p.t0 = p.w * a.K;
-    p.t1 = p.t0 + a.K < p.nt ? p.t0 + a.K : p.nt;
-    return p;
+    return c;
 }
 
-
-// dispatch index of the next / previous window of the same chain
-__device__ __forceinline__ int succ_d(int d, const FusedArgs& a) { return a.dense ? d + a.nseq * a.npairs : d + 1; }
-__device__ __forceinline__ int pred_d(int d, const FusedArgs& a) { return a.dense ? d - a.nseq * a.npairs : d - 1; }
-// the window publishes its aggregate: it has a successor (a successor in the same iteration folds the
-// aggregate in; for one in a later iteration the aggregate gives the end state early, see needs_end)
-__device__ __forceinline__ bool needs_agg(const Piece& c, const FusedArgs&) { return c.w + 1 < c.W; }
-// the window publishes its end state (decay(w) h_in + agg(w), as soon as its entering state is known):
-// its successor runs in a later iteration
-__device__ __forceinline__ bool needs_end(const Piece& c, const FusedArgs& a) {
-    return c.w + 1 < c.W && (unsigned)succ_d(c.d, a) / gridDim.x != (unsigned)c.d / gridDim.x;
-}
-
-// The tile stream of this CTA, walked identically by every role: for each of its windows, the
-// aggregate tiles from the last back to the first (when the window publishes an aggregate; in that
-// order each one's decay to the window's end is a running sum) and then the tiles in time order. It keeps only what every
-// role needs per tile; decode_piece(d()) gives the rest of the window.
+// The tile stream of this CTA, walked identically by every role: the aggregate tiles of its last window
+// from the last back to the first (when that window ends inside its chain; in that order each one's
+// decay to the window's end is a running sum), then every window's tiles in time order.
 struct Stream {
-    int kd, nwin;         // window ordinal on this CTA, windows dispatched to it
-    int t, t0, t1;        // tile, the window's tiles [t0, t1)
+    int g0, g1;           // this CTA's range of the chain-major tile run
+    int gw;               // run index of the current window's first tile
+    int t, t0, t1;        // tile, the window's tiles [t0, t1) of its chain
     int hp;               // head pair
     int32_t row0, len;    // first packed row and length of the sequence
     bool agg;             // an aggregate tile
     bool valid;
-    __device__ int d() const { return (int)blockIdx.x + kd * (int)gridDim.x; }
     __device__ int tile_row0() const { return row0 + kTile * t; }
     __device__ int tile_len() const {
         const int rem = len - kTile * t;
         return rem < kTile ? rem : kTile;
     }
-    __device__ void load(const FusedArgs& a) {
-        valid = false;
-        if (kd >= nwin) return;
-        const Piece c = decode_piece(d(), a);
-        if (!c.valid) return;          // a packed batch's bound overshoots; later windows are past the end too
-        agg = needs_agg(c, a);
-        t0 = c.t0;
-        t1 = c.t1;
-        t = agg ? c.t1 - 1 : c.t0;
+    __device__ void load_at(int g, const FusedArgs& a) {
+        const ChainPos c = decode_at(g, a);
+        gw = g;
+        t0 = t = c.t;
+        t1 = c.t + (g1 - g) < c.nt ? c.t + (g1 - g) : c.nt;
         hp = c.hp;
         row0 = c.seq_row0;
         len = c.seq_len;
-        valid = true;
     }
     __device__ void start(const FusedArgs& a) {
-        kd = 0;
-        nwin = a.npieces > (int)blockIdx.x ? (a.npieces - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-        load(a);
+        g0 = range_start((int)blockIdx.x, a);
+        g1 = range_start((int)blockIdx.x + 1, a);
+        valid = g1 > g0;
+        agg = false;
+        if (!valid) return;
+        const ChainPos cl = decode_at(g1 - 1, a);          // the last window holds the range's last tile
+        if (cl.t + 1 < cl.nt) {
+            agg = true;
+            t1 = cl.t + 1;
+            t0 = cl.t - (g1 - 1 - g0) > 0 ? cl.t - (g1 - 1 - g0) : 0;
+            t = t1 - 1;
+            gw = g1 - (t1 - t0);
+            hp = cl.hp;
+            row0 = cl.seq_row0;
+            len = cl.seq_len;
+        } else {
+            load_at(g0, a);
+        }
     }
     __device__ void next(const FusedArgs& a) {
         if (agg) {
             if (t > t0) { --t; return; }
             agg = false;
-            return;              // t == t0: the window's tiles follow
+            load_at(g0, a);
+            return;
         }
         if (++t < t1) return;
-        ++kd;
-        load(a);
+        const int g = gw + (t1 - t0);
+        if (g >= g1) { valid = false; return; }
+        load_at(g, a);
     }
 };
 
@@ -528,7 +523,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
         }
     }
-    if (a.npieces == 0 || (a.dense && a.nt_dense == 0)) return;
+    if (a.dense && a.nt_dense == 0) return;
     if ((smem_u32(smem_raw) & 1023u) != 0) {      // the swizzled layout needs a 1024-byte aligned base
         if (tid == 0) record_status(a.status, SSD_ERR_UNSUPPORTED);
         return;
@@ -562,28 +557,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             bool prev_agg[2] = {false, false};
             Stream it;
             it.start(a);
-            // x of the positions kPrefetch ahead is requested into L2 (the ring holds two positions,
-            // too few loads in flight to cover the memory latency); a window's tiles re-read the x
-            // its aggregate tiles brought in, so only first reads are prefetched
-            Stream pf;
-            pf.start(a);
-            int pfp = 0, pf_kd = -1;
-            bool pf_win_agg = false;       // the window of position pfp has aggregate tiles
-            auto prefetch_to = [&](int upto) {
-                for (; pf.valid && pfp < upto; pf.next(a), ++pfp) {
-                    if (pf.kd != pf_kd) { pf_kd = pf.kd; pf_win_agg = pf.agg; }
-                    if (pfp < 2 || !(pf.agg || !pf_win_agg)) continue;
-                    const int pr = pf.tile_row0();
-                    tma_prefetch_3d(&maps.x, 0, 2 * pf.hp, pr);
-                    tma_prefetch_3d(&maps.x, 0, 2 * pf.hp + 1, pr);
-                }
-            };
-            prefetch_to(kPrefetch);
             for (int p = 0; it.valid && ok; it.next(a), ++p) {
                 const int s = p & 1;
                 const int h0 = 2 * it.hp, g = h0 / (a.H / a.G);
                 const int row0 = it.tile_row0();
-                prefetch_to(p + kPrefetch + 1);
                 if (p >= 2 && !(ok = wait_bar(wt, kBCFree + s, ph))) break;
                 uint64_t* fbc = sm.bars() + kFullBC + s;
                 mbar_arrive_expect_tx(fbc, (uint32_t)((it.agg ? NB : 2 * NB) * kRegion));
@@ -644,10 +621,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 const int s = p & 1;
                 any = true;
                 if (it.agg) {
-                    // the window's first aggregate tile overwrites the state columns: the previous
-                    // window's end state must have been read (the state warps arrive once per window)
-                    if (it.t == it.t1 - 1 && it.kd > 0 &&
-                        !(ok = wait_par(wt, kSTFree, (uint32_t)(it.kd - 1) & 1u))) break;
+                    // (the aggregate tiles open the stream: the state columns hold nothing yet)
                     ok = wait_bar(wt, kFullBC + s, ph) && wait_bar(wt, kFullX + s, ph) && wait_bar(wt, kDrained + s, ph);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -1160,9 +1134,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             __syncwarp();
             if (lane == 0) st_release_gpu(a.flags + slot * 4 + q, flag);
         };
-        // bounded wait of lane 0 for a quadrant flag of another window; false on timeout or abort
-        auto wait_flag = [&](int slot, int want) {
+        // bounded wait of lane 0 until another CTA's quadrant flag is at least `want`; returns the flag
+        // value seen (1 aggregate, 2 end state), 0 on timeout or abort
+        auto wait_flag = [&](int slot, int want) -> int {
             bool good = true;
+            int seen = 0;
             if (lane == 0) {
                 const int* fp = a.flags + slot * 4 + q;
                 const int target = a.force_timeout ? 3 : want;
@@ -1183,158 +1159,200 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
             // each lane acquires the flag itself, so its later loads of the published state are ordered
-            // after the publisher's stores
-            if (good) (void)ld_acquire_gpu(a.flags + slot * 4 + q);
-            return good;
+            // after the publisher's stores (and the warp agrees on the value lane 0 saw)
+            if (good) {
+                seen = ld_acquire_gpu(a.flags + slot * 4 + q);
+                seen = __shfl_sync(0xffffffffu, seen, 0);
+            }
+            return good ? seen : 0;
         };
-        const int nwin = a.npieces > (int)blockIdx.x ? (a.npieces - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-        int p = 0;       // stream position of the window's first tile
-        for (int kd = 0; kd < nwin && ok; ++kd) {
-            const Piece c = decode_piece((int)blockIdx.x + kd * (int)gridDim.x, a);
-            if (!c.valid) break;       // a packed batch's bound overshoots; later windows are past the end too
-            const int h0 = 2 * c.hp;
-            const bool has_agg = needs_agg(c, a), early_end = needs_end(c, a);
-            float wdec = 0.f;     // the window's total decay
-            const int nagg_tiles = has_agg ? c.t1 - c.t0 : 0;
-            // the aggregate tiles' tables are not read here, but every role takes part in their release
-            for (int j = 0; j < nagg_tiles && ok; ++j) {
-                ok = wait_warp(wt, kTblAny + ((p + j) & 1), ph);
-                if (ok) warp_arrive(wt, kTblRead + ((p + j) & 1));
+        // this window's end state decay(w) h_in + agg(w) out, chunk k of it (the aggregate rows are this
+        // thread's own stores)
+        const int my_slot = slot_of((int)blockIdx.x, a);
+        auto incl_chunk = [&](int k, const float4 (&h)[4], float dec) {
+            const float4* ag = pub_ptr(a.agg, my_slot, k);
+            float4* dst = pub_ptr(a.incl, my_slot, k);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 g = __ldcg(ag + j * 128);
+                __stcg(dst + j * 128, make_float4(fmaf(dec, h[j].x, g.x), fmaf(dec, h[j].y, g.y),
+                                                  fmaf(dec, h[j].z, g.z), fmaf(dec, h[j].w, g.w)));
             }
-            if (!ok) break;
-            // ---- the aggregate out
+        };
+        auto release_incl = [&]() {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release_gpu(a.flags + my_slot * 4 + q, 2);
+        };
+        // the initial state's row r of sequence s, head pair hp (this launch's columns), or null
+        auto init_row_of = [&](int s_, int hp_) -> const float* {
+            return a.init ? a.init + (((int64_t)s_ * a.H + 2 * hp_ + hr) * 64 + pr) * a.n_full + a.n_off : nullptr;
+        };
+        auto load_init = [&](const float* row, int k, float4 (&h)[4]) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                h[j] = row ? __ldg(reinterpret_cast<const float4*>(row + 16 * k) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        const int g0 = range_start((int)blockIdx.x, a), g1 = range_start((int)blockIdx.x + 1, a);
+        int p = 0;       // stream position
+        if (g1 > g0) {
+            // ---- the last window's aggregate out, when the window ends inside its chain (it opens the
+            // stream); when that window also starts its chain, its end state follows at once
+            const ChainPos cl = decode_at(g1 - 1, a);
+            const bool has_agg = cl.t + 1 < cl.nt;
+            const int l_t0 = cl.t - (g1 - 1 - g0) > 0 ? cl.t - (g1 - 1 - g0) : 0;
+            float wdec = 0.f;    // its total decay
             if (has_agg) {
-                ok = wait_warp(wt, kAggDone, ph);
-                if (!ok) break;
-                tc_fence_after_sync();
-                // the window's total decay, left by the table warp with its last aggregate tile (ordered
-                // before the aggregate's completion through the barriers in between)
-                wdec = ex2(sm.wtotal()[hr]);
-                publish(a.agg, c.q, 1, wdec);
+                const int n = cl.t + 1 - l_t0;
+                // the aggregate tiles' tables are not read here, but every role takes part in their release
+                for (int j = 0; j < n && ok; ++j) {
+                    ok = wait_warp(wt, kTblAny + ((p + j) & 1), ph);
+                    if (ok) warp_arrive(wt, kTblRead + ((p + j) & 1));
+                }
+                p += n;
+                ok = ok && wait_warp(wt, kAggDone, ph);
+                if (ok) {
+                    tc_fence_after_sync();
+                    // the window's total decay, left by the table warp with its last aggregate tile (ordered
+                    // before the aggregate's completion through the barriers in between)
+                    wdec = ex2(sm.wtotal()[hr]);
+                    publish(a.agg, my_slot, 1, wdec);
+                    if (l_t0 == 0) {
+                        const float* irow = init_row_of(cl.s, cl.hp);
+#pragma unroll 1
+                        for (int k = 0; k < N / 16; ++k) {
+                            float4 h[4];
+                            load_init(irow, k, h);
+                            incl_chunk(k, h, wdec);
+                        }
+                        release_incl();
+                    }
+                }
             }
-            // ---- the entering state into TMEM: the initial state (or zero) at a chain's start, else
-            // the look-back: base = the end state of the last predecessor that ran in an earlier
-            // iteration (or the initial state), then h = decay(w') h + agg(w') over the predecessors
-            // in this iteration, oldest first
-            {
-                const unsigned iter = (unsigned)c.d / gridDim.x;
-                int m = 0;
-                int dd = c.d;
-                while (c.w - m - 1 >= 0 && (unsigned)pred_d(dd, a) / gridDim.x == iter) { dd = pred_d(dd, a); ++m; }
-                const bool from_end = c.w - m - 1 >= 0;
-                for (int j = 1; j <= m && ok; ++j) ok = wait_flag(c.q - j, 1);
-                if (ok && from_end) ok = wait_flag(c.q - m - 1, 2);
-                if (!ok) break;
-                const float* init_row = a.init ? a.init + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off
-                                               : nullptr;
+            for (int g = g0; g < g1 && ok;) {
+                const ChainPos c = decode_at(g, a);
+                const int t0 = c.t, t1 = c.t + (g1 - g) < c.nt ? c.t + (g1 - g) : c.nt;
+                const bool last = g + (t1 - t0) == g1;
+                const int h0 = 2 * c.hp;
+                // ---- the entering state into TMEM: the initial state (or zero) at a chain's start; else
+                // (the first window only) the look-back over the CTAs before this one, whose last windows
+                // are the chain's previous pieces, nearest first: stop at the nearest with its end state
+                // published, or at the one whose window starts the chain (its entering state is the initial
+                // state), then fold their aggregates onto that base, oldest first. Every path gives the same
+                // bits, since a published end state is this same fold done by its own window.
+                constexpr int kMaxFold = 8;
+                int fold[kMaxFold];
+                int nf = 0, base = -1;       // base: the slot whose end state starts the fold, -1 the initial state
+                if (t0 > 0) {
+                    const int cg0 = g - t0;  // run index of the chain's first tile
+                    for (int j = (int)blockIdx.x - 1;; --j) {
+                        if (range_start(j, a) == range_start(j + 1, a)) continue;   // a CTA without tiles
+                        const int sj = slot_of(j, a);
+                        const int f = wait_flag(sj, 1);
+                        if (f == 0) { ok = false; break; }
+                        if (f >= 2) { base = sj; break; }
+                        fold[nf++] = sj;
+                        if (range_start(j, a) <= cg0) break;
+                        if (nf == kMaxFold) {
+                            // a long chain: wait for this one's end state rather than walking further
+                            --nf;
+                            if (wait_flag(sj, 2) == 0) ok = false;
+                            base = sj;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                }
+                const float* irow = init_row_of(c.s, c.hp);
+                const bool out_incl = last && has_agg && t0 > 0;
 #pragma unroll 1
                 for (int k = 0; k < N / 16; ++k) {
                     float4 h[4];
-                    if (from_end) {
-                        const float4* src = pub_ptr(a.incl, c.q - m - 1, k);
+                    if (base >= 0) {
+                        const float4* src = pub_ptr(a.incl, base, k);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) h[j] = __ldcg(src + j * 128);
-                    } else if (init_row) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) h[j] = __ldg(reinterpret_cast<const float4*>(init_row + 16 * k) + j);
                     } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) h[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        load_init(irow, k, h);
                     }
-                    for (int jw = m; jw >= 1; --jw) {
-                        const float dcy = __ldcg(a.decay + (c.q - jw) * 4 + q);
-                        const float4* src = pub_ptr(a.agg, c.q - jw, k);
-                        float4 g[4];
+                    for (int f = nf - 1; f >= 0; --f) {
+                        const float dcy = __ldcg(a.decay + fold[f] * 4 + q);
+                        const float4* src = pub_ptr(a.agg, fold[f], k);
+                        float4 gg[4];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) g[j] = __ldcg(src + j * 128);
+                        for (int j = 0; j < 4; ++j) gg[j] = __ldcg(src + j * 128);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            h[j] = make_float4(fmaf(dcy, h[j].x, g[j].x), fmaf(dcy, h[j].y, g[j].y),
-                                               fmaf(dcy, h[j].z, g[j].z), fmaf(dcy, h[j].w, g[j].w));
+                            h[j] = make_float4(fmaf(dcy, h[j].x, gg[j].x), fmaf(dcy, h[j].y, gg[j].y),
+                                               fmaf(dcy, h[j].z, gg[j].z), fmaf(dcy, h[j].w, gg[j].w));
                     }
                     tmem_st16(lane_base + kColST + 16 * k, reinterpret_cast<const uint32_t*>(h));
-                    if (early_end) {
-                        // this window's end state, decay(w) h_in + agg(w), for a successor in a later
-                        // iteration (the aggregate rows are this thread's own stores)
-                        const float4* ag = pub_ptr(a.agg, c.q, k);
-                        float4* dst = pub_ptr(a.incl, c.q, k);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float4 g = __ldcg(ag + j * 128);
-                            __stcg(dst + j * 128, make_float4(fmaf(wdec, h[j].x, g.x), fmaf(wdec, h[j].y, g.y),
-                                                              fmaf(wdec, h[j].z, g.z), fmaf(wdec, h[j].w, g.w)));
-                        }
-                    }
+                    if (out_incl) incl_chunk(k, h, wdec);
                 }
                 tmem_wait_st();
-                if (early_end) {
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) st_release_gpu(a.flags + c.q * 4 + q, 2);
+                if (out_incl) release_incl();
+                // ---- the tiles: h_{t-1} to bf16 for Yo, a_t h_{t-1} back for S(t) to accumulate onto
+                for (int t = t0; t < t1 && ok; ++t, ++p) {
+                    const int s = p & 1;
+                    ok = wait_warp(wt, kTblAny + s, ph);
+                    if (!ok) break;
+                    const float at = ex2(sm.cs(s)[256 + 4 * hr + 3]);
+                    warp_arrive(wt, kTblRead + s);
+                    ok = t == t0 || wait_warp(wt, kSO, ph);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const float2 aa = make_float2(at, at);
+#pragma unroll 1
+                    for (int k = 0; k < N / 16; ++k) {
+                        uint32_t v[16];
+                        tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int n = 16 * k + 8 * cc;
+                            uint4 pk;
+                            pk.x = pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7]));
+                            *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(r, (n % 64) / 8)) = pk;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float2 s2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), aa);
+                            v[e] = __float_as_uint(s2.x);
+                            v[e + 1] = __float_as_uint(s2.y);
+                        }
+                        tmem_st16(lane_base + kColST + 16 * k, v);
+                    }
+                    tmem_wait_st();
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    warp_arrive(wt, kState);
                 }
-            }
-            p += nagg_tiles;
-            // ---- the tiles: h_{t-1} to bf16 for Yo, a_t h_{t-1} back for S(t) to accumulate onto
-            for (int t = c.t0; t < c.t1 && ok; ++t, ++p) {
-                const int s = p & 1;
-                ok = wait_warp(wt, kTblAny + s, ph);
                 if (!ok) break;
-                const float at = ex2(sm.cs(s)[256 + 4 * hr + 3]);
-                warp_arrive(wt, kTblRead + s);
-                ok = t == c.t0 || wait_warp(wt, kSO, ph);
+                // ---- the window's end: the last S, then a chain's final state out
+                ok = wait_warp(wt, kSO, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                const float2 aa = make_float2(at, at);
+                if (t1 == c.nt && a.final_state) {
+                    float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off;
 #pragma unroll 1
-                for (int k = 0; k < N / 16; ++k) {
-                    uint32_t v[16];
-                    tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
-                    tmem_wait_ld();
+                    for (int k = 0; k < N / 16; ++k) {
+                        uint32_t v[16];
+                        tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int n = 16 * k + 8 * cc;
-                        uint4 pk;
-                        pk.x = pack_bf16x2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1]));
-                        pk.y = pack_bf16x2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3]));
-                        pk.z = pack_bf16x2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5]));
-                        pk.w = pack_bf16x2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7]));
-                        *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(r, (n % 64) / 8)) = pk;
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<float4*>(fp + 16 * k + 4 * j) =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     }
-#pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        const float2 s2 = fmul2(make_float2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), aa);
-                        v[e] = __float_as_uint(s2.x);
-                        v[e + 1] = __float_as_uint(s2.y);
-                    }
-                    tmem_st16(lane_base + kColST + 16 * k, v);
                 }
-                tmem_wait_st();
-                fence_proxy_async_smem();
+                // (the next window's entering state overwrites the state columns: its S waits for it)
                 tc_fence_before_sync();
-                warp_arrive(wt, kState);
+                g += t1 - t0;
             }
-            if (!ok) break;
-            // ---- the window's end: the last S, then the end state out (a chain's final state, or the
-            // state a later iteration's successor starts from)
-            ok = wait_warp(wt, kSO, ph);
-            if (!ok) break;
-            tc_fence_after_sync();
-            if (c.t1 == c.nt && a.final_state) {
-                float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off;
-#pragma unroll 1
-                for (int k = 0; k < N / 16; ++k) {
-                    uint32_t v[16];
-                    tmem_ld16_nowait(lane_base + kColST + 16 * k, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<float4*>(fp + 16 * k + 4 * j) =
-                            make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                }
-            }
-            tc_fence_before_sync();
-            warp_arrive(wt, kSTFree);
         }
         if (!ok) set_abort();
     }
@@ -1407,49 +1425,15 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
 // Busiest CTA's time for a dense batch cut into windows of K tiles, in units of one tile: every window
 // costs its tiles plus a fixed overhead, and a window that publishes an aggregate (its successor runs
 // in the same iteration) also reads its tiles once more at `agg_cost` of a tile each.
-static double dense_plan_cost(int64_t nt, int64_t nchains, int grid, int K) {
-    constexpr double kAggCost = 0.45, kWindowCost = 1.5;
-    const int64_t W = (nt + K - 1) / K;
-    const int64_t np = nchains * W;
-    double worst = 0.0;
-    for (int b = 0; b < grid && b < np; ++b) {
-        double t = 0.0;
-        for (int64_t d = b; d < np; d += grid) {
-            const int64_t w = d / nchains;
-            const int64_t tiles = (w + 1 < W) ? K : nt - (W - 1) * K;
-            t += tiles + kWindowCost;
-            if (w + 1 < W) t += kAggCost * tiles;
-        }
-        if (t > worst) worst = t;
-    }
-    return worst;
-}
-
 void fused_plan(const Problem& p, int* K_out, int64_t* np_out) {
-    const int64_t npairs = p.s.nheads / 2;
-    const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
-    if (!p.varlen) {
-        // dense: the window K (tiles per piece) with the lowest estimated time of the busiest CTA
-        const int64_t nt = (p.s.seqlen + kFusedTile - 1) / kFusedTile;
-        const int64_t nchains = p.s.batch * npairs;
-        int bestK = kFusedMaxWindow;
-        double best = 1e300;
-        for (int K = kFusedMaxWindow; K >= kFusedMinWindow; --K) {
-            const double cost = dense_plan_cost(nt, nchains, grid, K);
-            if (cost < best - 1e-9) { best = cost; bestK = K; }
-        }
-        *K_out = bestK;
-        *np_out = nchains * ((nt + bestK - 1) / bestK);
-    } else {
-        // packed batch: windows of 8 tiles; the piece count is bounded here, exact on the device
-        const int K = 8;
-        *K_out = K;
-        const int64_t max_tiles = p.L.max_chunks;
-        *np_out = npairs * ((max_tiles - p.nseq + K - 1) / K + p.nseq);
-    }
+    // one contiguous range of the chain-major tile run per CTA; one published-state slot per CTA
+    *K_out = 0;
+    const int64_t grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
+    const int64_t all_tiles = (p.s.nheads / 2) * p.L.max_chunks;
+    *np_out = all_tiles < grid ? (all_tiles > 0 ? all_tiles : 1) : grid;
 }
 
-cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
+cudaError_t launch_fused(const Problem& p, int, int64_t, int part) {
     const int H = (int)p.s.nheads, Nf = (int)p.s.dstate, G = (int)p.s.ngroups;
     const int N = Nf > 128 ? 128 : Nf;            // state columns per launch
     const int64_t npairs = H / 2;
@@ -1466,7 +1450,6 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     fa.status = p.status();
     fa.tiles = p.chunks();
     fa.seqoff = p.seqoff();
-    fa.woff = p.varlen ? p.woff() : nullptr;
     fa.dt = p.dt;
     fa.A = p.A;
     fa.D = part == 0 ? p.D : nullptr;
@@ -1481,12 +1464,9 @@ cudaError_t launch_fused(const Problem& p, int K, int64_t np, int part) {
     fa.G = G;
     fa.nseq = (int)p.nseq;
     fa.npairs = (int)npairs;
-    fa.npieces = (int)np;
-    fa.K = K;
     fa.dense = p.varlen ? 0 : 1;
     fa.seqlen = (int)p.s.seqlen;
     fa.nt_dense = (int)((p.s.seqlen + kFusedTile - 1) / kFusedTile);
-    fa.W_dense = (fa.nt_dense + K - 1) / K;
     fa.n_off = part * N;
     fa.n_full = Nf;
     fa.y_accum = part > 0 ? 1 : 0;

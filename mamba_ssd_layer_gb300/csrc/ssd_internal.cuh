@@ -21,8 +21,8 @@ struct ChunkDesc {
 //   header  : int32 status, int32 number of chunks (tiles) actually built, int32 location
 //             code of the first device-side timeout (0 = none), int32 number of windows (packed
 //             batch, fused path), int32 spare x 4
-//   flags   : (fused path) int32[max_pieces * 4], per window and TMEM lane quadrant: 1 = the window's
-//             aggregate is published, 2 = the state at its end is published, 0 = neither yet
+//   flags   : (fused path) int32[max_pieces * 4], per CTA slot and TMEM lane quadrant: 1 = the aggregate of
+//             the CTA's last window is published, 2 = the state at its end is too, 0 = neither yet
 //   chunks  : ChunkDesc[max_chunks]  (chunks of `chunk` tokens; 128-token tiles on the fused path)
 //   seqoff  : int32[nseq + 1], first chunk of every sequence
 // fp32 path (three kernels):
@@ -31,19 +31,16 @@ struct ChunkDesc {
 //             local end state here and the state pass overwrites it in place with the
 //             true state entering the chunk
 // fused path (bf16, P = 64, N in {64, 128, 256}; 128 state columns per launch):
-//   woff    : int32[nseq + 1], first window of every sequence (packed batch)
-//   pdecay  : float[max_pieces * 4], decay of each window over its tiles, per lane quadrant (the
+//   pdecay  : float[max_pieces * 4], decay of each slot's window over its tiles, per lane quadrant (the
 //             head of quadrants 0, 1 is the pair's first head, of quadrants 2, 3 its second)
 //   agg     : float[max_pieces * 128 * Nl], the window's end state from a zero entering state
 //   incl    : float[max_pieces * 128 * Nl], the true state at the window's end
 //   (Nl = min(N, 128), the state columns of one launch)
 constexpr int kFusedTile = 128;
-constexpr int kFusedMaxGrid = 256;
-constexpr int kFusedMinWindow = 4;    // tiles per piece, lower bound (bounds the workspace)
-constexpr int kFusedMaxWindow = 16;
+constexpr int kFusedMaxGrid = 160;    // CTAs of the fused kernel, at most (one per SM)
 
 struct WsLayout {
-    size_t header, flags, chunks, seqoff, woff, decay, states, pdecay, agg, incl, total;
+    size_t header, flags, chunks, seqoff, decay, states, pdecay, agg, incl, total;
     size_t clear_bytes;          // bytes from the header on that every call clears before its kernels
     int64_t max_chunks, nseq, max_pieces;
     bool fused;
@@ -71,10 +68,10 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
     size_t off = 0;
     w.header = off; off += 32;
     if (w.fused) {
-        // pieces are windows of >= kFusedMinWindow tiles of one (sequence, head pair)
-        const int64_t per_seq = varlen ? ((w.max_chunks - nseq_eff) + kFusedMinWindow - 1) / kFusedMinWindow + nseq_eff
-                                       : s.batch * ((((s.seqlen + q - 1) / q) + kFusedMinWindow - 1) / kFusedMinWindow);
-        w.max_pieces = (s.nheads / 2) * (per_seq > 0 ? per_seq : 1);
+        // one published-state slot per CTA that has tiles (its last window, when it ends inside its
+        // chain): min(grid, tiles of all chains) slots
+        const int64_t all_tiles = (s.nheads / 2) * w.max_chunks;
+        w.max_pieces = all_tiles < kFusedMaxGrid ? (all_tiles > 0 ? all_tiles : 1) : kFusedMaxGrid;
         w.flags = off; off += sizeof(int32_t) * 4 * (size_t)w.max_pieces;
     }
     w.clear_bytes = off;
@@ -83,7 +80,6 @@ inline WsLayout ws_layout(const ssd_shape& s, ssd_dtype dtype, int chunk, int64_
     w.seqoff = off; off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
     if (w.fused) {
         const int64_t ncol = s.dstate > 128 ? 128 : s.dstate;   // state columns of one launch
-        w.woff = off;   off = align256(off + sizeof(int32_t) * (size_t)(nseq_eff + 1));
         w.pdecay = off; off = align256(off + sizeof(float) * 4 * (size_t)w.max_pieces);
         w.agg = off;    off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
         w.incl = off;   off = align256(off + sizeof(float) * (size_t)(w.max_pieces * 128 * ncol));
@@ -127,7 +123,6 @@ struct Problem {
     int32_t* seqoff() const { return reinterpret_cast<int32_t*>(ws + L.seqoff); }
     float* decay() const { return reinterpret_cast<float*>(ws + L.decay); }
     float* states() const { return reinterpret_cast<float*>(ws + L.states); }
-    int32_t* woff() const { return reinterpret_cast<int32_t*>(ws + L.woff); }
     int32_t* flags() const { return reinterpret_cast<int32_t*>(ws + L.flags); }
 };
 
@@ -140,14 +135,12 @@ void prof_launch();
 void prof_begin(cudaStream_t s, const char* kernel);
 void prof_end(cudaStream_t s);
 
-// ssd_common.cu: chunk (tile) table of `q` tokens; with woff, also the per-sequence offsets of
-// windows of K chunks
-cudaError_t launch_prep(const Problem& p, int q, int32_t* woff = nullptr, int K = 1);
+// ssd_common.cu: chunk (tile) table of `q` tokens
+cudaError_t launch_prep(const Problem& p, int q);
 cudaError_t launch_state_pass(const Problem& p);
 // ssd_f32.cu
 cudaError_t launch_f32_path(const Problem& p);
-// ssd_fused.cu (single-pass tcgen05 path): the window size K (tiles per piece) and the number of
-// pieces (exact for a dense batch, an upper bound for a packed batch)
+// ssd_fused.cu (single-pass tcgen05 path): K is unused (0); npieces = the published-state slots (one per CTA)
 void fused_plan(const Problem& p, int* K, int64_t* npieces);
 // part: which 128-column half of an N = 256 state (0 for N <= 128)
 cudaError_t launch_fused(const Problem& p, int K, int64_t npieces, int part);
