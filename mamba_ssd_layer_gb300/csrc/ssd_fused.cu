@@ -79,35 +79,35 @@ constexpr uint32_t kColGB = 256;   // two 128-column buffers, alternating per ti
 // mbarriers. [2]: one per stage of the ring (by stream position p & 1) or per C B^T buffer (by the
 // count of tiles c & 1). Expected arrivals in bar_count.
 enum : int {
-    kFullBC = 0,     // [2] B (and C) of the stage landed (TMA bytes)
+    kFullBC = 0,     // [2] B and C of the stage landed (a correction tile: C only) (TMA bytes)
     kFullX = 2,      // [2] x of the stage landed (TMA bytes)
     kTblRead = 4,    // [2] the stage's tables and record read: 8 epilogue, 4 mask and 4 state warps
     kTblAny = 6,     // [2] the stage's tables and tile record written (every position, and the end record)
     kBCFree = 8,     // [2] MMA done with the stage's B and C
-    kXFreeC = 10,    // [2] a tile's y (staged in the stage's x) stored: 8 epilogue warps
-    kXFreeA = 12,    // [2] MMA done with an aggregate tile's x
-    kGFull = 14,     // [2] C B^T in the buffer
-    kLGFull = 16,    // [2] L o G in the buffer: 4 mask warps
-    kGBFree = 18,    // [2] the buffer's Yo read: 8 epilogue warps
-    kDrained = 20,   // [2] the stage's x weighted (and, for a tile, Yd read): 8 epilogue warps
-    kYDFull = 22,    // Yd in TMEM
-    kState = 23,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM: 4 state warps
-    kSO = 24,        // S(t) and Yo(t) done
-    kVTFree = 25,    // the factored-mask table read: 4 mask warps
-    kAggDone = 26,   // the aggregate complete (and the MMA warp's final drain)
-    kNumBars = 27
+    kXFree = 10,     // [2] the tile's y (staged in the stage's x) stored: 8 epilogue warps
+    kGFull = 12,     // [2] C B^T in the buffer
+    kLGFull = 14,    // [2] L o G in the buffer: 4 mask warps
+    kGBFree = 16,    // [2] the buffer's Yo read: 8 epilogue warps
+    kDrained = 18,   // [2] the stage's Yd read and x weighted (a correction tile: begun): 8 epilogue warps
+    kYDFull = 20,    // Yd in TMEM
+    kState = 21,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM (correction: h_in staged): 4 state warps
+    kSO = 22,        // S(t) and Yo(t) done (correction: the correction product done)
+    kVTFree = 23,    // the factored-mask table read: 4 mask warps
+    kNcorr = 24,     // the correction tile count written (table warp, once)
+    kMmaDone = 25,   // the MMA warp's final drain
+    kNumBars = 26
 };
 
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-    return ((i >= kXFreeC && i < kXFreeC + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
+    return ((i >= kXFree && i < kXFree + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
                ? 8u
          : (i >= kTblRead && i < kTblRead + 2) ? 16u
          : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree) ? 4u
          : 1u;
 }
 
-// tile record flags: an aggregate tile; the end of this CTA's stream (no tile)
-constexpr int kRecAgg = 1, kRecEnd = 2;
+// tile record flags: a correction tile; the end of this CTA's stream (no tile)
+constexpr int kRecCorr = 1, kRecEnd = 2;
 
 // Timeout location codes (workspace header word 2): 0x100 + barrier for an mbarrier wait, 0x300 for a
 // look-back wait on another CTA's published state.
@@ -180,12 +180,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t* r) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -219,7 +213,7 @@ struct Lay {
     static constexpr uint32_t kVt = kCs + 2 * kCsStride * 4;           // [2][kVtCols] halves
     static constexpr uint32_t kRec = kVt + 2 * kVtCols * 2;            // [2] tile records (int4)
     static constexpr uint32_t kBars = kRec + 2 * 16;                   // [kNumBars] u64
-    static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag, window total
+    static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag, correction count
     static constexpr uint32_t kTotal = kMisc + 16;
     static_assert(kBars % 8 == 0, "barriers are 8-byte aligned");
     static_assert(kTotal <= 232448, "shared memory per CTA");
@@ -239,13 +233,13 @@ struct Smem {
     __device__ float* cs(int s) const { return reinterpret_cast<float*>(base + Lay<N>::kCs) + s * kCsStride; }
     // exp(cs_p - table_j) per head and token j < 96, p = last token of j's 32-token block: [2][96]
     __device__ __half* vt() const { return reinterpret_cast<__half*>(base + Lay<N>::kVt); }
-    // per stage: the tile record {first row, tokens, first head, flags} (flags: kRecAgg, kRecEnd)
+    // per stage: the tile record {first row, tokens, first head, flags} (flags: kRecCorr, kRecEnd)
     __device__ int4* rec(int s) const { return reinterpret_cast<int4*>(base + Lay<N>::kRec) + s; }
     __device__ uint64_t* bars() const { return reinterpret_cast<uint64_t*>(base + Lay<N>::kBars); }
     __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(base + Lay<N>::kMisc); }
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(base + Lay<N>::kMisc + 4); }
-    // the last window's total of dt*A (x log2 e), per head of the pair
-    __device__ float* wtotal() const { return reinterpret_cast<float*>(base + Lay<N>::kMisc + 8); }
+    // the number of correction tiles (written once by the table warp, see Stream)
+    __device__ volatile int* ncorr() const { return reinterpret_cast<volatile int*>(base + Lay<N>::kMisc + 8); }
 };
 
 // ---------------------------------------------------------------- bounded waits
@@ -396,16 +390,19 @@ __device__ __forceinline__ ChainPos decode_at(int g, const FusedArgs& a) {
     return c;
 }
 
-// The tile stream of this CTA, walked identically by every role: the aggregate tiles of its last window
-// from the last back to the first (when that window ends inside its chain; in that order each one's
-// decay to the window's end is a running sum), then every window's tiles in time order.
+// The tile stream of this CTA, walked identically by every role: every window's tiles in time order
+// (the first window from a zero state when it starts inside its chain, the others from their chain's
+// initial state), then, when the first window starts inside its chain, its correction tiles: its first
+// tiles again, for y += exp(cs_l) C_l h_in^T once the entering state h_in is known. The count of
+// correction tiles comes from the table warp (through shared memory): the tiles before the decay from
+// the window's start underflows in fp32 (after that the correction is exactly zero).
 struct Stream {
     int g0, g1;           // this CTA's range of the chain-major tile run
     int gw;               // run index of the current window's first tile
-    int t, t0, t1;        // tile, the window's tiles [t0, t1) of its chain
+    int t, t0, t1;        // tile, the window's tiles [t0, t1) of its chain (correction: [t0, t0 + count))
     int hp;               // head pair
     int32_t row0, len;    // first packed row and length of the sequence
-    bool agg;             // an aggregate tile
+    bool corr;            // a correction tile
     bool valid;
     __device__ int tile_row0() const { return row0 + kTile * t; }
     __device__ int tile_len() const {
@@ -425,33 +422,24 @@ struct Stream {
         g0 = range_start((int)blockIdx.x, a);
         g1 = range_start((int)blockIdx.x + 1, a);
         valid = g1 > g0;
-        agg = false;
-        if (!valid) return;
-        const ChainPos cl = decode_at(g1 - 1, a);          // the last window holds the range's last tile
-        if (cl.t + 1 < cl.nt) {
-            agg = true;
-            t1 = cl.t + 1;
-            t0 = cl.t - (g1 - 1 - g0) > 0 ? cl.t - (g1 - 1 - g0) : 0;
-            t = t1 - 1;
-            gw = g1 - (t1 - t0);
-            hp = cl.hp;
-            row0 = cl.seq_row0;
-            len = cl.seq_len;
-        } else {
-            load_at(g0, a);
-        }
+        corr = false;
+        if (valid) load_at(g0, a);
     }
-    __device__ void next(const FusedArgs& a) {
-        if (agg) {
-            if (t > t0) { --t; return; }
-            agg = false;
-            load_at(g0, a);
-            return;
-        }
+    // ncorr: the correction tile count, read once the window tiles are done and the table warp has
+    // published it (`ready` waits for that; false on timeout or abort)
+    template <class Ready>
+    __device__ void next(const FusedArgs& a, const volatile int* ncorr, Ready&& ready) {
         if (++t < t1) return;
+        if (corr) { valid = false; return; }
         const int g = gw + (t1 - t0);
-        if (g >= g1) { valid = false; return; }
-        load_at(g, a);
+        if (g < g1) { load_at(g, a); return; }
+        // the window tiles are done: the correction tiles of the first window, if any
+        load_at(g0, a);
+        if (t0 == 0 || !ready()) { valid = false; return; }
+        const int n = *ncorr;
+        if (n <= 0) { valid = false; return; }
+        corr = true;
+        t1 = t0 + n;
     }
 };
 
@@ -459,23 +447,6 @@ struct Stream {
 // of line so that they do not add to the registers of the per-tile path)
 // 16-byte chunk ch of a 128-byte row of a swizzled region (row pointer, row & 7)
 __device__ __forceinline__ uint8_t* chunk_ptr(uint8_t* rowp, int ix, int ch) { return rowp + ((ch ^ ix) << 4); }
-
-// an aggregate tile's x row (64 bf16 channels) times w in place, in fp32, rounded once
-__device__ __noinline__ void weight_row(uint8_t* rowp, int ix, float w) {
-    const float2 ww = make_float2(w, w);
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(rowp, ix, ch));
-        uint4 v = *pv;
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float2 f = __fmul2_rn(unpack_bf16x2(u[m]), ww);
-            u[m] = pack_bf16x2(f.x, f.y);
-        }
-        *pv = v;
-    }
-}
 
 // one staged y row (64 bf16 channels) to global memory; with `accum` added in fp32 onto the y there
 __device__ __noinline__ void store_row(uint8_t* rowp, int ix, __nv_bfloat16* yrow, bool accum) {
@@ -546,35 +517,35 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 
     if (warp == kWarpProducer) {
         // ============================================================ TMA producer (lane 0)
-        // Stage s = p & 1 of stream position p holds x (both heads), B and, for a tile, C. A stage is
-        // reloaded once the MMA warp is done with its B and C and its x is free: for a tile, once its
-        // y (staged there) has been stored; for an aggregate tile, once the MMA warp has read it.
+        // Stage s = p & 1 of stream position p holds x (both heads), B and C (a correction tile: C only).
+        // A stage is reloaded once the MMA warp is done with its B and C and, for x, once the tile's y
+        // (staged in its x region) has been stored.
         regs_dec<kRegsWG0>();
         if (lane == 0) {
             uint32_t ph = 0;
             bool ok = true;
             int nbc[2] = {0, 0}, nx[2] = {0, 0};
-            bool prev_agg[2] = {false, false};
             Stream it;
             it.start(a);
-            for (int p = 0; it.valid && ok; it.next(a), ++p) {
+            auto ready = [&]() { return wait_par(wt, kNcorr, 0u); };
+            for (int p = 0; it.valid && ok; it.next(a, sm.ncorr(), ready), ++p) {
                 const int s = p & 1;
                 const int h0 = 2 * it.hp, g = h0 / (a.H / a.G);
                 const int row0 = it.tile_row0();
                 if (p >= 2 && !(ok = wait_bar(wt, kBCFree + s, ph))) break;
                 uint64_t* fbc = sm.bars() + kFullBC + s;
-                mbar_arrive_expect_tx(fbc, (uint32_t)((it.agg ? NB : 2 * NB) * kRegion));
-                for (int k = 0; k < NB; ++k) tma_load_3d(sm.b(s) + k * kRegion, &maps.b, fbc, 64 * k, g, row0);
-                if (!it.agg)
-                    for (int k = 0; k < NB; ++k) tma_load_3d(sm.c(s) + k * kRegion, &maps.c, fbc, 64 * k, g, row0);
+                mbar_arrive_expect_tx(fbc, (uint32_t)((it.corr ? NB : 2 * NB) * kRegion));
+                if (!it.corr)
+                    for (int k = 0; k < NB; ++k) tma_load_3d(sm.b(s) + k * kRegion, &maps.b, fbc, 64 * k, g, row0);
+                for (int k = 0; k < NB; ++k) tma_load_3d(sm.c(s) + k * kRegion, &maps.c, fbc, 64 * k, g, row0);
                 ++nbc[s];
-                if (p >= 2 && !(ok = wait_bar(wt, (prev_agg[s] ? kXFreeA : kXFreeC) + s, ph))) break;
+                if (it.corr) continue;        // (correction tiles come last: no x load follows)
+                if (p >= 2 && !(ok = wait_bar(wt, kXFree + s, ph))) break;
                 uint64_t* fx = sm.bars() + kFullX + s;
                 mbar_arrive_expect_tx(fx, (uint32_t)(2 * kRegion));
                 tma_load_3d(sm.x(s, 0), &maps.x, fx, 0, h0, row0);
                 tma_load_3d(sm.x(s, 1), &maps.x, fx, 0, h0 + 1, row0);
                 ++nx[s];
-                prev_agg[s] = it.agg;
             }
             if (!ok) set_abort();
             // every load issued has landed before the CTA's shared memory goes away
@@ -589,8 +560,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         if (lane == 0) {
             uint32_t ph = 0;
             bool ok = true, any = false;
-            int cC = 0;                          // tiles (not aggregate tiles) so far: C B^T buffer cC & 1
-            int n_agg_commits = 0;
+            int cC = 0;                          // tiles so far (correction tiles too): TMEM buffer cC & 1
+            bool corr_started = false;
             bool g_next = false;                 // C B^T of the tile cC already issued
             const uint32_t id_g = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t id_yo = idesc_bf16_f32(128, 128, 0, 0);
@@ -606,32 +577,47 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 }
                 mma_commit(sm.bars() + kGFull + buf);
             };
-            // S += (w o X)^T B over the stage (M = 2 heads x 64 channels, N = state columns)
-            auto issue_s = [&](int st, bool acc) {
+            // S += (w o X)^T B over the stage (M = 2 heads x 64 channels, N = state columns), onto a_t h_{t-1}
+            auto issue_s = [&](int st) {
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t ad = smem_desc_sw128(smem_u32(sm.x(st, 0) + ks * 2048), kRegion, 1024);
                     const uint64_t bd = smem_desc_sw128(smem_u32(sm.b(st) + ks * 2048), kRegion, 1024);
-                    mma_bf16_ss(tmem + kColST, ad, bd, id_s, (acc || ks > 0) ? 1u : 0u);
+                    mma_bf16_ss(tmem + kColST, ad, bd, id_s, 1u);
+                }
+            };
+            // C h^T into the buffer's columns (M = tokens, N = 2 heads x 64 channels): Yo, or the correction
+            auto issue_yo = [&](int st, uint32_t gb) {
+#pragma unroll 1
+                for (int ks = 0; ks < N / 16; ++ks) {
+                    const int kk = ks / 4, off = (ks % 4) * 32;
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(st) + kk * kRegion + off), 0, 1024);
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
+                    mma_bf16_ss(tmem + gb, ad, bd, id_yo, ks > 0 ? 1u : 0u);
                 }
             };
             Stream it;
             it.start(a);
-            for (int p = 0; it.valid && ok; it.next(a), ++p) {
+            auto ready = [&]() { return wait_par(wt, kNcorr, 0u); };
+            for (int p = 0; it.valid && ok; it.next(a, sm.ncorr(), ready), ++p) {
                 const int s = p & 1;
                 any = true;
-                if (it.agg) {
-                    // (the aggregate tiles open the stream: the state columns hold nothing yet)
-                    ok = wait_bar(wt, kFullBC + s, ph) && wait_bar(wt, kFullX + s, ph) && wait_bar(wt, kDrained + s, ph);
+                const int buf = cC & 1;
+                if (it.corr) {
+                    // the correction product C(t) h_in^T: h_in staged by the state warps (once). The epilogue
+                    // has taken the previous product (Drained: it signals each correction tile as it starts
+                    // on it), so that its waits on SO never fall two phases behind.
+                    ok = wait_bar(wt, kFullBC + s, ph) && (cC < 2 || wait_bar(wt, kGBFree + buf, ph)) &&
+                         wait_bar(wt, kDrained + s, ph) && (corr_started || wait_bar(wt, kState, ph));
                     if (!ok) break;
+                    corr_started = true;
                     tc_fence_after_sync();
-                    issue_s(s, it.t < it.t1 - 1);
+                    issue_yo(s, kColGB + 128 * buf);
+                    mma_commit(sm.bars() + kSO);
                     mma_commit(sm.bars() + kBCFree + s);
-                    mma_commit(sm.bars() + kXFreeA + s);
-                    if (it.t == it.t0) { mma_commit(sm.bars() + kAggDone); ++n_agg_commits; }
+                    ++cC;
                     continue;
                 }
-                const int buf = cC & 1;
                 if (!g_next) {
                     ok = wait_bar(wt, kFullBC + s, ph) && (cC < 2 || wait_bar(wt, kGBFree + buf, ph));
                     if (!ok) break;
@@ -672,14 +658,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 ok = poll_bar(wt, kDrained + s, ph, try_g_next) && wait_bar(wt, kState, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                issue_s(s, true);
-#pragma unroll 1
-                for (int ks = 0; ks < N / 16; ++ks) {
-                    const int kk = ks / 4, off = (ks % 4) * 32;
-                    const uint64_t ad = smem_desc_sw128(smem_u32(sm.c(s) + kk * kRegion + off), 0, 1024);
-                    const uint64_t bd = smem_desc_sw128(smem_u32(sm.hs() + kk * kRegion + off), 0, 1024);
-                    mma_bf16_ss(tmem + gb, ad, bd, id_yo, ks > 0 ? 1u : 0u);
-                }
+                issue_s(s);
+                issue_yo(s, gb);
                 mma_commit(sm.bars() + kSO);
                 mma_commit(sm.bars() + kBCFree + s);
                 if (next_tile && !g_next) {
@@ -695,22 +675,24 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (!ok) set_abort();
             // every MMA issued has completed before TMEM is freed
             if (any) {
-                mma_commit(sm.bars() + kAggDone);
-                wait_par(wt, kAggDone, (uint32_t)n_agg_commits & 1u, false);
+                mma_commit(sm.bars() + kMmaDone);
+                wait_par(wt, kMmaDone, 0u, false);
             }
         }
     } else if (warp == kWarpTables) {
         // ============================================================ tables (whole warp)
         // Per stream position: dt of the tile for both heads of the pair (prefetched one position
-        // ahead), the cumsum of dt*A (x log2 e) -- window-relative for an aggregate tile, tile-local
-        // for a tile -- and, for a tile, the factored-mask column table (once the mask warps are done
-        // with the previous one).
+        // ahead), the cumsum of dt*A (x log2 e) -- tile-local for a tile, from the first window's start
+        // for a correction tile -- and, for a tile, the factored-mask column table (once the mask warps are
+        // done with the previous one). While walking the first window it counts the correction tiles.
         regs_dec<kRegsWG0>();
         uint32_t ph = 0;
         bool ok = true;
         bool vt_used = false;
         float carry[2] = {0.f, 0.f};
-        float suffix[2] = {0.f, 0.f};    // aggregate tiles: the decay of the window's later tiles
+        float ccarry[2] = {0.f, 0.f};    // correction tiles: cumsum of the first window's earlier tiles
+        float wcarry[2] = {0.f, 0.f};    // first window: cumsum before the current tile
+        int ncount = 0;                  // first window: tiles whose correction is not all zero
         Stream it;
         it.start(a);
         auto load_dt = [&](const Stream& st, float (&v)[2][4]) {
@@ -725,6 +707,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 v[1][k] = d2.y;
             }
         };
+        auto ready = [&]() { return __all_sync(0xffffffffu, wait_par(wt, kNcorr, 0u)); };
         float vn[2][4] = {};
         int np_done = 0;
         load_dt(it, vn);
@@ -736,12 +719,24 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) v[hh][k] = vn[hh][k];
-            const bool agg = it.agg, agg_last = it.agg && it.t == it.t1 - 1, agg_first = it.agg && it.t == it.t0;
+            const bool corr = it.corr;
+            const bool first_win = !corr && it.gw == it.g0;
             const int h0 = 2 * it.hp, len = it.tile_len(), row0 = it.tile_row0();
-            if (agg_last) suffix[0] = suffix[1] = 0.f;
-            it.next(a);
+            if (first_win) {
+                // the correction of tile t is exactly zero once exp2 of the cumsum before it underflows
+                // (ex2.approx.ftz gives 0 below 2^-126), for both heads
+                if (fmaxf(wcarry[0], wcarry[1]) > -126.f) ncount = it.t - it.t0 + 1;
+                if (it.t + 1 == it.t1) {
+                    // the first window's last tile: the count is final (zero when the window starts its chain)
+                    if (lane == 0) *sm.ncorr() = it.t0 > 0 ? ncount : 0;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.bars() + kNcorr);
+                }
+            }
+            it.next(a, sm.ncorr(), ready);
             load_dt(it, vn);
-            carry[0] = carry[1] = 0.f;
+            carry[0] = corr ? ccarry[0] : 0.f;
+            carry[1] = corr ? ccarry[1] : 0.f;
             if (p >= 2) {
                 // every role has read the tables this stage held two positions ago
                 ok = __all_sync(0xffffffffu, wait_bar(wt, kTblRead + s, ph));
@@ -767,28 +762,26 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 for (int k = 0; k < 4; ++k) cv[hh][k] = base + pz[k];
                 float4 col = make_float4(cv[hh][0], cv[hh][1], cv[hh][2], cv[hh][3]);
                 if constexpr (kScaleX) {
-                    col.x -= __log2f(fmaxf(v[hh][0], kMinDt));
-                    col.y -= __log2f(fmaxf(v[hh][1], kMinDt));
-                    col.z -= __log2f(fmaxf(v[hh][2], kMinDt));
-                    col.w -= __log2f(fmaxf(v[hh][3], kMinDt));
+                    if (!corr) {
+                        col.x -= __log2f(fmaxf(v[hh][0], kMinDt));
+                        col.y -= __log2f(fmaxf(v[hh][1], kMinDt));
+                        col.z -= __log2f(fmaxf(v[hh][2], kMinDt));
+                        col.w -= __log2f(fmaxf(v[hh][3], kMinDt));
+                    }
                 }
                 *reinterpret_cast<float4*>(cs + hh * 128 + 4 * lane) = col;
-                carry[hh] += __shfl_sync(0xffffffffu, sc, 31);
+                // the tile's total (dt is zero past the sequence)
+                const float ttot = __shfl_sync(0xffffffffu, sc, 31);
+                if (corr) ccarry[hh] += ttot;
+                if (first_win) wcarry[hh] += ttot;
                 // row-side values: the plain cumsum at tokens 31, 63, 95, and the last value
                 if (lane == 7 || lane == 15 || lane == 23) cs[256 + 4 * hh + (lane >> 3)] = cv[hh][3];
-                if (agg) {
-                    // the decay to the window's end: this tile's total (the cumsum at its last token; dt
-                    // is zero past the sequence) plus the later tiles'
-                    const float ttot = __shfl_sync(0xffffffffu, cv[hh][3], 31);
-                    if (lane == 0) cs[256 + 4 * hh + 3] = ttot + suffix[hh];
-                    suffix[hh] += ttot;
-                    if (agg_first && lane == 0) sm.wtotal()[hh] = suffix[hh];
-                } else if (lane == ((len - 1) >> 2)) {
+                if (lane == ((len - 1) >> 2)) {
                     const int k = (len - 1) & 3;
                     cs[256 + 4 * hh + 3] = k == 0 ? cv[hh][0] : k == 1 ? cv[hh][1] : k == 2 ? cv[hh][2] : cv[hh][3];
                 }
             }
-            if (!agg) {
+            if (!corr) {
                 // v_j = exp(cs_p - table_j), p the last token of j's 32-token block (j < 96), computed before
                 // the mask warps release the table so that only the stores follow the release
                 __half2 vv[2][2];
@@ -819,7 +812,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                 }
             }
-            if (lane == 0) *sm.rec(s) = make_int4(row0, len, h0, agg ? kRecAgg : 0);
+            if (lane == 0) *sm.rec(s) = make_int4(row0, len, h0, corr ? kRecCorr : 0);
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(sm.bars() + kTblAny + s);
@@ -856,9 +849,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         float lgd[2] = {0.f, 0.f};
         Stream it;
         it.start(a);
-        for (int p = 0; it.valid && ok; it.next(a), ++p) {
-            if (it.agg) {
-                // nothing to do for an aggregate tile but to take part in the release of its tables
+        auto ready = [&]() { return __all_sync(0xffffffffu, wait_par(wt, kNcorr, 0u)); };
+        for (int p = 0; it.valid && ok; it.next(a, sm.ncorr(), ready), ++p) {
+            if (it.corr) {
+                // nothing to do for a correction tile but to take part in the release of its tables
                 const int s = p & 1;
                 ok = wait_warp(wt, kTblAny + s, ph);
                 if (ok) warp_arrive(wt, kTblRead + s);
@@ -972,17 +966,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 8) {
         // ============================================================ epilogue (one warpgroup per head)
         // Row i = 32 q + lane of the tile, head hh of the pair, its 64 channels.
-        //   aggregate tile: x row times exp(total - cs_i) in place (the weights to the window's end)
         //   tile:  drain -- z = Yd + D x (fp32, kept in registers), x row times exp(last - cs_i) in place
         //          combine -- y = z + exp(cs_i) Yo, rounded once to bf16, staged in the x region of the
         //          stage (free once S and Yo are done), and stored: a row quadrant wholly inside the
         //          sequence as one bulk tensor store (kAccum: a bulk reduce-add), otherwise row by row
+        //   correction tile: z = the row's y as the window pass stored it, then the same combine with
+        //          exp(cs_i) (cs from the first window's start) and the correction product, stored
         regs_inc<kRegsEpi>();
         const int hh = (warp - kWarpEpi) >> 2, q = warp & 3, i = 32 * q + lane, ix = i & 7;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t ph = 0;
         bool ok = true;
         int cC = 0;
+        bool y_visible = false;     // this warp's own y stores of the window pass are complete
         for (int p = 0; ok; ++p) {
             const int s = p & 1;
             // the tile record tells what the stage holds (or that the stream has ended)
@@ -990,65 +986,90 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (!ok) break;
             const int4 rc = *sm.rec(s);
             if (rc.w & kRecEnd) break;
-            const bool is_agg = (rc.w & kRecAgg) != 0;
+            const bool is_corr = (rc.w & kRecCorr) != 0;
             const int row0 = rc.x, len = rc.y, h0 = rc.z;
             const float tab = sm.cs(s)[hh * 128 + i], last = sm.cs(s)[256 + 4 * hh + 3];
             warp_arrive(wt, kTblRead + s);
             float lgd = 0.f;
             if constexpr (kScaleX) {
-                if (!is_agg) {
+                if (!is_corr) {
                     float dti = 1.f;
                     if (i < len) dti = __ldg(a.dt + (int64_t)(row0 + i) * a.H + h0 + hh);
                     lgd = __log2f(fmaxf(dti, kMinDt));
                 }
             }
-            ok = wait_warp(wt, kFullX + s, ph);
-            if (!ok) break;
-            const float w = (i < len) ? ex2(last - tab) : 0.f;
             uint8_t* const xr = sm.x(s, hh);
             uint8_t* const xrow = xr + i * 128;
-            if (is_agg) {
-                weight_row(xrow, ix, w);
-                fence_proxy_async_smem();
-                // one Drained barrier per stage: a warp ahead of the others signals the other stage's
-                // barrier, and it cannot get two positions ahead (the stage is reloaded only once all
-                // eight warps have signalled it)
-                warp_arrive(wt, kDrained + s);
-                continue;
-            }
-            const float e_row = ex2(tab + lgd);
-            const float Dh = a.D ? __ldg(a.D + h0 + hh) : 0.f;
             const int buf = cC & 1;
-            // ---- drain
-            ok = wait_warp(wt, kYDFull, ph);
-            if (!ok) break;
-            tc_fence_after_sync();
             float z[64];
-            tmem_ld32_nowait(lane_base + kColYD + 64 * hh, reinterpret_cast<uint32_t*>(z));
-            tmem_ld32_nowait(lane_base + kColYD + 64 * hh + 32, reinterpret_cast<uint32_t*>(z + 32));
-            tmem_wait_ld();
-            {
-                const float2 dd = make_float2(Dh, Dh), ww = make_float2(w, w);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, ch));
-                    uint4 v = *pv;
-                    uint32_t* u = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float2 xf = unpack_bf16x2(u[m]);
-                        const float2 zz = __ffma2_rn(dd, xf, make_float2(z[8 * ch + 2 * m], z[8 * ch + 2 * m + 1]));
-                        z[8 * ch + 2 * m] = zz.x;
-                        z[8 * ch + 2 * m + 1] = zz.y;
-                        const float2 f = fmul2(xf, ww);
-                        u[m] = pack_bf16x2(f.x, f.y);
+            float e_row;
+            if (is_corr) {
+                // (this warp is done with the previous position, its SO wait included)
+                warp_arrive(wt, kDrained + s);
+                // the row's y from the window pass (this warp stored it: its bulk stores are waited for
+                // and made visible to ordinary loads once)
+                if (!y_visible) {
+                    if (lane == 0) {
+                        bulk_wait_all();
+                        fence_proxy_async_global();
                     }
-                    *pv = v;
+                    __syncwarp();
+                    y_visible = true;
                 }
+                if (i < len) {
+                    const uint4* yr = reinterpret_cast<const uint4*>(a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 v = yr[ch];
+                        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 f = unpack_bf16x2(u[m]);
+                            z[8 * ch + 2 * m] = f.x;
+                            z[8 * ch + 2 * m + 1] = f.y;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) z[e] = 0.f;
+                }
+                e_row = (i < len) ? ex2(tab) : 0.f;
+            } else {
+                ok = wait_warp(wt, kFullX + s, ph);
+                if (!ok) break;
+                const float w = (i < len) ? ex2(last - tab) : 0.f;
+                e_row = ex2(tab + lgd);
+                const float Dh = a.D ? __ldg(a.D + h0 + hh) : 0.f;
+                // ---- drain
+                ok = wait_warp(wt, kYDFull, ph);
+                if (!ok) break;
+                tc_fence_after_sync();
+                tmem_ld32_nowait(lane_base + kColYD + 64 * hh, reinterpret_cast<uint32_t*>(z));
+                tmem_ld32_nowait(lane_base + kColYD + 64 * hh + 32, reinterpret_cast<uint32_t*>(z + 32));
+                tmem_wait_ld();
+                {
+                    const float2 dd = make_float2(Dh, Dh), ww = make_float2(w, w);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, ch));
+                        uint4 v = *pv;
+                        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float2 xf = unpack_bf16x2(u[m]);
+                            const float2 zz = __ffma2_rn(dd, xf, make_float2(z[8 * ch + 2 * m], z[8 * ch + 2 * m + 1]));
+                            z[8 * ch + 2 * m] = zz.x;
+                            z[8 * ch + 2 * m + 1] = zz.y;
+                            const float2 f = fmul2(xf, ww);
+                            u[m] = pack_bf16x2(f.x, f.y);
+                        }
+                        *pv = v;
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                warp_arrive(wt, kDrained + s);
             }
-            fence_proxy_async_smem();
-            tc_fence_before_sync();
-            warp_arrive(wt, kDrained + s);
             // ---- combine
             ok = wait_warp(wt, kSO, ph);
             if (!ok) break;
@@ -1081,10 +1102,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             tc_fence_before_sync();
             fence_proxy_async_smem();
             warp_arrive(wt, kGBFree + buf);
-            if (32 * q + 32 <= len && !(a.y_accum && !kAccum)) {
+            // (a correction tile replaces the stored y: it already holds every other share)
+            const bool accum = !is_corr && (kAccum || a.y_accum);
+            if (32 * q + 32 <= len && (is_corr || !(a.y_accum && !kAccum))) {
                 // the quadrant's 32 rows all belong to the sequence: one bulk tensor store of 4 KB
                 if (lane == 0) {
-                    if constexpr (kAccum)
+                    if (accum)
                         tma_reduce_add_3d(&maps.y, xr + 32 * q * 128, 0, h0 + hh, row0 + 32 * q);
                     else
                         tma_store_3d(&maps.y, xr + 32 * q * 128, 0, h0 + hh, row0 + 32 * q);
@@ -1094,9 +1117,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             } else if (i < len) {
                 // a partial quadrant: each row from the staging (added in fp32 onto the other state
                 // columns' share when accumulating)
-                store_row(xrow, ix, a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64, kAccum || a.y_accum);
+                store_row(xrow, ix, a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64, accum);
             }
-            warp_arrive(wt, kXFreeC + s);
+            warp_arrive(wt, kXFree + s);
             ++cC;
         }
         if (!ok) set_abort();
@@ -1169,135 +1192,47 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
         // this window's end state decay(w) h_in + agg(w) out, chunk k of it (the aggregate rows are this
         // thread's own stores)
         const int my_slot = slot_of((int)blockIdx.x, a);
-        auto incl_chunk = [&](int k, const float4 (&h)[4], float dec) {
-            const float4* ag = pub_ptr(a.agg, my_slot, k);
-            float4* dst = pub_ptr(a.incl, my_slot, k);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 g = __ldcg(ag + j * 128);
-                __stcg(dst + j * 128, make_float4(fmaf(dec, h[j].x, g.x), fmaf(dec, h[j].y, g.y),
-                                                  fmaf(dec, h[j].z, g.z), fmaf(dec, h[j].w, g.w)));
-            }
-        };
-        auto release_incl = [&]() {
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) st_release_gpu(a.flags + my_slot * 4 + q, 2);
-        };
         // the initial state's row r of sequence s, head pair hp (this launch's columns), or null
         auto init_row_of = [&](int s_, int hp_) -> const float* {
             return a.init ? a.init + (((int64_t)s_ * a.H + 2 * hp_ + hr) * 64 + pr) * a.n_full + a.n_off : nullptr;
         };
-        auto load_init = [&](const float* row, int k, float4 (&h)[4]) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                h[j] = row ? __ldg(reinterpret_cast<const float4*>(row + 16 * k) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        auto final_row_of = [&](int s_, int hp_) -> float* {
+            return a.final_state + (((int64_t)s_ * a.H + 2 * hp_ + hr) * 64 + pr) * a.n_full + a.n_off;
         };
         const int g0 = range_start((int)blockIdx.x, a), g1 = range_start((int)blockIdx.x + 1, a);
-        int p = 0;       // stream position
+        int p = 0;                       // stream position
         if (g1 > g0) {
-            // ---- the last window's aggregate out, when the window ends inside its chain (it opens the
-            // stream); when that window also starts its chain, its end state follows at once
-            const ChainPos cl = decode_at(g1 - 1, a);
-            const bool has_agg = cl.t + 1 < cl.nt;
-            const int l_t0 = cl.t - (g1 - 1 - g0) > 0 ? cl.t - (g1 - 1 - g0) : 0;
-            float wdec = 0.f;    // its total decay
-            if (has_agg) {
-                const int n = cl.t + 1 - l_t0;
-                // the aggregate tiles' tables are not read here, but every role takes part in their release
-                for (int j = 0; j < n && ok; ++j) {
-                    ok = wait_warp(wt, kTblAny + ((p + j) & 1), ph);
-                    if (ok) warp_arrive(wt, kTblRead + ((p + j) & 1));
-                }
-                p += n;
-                ok = ok && wait_warp(wt, kAggDone, ph);
-                if (ok) {
-                    tc_fence_after_sync();
-                    // the window's total decay, left by the table warp with its last aggregate tile (ordered
-                    // before the aggregate's completion through the barriers in between)
-                    wdec = ex2(sm.wtotal()[hr]);
-                    publish(a.agg, my_slot, 1, wdec);
-                    if (l_t0 == 0) {
-                        const float* irow = init_row_of(cl.s, cl.hp);
-#pragma unroll 1
-                        for (int k = 0; k < N / 16; ++k) {
-                            float4 h[4];
-                            load_init(irow, k, h);
-                            incl_chunk(k, h, wdec);
-                        }
-                        release_incl();
-                    }
-                }
-            }
+            // ---- pass 1: the windows, each from its chain's initial state, or from zero when it starts
+            // inside its chain (the first window only; corrected below)
+            ChainPos cf{};
+            int f_t0 = 0, f_t1 = 0;      // the first window's tiles
+            float f_log = 0.f;           // its decay, log2
             for (int g = g0; g < g1 && ok;) {
                 const ChainPos c = decode_at(g, a);
                 const int t0 = c.t, t1 = c.t + (g1 - g) < c.nt ? c.t + (g1 - g) : c.nt;
-                const bool last = g + (t1 - t0) == g1;
-                const int h0 = 2 * c.hp;
-                // ---- the entering state into TMEM: the initial state (or zero) at a chain's start; else
-                // (the first window only) the look-back over the CTAs before this one, whose last windows
-                // are the chain's previous pieces, nearest first: stop at the nearest with its end state
-                // published, or at the one whose window starts the chain (its entering state is the initial
-                // state), then fold their aggregates onto that base, oldest first. Every path gives the same
-                // bits, since a published end state is this same fold done by its own window.
-                constexpr int kMaxFold = 8;
-                int fold[kMaxFold];
-                int nf = 0, base = -1;       // base: the slot whose end state starts the fold, -1 the initial state
-                if (t0 > 0) {
-                    const int cg0 = g - t0;  // run index of the chain's first tile
-                    for (int j = (int)blockIdx.x - 1;; --j) {
-                        if (range_start(j, a) == range_start(j + 1, a)) continue;   // a CTA without tiles
-                        const int sj = slot_of(j, a);
-                        const int f = wait_flag(sj, 1);
-                        if (f == 0) { ok = false; break; }
-                        if (f >= 2) { base = sj; break; }
-                        fold[nf++] = sj;
-                        if (range_start(j, a) <= cg0) break;
-                        if (nf == kMaxFold) {
-                            // a long chain: wait for this one's end state rather than walking further
-                            --nf;
-                            if (wait_flag(sj, 2) == 0) ok = false;
-                            base = sj;
-                            break;
-                        }
-                    }
-                    if (!ok) break;
-                }
-                const float* irow = init_row_of(c.s, c.hp);
-                const bool out_incl = last && has_agg && t0 > 0;
+                const bool first = g == g0, last = g + (t1 - t0) == g1;
+                {
+                    const float* irow = t0 == 0 ? init_row_of(c.s, c.hp) : nullptr;
 #pragma unroll 1
-                for (int k = 0; k < N / 16; ++k) {
-                    float4 h[4];
-                    if (base >= 0) {
-                        const float4* src = pub_ptr(a.incl, base, k);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) h[j] = __ldcg(src + j * 128);
-                    } else {
-                        load_init(irow, k, h);
-                    }
-                    for (int f = nf - 1; f >= 0; --f) {
-                        const float dcy = __ldcg(a.decay + fold[f] * 4 + q);
-                        const float4* src = pub_ptr(a.agg, fold[f], k);
-                        float4 gg[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) gg[j] = __ldcg(src + j * 128);
+                    for (int k = 0; k < N / 16; ++k) {
+                        float4 h[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            h[j] = make_float4(fmaf(dcy, h[j].x, gg[j].x), fmaf(dcy, h[j].y, gg[j].y),
-                                               fmaf(dcy, h[j].z, gg[j].z), fmaf(dcy, h[j].w, gg[j].w));
+                            h[j] = irow ? __ldg(reinterpret_cast<const float4*>(irow + 16 * k) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        tmem_st16(lane_base + kColST + 16 * k, reinterpret_cast<const uint32_t*>(h));
                     }
-                    tmem_st16(lane_base + kColST + 16 * k, reinterpret_cast<const uint32_t*>(h));
-                    if (out_incl) incl_chunk(k, h, wdec);
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
-                if (out_incl) release_incl();
+                float wlog = 0.f;        // the window's decay, log2 (sum of its tiles' totals, in order)
                 // ---- the tiles: h_{t-1} to bf16 for Yo, a_t h_{t-1} back for S(t) to accumulate onto
                 for (int t = t0; t < t1 && ok; ++t, ++p) {
                     const int s = p & 1;
                     ok = wait_warp(wt, kTblAny + s, ph);
                     if (!ok) break;
-                    const float at = ex2(sm.cs(s)[256 + 4 * hr + 3]);
+                    const float tl = sm.cs(s)[256 + 4 * hr + 3];
                     warp_arrive(wt, kTblRead + s);
+                    wlog += tl;
+                    const float at = ex2(tl);
                     ok = t == t0 || wait_warp(wt, kSO, ph);
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -1331,12 +1266,14 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     warp_arrive(wt, kState);
                 }
                 if (!ok) break;
-                // ---- the window's end: the last S, then a chain's final state out
+                // ---- the window's end: the last S, then its end state out -- a chain's final state, and
+                // the state the next CTA looks back for when the window ends inside its chain (1: from a
+                // zero start, to be folded; 2: from the chain's start, the true state)
                 ok = wait_warp(wt, kSO, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
                 if (t1 == c.nt && a.final_state) {
-                    float* fp = a.final_state + (((int64_t)c.s * a.H + h0 + hr) * 64 + pr) * a.n_full + a.n_off;
+                    float* fp = final_row_of(c.s, c.hp);
 #pragma unroll 1
                     for (int k = 0; k < N / 16; ++k) {
                         uint32_t v[16];
@@ -1349,9 +1286,124 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     }
                 }
+                if (last && t1 < c.nt) {
+                    if (t0 > 0) publish(a.agg, my_slot, 1, ex2(wlog));
+                    else publish(a.incl, my_slot, 2, 0.f);
+                }
+                if (first) { cf = c; f_t0 = t0; f_t1 = t1; f_log = wlog; }
                 // (the next window's entering state overwrites the state columns: its S waits for it)
                 tc_fence_before_sync();
                 g += t1 - t0;
+            }
+            // ---- the first window's entering state, when it starts inside its chain: the look-back over
+            // the CTAs before this one, whose last windows are the chain's previous pieces, nearest first:
+            // stop at the nearest with its true end state published, or at the one whose window starts the
+            // chain (its entering state is the initial state), then fold their zero-start end states onto
+            // that base, oldest first. Every path gives the same bits, since a published true end state is
+            // this same fold, done by its window. h_in then goes to shared memory (bf16) for the correction
+            // products, onto the final state when the window ends its chain, and, when the window also ends
+            // this range inside its chain, into this window's own true end state.
+            if (ok && f_t0 > 0) {
+                constexpr int kMaxFold = 8;
+                int fold[kMaxFold];
+                int nf = 0, base = -1;       // base: the slot whose end state starts the fold, -1 the initial state
+                const int cg0 = g0 - f_t0;   // run index of the chain's first tile
+                for (int j = (int)blockIdx.x - 1;; --j) {
+                    if (range_start(j, a) == range_start(j + 1, a)) continue;   // a CTA without tiles
+                    const int sj = slot_of(j, a);
+                    const int f = wait_flag(sj, 1);
+                    if (f == 0) { ok = false; break; }
+                    if (f >= 2) { base = sj; break; }
+                    fold[nf++] = sj;
+                    if (range_start(j, a) <= cg0) break;
+                    if (nf == kMaxFold) {
+                        // a long chain: wait for this one's true end state rather than walking further
+                        --nf;
+                        if (wait_flag(sj, 2) == 0) ok = false;
+                        base = sj;
+                        break;
+                    }
+                }
+                if (ok) {
+                    const float* irow = init_row_of(cf.s, cf.hp);
+                    const bool fin = f_t1 == cf.nt && a.final_state;
+                    const bool out_incl = f_t1 < cf.nt;      // (then the first window is also the last)
+                    const float fdec = ex2(f_log);
+                    float* frow = fin ? final_row_of(cf.s, cf.hp) : nullptr;
+#pragma unroll 1
+                    for (int k = 0; k < N / 16; ++k) {
+                        float4 h[4];
+                        if (base >= 0) {
+                            const float4* src = pub_ptr(a.incl, base, k);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) h[j] = __ldcg(src + j * 128);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                h[j] = irow ? __ldg(reinterpret_cast<const float4*>(irow + 16 * k) + j)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        for (int f = nf - 1; f >= 0; --f) {
+                            const float dcy = __ldcg(a.decay + fold[f] * 4 + q);
+                            const float4* src = pub_ptr(a.agg, fold[f], k);
+                            float4 gg[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) gg[j] = __ldcg(src + j * 128);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                h[j] = make_float4(fmaf(dcy, h[j].x, gg[j].x), fmaf(dcy, h[j].y, gg[j].y),
+                                                   fmaf(dcy, h[j].z, gg[j].z), fmaf(dcy, h[j].w, gg[j].w));
+                        }
+                        // h_in as bf16 for the correction products
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int n = 16 * k + 8 * cc;
+                            uint4 pk;
+                            pk.x = pack_bf16x2(h[2 * cc].x, h[2 * cc].y);
+                            pk.y = pack_bf16x2(h[2 * cc].z, h[2 * cc].w);
+                            pk.z = pack_bf16x2(h[2 * cc + 1].x, h[2 * cc + 1].y);
+                            pk.w = pack_bf16x2(h[2 * cc + 1].z, h[2 * cc + 1].w);
+                            *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(r, (n % 64) / 8)) = pk;
+                        }
+                        if (fin) {
+                            // the chain's final state from its zero-start value (this thread's own stores)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                float4* fp4 = reinterpret_cast<float4*>(frow + 16 * k + 4 * j);
+                                const float4 o = *fp4;
+                                *fp4 = make_float4(fmaf(fdec, h[j].x, o.x), fmaf(fdec, h[j].y, o.y),
+                                                   fmaf(fdec, h[j].z, o.z), fmaf(fdec, h[j].w, o.w));
+                            }
+                        }
+                        if (out_incl) {
+                            // this window's true end state, decay * h_in + its zero-start end state
+                            const float4* ag = pub_ptr(a.agg, my_slot, k);
+                            float4* dst = pub_ptr(a.incl, my_slot, k);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float4 gg = __ldcg(ag + j * 128);
+                                __stcg(dst + j * 128, make_float4(fmaf(fdec, h[j].x, gg.x), fmaf(fdec, h[j].y, gg.y),
+                                                                  fmaf(fdec, h[j].z, gg.z), fmaf(fdec, h[j].w, gg.w)));
+                            }
+                        }
+                    }
+                    if (out_incl) {
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) st_release_gpu(a.flags + my_slot * 4 + q, 2);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before_sync();
+                    warp_arrive(wt, kState);
+                    // the correction tiles' tables are not read here, but every role takes part in their
+                    // release
+                    ok = __all_sync(0xffffffffu, wait_par(wt, kNcorr, 0u));
+                    const int nc = ok ? *sm.ncorr() : 0;
+                    for (int j = 0; j < nc && ok; ++j, ++p) {
+                        ok = wait_warp(wt, kTblAny + (p & 1), ph);
+                        if (ok) warp_arrive(wt, kTblRead + (p & 1));
+                    }
+                }
             }
         }
         if (!ok) set_abort();
