@@ -214,7 +214,8 @@ struct Lay {
     static constexpr uint32_t kRec = kVt + 2 * kVtCols * 2;            // [2] tile records (int4)
     static constexpr uint32_t kBars = kRec + 2 * 16;                   // [kNumBars] u64
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag, correction count
-    static constexpr uint32_t kTotal = kMisc + 16;
+    static constexpr uint32_t kFold = kMisc + 16;                      // [4][8] slots, [4][8] decays
+    static constexpr uint32_t kTotal = kFold + 256;
     static_assert(kBars % 8 == 0, "barriers are 8-byte aligned");
     static_assert(kTotal <= 232448, "shared memory per CTA");
 };
@@ -240,6 +241,9 @@ struct Smem {
     __device__ int* abort_flag() const { return reinterpret_cast<int*>(base + Lay<N>::kMisc + 4); }
     // the number of correction tiles (written once by the table warp, see Stream)
     __device__ volatile int* ncorr() const { return reinterpret_cast<volatile int*>(base + Lay<N>::kMisc + 8); }
+    // a state warp's look-back: the slots folded onto the base and their decays, per lane quadrant
+    __device__ int* fold_slot(int q) const { return reinterpret_cast<int*>(base + Lay<N>::kFold) + 8 * q; }
+    __device__ float* fold_dec(int q) const { return reinterpret_cast<float*>(base + Lay<N>::kFold + 128) + 8 * q; }
 };
 
 // ---------------------------------------------------------------- bounded waits
@@ -1305,7 +1309,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             // this range inside its chain, into this window's own true end state.
             if (ok && f_t0 > 0) {
                 constexpr int kMaxFold = 8;
-                int fold[kMaxFold];
+                int* fold = sm.fold_slot(q);  // (shared memory: read in the loop below without a round trip)
                 int nf = 0, base = -1;       // base: the slot whose end state starts the fold, -1 the initial state
                 const int cg0 = g0 - f_t0;   // run index of the chain's first tile
                 for (int j = (int)blockIdx.x - 1;; --j) {
@@ -1314,7 +1318,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     const int f = wait_flag(sj, 1);
                     if (f == 0) { ok = false; break; }
                     if (f >= 2) { base = sj; break; }
-                    fold[nf++] = sj;
+                    if (lane == 0) fold[nf] = sj;
+                    ++nf;
                     if (range_start(j, a) <= cg0) break;
                     if (nf == kMaxFold) {
                         // a long chain: wait for this one's true end state rather than walking further
@@ -1325,66 +1330,90 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
                 }
                 if (ok) {
+                    // the folded slots' decays, once
+                    __syncwarp();
+                    if (lane < nf) sm.fold_dec(q)[lane] = __ldcg(a.decay + fold[lane] * 4 + q);
+                    __syncwarp();
+                    const float* fdecs = sm.fold_dec(q);
                     const float* irow = init_row_of(cf.s, cf.hp);
                     const bool fin = f_t1 == cf.nt && a.final_state;
                     const bool out_incl = f_t1 < cf.nt;      // (then the first window is also the last)
                     const float fdec = ex2(f_log);
                     float* frow = fin ? final_row_of(cf.s, cf.hp) : nullptr;
+                    // 8 state columns at a time. Every load of a column group (the base, up to four folded
+                    // states, this thread's own final-state and zero-start end-state values) goes out before
+                    // any of them is used, so that a group costs about one round trip to L2.
 #pragma unroll 1
-                    for (int k = 0; k < N / 16; ++k) {
-                        float4 h[4];
+                    for (int k8 = 0; k8 < N / 8; ++k8) {
+                        const int ck = k8 >> 1, j0 = 2 * (k8 & 1);
+                        float4 h[2], fo[2], ow[2];
                         if (base >= 0) {
-                            const float4* src = pub_ptr(a.incl, base, k);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) h[j] = __ldcg(src + j * 128);
+                            const float4* src = pub_ptr(a.incl, base, ck) + j0 * 128;
+                            h[0] = __ldcg(src);
+                            h[1] = __ldcg(src + 128);
+                        } else if (irow) {
+                            h[0] = __ldg(reinterpret_cast<const float4*>(irow + 8 * k8));
+                            h[1] = __ldg(reinterpret_cast<const float4*>(irow + 8 * k8) + 1);
                         } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                h[j] = irow ? __ldg(reinterpret_cast<const float4*>(irow + 16 * k) + j)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                            h[0] = h[1] = make_float4(0.f, 0.f, 0.f, 0.f);
                         }
-                        for (int f = nf - 1; f >= 0; --f) {
-                            const float dcy = __ldcg(a.decay + fold[f] * 4 + q);
-                            const float4* src = pub_ptr(a.agg, fold[f], k);
-                            float4 gg[4];
+                        if (fin) {
+                            fo[0] = __ldcg(reinterpret_cast<const float4*>(frow + 8 * k8));
+                            fo[1] = __ldcg(reinterpret_cast<const float4*>(frow + 8 * k8) + 1);
+                        }
+                        if (out_incl) {
+                            const float4* ag = pub_ptr(a.agg, my_slot, ck) + j0 * 128;
+                            ow[0] = __ldcg(ag);
+                            ow[1] = __ldcg(ag + 128);
+                        }
+                        for (int f0 = nf - 1; f0 >= 0; f0 -= 4) {
+                            float dcy[4];
+                            float4 gg[4][2];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) gg[j] = __ldcg(src + j * 128);
+                            for (int u = 0; u < 4; ++u) {
+                                if (f0 - u >= 0) {
+                                    const int sl = fold[f0 - u];
+                                    dcy[u] = fdecs[f0 - u];
+                                    const float4* src = pub_ptr(a.agg, sl, ck) + j0 * 128;
+                                    gg[u][0] = __ldcg(src);
+                                    gg[u][1] = __ldcg(src + 128);
+                                }
+                            }
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                h[j] = make_float4(fmaf(dcy, h[j].x, gg[j].x), fmaf(dcy, h[j].y, gg[j].y),
-                                                   fmaf(dcy, h[j].z, gg[j].z), fmaf(dcy, h[j].w, gg[j].w));
+                            for (int u = 0; u < 4; ++u) {
+                                if (f0 - u >= 0) {
+#pragma unroll
+                                    for (int jj = 0; jj < 2; ++jj)
+                                        h[jj] = make_float4(fmaf(dcy[u], h[jj].x, gg[u][jj].x), fmaf(dcy[u], h[jj].y, gg[u][jj].y),
+                                                            fmaf(dcy[u], h[jj].z, gg[u][jj].z), fmaf(dcy[u], h[jj].w, gg[u][jj].w));
+                                }
+                            }
                         }
                         // h_in as bf16 for the correction products
-#pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int n = 16 * k + 8 * cc;
+                        {
+                            const int n = 8 * k8;
                             uint4 pk;
-                            pk.x = pack_bf16x2(h[2 * cc].x, h[2 * cc].y);
-                            pk.y = pack_bf16x2(h[2 * cc].z, h[2 * cc].w);
-                            pk.z = pack_bf16x2(h[2 * cc + 1].x, h[2 * cc + 1].y);
-                            pk.w = pack_bf16x2(h[2 * cc + 1].z, h[2 * cc + 1].w);
+                            pk.x = pack_bf16x2(h[0].x, h[0].y);
+                            pk.y = pack_bf16x2(h[0].z, h[0].w);
+                            pk.z = pack_bf16x2(h[1].x, h[1].y);
+                            pk.w = pack_bf16x2(h[1].z, h[1].w);
                             *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(r, (n % 64) / 8)) = pk;
                         }
                         if (fin) {
                             // the chain's final state from its zero-start value (this thread's own stores)
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                float4* fp4 = reinterpret_cast<float4*>(frow + 16 * k + 4 * j);
-                                const float4 o = *fp4;
-                                *fp4 = make_float4(fmaf(fdec, h[j].x, o.x), fmaf(fdec, h[j].y, o.y),
-                                                   fmaf(fdec, h[j].z, o.z), fmaf(fdec, h[j].w, o.w));
-                            }
+                            for (int jj = 0; jj < 2; ++jj)
+                                reinterpret_cast<float4*>(frow + 8 * k8)[jj] =
+                                    make_float4(fmaf(fdec, h[jj].x, fo[jj].x), fmaf(fdec, h[jj].y, fo[jj].y),
+                                                fmaf(fdec, h[jj].z, fo[jj].z), fmaf(fdec, h[jj].w, fo[jj].w));
                         }
                         if (out_incl) {
                             // this window's true end state, decay * h_in + its zero-start end state
-                            const float4* ag = pub_ptr(a.agg, my_slot, k);
-                            float4* dst = pub_ptr(a.incl, my_slot, k);
+                            float4* dst = pub_ptr(a.incl, my_slot, ck) + j0 * 128;
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float4 gg = __ldcg(ag + j * 128);
-                                __stcg(dst + j * 128, make_float4(fmaf(fdec, h[j].x, gg.x), fmaf(fdec, h[j].y, gg.y),
-                                                                  fmaf(fdec, h[j].z, gg.z), fmaf(fdec, h[j].w, gg.w)));
-                            }
+                            for (int jj = 0; jj < 2; ++jj)
+                                __stcg(dst + jj * 128, make_float4(fmaf(fdec, h[jj].x, ow[jj].x), fmaf(fdec, h[jj].y, ow[jj].y),
+                                                                   fmaf(fdec, h[jj].z, ow[jj].z), fmaf(fdec, h[jj].w, ow[jj].w)));
                         }
                     }
                     if (out_incl) {
