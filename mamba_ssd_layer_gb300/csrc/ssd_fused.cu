@@ -908,7 +908,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     }
 #pragma unroll
                     for (int gg = 0; gg < 2; ++gg) {     // the block's two 16-column groups
-#pragma unroll
+#pragma unroll 1  // (a rolled loop: the code of every role's per-tile path shares the instruction cache)
                         for (int hh = 0; hh < 2; ++hh) {  // head 0's 8 packed columns, then head 1's
                             uint32_t pk[8];
                             const float ci = hh ? ci1 : ci0;
