@@ -92,14 +92,16 @@ enum : int {
     kYDFull = 20,    // Yd in TMEM
     kState = 21,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM (correction: h_in staged): 4 state warps
     kSO = 22,        // S(t) and Yo(t) done (correction: the correction product done)
-    kVTFree = 23,    // the factored-mask table read: 4 mask warps
+    kVTFree = 23,    // the factored-mask table read (off-diagonal blocks done): 4 mask warps
     kNcorr = 24,     // the correction tile count written (table warp, once)
     kMmaDone = 25,   // the MMA warp's final drain
-    kNumBars = 26
+    kYDFree = 26,    // the tile's z (held in the Yd columns) read by the combine: 8 epilogue warps
+    kNumBars = 27
 };
 
 __host__ __device__ constexpr uint32_t bar_count(int i) {
-    return ((i >= kXFree && i < kXFree + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2))
+    return ((i >= kXFree && i < kXFree + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2) ||
+            i == kYDFree)
                ? 8u
          : (i >= kTblRead && i < kTblRead + 2) ? 16u
          : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree) ? 4u
@@ -197,8 +199,8 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(
 
 // Per-warpgroup register budgets (setmaxnreg): the launch gives every thread kLaunchRegs; the
 // producer / MMA / tables warpgroup and the mask warpgroup hand some back and the two epilogue
-// warpgroups take them. 128 (56 + 88 + 96) + 256 * 120 = 640 * 96.
-constexpr uint32_t kLaunchRegs = 96, kRegsWG0 = 56, kRegsMask = 88, kRegsEpi = 120;
+// warpgroups take them: 128 (80 + 88 + 96) + 256 * 96 <= 640 * 96.
+constexpr uint32_t kLaunchRegs = 96, kRegsWG0 = 80, kRegsMask = 88, kRegsEpi = 96;
 static_assert(128 * (kRegsWG0 + kRegsMask + kLaunchRegs) + 256 * kRegsEpi <= 640 * kLaunchRegs, "register split");
 template <uint32_t R> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(R)); }
 template <uint32_t R> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(R)); }
@@ -210,7 +212,7 @@ struct Lay {
     static constexpr uint32_t kStage = (2 + 2 * NB) * kRegion;         // x (2 heads), B, C
     static constexpr uint32_t kHS = 2 * kStage;                        // h_{t-1} in bf16 for Yo
     static constexpr uint32_t kCs = kHS + NB * kRegion;                // [2][kCsStride] floats
-    static constexpr uint32_t kVt = kCs + 2 * kCsStride * 4;           // [2][kVtCols] halves
+    static constexpr uint32_t kVt = kCs + 2 * kCsStride * 4;           // [2 heads][kVtCols] halves
     static constexpr uint32_t kRec = kVt + 2 * kVtCols * 2;            // [2] tile records (int4)
     static constexpr uint32_t kBars = kRec + 2 * 16;                   // [kNumBars] u64
     static constexpr uint32_t kMisc = kBars + kNumBars * 8;            // tmem slot, abort flag, correction count
@@ -645,7 +647,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 };
                 // Yd(t), both heads interleaved: needs L o G(t) and x(t); the previous tile's Yd has been
                 // drained (its Drained phase was waited for before its S)
-                ok = poll_bar(wt, kLGFull + buf, ph, try_g_next) && wait_bar(wt, kFullX + s, ph);
+                ok = poll_bar(wt, kLGFull + buf, ph, try_g_next) && wait_bar(wt, kFullX + s, ph) &&
+                     (cC == 0 || wait_bar(wt, kYDFree, ph));
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t gb = kColGB + 128 * buf;
@@ -787,7 +790,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
             if (!corr) {
                 // v_j = exp(cs_p - table_j), p the last token of j's 32-token block (j < 96), computed before
-                // the mask warps release the table so that only the stores follow the release
+                // the mask warps release the table (after their off-diagonal blocks) so that only the
+                // stores follow the release
                 __half2 vv[2][2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -884,6 +888,7 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) zero[e] = 0u;
             if (!__any_sync(0xffffffffu, rv)) {
+                if (lane == 0) mbar_arrive(sm.bars() + kVTFree);
 #pragma unroll
                 for (int g = 0; g < 8; ++g) { tmem_st8(gcol + 16 * g, zero); tmem_st8(gcol + 16 * g + 8, zero); }
             } else {
@@ -895,6 +900,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                         tmem_st8(gcol + 32 * b + 16, zero);
                         tmem_st8(gcol + 32 * b + 24, zero);
                         continue;
+                    }
+                    if (b == q) {
+                        // the off-diagonal blocks are done: the next tile's column table may be written
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(sm.bars() + kVTFree);
                     }
                     uint32_t gr[32];
                     tmem_ld16_nowait(gcol + 32 * b, gr);
@@ -961,7 +971,6 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(sm.bars() + kLGFull + buf);
-                mbar_arrive(sm.bars() + kVTFree);
                 mbar_arrive(sm.bars() + kTblRead + s);
             }
             ++cC;
@@ -1005,7 +1014,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             uint8_t* const xr = sm.x(s, hh);
             uint8_t* const xrow = xr + i * 128;
             const int buf = cC & 1;
-            float z[64];
+            // z = Yd + D x of this row (64 columns), kept in TMEM in place of Yd until the combine
+            const uint32_t zcol = lane_base + kColYD + 64 * hh;
             float e_row;
             if (is_corr) {
                 // (this warp is done with the previous position, its SO wait included)
@@ -1020,23 +1030,23 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     __syncwarp();
                     y_visible = true;
                 }
-                if (i < len) {
-                    const uint4* yr = reinterpret_cast<const uint4*>(a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64);
+                // z = that y, into the z columns (no Yd product follows a correction tile)
+                const uint4* yr = reinterpret_cast<const uint4*>(a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64);
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        const uint4 v = yr[ch];
-                        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (i < len) v = yr[ch];
+                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+                    uint32_t f[8];
 #pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const float2 f = unpack_bf16x2(u[m]);
-                            z[8 * ch + 2 * m] = f.x;
-                            z[8 * ch + 2 * m + 1] = f.y;
-                        }
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 ff = unpack_bf16x2(u[m]);
+                        f[2 * m] = __float_as_uint(ff.x);
+                        f[2 * m + 1] = __float_as_uint(ff.y);
                     }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) z[e] = 0.f;
+                    tmem_st8(zcol + 8 * ch, f);
                 }
+                tmem_wait_st();
                 e_row = (i < len) ? ex2(tab) : 0.f;
             } else {
                 ok = wait_warp(wt, kFullX + s, ph);
@@ -1044,32 +1054,36 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                 const float w = (i < len) ? ex2(last - tab) : 0.f;
                 e_row = ex2(tab + lgd);
                 const float Dh = a.D ? __ldg(a.D + h0 + hh) : 0.f;
-                // ---- drain
+                // ---- drain: z = Yd + D x back into the Yd columns, the x row times w in place
                 ok = wait_warp(wt, kYDFull, ph);
                 if (!ok) break;
                 tc_fence_after_sync();
-                tmem_ld32_nowait(lane_base + kColYD + 64 * hh, reinterpret_cast<uint32_t*>(z));
-                tmem_ld32_nowait(lane_base + kColYD + 64 * hh + 32, reinterpret_cast<uint32_t*>(z + 32));
-                tmem_wait_ld();
-                {
-                    const float2 dd = make_float2(Dh, Dh), ww = make_float2(w, w);
+                const float2 dd = make_float2(Dh, Dh), ww = make_float2(w, w);
+#pragma unroll 1  // (rolled: the code of every role's per-tile path shares the instruction cache)
+                for (int c16 = 0; c16 < 4; ++c16) {
+                    uint32_t zv[16];
+                    tmem_ld16_nowait(zcol + 16 * c16, zv);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, ch));
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint4* pv = reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, 2 * c16 + cc));
                         uint4 v = *pv;
                         uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
+                            const int e = 8 * cc + 2 * m;
                             const float2 xf = unpack_bf16x2(u[m]);
-                            const float2 zz = __ffma2_rn(dd, xf, make_float2(z[8 * ch + 2 * m], z[8 * ch + 2 * m + 1]));
-                            z[8 * ch + 2 * m] = zz.x;
-                            z[8 * ch + 2 * m + 1] = zz.y;
+                            const float2 zz = __ffma2_rn(dd, xf, make_float2(__uint_as_float(zv[e]), __uint_as_float(zv[e + 1])));
+                            zv[e] = __float_as_uint(zz.x);
+                            zv[e + 1] = __float_as_uint(zz.y);
                             const float2 f = fmul2(xf, ww);
                             u[m] = pack_bf16x2(f.x, f.y);
                         }
                         *pv = v;
                     }
+                    tmem_st16(zcol + 16 * c16, zv);
                 }
+                tmem_wait_st();
                 fence_proxy_async_smem();
                 tc_fence_before_sync();
                 warp_arrive(wt, kDrained + s);
@@ -1081,31 +1095,31 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             {
                 const float2 ee = make_float2(e_row, e_row);
                 const uint32_t yo_col = lane_base + kColGB + 128 * buf + 64 * hh;
-                // two 32-column loads (one TMEM round trip each) against the 64 z values in registers
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t yo[32];
-                    tmem_ld32_nowait(yo_col + 32 * half, yo);
+#pragma unroll 1
+                for (int c16 = 0; c16 < 4; ++c16) {
+                    uint32_t zv[16], yo[16];
+                    tmem_ld16_nowait(zcol + 16 * c16, zv);
+                    tmem_ld16_nowait(yo_col + 16 * c16, yo);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int k = 4 * half + kk;
+                    for (int cc = 0; cc < 2; ++cc) {
                         uint4 v;
                         uint32_t* vu = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
-                            const float2 r = __ffma2_rn(
-                                ee, make_float2(__uint_as_float(yo[8 * kk + 2 * m]), __uint_as_float(yo[8 * kk + 2 * m + 1])),
-                                make_float2(z[8 * k + 2 * m], z[8 * k + 2 * m + 1]));
+                            const int e = 8 * cc + 2 * m;
+                            const float2 r = __ffma2_rn(ee, make_float2(__uint_as_float(yo[e]), __uint_as_float(yo[e + 1])),
+                                                        make_float2(__uint_as_float(zv[e]), __uint_as_float(zv[e + 1])));
                             vu[m] = pack_bf16x2(r.x, r.y);
                         }
-                        *reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, k)) = v;
+                        *reinterpret_cast<uint4*>(chunk_ptr(xrow, ix, 2 * c16 + cc)) = v;
                     }
                 }
             }
             tc_fence_before_sync();
             fence_proxy_async_smem();
             warp_arrive(wt, kGBFree + buf);
+            if (!is_corr) warp_arrive(wt, kYDFree);
             // (a correction tile replaces the stored y: it already holds every other share)
             const bool accum = !is_corr && (kAccum || a.y_accum);
             if (32 * q + 32 <= len && (is_corr || !(a.y_accum && !kAccum))) {
