@@ -43,10 +43,13 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 240262656 + 149278464, "stamp": "020e1f5835ff3b16"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 218742784 + 149128192, "stamp": "e69bfc6f948fd355"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 457100800 + 177253760, "stamp": "532861e9adad5c2b"},
-    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 375994112 + 182185472, "stamp": "532861e9adad5c2b"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 296367232 + 144798720, "stamp": "e69bfc6f948fd355"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 210029568 + 149562368, "stamp": "e69bfc6f948fd355"},
+    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 68816384 + 26795520, "stamp": "e69bfc6f948fd355"},
+    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 216609792 + 155288320, "stamp": "e69bfc6f948fd355"},
+    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 179837184 + 122071040, "stamp": "e69bfc6f948fd355"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
     "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168495104 + 117637120, "stamp": "154fb82720b02848"},
     "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609280 + 34404352,
