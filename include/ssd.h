@@ -78,7 +78,8 @@ size_t ssd_workspace_size(const ssd_shape *shape, ssd_dtype dtype, int chunk, in
  *   B, C          (batch, seqlen, G, N)  dtype
  *   D             (H)                    fp32, or NULL for no skip term
  *   chunk         block length Q of the decomposition: 64, 128 or 256. The result does not
- *                 depend on it beyond rounding; it sets the granularity of the state pass.
+ *                 depend on it beyond rounding. The fp32 path uses it as its block length; the
+ *                 bf16 path validates it and otherwise ignores it (its tile is always 128 tokens).
  *   initial_state (nseq_or_batch, H, P, N) fp32, or NULL for zero states
  *   cu_seqlens    (nseq + 1) int32 DEVICE array of segment offsets into the packed row
  *                 (first 0, last seqlen, non-decreasing), or NULL for a dense batch.
