@@ -43,13 +43,15 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 218742784 + 149128192, "stamp": "e69bfc6f948fd355"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 217451264 + 149019648, "stamp": "0d8ccc6fd48c2fca"},
+    "long_n64": {"kernel": "ssd_fused_kernel", "bytes": 201287424 + 140782848, "stamp": "0d8ccc6fd48c2fca"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 296367232 + 144798720, "stamp": "e69bfc6f948fd355"},
-    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 210029568 + 149562368, "stamp": "e69bfc6f948fd355"},
-    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 68816384 + 26795520, "stamp": "e69bfc6f948fd355"},
-    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 216609792 + 155288320, "stamp": "e69bfc6f948fd355"},
-    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 179837184 + 122071040, "stamp": "e69bfc6f948fd355"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 295571328 + 144533120, "stamp": "0d8ccc6fd48c2fca"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 209037568 + 149345024, "stamp": "0d8ccc6fd48c2fca"},
+    # y (50 MB) largely still in L2 when the launch ends
+    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 60473856 + 12647680, "stamp": "0d8ccc6fd48c2fca"},
+    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 214944768 + 154399232, "stamp": "0d8ccc6fd48c2fca"},
+    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 178471936 + 121808128, "stamp": "0d8ccc6fd48c2fca"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
     "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168495104 + 117637120, "stamp": "154fb82720b02848"},
     "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609280 + 34404352,
