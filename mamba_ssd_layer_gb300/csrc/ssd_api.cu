@@ -206,13 +206,67 @@ int ssd_forward(const ssd_shape* s, ssd_dtype dtype, const void* x, const float*
                           workspace, workspace_bytes, stream);
 }
 
+namespace {
+
+// The host entry point on a large dense bf16 batch runs as a pipeline of pieces, so that the copies in
+// of piece k + 1, the forward of piece k and the copies out of piece k - 1 overlap (the copy engines
+// move both directions at once): batch rows when there are several, else time slices of the one
+// sequence, joined by the sequence-parallel hand-off ("LLM(十一)——Mamba" §3.7.2): every slice after the
+// first runs from a zero state and is corrected for the state its predecessor ends with.
+struct HostPlan {
+    int K = 1;              // pieces; 1: one piece, no pipeline
+    bool time = false;      // time slices of one sequence (else groups of batch rows)
+    int64_t len = 0;        // batch rows per piece, or tokens per slice (a multiple of the 128-token tile)
+};
+
+constexpr int kHostPieces = 4;
+constexpr int64_t kHostPipelineBytes = int64_t(32) << 20;   // x bytes below which one piece is used
+
+HostPlan host_plan(const ssd_shape& s, ssd_dtype dtype, bool varlen) {
+    HostPlan h;
+    if (dtype != SSD_BF16 || varlen || !use_fused_path(s, dtype)) return h;
+    if (s.batch * s.seqlen * s.nheads * s.headdim * 2 < kHostPipelineBytes) return h;
+    if (s.batch >= 2) {
+        h.len = (s.batch + kHostPieces - 1) / kHostPieces;
+        h.K = (int)((s.batch + h.len - 1) / h.len);
+    } else if (s.seqlen >= kHostPieces * 1024) {
+        h.time = true;
+        h.len = ((s.seqlen + kHostPieces - 1) / kHostPieces + 127) / 128 * 128;
+        h.K = (int)((s.seqlen + h.len - 1) / h.len);
+    }
+    return h;
+}
+
+// the shape of the largest piece
+ssd_shape piece_shape(const ssd_shape& s, const HostPlan& h) {
+    ssd_shape p = s;
+    if (h.K > 1) {
+        if (h.time) p.seqlen = h.len;
+        else p.batch = h.len;
+    }
+    return p;
+}
+
+}  // namespace
+
 size_t ssd_host_buffer_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int nseq) {
-    const size_t ws = ssd_workspace_size(s, dtype, chunk, nseq);
-    if (!ws) return 0;
+    const size_t ws1 = ssd_workspace_size(s, dtype, chunk, nseq);
+    if (!ws1) return 0;
     const int64_t rows = s->batch * s->seqlen;
     const int64_t nseq_eff = nseq > 0 ? nseq : s->batch;
     const size_t e = elt(dtype);
-    size_t tot = ws;
+    const HostPlan h = host_plan(*s, dtype, nseq > 0);
+    size_t tot = 0;
+    if (h.K > 1) {
+        const ssd_shape ps = piece_shape(*s, h);
+        tot += align256(ssd_workspace_size(&ps, dtype, chunk, 0)) * h.K;    // one workspace per piece
+        if (h.time) {
+            tot += align256(ssd_slice_workspace_size(&ps)) * h.K;           // the slices' corrections
+            tot += align256(s->nheads * s->headdim * s->dstate * 4) * h.K;  // every slice's final state
+        }
+    } else {
+        tot += ws1;
+    }
     tot += align256(rows * s->nheads * s->headdim * e) * 2;                 // x, y
     tot += align256(rows * s->nheads * 4);                                  // dt
     tot += align256(s->nheads * 4) * 2;                                     // A, D
@@ -221,6 +275,133 @@ size_t ssd_host_buffer_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int 
     tot += align256((nseq_eff + 1) * 4);                                    // cu_seqlens
     return tot;
 }
+
+namespace {
+
+// The pipelined host call (see HostPlan). The caller's stream runs the forwards; one internal stream
+// copies in and one copies out, ordered by events; everything is finished when it returns.
+int host_pipelined(const ssd_shape* s, const HostPlan& h, unsigned flags, const void* x, const float* dt,
+                   const float* A, const void* B, const void* C, const float* D, int chunk,
+                   const float* initial_state, void* y, float* final_state, char* base, cudaStream_t st) {
+    const int64_t H = s->nheads, P = s->headdim, N = s->dstate, G = s->ngroups, T = s->seqlen;
+    const size_t e = 2;
+    const size_t xrow = (size_t)H * P * e, dtrow = (size_t)H * 4, bcrow = (size_t)G * N * e;
+    const size_t st1 = (size_t)H * P * N * 4;     // one sequence's state
+    const int64_t rows = s->batch * T;
+    size_t off = 0;
+    auto carve = [&](size_t bytes) { char* p = base + off; off += align256(bytes); return p; };
+    const ssd_shape ps = piece_shape(*s, h);
+    const size_t wsb = ssd_workspace_size(&ps, SSD_BF16, chunk, 0);
+    const size_t swsb = h.time ? ssd_slice_workspace_size(&ps) : 0;
+    std::vector<char*> ws(h.K), sws(h.K, nullptr), fin(h.K, nullptr);
+    for (int k = 0; k < h.K; ++k) ws[k] = carve(wsb);
+    if (h.time)
+        for (int k = 0; k < h.K; ++k) { sws[k] = carve(swsb); fin[k] = carve(st1); }
+    char* dx = carve(rows * xrow);
+    char* dy = carve(rows * xrow);
+    char* ddt = carve(rows * dtrow);
+    char* dA = carve(H * 4);
+    char* dD = carve(H * 4);
+    char* dB = carve(rows * bcrow);
+    char* dC = carve(rows * bcrow);
+    char* dinit = carve(s->batch * st1);
+    char* dfinal = carve(s->batch * st1);
+
+    cudaStream_t si = nullptr, so = nullptr;
+    std::vector<cudaEvent_t> ev(2 * h.K + 1, nullptr);
+    cudaError_t err = cudaStreamCreateWithFlags(&si, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&so, cudaStreamNonBlocking);
+    for (auto& v : ev)
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    int rc = SSD_OK;
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && src && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si);
+    };
+    auto d2h = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && dst && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, so);
+    };
+    // the copies in wait for the caller's earlier work on its stream (it may still use the buffer)
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], st);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(si, ev[0], 0);
+    h2d(dA, A, H * 4);
+    h2d(dD, D, H * 4);
+    h2d(dinit, initial_state, s->batch * st1);
+    // piece k: rows [r0, r0 + nr) of the (batch x time) row order, sequences [q0, q0 + nq)
+    auto piece = [&](int k, int64_t* r0, int64_t* nr, int64_t* q0, ssd_shape* pk) {
+        *pk = *s;
+        const int64_t a0 = k * h.len;
+        if (h.time) {
+            pk->seqlen = T - a0 < h.len ? T - a0 : h.len;
+            *r0 = a0; *nr = pk->seqlen; *q0 = 0;
+        } else {
+            pk->batch = s->batch - a0 < h.len ? s->batch - a0 : h.len;
+            *r0 = a0 * T; *nr = pk->batch * T; *q0 = a0;
+        }
+    };
+    for (int k = 0; k < h.K; ++k) {
+        int64_t r0, nr, q0;
+        ssd_shape pk;
+        piece(k, &r0, &nr, &q0, &pk);
+        h2d(dx + r0 * xrow, static_cast<const char*>(x) + r0 * xrow, nr * xrow);
+        h2d(ddt + r0 * dtrow, reinterpret_cast<const char*>(dt) + r0 * dtrow, nr * dtrow);
+        h2d(dB + r0 * bcrow, static_cast<const char*>(B) + r0 * bcrow, nr * bcrow);
+        h2d(dC + r0 * bcrow, static_cast<const char*>(C) + r0 * bcrow, nr * bcrow);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[1 + k], si);
+    }
+    for (int k = 0; k < h.K && err == cudaSuccess && rc == SSD_OK; ++k) {
+        int64_t r0, nr, q0;
+        ssd_shape pk;
+        piece(k, &r0, &nr, &q0, &pk);
+        err = cudaStreamWaitEvent(st, ev[1 + k], 0);
+        if (err != cudaSuccess) break;
+        const void* px = dx + r0 * xrow;
+        const float* pdt = reinterpret_cast<const float*>(ddt + r0 * dtrow);
+        const void* pB = dB + r0 * bcrow;
+        const void* pC = dC + r0 * bcrow;
+        void* py = dy + r0 * xrow;
+        const float* pD = D ? reinterpret_cast<const float*>(dD) : nullptr;
+        if (!h.time) {
+            rc = ssd_forward_ex(&pk, SSD_BF16, flags, px, pdt, reinterpret_cast<const float*>(dA), pB, pC, pD, chunk,
+                                initial_state ? reinterpret_cast<const float*>(dinit + q0 * st1) : nullptr, nullptr, 0,
+                                py, final_state ? reinterpret_cast<float*>(dfinal + q0 * st1) : nullptr, ws[k], wsb, st);
+        } else {
+            const float* h0 = (k == 0 && initial_state) ? reinterpret_cast<const float*>(dinit) : nullptr;
+            rc = ssd_forward_ex(&pk, SSD_BF16, flags, px, pdt, reinterpret_cast<const float*>(dA), pB, pC, pD, chunk,
+                                h0, nullptr, 0, py, reinterpret_cast<float*>(fin[k]), ws[k], wsb, st);
+            if (rc == SSD_OK && k > 0)
+                rc = ssd_slice_correct(&pk, SSD_BF16, pdt, reinterpret_cast<const float*>(dA), pC,
+                                       reinterpret_cast<const float*>(fin[k - 1]), py, reinterpret_cast<float*>(fin[k]),
+                                       sws[k], swsb, st);
+        }
+        if (rc != SSD_OK) break;
+        err = cudaEventRecord(ev[1 + h.K + k], st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(so, ev[1 + h.K + k], 0);
+        d2h(static_cast<char*>(y) + r0 * xrow, dy + r0 * xrow, nr * xrow);
+        if (final_state && !h.time) d2h(reinterpret_cast<char*>(final_state) + q0 * st1, dfinal + q0 * st1, pk.batch * st1);
+    }
+    if (final_state && h.time && rc == SSD_OK) d2h(final_state, fin[h.K - 1], st1);
+    // everything issued has finished before the buffers are handed back, whatever happened above
+    const cudaError_t e1 = si ? cudaStreamSynchronize(si) : cudaSuccess;
+    const cudaError_t e2 = cudaStreamSynchronize(st);
+    const cudaError_t e3 = so ? cudaStreamSynchronize(so) : cudaSuccess;
+    for (auto& v : ev)
+        if (v) cudaEventDestroy(v);
+    if (si) cudaStreamDestroy(si);
+    if (so) cudaStreamDestroy(so);
+    if (rc != SSD_OK) return rc;
+    if (err != cudaSuccess || e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+        note_cuda_error("pipelined host call", err != cudaSuccess ? err : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3)));
+        return SSD_ERR_CUDA;
+    }
+    for (int k = 0; k < h.K; ++k) {
+        int r = ssd_status(ws[k], st);
+        if (r == SSD_OK && h.time && k > 0) r = ssd_status(sws[k], st);
+        if (r != SSD_OK) return r;
+    }
+    return SSD_OK;
+}
+
+}  // namespace
 
 int ssd_forward_host_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, const void* x, const float* dt,
                         const float* A, const void* B, const void* C, const float* D, int chunk,
@@ -241,6 +422,9 @@ int ssd_forward_host_ex(const ssd_shape* s, ssd_dtype dtype, unsigned flags, con
     const size_t e = elt(dtype);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(device_buffer);
+    const HostPlan hp = host_plan(*s, dtype, varlen);
+    if (hp.K > 1)
+        return host_pipelined(s, hp, flags, x, dt, A, B, C, D, chunk, initial_state, y, final_state, base, st);
     size_t off = 0;
     auto carve = [&](size_t bytes) { char* p = base + off; off += align256(bytes); return p; };
     const size_t ws_bytes = ssd_workspace_size(s, dtype, chunk, varlen ? nseq : 0);

@@ -216,3 +216,30 @@ def test_fp32_dt_scaled_input():
 def test_dt_scaled_full_workload_sampled_heads():
     w = WORKLOADS["long_n128"]
     check(make_inputs(w), "bf16", w.chunk, heads=[0, 79], scale_x_by_dt=True)
+
+
+# ---------------------------------------------------------------- the host entry point's pipeline
+# A large dense bf16 batch is cut into pieces whose copies and forwards overlap: batch rows, or time
+# slices of one sequence joined by the state hand-off. Both must match the oracle like the device path.
+PIPELINED = [
+    ("batch_rows", dict(batch=3, seqlen=4096, nheads=32), [0, 17, 31]),      # 3 pieces of one row
+    ("time_slices", dict(batch=1, seqlen=16384, nheads=16), [0, 9, 15]),     # 4 slices of 4096 tokens
+    ("time_ragged", dict(batch=1, seqlen=17000, nheads=16), [2, 13]),        # slices of 4352, the last short
+]
+
+
+@pytest.mark.parametrize("name,shape,heads", PIPELINED, ids=[p[0] for p in PIPELINED])
+def test_host_entry_point_pipeline(name, shape, heads):
+    import torch
+    from mamba_ssd_layer_gb300 import ssd_forward_host
+    w = small_variant(WORKLOADS["m2_2p7b"], **shape).with_(seed=400 + shape["seqlen"] % 97)
+    d = make_inputs(w)
+    h = {k: (torch.from_numpy(d[k]).bfloat16() if k in ("x", "B", "C") else torch.from_numpy(d[k]))
+         for k in ("x", "dt", "A", "B", "C", "D", "initial_state")}
+    pin = {k: v.pin_memory() for k, v in h.items()}
+    y, f = ssd_forward_host(pin["x"], pin["dt"], pin["A"], pin["B"], pin["C"], pin["D"], chunk=256,
+                            initial_state=pin["initial_state"])
+    y_ref, f_ref = run_oracle(d, heads=heads)
+    hs = np.asarray(heads)
+    assert normwise(y.float().numpy()[:, :, hs], y_ref) <= TOL["bf16"]
+    assert normwise(f.numpy()[:, hs], f_ref) <= TOL["bf16"]
