@@ -21,6 +21,7 @@
 // The dot product with C is reduced across the row's L lanes with xor shuffles.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <vector>
 
 #include "ssd.h"
 #include "ssd_internal.cuh"
@@ -313,6 +314,84 @@ size_t ssd_decode_host_buffer_size(const ssd_shape* s, ssd_dtype dtype) {
     return tot > 0 ? tot : 256;
 }
 
+namespace {
+
+// The host step on many carried states (a state of at least 32 MB) runs as a pipeline over groups of
+// batch rows, which are independent: the copies in of group k + 1, the step of group k and the copies
+// out of group k - 1 overlap (the copy engines move both directions at once). The caller's stream runs
+// the steps; one internal stream copies in and one copies out, ordered by events.
+constexpr int kDecodePieces = 4;
+constexpr size_t kDecodePipelineBytes = size_t(32) << 20;
+
+int decode_host_pipelined(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags, const void* x,
+                          const float* dt, const float* A, const void* B, const void* C, const float* D,
+                          const void* state, void* new_state, void* y, char* dx, char* dy, char* ddt, char* dA,
+                          char* dD, char* dB, char* dC, char* dS, cudaStream_t st) {
+    const size_t e = decode_elt(dtype);
+    const size_t xrow = (size_t)s->nheads * s->headdim * e, dtrow = (size_t)s->nheads * 4;
+    const size_t bcrow = (size_t)s->ngroups * s->dstate * e;
+    const size_t srow = (size_t)s->nheads * s->headdim * s->dstate * decode_elt(state_dtype);
+    const size_t hb = (size_t)s->nheads * 4;
+    const int64_t len = (s->batch + kDecodePieces - 1) / kDecodePieces;
+    const int K = (int)((s->batch + len - 1) / len);
+    cudaStream_t si = nullptr, so = nullptr;
+    std::vector<cudaEvent_t> ev(2 * K + 1, nullptr);
+    cudaError_t err = cudaStreamCreateWithFlags(&si, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&so, cudaStreamNonBlocking);
+    for (auto& v : ev)
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && src && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si);
+    };
+    auto d2h = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, so);
+    };
+    // the copies in wait for the caller's earlier work on its stream (it may still use the buffer)
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], st);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(si, ev[0], 0);
+    h2d(dA, A, hb);
+    h2d(dD, D, hb);
+    for (int k = 0; k < K; ++k) {
+        const int64_t b0 = k * len, bk = s->batch - b0 < len ? s->batch - b0 : len;
+        h2d(dx + b0 * xrow, static_cast<const char*>(x) + b0 * xrow, bk * xrow);
+        h2d(ddt + b0 * dtrow, reinterpret_cast<const char*>(dt) + b0 * dtrow, bk * dtrow);
+        h2d(dB + b0 * bcrow, static_cast<const char*>(B) + b0 * bcrow, bk * bcrow);
+        h2d(dC + b0 * bcrow, static_cast<const char*>(C) + b0 * bcrow, bk * bcrow);
+        h2d(dS + b0 * srow, static_cast<const char*>(state) + b0 * srow, bk * srow);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[1 + k], si);
+    }
+    int rc = SSD_OK;
+    for (int k = 0; k < K && err == cudaSuccess; ++k) {
+        const int64_t b0 = k * len, bk = s->batch - b0 < len ? s->batch - b0 : len;
+        ssd_shape pk = *s;
+        pk.batch = bk;
+        err = cudaStreamWaitEvent(st, ev[1 + k], 0);
+        if (err != cudaSuccess) break;
+        rc = ssd_decode_step_ex(&pk, dtype, state_dtype, flags, dx + b0 * xrow,
+                                reinterpret_cast<const float*>(ddt + b0 * dtrow), reinterpret_cast<const float*>(dA),
+                                dB + b0 * bcrow, dC + b0 * bcrow, D ? reinterpret_cast<const float*>(dD) : nullptr,
+                                dS + b0 * srow, dS + b0 * srow, dy + b0 * xrow, st);
+        if (rc != SSD_OK) break;
+        err = cudaEventRecord(ev[1 + K + k], st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(so, ev[1 + K + k], 0);
+        d2h(static_cast<char*>(y) + b0 * xrow, dy + b0 * xrow, bk * xrow);
+        d2h(static_cast<char*>(new_state) + b0 * srow, dS + b0 * srow, bk * srow);
+    }
+    // everything issued has finished before the buffers are handed back, whatever happened above
+    const cudaError_t e1 = si ? cudaStreamSynchronize(si) : cudaSuccess;
+    const cudaError_t e2 = cudaStreamSynchronize(st);
+    const cudaError_t e3 = so ? cudaStreamSynchronize(so) : cudaSuccess;
+    for (auto& v : ev)
+        if (v) cudaEventDestroy(v);
+    if (si) cudaStreamDestroy(si);
+    if (so) cudaStreamDestroy(so);
+    if (rc != SSD_OK) return rc;
+    const cudaError_t ef = err != cudaSuccess ? err : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+    return note_cuda_error("decode host pipeline", ef) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
 int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state_dtype, unsigned flags,
                             const void* x, const float* dt, const float* A, const void* B, const void* C,
                             const float* D, const void* state, void* new_state, void* y, void* device_buffer,
@@ -343,6 +422,9 @@ int ssd_decode_step_host_ex(const ssd_shape* s, ssd_dtype dtype, ssd_dtype state
     char* dS = carve(stb);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t err = cudaSuccess;
+    if (stb >= kDecodePipelineBytes && s->batch >= kDecodePieces)
+        return decode_host_pipelined(s, dtype, state_dtype, flags, x, dt, A, B, C, D, state, new_state, y, dx, dy, ddt,
+                                     dA, dD, dB, dC, dS, st);
     auto h2d = [&](void* dst, const void* src, size_t bytes) {
         if (err == cudaSuccess && src && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
     };

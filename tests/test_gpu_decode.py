@@ -201,3 +201,26 @@ def test_decode_dt_scaled_input(dtype):
     y, s = gpu_step(d, dtype, scale_x_by_dt=True)
     yr, sr = oracle.ssd_decode_step(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], scale_x_by_dt=True)
     assert normwise(y, yr) <= TOL[dtype] and normwise(s, sr) <= 1e-5
+
+
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_decode_host_pipeline_matches_device_entry(state_dtype):
+    # enough carried states (at least 32 MB of state) that the host step runs as a pipeline over groups of
+    # batch rows, with a ragged last group; rows are independent, so it must equal the device step exactly
+    import torch
+    from mamba_ssd_layer_gb300 import ssd_decode_step_host
+    from mamba_ssd_layer_gb300.inputs import bf16_round
+    d = decode_inputs(70, 32, 64, 128, 1, "bf16", seed=450)
+    if state_dtype == "bf16":
+        d["state"] = bf16_round(d["state"])
+        y_dev, s_dev = bf16_state_step(d, "bf16")
+    else:
+        y_dev, s_dev = gpu_step(d, "bf16")
+    h = {k: torch.from_numpy(np.ascontiguousarray(d[k])) for k in d}
+    for k in ("x", "B", "C") + (("state",) if state_dtype == "bf16" else ()):
+        h[k] = h[k].bfloat16()
+    h = {k: v.pin_memory() for k, v in h.items()}
+    new = torch.empty_like(h["state"]).pin_memory()
+    y, s = ssd_decode_step_host(h["x"], h["dt"], h["A"], h["B"], h["C"], h["D"], h["state"], new)
+    assert np.array_equal(y.float().numpy().astype(np.float64), np.asarray(y_dev, dtype=np.float64))
+    assert np.array_equal(s.float().numpy().astype(np.float64), np.asarray(s_dev, dtype=np.float64))
