@@ -213,27 +213,37 @@ namespace {
 // move both directions at once): batch rows when there are several, else time slices of the one
 // sequence, joined by the sequence-parallel hand-off ("LLM(十一)——Mamba" §3.7.2): every slice after the
 // first runs from a zero state and is corrected for the state its predecessor ends with.
-struct HostPlan {
-    int K = 1;              // pieces; 1: one piece, no pipeline
-    bool time = false;      // time slices of one sequence (else groups of batch rows)
-    int64_t len = 0;        // batch rows per piece, or tokens per slice (a multiple of the 128-token tile)
-};
-
 constexpr int kHostPieces = 4;
 constexpr int64_t kHostPipelineBytes = int64_t(32) << 20;   // x bytes below which one piece is used
 
+struct HostPlan {
+    int K = 1;                        // pieces; 1: one piece, no pipeline
+    bool time = false;                // time slices of one sequence (else groups of batch rows)
+    int64_t cut[kHostPieces + 1];     // piece k: batch rows, or tokens, [cut[k], cut[k + 1])
+    int64_t len = 0;                  // the largest piece
+};
+
+// Time slices end at 30, 60 and 85 % of the sequence (multiples of the 128-token tile): the last piece's
+// forward and copies out are what the pipeline cannot overlap, so it is the smallest.
 HostPlan host_plan(const ssd_shape& s, ssd_dtype dtype, bool varlen) {
     HostPlan h;
     if (dtype != SSD_BF16 || varlen || !use_fused_path(s, dtype)) return h;
     if (s.batch * s.seqlen * s.nheads * s.headdim * 2 < kHostPipelineBytes) return h;
     if (s.batch >= 2) {
-        h.len = (s.batch + kHostPieces - 1) / kHostPieces;
-        h.K = (int)((s.batch + h.len - 1) / h.len);
+        const int64_t len = (s.batch + kHostPieces - 1) / kHostPieces;
+        h.K = (int)((s.batch + len - 1) / len);
+        for (int k = 0; k <= h.K; ++k) h.cut[k] = k * len < s.batch ? k * len : s.batch;
     } else if (s.seqlen >= kHostPieces * 1024) {
+        static constexpr int kPct[kHostPieces + 1] = {0, 30, 60, 85, 100};
         h.time = true;
-        h.len = ((s.seqlen + kHostPieces - 1) / kHostPieces + 127) / 128 * 128;
-        h.K = (int)((s.seqlen + h.len - 1) / h.len);
+        h.K = kHostPieces;
+        for (int k = 0; k < kHostPieces; ++k) h.cut[k] = s.seqlen * kPct[k] / 100 / 128 * 128;
+        h.cut[kHostPieces] = s.seqlen;
+    } else {
+        return h;
     }
+    for (int k = 0; k < h.K; ++k)
+        if (h.cut[k + 1] - h.cut[k] > h.len) h.len = h.cut[k + 1] - h.cut[k];
     return h;
 }
 
@@ -264,6 +274,7 @@ size_t ssd_host_buffer_size(const ssd_shape* s, ssd_dtype dtype, int chunk, int 
             tot += align256(ssd_slice_workspace_size(&ps)) * h.K;           // the slices' corrections
             tot += align256(s->nheads * s->headdim * s->dstate * 4) * h.K;  // every slice's final state
         }
+        tot += align256(2 * kHostPieces * sizeof(int));                     // the pieces' status words
     } else {
         tot += ws1;
     }
@@ -306,6 +317,7 @@ int host_pipelined(const ssd_shape* s, const HostPlan& h, unsigned flags, const 
     char* dC = carve(rows * bcrow);
     char* dinit = carve(s->batch * st1);
     char* dfinal = carve(s->batch * st1);
+    int* dstat = reinterpret_cast<int*>(carve(2 * kHostPieces * sizeof(int)));   // every call's status word
 
     cudaStream_t si = nullptr, so = nullptr;
     std::vector<cudaEvent_t> ev(2 * h.K + 1, nullptr);
@@ -329,13 +341,13 @@ int host_pipelined(const ssd_shape* s, const HostPlan& h, unsigned flags, const 
     // piece k: rows [r0, r0 + nr) of the (batch x time) row order, sequences [q0, q0 + nq)
     auto piece = [&](int k, int64_t* r0, int64_t* nr, int64_t* q0, ssd_shape* pk) {
         *pk = *s;
-        const int64_t a0 = k * h.len;
+        const int64_t a0 = h.cut[k], n = h.cut[k + 1] - h.cut[k];
         if (h.time) {
-            pk->seqlen = T - a0 < h.len ? T - a0 : h.len;
-            *r0 = a0; *nr = pk->seqlen; *q0 = 0;
+            pk->seqlen = n;
+            *r0 = a0; *nr = n; *q0 = 0;
         } else {
-            pk->batch = s->batch - a0 < h.len ? s->batch - a0 : h.len;
-            *r0 = a0 * T; *nr = pk->batch * T; *q0 = a0;
+            pk->batch = n;
+            *r0 = a0 * T; *nr = n * T; *q0 = a0;
         }
     };
     for (int k = 0; k < h.K; ++k) {
@@ -374,6 +386,12 @@ int host_pipelined(const ssd_shape* s, const HostPlan& h, unsigned flags, const 
                                        sws[k], swsb, st);
         }
         if (rc != SSD_OK) break;
+        // the status words of this piece's calls, gathered so that one copy reads them all at the end
+        err = cudaMemcpyAsync(dstat + 2 * k, ws[k], sizeof(int), cudaMemcpyDeviceToDevice, st);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(dstat + 2 * k + 1, h.time && k > 0 ? sws[k] : ws[k], sizeof(int),
+                                  cudaMemcpyDeviceToDevice, st);
+        if (err != cudaSuccess) break;
         err = cudaEventRecord(ev[1 + h.K + k], st);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(so, ev[1 + h.K + k], 0);
         d2h(static_cast<char*>(y) + r0 * xrow, dy + r0 * xrow, nr * xrow);
@@ -393,11 +411,12 @@ int host_pipelined(const ssd_shape* s, const HostPlan& h, unsigned flags, const 
         note_cuda_error("pipelined host call", err != cudaSuccess ? err : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3)));
         return SSD_ERR_CUDA;
     }
-    for (int k = 0; k < h.K; ++k) {
-        int r = ssd_status(ws[k], st);
-        if (r == SSD_OK && h.time && k > 0) r = ssd_status(sws[k], st);
-        if (r != SSD_OK) return r;
-    }
+    int stat[2 * kHostPieces];
+    if (note_cuda_error("status copy", cudaMemcpy(stat, dstat, 2 * h.K * sizeof(int), cudaMemcpyDeviceToHost)) !=
+        cudaSuccess)
+        return SSD_ERR_CUDA;
+    for (int k = 0; k < 2 * h.K; ++k)
+        if (stat[k] != SSD_OK) return stat[k];
     return SSD_OK;
 }
 
