@@ -29,6 +29,7 @@ import threading
 import numpy as np
 
 from .decode import ssd_decode_step  # noqa: F401
+from .gated_norm import gated_rmsnorm, silu  # noqa: F401
 from .quadratic import ssd_quadratic  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
