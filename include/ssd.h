@@ -293,6 +293,27 @@ int ssd_slice_correct(const ssd_shape *shape, ssd_dtype dtype, const float *dt, 
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * The Mamba-2 block's output gate and extra normalization, after the SSD layer ("LLM(十一)——Mamba"
+ * §3.6.1, Block Design: a normalization layer is added before the output projection, after the
+ * multiplicative gate branch). Per token and per group of H*P/groups consecutive channels:
+ *     v   = y * silu(z),   silu(z) = z / (1 + exp(-z))        (z NULL: v = y, no gate)
+ *     out = v / sqrt(mean over the group of v^2 + eps) * weight
+ * The pages print neither formula: the gate's nonlinearity is taken as SiLU, the default nonlinearity of
+ * "LLM(十一)——Mamba" §3.6.2, and the normalization as RMSNorm (one group: the whole token; groups > 1:
+ * the GroupNorm-style variant).
+ *
+ *   y, z, out  (batch, seqlen, H, P) bf16 device arrays (shape's dstate and ngroups are ignored); out may
+ *              be y itself (in place)
+ *   weight     (H*P) fp32, or NULL for ones
+ *   eps        >= 0 (silu is computed with the fast exponential and division; below z = -80 it is 0)
+ *   groups     divides H*P; a group must be a multiple of 8 channels, and H*P at most 6144
+ *              (SSD_ERR_UNSUPPORTED otherwise)
+ * Enqueued on `stream`; no workspace, no device-side status. Pointers 16-byte aligned.
+ */
+int ssd_gated_rmsnorm(const ssd_shape *shape, const void *y, const void *z, const float *weight, float eps,
+                      int groups, void *out, void *stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status recorded in the
  * workspace by the last ssd_forward (or ssd_slice_* call) that used it: SSD_OK, SSD_ERR_TIMEOUT (a bounded wait gave up),
  * SSD_ERR_INVALID_ARG (malformed cu_seqlens, found by the device-side table builder; y is then not

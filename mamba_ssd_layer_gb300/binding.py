@@ -85,6 +85,8 @@ def load_library():
     lib.ssd_slice_decay.restype = i32
     lib.ssd_slice_correct.argtypes = [shp, i32, fp, fp, vp, fp, vp, fp, vp, sz, vp]
     lib.ssd_slice_correct.restype = i32
+    lib.ssd_gated_rmsnorm.argtypes = [shp, vp, vp, fp, ctypes.c_float, i32, vp, vp]
+    lib.ssd_gated_rmsnorm.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
     lib.ssd_profile_enable.argtypes = [i32]
@@ -409,3 +411,28 @@ def profile_kernel_launches() -> int:
 def profile_kernel_name() -> str:
     """Name of the kernel the recorded events bracket."""
     return load_library().ssd_profile_kernel_name().decode()
+
+
+def ssd_gated_rmsnorm(y, z=None, weight=None, eps: float = 1e-5, groups: int = 1, out=None, stream=None):
+    """The block's output gate and extra normalization (``ssd_gated_rmsnorm``): per token and group of
+    H*P/groups channels, v = y * silu(z) (no gate when z is None), out = v / sqrt(mean(v^2) + eps) * weight.
+    y, z, out (batch, T, H, P) bfloat16 on the device (out may be y); weight (H*P,) float32 or None.
+    Returns out."""
+    import torch
+    batch, T, H, P = y.shape
+    dev = y.device
+    _check(y, "y", (batch, T, H, P), torch.bfloat16, dev)
+    _check(z, "z", (batch, T, H, P), torch.bfloat16, dev)
+    _check(weight, "weight", (H * P,), torch.float32, dev)
+    if out is None:
+        out = torch.empty_like(y)
+    _check(out, "out", (batch, T, H, P), torch.bfloat16, dev)
+    shape = _shape(batch, T, H, P, 1, 1)
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = lib.ssd_gated_rmsnorm(ctypes.byref(shape), _ptr(y), _ptr(z), _ptr(weight), float(eps), int(groups),
+                               _ptr(out), ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_gated_rmsnorm")
+    return out

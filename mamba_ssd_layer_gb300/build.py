@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libssd_gb300.so")
-SOURCES = ["ssd_api.cu", "ssd_common.cu", "ssd_f32.cu", "ssd_fused.cu", "ssd_noalloc.cu", "ssd_decode.cu", "ssd_handoff.cu"]
+SOURCES = ["ssd_api.cu", "ssd_common.cu", "ssd_f32.cu", "ssd_fused.cu", "ssd_noalloc.cu", "ssd_decode.cu", "ssd_handoff.cu", "ssd_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -569,4 +569,25 @@ const char* ssd_status_string(int code) {
     }
 }
 
+int ssd_gated_rmsnorm(const ssd_shape* s, const void* y, const void* z, const float* weight, float eps, int groups,
+                      void* out, void* stream) {
+    if (!s || s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0) return SSD_ERR_INVALID_ARG;
+    if (groups <= 0 || !(eps >= 0.f) || !(eps < 3.0e38f)) return SSD_ERR_INVALID_ARG;
+    const int64_t rows = s->batch * s->seqlen, channels = s->nheads * s->headdim;
+    if (channels % groups != 0) return SSD_ERR_INVALID_ARG;
+    const int64_t gsize = channels / groups;
+    if (gsize % 8 != 0 || channels > norm_max_channels()) return SSD_ERR_UNSUPPORTED;
+    if (rows > 0 && (!y || !out)) return SSD_ERR_INVALID_ARG;
+    const void* ptrs[] = {y, z, weight, out};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
+    if (rows == 0) return SSD_OK;
+    int num_sms = 0;
+    const int rc = check_device(&num_sms);
+    if (rc != SSD_OK) return rc;
+    const cudaError_t e = launch_gated_rmsnorm(y, z, weight, eps, rows, channels, groups, out, num_sms,
+                                               static_cast<cudaStream_t>(stream));
+    return note_cuda_error("gated rmsnorm launch", e) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 }  // extern "C"

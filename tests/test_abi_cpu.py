@@ -166,3 +166,20 @@ def test_slice_handoff_argument_errors_before_any_device_work(lib):
     assert cor(s, dtype=7) == bd.SSD_ERR_INVALID_ARG
     assert cor(s, h=None) == bd.SSD_ERR_INVALID_ARG
     assert cor(s, y=FAKE + 2) == bd.SSD_ERR_INVALID_ARG
+
+
+def test_gated_rmsnorm_argument_errors_before_any_device_work(lib):
+    s = shape(batch=2, T=100, H=4, P=64, N=128)
+    norm = lambda sh, y=FAKE, z=FAKE, w=FAKE, eps=1e-5, groups=1, out=FAKE: lib.ssd_gated_rmsnorm(
+        ctypes.byref(sh), y, z, w, eps, groups, out, None)
+    assert norm(s, groups=0) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, groups=3) == bd.SSD_ERR_INVALID_ARG              # 256 channels are not 3 groups
+    assert norm(s, groups=64) == bd.SSD_ERR_UNSUPPORTED             # a group of 4 channels: not 16-byte pieces
+    assert norm(shape(batch=1, T=4, H=98, P=64, N=128)) == bd.SSD_ERR_UNSUPPORTED    # 6272 channels a token
+    assert norm(s, eps=-1.0) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, eps=float("nan")) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, y=None) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, out=None) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, z=FAKE + 8) == bd.SSD_ERR_INVALID_ARG
+    assert norm(s, w=FAKE + 4) == bd.SSD_ERR_INVALID_ARG
+    assert norm(shape(batch=0, T=100, H=4, P=64, N=128), y=None, out=None) == bd.SSD_OK   # nothing to do
