@@ -51,18 +51,61 @@ __host__ __device__ inline size_t norm_smem_bytes(int C, int groups, int stages)
            (size_t)16 * stages;
 }
 
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+// pairs of fp32 in one 64-bit register, with the packed fp32 arithmetic of sm_100 and later (mul/add/fma .f32x2)
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// two bf16 (low half first) widened exactly to a pair of fp32
+__device__ __forceinline__ uint64_t bf2_to_pair(uint32_t u) {
+    return pk2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// a pair of fp32 rounded to nearest-even bf16, low half first
+__device__ __forceinline__ uint32_t pair_to_bf2(uint64_t p) {
+    const float2 f = upk2(p);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(f.y), "f"(f.x));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__device__ __forceinline__ uint32_t f2_to_bf2(float a, float b) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
+// silu of a pair: z * 1 / (1 + 2^(-z log2 e)). For very negative z the power is +inf, its reciprocal 0
+// and silu 0 (rcp.approx of +inf is +0); for very positive z the power is 0 and silu z.
+__device__ __forceinline__ uint64_t silu2(uint64_t z) {
+    const float2 t = upk2(mul2(z, pk2(-1.4426950408889634f, -1.4426950408889634f)));
+    const float2 d = upk2(add2(pk2(ex2_approx(t.x), ex2_approx(t.y)), pk2(1.f, 1.f)));
+    return mul2(z, pk2(rcp_approx(d.x), rcp_approx(d.y)));
 }
-
-// silu(z) = z * logistic(z), with the fast exponential and division; below -80, where it is smaller than
-// 2e-33 in magnitude, it is taken as 0 (the divisor of the quotient would overflow)
-__device__ __forceinline__ float silu_f(float z) { return z < -80.f ? 0.f : __fdividef(z, 1.f + __expf(-z)); }
 
 // 1-D bulk copy global -> shared, counted on `bar` (16-byte aligned addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -89,6 +132,8 @@ __device__ __forceinline__ bool norm_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// NV: 8-channel pieces a compute thread holds per token (ceil(C / 8 / kTeamThreads)); kGated: z is given
+template <int NV, bool kGated>
 __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) gated_rmsnorm_kernel(const NormArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int C = a.C, S = a.stages, groups = C / a.gsize;
@@ -115,9 +160,9 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) gated_rmsnorm_ke
                 const int s = k % S;
                 if (k >= S && !norm_wait(empty + s, (uint32_t)((k / S - 1) & 1), &stop)) break;
                 uint8_t* st = smem + (size_t)s * stb;
-                mbar_arrive_expect_tx(full + s, a.z ? 2 * rowb : rowb);
+                mbar_arrive_expect_tx(full + s, kGated ? 2 * rowb : rowb);
                 bulk_load(st, a.y + i * C, rowb, full + s);
-                if (a.z) bulk_load(st + rowb, a.z + i * C, rowb, full + s);
+                if (kGated) bulk_load(st + rowb, a.z + i * C, rowb, full + s);
                 ++issued[s];
             }
             // the copies issued land before the CTA's shared memory goes away
@@ -135,13 +180,32 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) gated_rmsnorm_ke
     for (int g = tid; g < 2 * kNormTeams * gpad; g += 32 * kNormWarps) part[g] = 0.f;
     compute_sync();
     // team t takes this CTA's tokens k = t, t + kNormTeams, ...; its thread r holds pieces r + m * kTeamThreads
-    const int team = tid / kTeamThreads, r = tid % kTeamThreads;
+    const int team = tid / kTeamThreads, r = tid % kTeamThreads, lane = tid & 31;
     float* tpart = part + team * 2 * gpad;
     const int nvec = C / 8;
-    // the group of piece j: (8 j + 4) / gsize rounded down, in float (exact enough: 8 j + 4 lies at least 4
-    // channels inside its group, and gsize is at most 8192)
     const float inv_gsize = 1.f / (float)a.gsize;
-    auto group_of = [&](int j) { return (int)((float)(8 * j + 4) * inv_gsize); };
+    // Each thread's pieces, and so their groups, are the same for every token; so is which lanes of the
+    // warp share a group. Worked out once: grp[m] (-1 past the row), and per piece the bits of the segmented
+    // warp sum: bit o (o = 0..4) adds the partial sum of lane + 2^o (same group, inside the warp and the row),
+    // bit 5 marks the first lane of a run of one group, which adds the run's sum to the group's total.
+    int grp[NV];
+    uint32_t segbits[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+        const int j = r + m * kTeamThreads;
+        // the group of piece j: (8 j + 4) / gsize rounded down, in float (exact enough: 8 j + 4 lies at least
+        // 4 channels inside its group, and gsize is at most 6144)
+        grp[m] = j < nvec ? (int)((float)(8 * j + 4) * inv_gsize) : -1;
+        uint32_t bits = 0;
+#pragma unroll
+        for (int b = 0; b < 5; ++b) {
+            const int tg = __shfl_down_sync(0xffffffffu, grp[m], 1 << b);
+            if (lane + (1 << b) < 32 && tg == grp[m] && grp[m] >= 0) bits |= 1u << b;
+        }
+        const int prev = __shfl_up_sync(0xffffffffu, grp[m], 1);
+        if (grp[m] >= 0 && (lane == 0 || prev != grp[m])) bits |= 1u << 5;
+        segbits[m] = bits;
+    }
     int n = 0;                                               // tokens this team has taken
     for (int k = team; blockIdx.x + (int64_t)k * gridDim.x < a.rows; k += kNormTeams, ++n) {
         const int64_t i = blockIdx.x + (int64_t)k * gridDim.x;
@@ -150,63 +214,60 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) gated_rmsnorm_ke
         const uint4* yv = reinterpret_cast<const uint4*>(smem + (size_t)s * stb);
         const uint4* zv = reinterpret_cast<const uint4*>(smem + (size_t)s * stb + rowb);
         float* ps = tpart + (n & 1) * gpad;
-        // v = y * silu(z), kept in registers; v^2 summed per group: a warp takes 32 consecutive 8-channel
-        // pieces, sums each run of lanes in the same group (groups are contiguous), and the run's first lane
-        // adds it to the group's total
-        const int lane = tid & 31;
-        float v[kNormVecs][8];
+        // v = y * silu(z) for every piece, kept in registers as fp32 pairs, and each piece's sum of v^2
+        uint64_t v[NV][4];
+        float ss[NV];
 #pragma unroll
-        for (int m = 0; m < kNormVecs; ++m) {
+        for (int m = 0; m < NV; ++m) {
             const int j = r + m * kTeamThreads;
-            if (j - lane >= nvec) break;                     // (the whole warp is past the row)
-            float ss = 0.f;
-            int grp = -1;
-            if (j < nvec) {
-                const uint4 yy = yv[j];
-                const uint32_t* uy = reinterpret_cast<const uint32_t*>(&yy);
-                uint4 zz4 = make_uint4(0u, 0u, 0u, 0u);
-                if (a.z) zz4 = zv[j];
-                const uint32_t* uz = reinterpret_cast<const uint32_t*>(&zz4);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float2 f = bf2_to_f2(uy[e]);
-                    if (a.z) {
-                        const float2 zz = bf2_to_f2(uz[e]);
-                        f.x *= silu_f(zz.x);
-                        f.y *= silu_f(zz.y);
-                    }
-                    v[m][2 * e] = f.x;
-                    v[m][2 * e + 1] = f.y;
-                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                }
-                grp = group_of(j);
+            uint4 yy = make_uint4(0u, 0u, 0u, 0u), zz = make_uint4(0u, 0u, 0u, 0u);
+            if (grp[m] >= 0) {
+                yy = yv[j];
+                if (kGated) zz = zv[j];
             }
+            const uint32_t* uy = reinterpret_cast<const uint32_t*>(&yy);
+            const uint32_t* uz = reinterpret_cast<const uint32_t*>(&zz);
+            uint64_t acc = pk2(0.f, 0.f);
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float t = __shfl_down_sync(0xffffffffu, ss, o);
-                const int tg = __shfl_down_sync(0xffffffffu, grp, o);
-                if (lane + o < 32 && tg == grp) ss += t;
+            for (int e = 0; e < 4; ++e) {
+                uint64_t f = bf2_to_pair(uy[e]);
+                if (kGated) f = mul2(f, silu2(bf2_to_pair(uz[e])));
+                v[m][e] = f;
+                acc = fma2(f, f, acc);
             }
-            const int prev = __shfl_up_sync(0xffffffffu, grp, 1);
-            if (grp >= 0 && (lane == 0 || prev != grp)) atomicAdd(ps + grp, ss);
+            const float2 a2 = upk2(acc);
+            ss[m] = a2.x + a2.y;
         }
+        // segmented warp sums: a warp holds 32 consecutive pieces, and groups are contiguous runs of pieces
+#pragma unroll
+        for (int b = 0; b < 5; ++b) {
+#pragma unroll
+            for (int m = 0; m < NV; ++m) {
+                const float t = __shfl_down_sync(0xffffffffu, ss[m], 1 << b);
+                if (segbits[m] & (1u << b)) ss[m] += t;
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < NV; ++m)
+            if (segbits[m] & (1u << 5)) atomicAdd(ps + grp[m], ss[m]);
         // (the team's other buffer is cleared for its next token: its sums were last read a token ago)
         for (int g = r; g < groups; g += kTeamThreads) tpart[((n + 1) & 1) * gpad + g] = 0.f;
         team_sync(team);
         // out = v * rsqrt(mean + eps) * weight
         __nv_bfloat16* orow = a.out + i * C;
 #pragma unroll
-        for (int m = 0; m < kNormVecs; ++m) {
+        for (int m = 0; m < NV; ++m) {
             const int j = r + m * kTeamThreads;
-            if (j < nvec) {
-                const float rinv = rsqrtf(ps[group_of(j)] * inv_gsize + a.eps);
+            if (grp[m] >= 0) {
+                const float rinv = rsqrtf(ps[grp[m]] * inv_gsize + a.eps);
+                const uint64_t rr = pk2(rinv, rinv);
                 const float4 w0 = reinterpret_cast<const float4*>(wsm)[2 * j];
                 const float4 w1 = reinterpret_cast<const float4*>(wsm)[2 * j + 1];
                 uint4 o;
-                o.x = f2_to_bf2(v[m][0] * rinv * w0.x, v[m][1] * rinv * w0.y);
-                o.y = f2_to_bf2(v[m][2] * rinv * w0.z, v[m][3] * rinv * w0.w);
-                o.z = f2_to_bf2(v[m][4] * rinv * w1.x, v[m][5] * rinv * w1.y);
-                o.w = f2_to_bf2(v[m][6] * rinv * w1.z, v[m][7] * rinv * w1.w);
+                o.x = pair_to_bf2(mul2(v[m][0], mul2(pk2(w0.x, w0.y), rr)));
+                o.y = pair_to_bf2(mul2(v[m][1], mul2(pk2(w0.z, w0.w), rr)));
+                o.z = pair_to_bf2(mul2(v[m][2], mul2(pk2(w1.x, w1.y), rr)));
+                o.w = pair_to_bf2(mul2(v[m][3], mul2(pk2(w1.z, w1.w), rr)));
                 reinterpret_cast<uint4*>(orow)[j] = o;
             }
         }
@@ -214,6 +275,23 @@ __global__ void __launch_bounds__(kNormThreads, kNormCtasPerSm) gated_rmsnorm_ke
         team_sync(team);
         if (r == 0) mbar_arrive(empty + s);
     }
+}
+
+template <int NV, bool kGated>
+cudaError_t launch_norm(const NormArgs& a, size_t smem, unsigned grid, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(gated_rmsnorm_kernel<NV, kGated>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_launch();
+    gated_rmsnorm_kernel<NV, kGated><<<grid, kNormThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <int NV>
+cudaError_t launch_norm_nv(int nv, const NormArgs& a, size_t smem, unsigned grid, cudaStream_t stream) {
+    if (nv == NV) return a.z ? launch_norm<NV, true>(a, smem, grid, stream) : launch_norm<NV, false>(a, smem, grid, stream);
+    if constexpr (NV < kNormVecs) return launch_norm_nv<NV + 1>(nv, a, smem, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -236,12 +314,9 @@ cudaError_t launch_gated_rmsnorm(const void* y, const void* z, const float* weig
     while (S > 2 && norm_smem_bytes(a.C, groups, S) > kNormSmemBudget) --S;
     a.stages = S;
     const size_t smem = norm_smem_bytes(a.C, groups, S);
-    cudaError_t e = cudaFuncSetAttribute(gated_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int64_t grid = rows < (int64_t)kNormCtasPerSm * num_sms ? rows : (int64_t)kNormCtasPerSm * num_sms;
-    prof_launch();
-    gated_rmsnorm_kernel<<<(unsigned)grid, kNormThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    const int nv = (int)((channels / 8 + kTeamThreads - 1) / kTeamThreads);
+    return launch_norm_nv<1>(nv, a, smem, (unsigned)grid, stream);
 }
 
 }  // namespace ssd
