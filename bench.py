@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "SSD fwd tokens/s and % of bf16 tensor/HBM roofline, T=2K–16K, N=128"
 DECODE_METRIC = "SSD recurrent step tokens/s (one token per carried state) and % of HBM roofline"
+NORM_METRIC = "output gate and RMSNorm tokens/s (y * silu(z), normalized per group, scaled) and % of HBM roofline"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # seconds of untimed steps before the timed loop, with the clock sampler running
@@ -41,6 +42,8 @@ KERNEL_SOURCES = {
     "ssd_fused_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_fused.cu", "mamba_ssd_layer_gb300/csrc/ptx.cuh",
                          "mamba_ssd_layer_gb300/csrc/ssd_internal.cuh"),
     "ssd_decode_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_decode.cu",),
+    "gated_rmsnorm_kernel": ("mamba_ssd_layer_gb300/csrc/ssd_norm.cu", "mamba_ssd_layer_gb300/csrc/ssd_norm.cuh",
+                             "mamba_ssd_layer_gb300/csrc/ptx.cuh"),
 }
 NCU_TRAFFIC = {
     "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 217451264 + 149019648, "stamp": "0d8ccc6fd48c2fca"},
@@ -53,9 +56,11 @@ NCU_TRAFFIC = {
     "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 214944768 + 154399232, "stamp": "0d8ccc6fd48c2fca"},
     "varlen": {"kernel": "ssd_fused_kernel", "bytes": 178471936 + 121808128, "stamp": "0d8ccc6fd48c2fca"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
-    "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168495104 + 117637120, "stamp": "154fb82720b02848"},
-    "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84609280 + 34404352,
-                              "stamp": "154fb82720b02848"},
+    "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168496384 + 117444864, "stamp": "e82f933ea29a60b6"},
+    "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84610304 + 34867712,
+                              "stamp": "e82f933ea29a60b6"},
+    # gate and normalization: part of out is still in L2 when the launch ends
+    "gated_norm_long": {"kernel": "gated_rmsnorm_kernel", "bytes": 335802368 + 132897792, "stamp": "4410e131393c4b8a"},
 }
 
 
@@ -118,6 +123,12 @@ def decode_algorithmic_bytes(w) -> int:
     e = 2 if w.dtype == "bf16" else 4
     es = 2 if w.state_dtype == "bf16" else 4
     return int(2 * b * H * P * N * es + 2 * b * H * P * e + 2 * b * G * N * e + 4 * b * H + 8 * H)
+
+
+def norm_algorithmic_bytes(w) -> int:
+    """Bytes the gate and normalization must move: y and z in, out back (bf16), the fp32 weight."""
+    C = w.nheads * w.headdim
+    return int(3 * w.batch * w.seqlen * C * 2 + C * 4)
 
 
 def algorithmic_flops(w, batch_rows) -> int:
@@ -370,12 +381,168 @@ def run_decode(args, w):
         torch.distributed.destroy_process_group()
 
 
+def norm_config(w):
+    mb = w.batch * w.seqlen * w.nheads * w.headdim * 2 / 1e6
+    return {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+            "groups": w.norm_groups, "gated": True, "parallelism": "replicas",
+            "l2": f"inputs larger than L2 (two rotating sets of y, z and out, ~{3 * mb:.0f} MB each)",
+            "clock_soak_s": CLOCK_SOAK_S}
+
+
+def norm_sample_rows(budget_tokens: int) -> int:
+    return max(1, min(2048, budget_tokens // 8))
+
+
+def norm_cpu_baseline(w, budget_tokens: int, min_seconds: float = 10.0, max_runs: int = 500):
+    """The oracle's gate and normalization as it stands (numpy, one core) on a sample of tokens of the
+    workload's shape, repeated for about `min_seconds`."""
+    import oracle
+    from mamba_ssd_layer_gb300.inputs import make_norm_inputs
+    rows = norm_sample_rows(budget_tokens)
+    d = make_norm_inputs(w, rows=rows)
+    runs, t0 = 0, time.perf_counter()
+    while runs < max_runs and (runs == 0 or time.perf_counter() - t0 < min_seconds):
+        oracle.gated_rmsnorm(d["y"], d["z"], d["weight"], eps=1e-5, groups=w.norm_groups)
+        runs += 1
+    dt = time.perf_counter() - t0
+    return {"value": rows * runs / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of {w.batch * w.seqlen} tokens (all {w.nheads * w.headdim} channels), "
+                      f"{runs} runs in {dt:.1f} s"}
+
+
+def run_reference_norm(args, w):
+    """The oracle's gate and normalization on the host, bounded: each step runs a sample of the tokens."""
+    import oracle
+    from mamba_ssd_layer_gb300.inputs import make_norm_inputs
+    rows = norm_sample_rows(args.ref_tokens)
+    d = make_norm_inputs(w, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gated_rmsnorm(d["y"], d["z"], d["weight"], eps=1e-5, groups=w.norm_groups)
+        times.append(time.perf_counter() - t0)
+    tot = float(np.sum(times))
+    val = rows * args.steps / tot
+    sample = f"{rows} of {w.batch * w.seqlen} tokens, all {w.nheads * w.headdim} channels, per step"
+    line = {"impl": "reference", "metric": NORM_METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": norm_config(w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_norm(args, w):
+    """The output gate and normalization on the GPU: each step normalizes every token of the workload."""
+    import torch
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    from mamba_ssd_layer_gb300 import binding as bd
+    from mamba_ssd_layer_gb300 import ssd_gated_rmsnorm, ssd_gated_rmsnorm_host
+    from mamba_ssd_layer_gb300.inputs import make_norm_inputs
+
+    d = make_norm_inputs(w)
+    rows = w.batch * w.seqlen
+    hy = torch.from_numpy(d["y"]).to(torch.bfloat16).pin_memory()
+    hz = torch.from_numpy(d["z"]).to(torch.bfloat16).pin_memory()
+    hw = torch.from_numpy(d["weight"]).pin_memory()
+    wt = hw.to(dev)
+    # two rotating sets of y, z and out: the previous step's data is out of L2
+    sets = [(hy.to(dev), hz.to(dev), torch.empty(hy.shape, dtype=torch.bfloat16, device=dev)) for _ in range(2)]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        y, z, out = sets[i % 2]
+        ssd_gated_rmsnorm(y, z, wt, eps=1e-5, groups=w.norm_groups, out=out, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        soak0 = soak(step, torch)
+        bd.profile_enable(True)
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        wall1 = time.time()
+    bd.profile_enable(False)
+    kern_ms, kern_n = bd.profile_read()
+    launches = bd.profile_kernel_launches()
+    kernel = bd.profile_kernel_name()
+    ms = ev0.elapsed_time(ev1)
+    ms, value = reduce_over_ranks(ms, rows, args.steps, world, dev)
+    ms_per_step = ms / args.steps
+
+    # end to end through the host entry point: pinned y, z and weight in, out back
+    hout = torch.empty_like(hy).pin_memory()
+    import ctypes
+    need = int(bd.load_library().ssd_gated_rmsnorm_host_buffer_size(
+        ctypes.byref(bd._shape(w.batch, w.seqlen, w.nheads, w.headdim, 1, 1)), 1))
+    devbuf = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        ssd_gated_rmsnorm_host(hy, hz, hw, eps=1e-5, groups=w.norm_groups, out=hout, device_buffer=devbuf,
+                               stream=stream)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = time.perf_counter() - t0
+    h2d = hy.numel() * 2 + hz.numel() * 2 + hw.numel() * 4
+    d2h = hout.numel() * 2
+
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    alg_bytes = norm_algorithmic_bytes(w)
+    kern_avg_ms = kern_ms / max(kern_n, 1)
+    achieved = alg_bytes / (kern_avg_ms / 1e3) / 1e9 if kern_n else None
+    line = {
+        "metric": NORM_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": norm_config(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None,
+                     "traffic": measured_traffic(w.name, kernel), "peak_source": src, "kernel": kernel,
+                     "kernel_ms": kern_avg_ms, "alg_bytes_per_launch": alg_bytes, "launches_per_step": 1.0,
+                     "step_frac": alg_bytes / (ms_per_step / 1e3) / 1e9 / hbm},
+        "e2e": {"value": world * rows * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(soak0, wall1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = norm_cpu_baseline(w, args.ref_tokens)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def run_reference(args, w):
     """The oracle on the host cores, bounded: each step runs a sample of the workload."""
     import oracle
     from mamba_ssd_layer_gb300.inputs import make_inputs, small_variant
     world, rank, _ = dist_setup()
     if rank != 0:
+        return
+    if w.norm_groups:
+        run_reference_norm(args, w)
         return
     if w.seqlen == 1:
         run_reference_decode(args, w)
@@ -453,6 +620,9 @@ def main():
         return
     if w.seqlen == 1:
         run_decode(args, w)
+        return
+    if w.norm_groups:
+        run_norm(args, w)
         return
 
     import torch

@@ -305,13 +305,27 @@ int ssd_slice_correct(const ssd_shape *shape, ssd_dtype dtype, const float *dt, 
  *   y, z, out  (batch, seqlen, H, P) bf16 device arrays (shape's dstate and ngroups are ignored); out may
  *              be y itself (in place)
  *   weight     (H*P) fp32, or NULL for ones
- *   eps        >= 0 (silu is computed with the fast exponential and division; below z = -80 it is 0)
+ *   eps        >= 0 (silu is computed in fp32 with the hardware approximations of 2^x and 1/x; for very
+ *              negative z it is 0)
  *   groups     divides H*P; a group must be a multiple of 8 channels, and H*P at most 6144
  *              (SSD_ERR_UNSUPPORTED otherwise)
- * Enqueued on `stream`; no workspace, no device-side status. Pointers 16-byte aligned.
+ * Enqueued on `stream`; no workspace, no device-side status. Pointers 16-byte aligned. Errors: argument
+ * checks before any launch (SSD_ERR_INVALID_ARG, SSD_ERR_UNSUPPORTED), SSD_ERR_CUDA for a failed launch.
  */
 int ssd_gated_rmsnorm(const ssd_shape *shape, const void *y, const void *z, const float *weight, float eps,
                       int groups, void *out, void *stream);
+
+/*
+ * The same on host buffers: y, z (NULL: no gate), weight (NULL: ones) and out are host arrays (pinned for
+ * speed; out may be y). The call copies them through `device_buffer` (device memory the caller owns, 256-byte
+ * aligned, at least ssd_gated_rmsnorm_host_buffer_size(shape, z != NULL) bytes), runs the kernel and
+ * returns when out holds the result. Tokens of at least 32 MB of y run as a pipeline of four groups of
+ * rows whose copies in, kernels and copies out overlap (on the caller's stream and two internal ones).
+ * Errors as ssd_gated_rmsnorm, plus SSD_ERR_WORKSPACE for a missing, misaligned or short buffer.
+ */
+size_t ssd_gated_rmsnorm_host_buffer_size(const ssd_shape *shape, int gated);
+int ssd_gated_rmsnorm_host(const ssd_shape *shape, const void *y, const void *z, const float *weight, float eps,
+                           int groups, void *out, void *device_buffer, size_t device_buffer_bytes, void *stream);
 
 /*
  * Synchronises `stream`, then returns the device-side status recorded in the

@@ -9,7 +9,7 @@ from __future__ import annotations
 __all__ = ["ssd_forward", "ssd_forward_host", "ssd_workspace_size", "ssd_status",
            "ssd_status_string", "library_path", "SSDError", "profile_enable", "profile_read",
            "ssd_decode_step", "ssd_decode_step_host", "ssd_slice_decay", "ssd_slice_correct",
-           "ssd_gated_rmsnorm"]
+           "ssd_gated_rmsnorm", "ssd_gated_rmsnorm_host"]
 
 
 def __getattr__(name):

@@ -87,6 +87,10 @@ def load_library():
     lib.ssd_slice_correct.restype = i32
     lib.ssd_gated_rmsnorm.argtypes = [shp, vp, vp, fp, ctypes.c_float, i32, vp, vp]
     lib.ssd_gated_rmsnorm.restype = i32
+    lib.ssd_gated_rmsnorm_host_buffer_size.argtypes = [shp, i32]
+    lib.ssd_gated_rmsnorm_host_buffer_size.restype = sz
+    lib.ssd_gated_rmsnorm_host.argtypes = [shp, vp, vp, fp, ctypes.c_float, i32, vp, vp, sz, vp]
+    lib.ssd_gated_rmsnorm_host.restype = i32
     lib.ssd_status.argtypes = [vp, vp]
     lib.ssd_status.restype = i32
     lib.ssd_profile_enable.argtypes = [i32]
@@ -388,8 +392,8 @@ def ssd_decode_step_host(x, dt, A, B, C, D=None, state=None, new_state=None, y=N
 
 
 def profile_enable(on: bool = True) -> None:
-    """Record CUDA events around the dominant kernel of every later ssd_forward or ssd_decode_step on
-    this thread."""
+    """Record CUDA events around the dominant kernel of every later ssd_forward, ssd_decode_step or
+    ssd_gated_rmsnorm on this thread."""
     load_library().ssd_profile_enable(1 if on else 0)
 
 
@@ -435,4 +439,33 @@ def ssd_gated_rmsnorm(y, z=None, weight=None, eps: float = 1e-5, groups: int = 1
                                _ptr(out), ctypes.c_void_p(stream.cuda_stream))
     if rc != SSD_OK:
         raise SSDError(rc, "ssd_gated_rmsnorm")
+    return out
+
+
+def ssd_gated_rmsnorm_host(y, z=None, weight=None, eps: float = 1e-5, groups: int = 1, out=None, device_buffer=None,
+                           stream=None):
+    """The same on HOST (CPU, ideally pinned) tensors through ``ssd_gated_rmsnorm_host``: the copies in, the
+    kernel and the copy out all happen inside the C call, which synchronises. Returns out."""
+    import torch
+    batch, T, H, P = y.shape
+    cpu = torch.device("cpu")
+    _check(y, "y", (batch, T, H, P), torch.bfloat16, cpu)
+    _check(z, "z", (batch, T, H, P), torch.bfloat16, cpu)
+    _check(weight, "weight", (H * P,), torch.float32, cpu)
+    if out is None:
+        out = torch.empty_like(y)
+    _check(out, "out", (batch, T, H, P), torch.bfloat16, cpu)
+    shape = _shape(batch, T, H, P, 1, 1)
+    lib = load_library()
+    need = int(lib.ssd_gated_rmsnorm_host_buffer_size(ctypes.byref(shape), 1 if z is not None else 0))
+    if need == 0:
+        raise SSDError(SSD_ERR_INVALID_ARG, "ssd_gated_rmsnorm_host_buffer_size")
+    if device_buffer is None or device_buffer.numel() < need:
+        device_buffer = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(device_buffer.device)
+    rc = lib.ssd_gated_rmsnorm_host(ctypes.byref(shape), _ptr(y), _ptr(z), _ptr(weight), float(eps), int(groups),
+                                    _ptr(out), device_buffer.data_ptr(), need, ctypes.c_void_p(stream.cuda_stream))
+    if rc != SSD_OK:
+        raise SSDError(rc, "ssd_gated_rmsnorm_host")
     return out

@@ -10,6 +10,7 @@
 
 #include "ssd.h"
 #include "ssd_internal.cuh"
+#include "ssd_norm.cuh"
 #include "ssd_profile.h"
 
 using namespace ssd;
@@ -569,25 +570,125 @@ const char* ssd_status_string(int code) {
     }
 }
 
-int ssd_gated_rmsnorm(const ssd_shape* s, const void* y, const void* z, const float* weight, float eps, int groups,
-                      void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// argument checks shared by the device and host forms of the gate and normalization
+int check_norm(const ssd_shape* s, float eps, int groups) {
     if (!s || s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0) return SSD_ERR_INVALID_ARG;
     if (groups <= 0 || !(eps >= 0.f) || !(eps < 3.0e38f)) return SSD_ERR_INVALID_ARG;
-    const int64_t rows = s->batch * s->seqlen, channels = s->nheads * s->headdim;
+    const int64_t channels = s->nheads * s->headdim;
     if (channels % groups != 0) return SSD_ERR_INVALID_ARG;
-    const int64_t gsize = channels / groups;
-    if (gsize % 8 != 0 || channels > norm_max_channels()) return SSD_ERR_UNSUPPORTED;
+    if ((channels / groups) % 8 != 0 || channels > norm_max_channels()) return SSD_ERR_UNSUPPORTED;
+    return SSD_OK;
+}
+
+// The host form on a large block of tokens (y of at least 32 MB) runs as a pipeline over groups of rows,
+// which are independent: the copies in of group k + 1, the kernel on group k and the copy out of group
+// k - 1 overlap. The caller's stream runs the kernels; one internal stream copies in and one copies out,
+// ordered by events. out is written in place over the device copy of y.
+constexpr int kNormPieces = 4;
+constexpr size_t kNormPipelineBytes = size_t(32) << 20;
+
+int norm_host_run(int64_t rows, int64_t channels, const void* y, const void* z, const float* weight, float eps,
+                  int groups, void* out, char* dy, char* dz, char* dw, int num_sms, cudaStream_t st) {
+    const size_t rowb = (size_t)channels * 2;
+    const bool pipe = rows * rowb >= kNormPipelineBytes && rows >= kNormPieces;
+    const int64_t len = pipe ? (rows + kNormPieces - 1) / kNormPieces : rows;
+    const int K = (int)((rows + len - 1) / len);
+    cudaStream_t si = nullptr, so = nullptr;
+    std::vector<cudaEvent_t> ev(2 * K + 1, nullptr);
+    cudaError_t err = cudaStreamCreateWithFlags(&si, cudaStreamNonBlocking);
+    if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&so, cudaStreamNonBlocking);
+    for (auto& v : ev)
+        if (err == cudaSuccess) err = cudaEventCreateWithFlags(&v, cudaEventDisableTiming);
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        if (err == cudaSuccess && bytes) err = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si);
+    };
+    // the copies in wait for the caller's earlier work on its stream (it may still use the buffer)
+    if (err == cudaSuccess) err = cudaEventRecord(ev[0], st);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(si, ev[0], 0);
+    if (weight) h2d(dw, weight, (size_t)channels * 4);
+    for (int k = 0; k < K; ++k) {
+        const int64_t r0 = k * len, rk = rows - r0 < len ? rows - r0 : len;
+        h2d(dy + r0 * rowb, static_cast<const char*>(y) + r0 * rowb, rk * rowb);
+        if (z) h2d(dz + r0 * rowb, static_cast<const char*>(z) + r0 * rowb, rk * rowb);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[1 + k], si);
+    }
+    for (int k = 0; k < K && err == cudaSuccess; ++k) {
+        const int64_t r0 = k * len, rk = rows - r0 < len ? rows - r0 : len;
+        err = cudaStreamWaitEvent(st, ev[1 + k], 0);
+        if (err == cudaSuccess)
+            err = launch_gated_rmsnorm(dy + r0 * rowb, z ? dz + r0 * rowb : nullptr,
+                                       weight ? reinterpret_cast<const float*>(dw) : nullptr, eps, rk, channels,
+                                       groups, dy + r0 * rowb, num_sms, st);
+        if (err == cudaSuccess) err = cudaEventRecord(ev[1 + K + k], st);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(so, ev[1 + K + k], 0);
+        if (err == cudaSuccess)
+            err = cudaMemcpyAsync(static_cast<char*>(out) + r0 * rowb, dy + r0 * rowb, rk * rowb,
+                                  cudaMemcpyDeviceToHost, so);
+    }
+    // everything issued has finished before the buffers are handed back, whatever happened above
+    const cudaError_t e1 = si ? cudaStreamSynchronize(si) : cudaSuccess;
+    const cudaError_t e2 = cudaStreamSynchronize(st);
+    const cudaError_t e3 = so ? cudaStreamSynchronize(so) : cudaSuccess;
+    for (auto& v : ev)
+        if (v) cudaEventDestroy(v);
+    if (si) cudaStreamDestroy(si);
+    if (so) cudaStreamDestroy(so);
+    const cudaError_t ef = err != cudaSuccess ? err : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+    return note_cuda_error("gated rmsnorm host pipeline", ef) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssd_gated_rmsnorm(const ssd_shape* s, const void* y, const void* z, const float* weight, float eps, int groups,
+                      void* out, void* stream) {
+    int rc = check_norm(s, eps, groups);
+    if (rc != SSD_OK) return rc;
+    const int64_t rows = s->batch * s->seqlen, channels = s->nheads * s->headdim;
     if (rows > 0 && (!y || !out)) return SSD_ERR_INVALID_ARG;
     const void* ptrs[] = {y, z, weight, out};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return SSD_ERR_INVALID_ARG;
     if (rows == 0) return SSD_OK;
     int num_sms = 0;
-    const int rc = check_device(&num_sms);
+    rc = check_device(&num_sms);
     if (rc != SSD_OK) return rc;
     const cudaError_t e = launch_gated_rmsnorm(y, z, weight, eps, rows, channels, groups, out, num_sms,
                                                static_cast<cudaStream_t>(stream));
     return note_cuda_error("gated rmsnorm launch", e) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+size_t ssd_gated_rmsnorm_host_buffer_size(const ssd_shape* s, int gated) {
+    if (!s || s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0) return 0;
+    const size_t yb = (size_t)(s->batch * s->seqlen) * s->nheads * s->headdim * 2;
+    const size_t tot = align256(yb) * (gated ? 2 : 1) + align256((size_t)s->nheads * s->headdim * 4);
+    return tot > 0 ? tot : 256;
+}
+
+int ssd_gated_rmsnorm_host(const ssd_shape* s, const void* y, const void* z, const float* weight, float eps,
+                           int groups, void* out, void* device_buffer, size_t device_buffer_bytes, void* stream) {
+    int rc = check_norm(s, eps, groups);
+    if (rc != SSD_OK) return rc;
+    const size_t need = ssd_gated_rmsnorm_host_buffer_size(s, z != nullptr);
+    if (!device_buffer || (reinterpret_cast<uintptr_t>(device_buffer) & 255u) || device_buffer_bytes < need)
+        return SSD_ERR_WORKSPACE;
+    const int64_t rows = s->batch * s->seqlen, channels = s->nheads * s->headdim;
+    if (rows == 0) return SSD_OK;
+    if (!y || !out) return SSD_ERR_INVALID_ARG;
+    int num_sms = 0;
+    rc = check_device(&num_sms);
+    if (rc != SSD_OK) return rc;
+    const size_t yb = align256((size_t)rows * channels * 2);
+    char* dy = static_cast<char*>(device_buffer);
+    char* dz = z ? dy + yb : nullptr;
+    char* dw = dy + yb * (z ? 2 : 1);
+    return norm_host_run(rows, channels, y, z, weight, eps, groups, out, dy, dz, dw, num_sms,
+                         static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -152,11 +152,6 @@ bool make_map_fused(CUtensorMap* m, const void* ptr, int64_t inner, int64_t mid,
 
 // The sequence-slice hand-off (ssd_handoff.cu).
 size_t slice_ws_bytes(const ssd_shape& s);
-// the output gate and extra normalization (ssd_norm.cu): most channels per token it handles, and its
-// launcher (one persistent CTA per SM)
-int64_t norm_max_channels();
-cudaError_t launch_gated_rmsnorm(const void* y, const void* z, const float* weight, float eps, int64_t rows,
-                                 int64_t channels, int groups, void* out, int num_sms, cudaStream_t stream);
 cudaError_t launch_slice_decay(const ssd_shape& s, const float* dt, const float* A, float* decay, char* ws,
                                cudaStream_t st);
 cudaError_t launch_slice_correct(const ssd_shape& s, const float* dt, const float* A, const void* C,

@@ -18,6 +18,7 @@
 #include "ptx.cuh"
 #include "ssd.h"
 #include "ssd_internal.cuh"
+#include "ssd_norm.cuh"
 
 namespace ssd {
 namespace {
@@ -283,8 +284,11 @@ cudaError_t launch_norm(const NormArgs& a, size_t smem, unsigned grid, cudaStrea
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     prof_launch();
+    prof_begin(stream, "gated_rmsnorm_kernel");
     gated_rmsnorm_kernel<NV, kGated><<<grid, kNormThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e2 = cudaGetLastError();
+    prof_end(stream);
+    return e2;
 }
 
 template <int NV>

@@ -10,6 +10,10 @@ D ~ N(0, 1) per head; a nonzero initial state, where used, ~ N(0, std 0.1).
 Draw order: x, dt, A, B, C, D, segment lengths, initial state. Generator:
 numpy PCG64 with the workload's seed. For bf16 workloads x, B, C are rounded
 to bf16 (round-to-nearest-even) once, and both sides consume those values.
+
+The output gate and normalization workloads (norm_groups > 0) draw y ~ N(0, 1) (the layer's output),
+z ~ N(0, 1) (the gate branch), both rounded to bf16, and the scale weight ~ U(0.5, 1.5) per channel, fp32;
+draw order y, z, weight.
 """
 from __future__ import annotations
 
@@ -37,6 +41,7 @@ class Workload:
     seg_max: int = 4096
     state_dtype: str = "f32"  # recurrent-step workloads: storage type of the carried state
     scale_x_by_dt: bool = False  # the input term is dt x B^T (the layer's option, not an input draw)
+    norm_groups: int = 0      # >0: an output gate and normalization workload with this many groups per token
     note: str = field(default="", compare=False)
 
     def with_(self, **kw) -> "Workload":
@@ -62,6 +67,9 @@ WORKLOADS = {
     # the same step with the carried state stored in bf16 (the state is rounded to bf16 once on the host)
     "decode_2p7b_bf16state": Workload("decode_2p7b_bf16state", 64, 1, 80, 64, 128, 1, 256, "bf16", 1005,
                                       init_state=True, state_dtype="bf16"),
+    # the block's output gate and normalization over the long-sequence layer's output (16384 tokens of
+    # 80 heads x 64 channels), one RMSNorm group per token (dstate, ngroups and chunk are unused)
+    "gated_norm_long": Workload("gated_norm_long", 1, 16384, 80, 64, 128, 1, 256, "bf16", 1006, norm_groups=1),
 }
 
 
@@ -124,6 +132,18 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     if init is not None and w.state_dtype == "bf16":
         init = bf16_round(init)
     return dict(x=x, dt=dt, A=A, B=B, C=C, D=D, initial_state=init, cu_seqlens=cu)
+
+
+def make_norm_inputs(w: Workload, rows: Optional[int] = None) -> dict:
+    """Draw a gate and normalization workload's inputs: y, z (batch, T, H, P) fp32 holding bf16 values and
+    weight (H*P,) fp32. With `rows`: a draw of that many tokens (batch 1), the CPU side's sample."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    b, T = (w.batch, w.seqlen) if rows is None else (1, rows)
+    shp = (b, T, w.nheads, w.headdim)
+    y = bf16_round(rng.standard_normal(shp, dtype=np.float32))
+    z = bf16_round(rng.standard_normal(shp, dtype=np.float32))
+    weight = rng.uniform(0.5, 1.5, w.nheads * w.headdim).astype(np.float32)
+    return dict(y=y, z=z, weight=weight)
 
 
 def small_variant(w: Workload, seqlen: int, nheads: int, batch: Optional[int] = None, **kw) -> Workload:

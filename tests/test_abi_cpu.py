@@ -183,3 +183,25 @@ def test_gated_rmsnorm_argument_errors_before_any_device_work(lib):
     assert norm(s, z=FAKE + 8) == bd.SSD_ERR_INVALID_ARG
     assert norm(s, w=FAKE + 4) == bd.SSD_ERR_INVALID_ARG
     assert norm(shape(batch=0, T=100, H=4, P=64, N=128), y=None, out=None) == bd.SSD_OK   # nothing to do
+
+
+def test_gated_rmsnorm_host_buffer_and_argument_errors(lib):
+    s = shape(batch=2, T=100, H=4, P=64, N=128)
+    size = lambda sh, gated: lib.ssd_gated_rmsnorm_host_buffer_size(ctypes.byref(sh), gated)
+    # y (and z when gated) of 200 tokens x 256 bf16 channels, 256-byte aligned, then the fp32 weight
+    assert size(s, 0) == 200 * 256 * 2 + 256 * 4
+    assert size(s, 1) == 2 * 200 * 256 * 2 + 256 * 4
+    assert size(shape(batch=1, T=3, H=1, P=64), 1) == 2 * 512 + 256
+    assert size(shape(batch=-1), 1) == 0
+    need = size(s, 1)
+    host = lambda sh, y=FAKE, z=FAKE, w=FAKE, eps=1e-5, groups=1, out=FAKE, buf=FAKE, nb=need: \
+        lib.ssd_gated_rmsnorm_host(ctypes.byref(sh), y, z, w, eps, groups, out, buf, nb, None)
+    assert host(s, buf=None) == bd.SSD_ERR_WORKSPACE
+    assert host(s, buf=FAKE + 16) == bd.SSD_ERR_WORKSPACE                # not 256-aligned
+    assert host(s, nb=need - 1) == bd.SSD_ERR_WORKSPACE
+    assert host(s, groups=3) == bd.SSD_ERR_INVALID_ARG
+    assert host(s, groups=64) == bd.SSD_ERR_UNSUPPORTED
+    assert host(s, eps=-1.0) == bd.SSD_ERR_INVALID_ARG
+    assert host(s, y=None) == bd.SSD_ERR_INVALID_ARG
+    assert host(s, out=None) == bd.SSD_ERR_INVALID_ARG
+    assert host(shape(batch=0, T=100, H=4, P=64, N=128), y=None, out=None) == bd.SSD_OK   # nothing to do

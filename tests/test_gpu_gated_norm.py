@@ -78,3 +78,19 @@ def test_widest_token(groups):
     y, z, w = _data(1, 157, 96, 64, seed=540 + groups)
     out = ssd_gated_rmsnorm(y.cuda(), z.cuda(), w.cuda(), eps=1e-5, groups=groups)
     _check_rows(out, y, z, w, 1e-5, groups, np.arange(157))
+
+
+@pytest.mark.parametrize("T,H,gated", [(16384, 80, True), (4099, 48, False), (37, 4, True)])
+def test_host_form_equals_device_form(T, H, gated):
+    # ssd_gated_rmsnorm_host: 16384 x 80 x 64 (168 MB of y) runs as a pipeline of row groups, the others in
+    # one piece; either way the result is bit for bit the device form's, and out may be y itself
+    import torch
+    from mamba_ssd_layer_gb300 import ssd_gated_rmsnorm, ssd_gated_rmsnorm_host
+    y, z, w = _data(1, T, H, 64, seed=550 + H)
+    zz = z if gated else None
+    ref = ssd_gated_rmsnorm(y.cuda(), None if zz is None else zz.cuda(), w.cuda(), eps=1e-5, groups=H // 4 or 1)
+    yh = y.pin_memory()
+    got = ssd_gated_rmsnorm_host(yh, None if zz is None else zz.pin_memory(), w.pin_memory(), eps=1e-5,
+                                 groups=H // 4 or 1, out=yh)
+    assert got.data_ptr() == yh.data_ptr()
+    assert torch.equal(got, ref.cpu())
