@@ -124,6 +124,7 @@ struct FusedArgs {
     int* status;                // workspace header: [0] status word, [2] first timeout location
     const ChunkDesc* tiles;     // tile table (packed batch)
     const int32_t* seqoff;      // first tile of each sequence (packed batch)
+    const int32_t* cu;          // sequence offsets in rows (packed batch)
     const float* dt;
     const float* A;
     const float* D;
@@ -377,21 +378,20 @@ __device__ __forceinline__ ChainPos decode_at(int g, const FusedArgs& a) {
         c.seq_row0 = (int32_t)(c.s * a.seqlen);
         c.seq_len = (int32_t)a.seqlen;
     } else {
-        // the last sequence whose first chain starts at or before g (an empty sequence is never it)
-        int lo = 0, hi = a.nseq - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (a.npairs * a.seqoff[mid] <= g) lo = mid; else hi = mid - 1;
-        }
-        const int32_t f0 = a.seqoff[lo], f1 = a.seqoff[lo + 1];
-        c.s = lo;
-        c.nt = f1 - f0;
+        // The chains of sequence s hold run indices [npairs f0, npairs f1), f0..f1 its tiles in the
+        // sequence-major tile table, so tile g / npairs of the table is one of g's sequence (an empty
+        // sequence has no tile). Its record gives the sequence, its first tile and its first row, and the
+        // sequence's end offset its length: two dependent loads.
+        const int f = g / a.npairs;
+        const ChunkDesc d = a.tiles[f];
+        c.s = d.seq;
+        const int f0 = f - d.ci;
+        c.seq_row0 = d.row0 - kTile * d.ci;
+        c.seq_len = __ldg(a.cu + c.s + 1) - c.seq_row0;
+        c.nt = (c.seq_len + kTile - 1) / kTile;
         const int local = g - a.npairs * f0;
         c.hp = local / c.nt;
         c.t = local - c.hp * c.nt;
-        const ChunkDesc first = a.tiles[f0], last = a.tiles[f1 - 1];
-        c.seq_row0 = first.row0;
-        c.seq_len = last.row0 + last.len - first.row0;
     }
     return c;
 }
@@ -631,9 +631,10 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     issue_g(s, buf);
                 }
                 g_next = false;
-                // C B^T of the window's next tile goes out as soon as its B and C are there and its buffer
-                // is free, also while this tile waits for its L o G, so that the mask warps can go on
-                const bool next_tile = it.t + 1 < it.t1;
+                // C B^T of the stream's next tile (of this window or the next one; it needs only the stage and
+                // the buffer) goes out as soon as its B and C are there and its buffer is free, also while
+                // this tile waits for its L o G, so that the mask warps can go on
+                const bool next_tile = it.t + 1 < it.t1 || it.gw + (it.t1 - it.t0) < it.g1;
                 bool bc_ok = false, gb_ok = false;
                 auto try_g_next = [&]() -> bool {
                     if (!next_tile || g_next) return true;
@@ -1561,6 +1562,7 @@ cudaError_t launch_fused(const Problem& p, int, int64_t, int part) {
     fa.status = p.status();
     fa.tiles = p.chunks();
     fa.seqoff = p.seqoff();
+    fa.cu = p.varlen ? p.cu_seqlens : nullptr;
     fa.dt = p.dt;
     fa.A = p.A;
     fa.D = part == 0 ? p.D : nullptr;

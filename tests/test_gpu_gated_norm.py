@@ -94,3 +94,15 @@ def test_host_form_equals_device_form(T, H, gated):
                                  groups=H // 4 or 1, out=yh)
     assert got.data_ptr() == yh.data_ptr()
     assert torch.equal(got, ref.cpu())
+
+
+# channel counts for every number of 8-channel pieces a thread holds (1 to 6 of 128 threads), most of them
+# ragged, and group sizes that split a warp's 32 pieces unevenly (5 pieces), span two warps (64 pieces) or
+# are the finest allowed (8 channels)
+@pytest.mark.parametrize("H,P,groups", [(1, 64, 8), (20, 64, 32), (72, 32, 12), (64, 64, 64), (72, 64, 9),
+                                        (88, 64, 88)])
+def test_every_piece_count_and_ragged_groups(H, P, groups):
+    from mamba_ssd_layer_gb300 import ssd_gated_rmsnorm
+    y, z, w = _data(1, 1500, H, P, seed=560 + H + groups)
+    out = ssd_gated_rmsnorm(y.cuda(), z.cuda(), w.cuda(), eps=1e-6, groups=groups)
+    _check_rows(out, y, z, w, 1e-6, groups, np.arange(1500))
