@@ -1355,80 +1355,78 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     const bool out_incl = f_t1 < cf.nt;      // (then the first window is also the last)
                     const float fdec = ex2(f_log);
                     float* frow = fin ? final_row_of(cf.s, cf.hp) : nullptr;
-                    // 8 state columns at a time. Every load of a column group (the base, up to four folded
-                    // states, this thread's own final-state and zero-start end-state values) goes out before
-                    // any of them is used, so that a group costs about one round trip to L2.
+                    // 16 state columns at a time. Every load of a column group (the base, up to two folded
+                    // states, this thread's own final-state or zero-start end-state values: never both) goes
+                    // out before any of them is used, so that a group costs about one round trip to L2.
 #pragma unroll 1
-                    for (int k8 = 0; k8 < N / 8; ++k8) {
-                        const int ck = k8 >> 1, j0 = 2 * (k8 & 1);
-                        float4 h[2], fo[2], ow[2];
+                    for (int ck = 0; ck < N / 16; ++ck) {
+                        float4 h[4], ot[4];
                         if (base >= 0) {
-                            const float4* src = pub_ptr(a.incl, base, ck) + j0 * 128;
-                            h[0] = __ldcg(src);
-                            h[1] = __ldcg(src + 128);
+                            const float4* src = pub_ptr(a.incl, base, ck);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) h[j] = __ldcg(src + j * 128);
                         } else if (irow) {
-                            h[0] = __ldg(reinterpret_cast<const float4*>(irow + 8 * k8));
-                            h[1] = __ldg(reinterpret_cast<const float4*>(irow + 8 * k8) + 1);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) h[j] = __ldg(reinterpret_cast<const float4*>(irow + 16 * ck) + j);
                         } else {
-                            h[0] = h[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) h[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                         if (fin) {
-                            fo[0] = __ldcg(reinterpret_cast<const float4*>(frow + 8 * k8));
-                            fo[1] = __ldcg(reinterpret_cast<const float4*>(frow + 8 * k8) + 1);
-                        }
-                        if (out_incl) {
-                            const float4* ag = pub_ptr(a.agg, my_slot, ck) + j0 * 128;
-                            ow[0] = __ldcg(ag);
-                            ow[1] = __ldcg(ag + 128);
-                        }
-                        for (int f0 = nf - 1; f0 >= 0; f0 -= 4) {
-                            float dcy[4];
-                            float4 gg[4][2];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
+                            for (int j = 0; j < 4; ++j) ot[j] = __ldcg(reinterpret_cast<const float4*>(frow + 16 * ck) + j);
+                        } else if (out_incl) {
+                            const float4* ag = pub_ptr(a.agg, my_slot, ck);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) ot[j] = __ldcg(ag + j * 128);
+                        }
+                        for (int f0 = nf - 1; f0 >= 0; f0 -= 2) {
+                            float dcy[2];
+                            float4 gg[2][4];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
                                 if (f0 - u >= 0) {
-                                    const int sl = fold[f0 - u];
                                     dcy[u] = fdecs[f0 - u];
-                                    const float4* src = pub_ptr(a.agg, sl, ck) + j0 * 128;
-                                    gg[u][0] = __ldcg(src);
-                                    gg[u][1] = __ldcg(src + 128);
+                                    const float4* src = pub_ptr(a.agg, fold[f0 - u], ck);
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) gg[u][j] = __ldcg(src + j * 128);
                                 }
                             }
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
+                            for (int u = 0; u < 2; ++u) {
                                 if (f0 - u >= 0) {
 #pragma unroll
-                                    for (int jj = 0; jj < 2; ++jj)
+                                    for (int jj = 0; jj < 4; ++jj)
                                         h[jj] = make_float4(fmaf(dcy[u], h[jj].x, gg[u][jj].x), fmaf(dcy[u], h[jj].y, gg[u][jj].y),
                                                             fmaf(dcy[u], h[jj].z, gg[u][jj].z), fmaf(dcy[u], h[jj].w, gg[u][jj].w));
                                 }
                             }
                         }
                         // h_in as bf16 for the correction products
-                        {
-                            const int n = 8 * k8;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int n = 16 * ck + 8 * hf;
                             uint4 pk;
-                            pk.x = pack_bf16x2(h[0].x, h[0].y);
-                            pk.y = pack_bf16x2(h[0].z, h[0].w);
-                            pk.z = pack_bf16x2(h[1].x, h[1].y);
-                            pk.w = pack_bf16x2(h[1].z, h[1].w);
+                            pk.x = pack_bf16x2(h[2 * hf].x, h[2 * hf].y);
+                            pk.y = pack_bf16x2(h[2 * hf].z, h[2 * hf].w);
+                            pk.z = pack_bf16x2(h[2 * hf + 1].x, h[2 * hf + 1].y);
+                            pk.w = pack_bf16x2(h[2 * hf + 1].z, h[2 * hf + 1].w);
                             *reinterpret_cast<uint4*>(sm.hs() + (n / 64) * kRegion + sw128_offset(r, (n % 64) / 8)) = pk;
                         }
                         if (fin) {
                             // the chain's final state from its zero-start value (this thread's own stores)
 #pragma unroll
-                            for (int jj = 0; jj < 2; ++jj)
-                                reinterpret_cast<float4*>(frow + 8 * k8)[jj] =
-                                    make_float4(fmaf(fdec, h[jj].x, fo[jj].x), fmaf(fdec, h[jj].y, fo[jj].y),
-                                                fmaf(fdec, h[jj].z, fo[jj].z), fmaf(fdec, h[jj].w, fo[jj].w));
-                        }
-                        if (out_incl) {
+                            for (int jj = 0; jj < 4; ++jj)
+                                reinterpret_cast<float4*>(frow + 16 * ck)[jj] =
+                                    make_float4(fmaf(fdec, h[jj].x, ot[jj].x), fmaf(fdec, h[jj].y, ot[jj].y),
+                                                fmaf(fdec, h[jj].z, ot[jj].z), fmaf(fdec, h[jj].w, ot[jj].w));
+                        } else if (out_incl) {
                             // this window's true end state, decay * h_in + its zero-start end state
-                            float4* dst = pub_ptr(a.incl, my_slot, ck) + j0 * 128;
+                            float4* dst = pub_ptr(a.incl, my_slot, ck);
 #pragma unroll
-                            for (int jj = 0; jj < 2; ++jj)
-                                __stcg(dst + jj * 128, make_float4(fmaf(fdec, h[jj].x, ow[jj].x), fmaf(fdec, h[jj].y, ow[jj].y),
-                                                                   fmaf(fdec, h[jj].z, ow[jj].z), fmaf(fdec, h[jj].w, ow[jj].w)));
+                            for (int jj = 0; jj < 4; ++jj)
+                                __stcg(dst + jj * 128, make_float4(fmaf(fdec, h[jj].x, ot[jj].x), fmaf(fdec, h[jj].y, ot[jj].y),
+                                                                   fmaf(fdec, h[jj].z, ot[jj].z), fmaf(fdec, h[jj].w, ot[jj].w)));
                         }
                     }
                     if (out_incl) {
