@@ -46,15 +46,15 @@ KERNEL_SOURCES = {
                              "mamba_ssd_layer_gb300/csrc/ptx.cuh"),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 217451264 + 149019648, "stamp": "0d8ccc6fd48c2fca"},
-    "long_n64": {"kernel": "ssd_fused_kernel", "bytes": 201287424 + 140782848, "stamp": "0d8ccc6fd48c2fca"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 216657920 + 149097984, "stamp": "28e277d349734659"},
+    "long_n64": {"kernel": "ssd_fused_kernel", "bytes": 200741888 + 140881920, "stamp": "28e277d349734659"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 295571328 + 144533120, "stamp": "0d8ccc6fd48c2fca"},
-    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 209037568 + 149345024, "stamp": "0d8ccc6fd48c2fca"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 292590080 + 144763264, "stamp": "28e277d349734659"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 207759616 + 149413888, "stamp": "28e277d349734659"},
     # y (50 MB) largely still in L2 when the launch ends
-    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 60473856 + 12647680, "stamp": "0d8ccc6fd48c2fca"},
-    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 214944768 + 154399232, "stamp": "0d8ccc6fd48c2fca"},
-    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 178471936 + 121808128, "stamp": "0d8ccc6fd48c2fca"},
+    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 60471296 + 12652544, "stamp": "28e277d349734659"},
+    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 214985984 + 154567424, "stamp": "28e277d349734659"},
+    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 177894912 + 122017280, "stamp": "28e277d349734659"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
     "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168496384 + 117444864, "stamp": "e82f933ea29a60b6"},
     "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84610304 + 34867712,
