@@ -1021,8 +1021,9 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             if (is_corr) {
                 // (this warp is done with the previous position, its SO wait included)
                 warp_arrive(wt, kDrained + s);
-                // the row's y from the window pass (this warp stored it: its bulk stores are waited for
-                // and made visible to ordinary loads once)
+                // the correction is added onto the y of the window pass where it is stored (a bulk tensor
+                // reduce-add, or an fp32 add per row of a partial quadrant), so z is zero. This warp stored
+                // those rows: its bulk stores are waited for, and made visible to ordinary loads, once.
                 if (!y_visible) {
                     if (lane == 0) {
                         bulk_wait_all();
@@ -1031,21 +1032,12 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                     __syncwarp();
                     y_visible = true;
                 }
-                // z = that y, into the z columns (no Yd product follows a correction tile)
-                const uint4* yr = reinterpret_cast<const uint4*>(a.y + ((int64_t)(row0 + i) * a.H + h0 + hh) * 64);
+                {
+                    uint32_t f[16];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (i < len) v = yr[ch];
-                    const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
-                    uint32_t f[8];
+                    for (int m = 0; m < 16; ++m) f[m] = 0u;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float2 ff = unpack_bf16x2(u[m]);
-                        f[2 * m] = __float_as_uint(ff.x);
-                        f[2 * m + 1] = __float_as_uint(ff.y);
-                    }
-                    tmem_st8(zcol + 8 * ch, f);
+                    for (int c16 = 0; c16 < 4; ++c16) tmem_st16(zcol + 16 * c16, f);
                 }
                 tmem_wait_st();
                 e_row = (i < len) ? ex2(tab) : 0.f;
@@ -1121,8 +1113,8 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             fence_proxy_async_smem();
             warp_arrive(wt, kGBFree + buf);
             if (!is_corr) warp_arrive(wt, kYDFree);
-            // (a correction tile replaces the stored y: it already holds every other share)
-            const bool accum = !is_corr && (kAccum || a.y_accum);
+            // (a correction tile adds its product onto the stored y, which holds every other share)
+            const bool accum = is_corr || kAccum || a.y_accum;
             if (32 * q + 32 <= len && (is_corr || !(a.y_accum && !kAccum))) {
                 // the quadrant's 32 rows all belong to the sequence: one bulk tensor store of 4 KB
                 if (lane == 0) {
