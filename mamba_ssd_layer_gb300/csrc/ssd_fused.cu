@@ -35,7 +35,7 @@
 //   warp 1        MMA issuer and TMEM owner
 //   warp 2        tables: per-tile cumsums of dt*A (x log2 e), the factored-mask column table,
 //                 the window totals
-//   warp 3        no role
+//   warp 3        L o G of lane quadrant 3, its right two 32-column blocks (with warp 7)
 //   warps 4..7    L o G, one warp per TMEM lane quadrant
 //   warps 8..15   epilogue, one warpgroup per head: drains Yd (plus D x) into registers as soon as it
 //                 is there, weights x in place for S, then combines with Yo and stores y
@@ -55,7 +55,7 @@ namespace {
 
 constexpr int kTile = kFusedTile;
 constexpr int kRegion = kTile * 128;          // one 128-row x 128-byte swizzled box (16 KB)
-constexpr int kThreads = 640;                 // 20 warps (warp 3 has no role)
+constexpr int kThreads = 640;                 // 20 warps
 constexpr float kLog2e = 1.4426950408889634f;
 // floor of dt in log2(dt): dt = 0 contributes exp(-99.7) ~ 0 instead of an infinity
 constexpr float kMinDt = 1e-30f;
@@ -66,6 +66,7 @@ constexpr int kVtCols = 96;
 
 constexpr int kWarpProducer = 0, kWarpMMA = 1, kWarpTables = 2;
 constexpr int kWarpMask = 4, kWarpEpi = 8, kWarpState = 16;   // TMEM lane quadrant = warp & 3
+constexpr int kWarpMaskQ3 = 3;    // the second L o G warp of lane quadrant 3 (the quadrant with the most work)
 
 // TMEM column map (512 allocated)
 constexpr uint32_t kColST = 0;     // state / aggregate: rows (head, channel), N columns
@@ -81,18 +82,18 @@ constexpr uint32_t kColGB = 256;   // two 128-column buffers, alternating per ti
 enum : int {
     kFullBC = 0,     // [2] B and C of the stage landed (a correction tile: C only) (TMA bytes)
     kFullX = 2,      // [2] x of the stage landed (TMA bytes)
-    kTblRead = 4,    // [2] the stage's tables and record read: 8 epilogue, 4 mask and 4 state warps
+    kTblRead = 4,    // [2] the stage's tables and record read: 8 epilogue, 5 mask and 4 state warps
     kTblAny = 6,     // [2] the stage's tables and tile record written (every position, and the end record)
     kBCFree = 8,     // [2] MMA done with the stage's B and C
     kXFree = 10,     // [2] the tile's y (staged in the stage's x) stored: 8 epilogue warps
     kGFull = 12,     // [2] C B^T in the buffer
-    kLGFull = 14,    // [2] L o G in the buffer: 4 mask warps
+    kLGFull = 14,    // [2] L o G in the buffer: 5 mask warps
     kGBFree = 16,    // [2] the buffer's Yo read: 8 epilogue warps
     kDrained = 18,   // [2] the stage's Yd read and x weighted (a correction tile: begun): 8 epilogue warps
     kYDFull = 20,    // Yd in TMEM
     kState = 21,     // h_{t-1} staged as bf16, a_t h_{t-1} back in TMEM (correction: h_in staged): 4 state warps
     kSO = 22,        // S(t) and Yo(t) done (correction: the correction product done)
-    kVTFree = 23,    // the factored-mask table read (off-diagonal blocks done): 4 mask warps
+    kVTFree = 23,    // the factored-mask table read (off-diagonal blocks done): 5 mask warps
     kNcorr = 24,     // the correction tile count written (table warp, once)
     kMmaDone = 25,   // the MMA warp's final drain
     kYDFree = 26,    // the tile's z (held in the Yd columns) read by the combine: 8 epilogue warps
@@ -103,8 +104,9 @@ __host__ __device__ constexpr uint32_t bar_count(int i) {
     return ((i >= kXFree && i < kXFree + 2) || (i >= kGBFree && i < kGBFree + 2) || (i >= kDrained && i < kDrained + 2) ||
             i == kYDFree)
                ? 8u
-         : (i >= kTblRead && i < kTblRead + 2) ? 16u
-         : ((i >= kLGFull && i < kLGFull + 2) || i == kState || i == kVTFree) ? 4u
+         : (i >= kTblRead && i < kTblRead + 2) ? 17u
+         : ((i >= kLGFull && i < kLGFull + 2) || i == kVTFree) ? 5u
+         : i == kState ? 4u
          : 1u;
 }
 
@@ -199,9 +201,10 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 // Per-warpgroup register budgets (setmaxnreg): the launch gives every thread kLaunchRegs; the
-// producer / MMA / tables warpgroup and the mask warpgroup hand some back and the two epilogue
-// warpgroups take them: 128 (80 + 88 + 96) + 256 * 96 <= 640 * 96.
-constexpr uint32_t kLaunchRegs = 96, kRegsWG0 = 80, kRegsMask = 88, kRegsEpi = 96;
+// producer / MMA / tables / quadrant-3 mask warpgroup and the mask warpgroup hand some back and the two
+// epilogue warpgroups take them: 128 (88 + 88 + 96) + 256 * 96 <= 640 * 96. The first warpgroup's budget
+// equals the mask warpgroup's, since warp 3 runs the mask code.
+constexpr uint32_t kLaunchRegs = 96, kRegsWG0 = 88, kRegsMask = 88, kRegsEpi = 96;
 static_assert(128 * (kRegsWG0 + kRegsMask + kLaunchRegs) + 256 * kRegsEpi <= 640 * kLaunchRegs, "register split");
 template <uint32_t R> __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(R)); }
 template <uint32_t R> __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(R)); }
@@ -838,17 +841,19 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             }
         }
         if (!ok) set_abort();
-    } else if (warp == 3) {
-        regs_dec<kRegsWG0>();          // no role; its share of the registers goes to the epilogue
-    } else if (warp >= kWarpMask && warp < kWarpMask + 4) {
+    } else if ((warp >= kWarpMask && warp < kWarpMask + 4) || warp == kWarpMaskQ3) {
         // ============================================================ L o G (one warp per lane quadrant)
         // Row i = 32 q + lane of the tile; 16-column group g holds tokens j = 16 g .. 16 g + 15 and is
         // written as packed bf16 (8 columns of head 0, then 8 of head 1). 32-block b = g / 2:
         //   b < q   exp(cs_i - cs_p) exp(cs_p - cs_j), p the block's last token (both factors <= 1)
         //   b = q   exp(cs_i - cs_j), zero where j > i
         //   b > q   zero
+        // Quadrant 3 has the most: its four blocks are split between warp 7 (blocks 0, 1) and warp 3
+        // (blocks 2, 3), which write disjoint columns. (Warp 3 belongs to the first warpgroup, whose
+        // register budget equals the mask warpgroup's.)
         regs_dec<kRegsMask>();
         const int q = warp & 3, i = 32 * q + lane;
+        const int b_lo = warp == kWarpMaskQ3 ? 2 : 0, b_hi = warp == kWarpMask + 3 ? 2 : 4;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
         uint32_t ph = 0;
         bool ok = true;
@@ -890,11 +895,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
             for (int e = 0; e < 8; ++e) zero[e] = 0u;
             if (!__any_sync(0xffffffffu, rv)) {
                 if (lane == 0) mbar_arrive(sm.bars() + kVTFree);
-#pragma unroll
-                for (int g = 0; g < 8; ++g) { tmem_st8(gcol + 16 * g, zero); tmem_st8(gcol + 16 * g + 8, zero); }
+#pragma unroll 1
+                for (int g = 2 * b_lo; g < 2 * b_hi; ++g) { tmem_st8(gcol + 16 * g, zero); tmem_st8(gcol + 16 * g + 8, zero); }
             } else {
 #pragma unroll 1
-                for (int b = 0; b < 4; ++b) {
+                for (int b = b_lo; b < b_hi; ++b) {
                     if (b > q) {
                         tmem_st8(gcol + 32 * b, zero);
                         tmem_st8(gcol + 32 * b + 8, zero);
@@ -965,6 +970,11 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
                             tmem_st8(gcol + 32 * b + 16 * gg + 8 * hh, pk);
                         }
                     }
+                }
+                if (b_hi <= q) {
+                    // (this warp's blocks are all off-diagonal: done with the column table)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sm.bars() + kVTFree);
                 }
             }
             tmem_wait_st();
