@@ -46,15 +46,15 @@ KERNEL_SOURCES = {
                              "mamba_ssd_layer_gb300/csrc/ptx.cuh"),
 }
 NCU_TRAFFIC = {
-    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 216657920 + 149097984, "stamp": "28e277d349734659"},
-    "long_n64": {"kernel": "ssd_fused_kernel", "bytes": 200741888 + 140881920, "stamp": "28e277d349734659"},
+    "long_n128": {"kernel": "ssd_fused_kernel", "bytes": 215609856 + 147755520, "stamp": "3e8598256e8f7998"},
+    "long_n64": {"kernel": "ssd_fused_kernel", "bytes": 200652032 + 138599168, "stamp": "3e8598256e8f7998"},
     # N = 256: the mean of the two launches of one pass (one per 128-column half of the state)
-    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 292590080 + 144763264, "stamp": "28e277d349734659"},
-    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 207759616 + 149413888, "stamp": "28e277d349734659"},
+    "long_n256": {"kernel": "ssd_fused_kernel", "bytes": 293294464 + 143305216, "stamp": "3e8598256e8f7998"},
+    "long_n128_dtscaled": {"kernel": "ssd_fused_kernel", "bytes": 207725312 + 147934976, "stamp": "3e8598256e8f7998"},
     # y (50 MB) largely still in L2 when the launch ends
-    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 60471296 + 12652544, "stamp": "28e277d349734659"},
-    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 214985984 + 154567424, "stamp": "28e277d349734659"},
-    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 177894912 + 122017280, "stamp": "28e277d349734659"},
+    "m2_130m": {"kernel": "ssd_fused_kernel", "bytes": 60464384 + 12846336, "stamp": "3e8598256e8f7998"},
+    "m2_2p7b": {"kernel": "ssd_fused_kernel", "bytes": 215682048 + 153395712, "stamp": "3e8598256e8f7998"},
+    "varlen": {"kernel": "ssd_fused_kernel", "bytes": 178385408 + 121009664, "stamp": "3e8598256e8f7998"},
     # recurrent step: part of the state's write-back is still in L2 when the launch ends
     "decode_2p7b": {"kernel": "ssd_decode_kernel", "bytes": 168496384 + 117444864, "stamp": "e82f933ea29a60b6"},
     "decode_2p7b_bf16state": {"kernel": "ssd_decode_kernel", "bytes": 84610304 + 34867712,
