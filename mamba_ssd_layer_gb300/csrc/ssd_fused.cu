@@ -1518,15 +1518,12 @@ cudaError_t launch_fused_n(const Problem& p, const FusedArgs& fa, const FusedMap
 
 }  // namespace
 
-// Busiest CTA's time for a dense batch cut into windows of K tiles, in units of one tile: every window
-// costs its tiles plus a fixed overhead, and a window that publishes an aggregate (its successor runs
-// in the same iteration) also reads its tiles once more at `agg_cost` of a tile each.
 // CTAs of the fused launch. Each takes one contiguous range of the chain-major tile run. A range that
 // starts inside its chain pays a tail at the end (the look-back, the fold and the correction tiles),
 // worth about kTailTiles tiles (measured on GB300). When a dense batch has at most one chain per SM and
 // a chain is not longer than an even range plus that tail, one CTA per chain does without any tail (and
 // with fewer CTAs its tiles run a little faster): the Mamba-2-130M-shaped layer, 96 chains of 16 tiles,
-// takes 83 us that way against 94 us on 152 ranges of 10 or 11 tiles.
+// takes 80 us that way against 86 us on 152 ranges of 10 or 11 tiles.
 constexpr int64_t kTailTiles = 6;
 static int fused_grid(const Problem& p) {
     const int grid = p.num_sms < kFusedMaxGrid ? p.num_sms : kFusedMaxGrid;
