@@ -990,12 +990,13 @@ ssd_fused_kernel(const __grid_constant__ FusedMaps maps, const FusedArgs a) {
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 8) {
         // ============================================================ epilogue (one warpgroup per head)
         // Row i = 32 q + lane of the tile, head hh of the pair, its 64 channels.
-        //   tile:  drain -- z = Yd + D x (fp32, kept in registers), x row times exp(last - cs_i) in place
+        //   tile:  drain -- z = Yd + D x (fp32, back into the Yd columns), x row times exp(last - cs_i)
+        //          in place
         //          combine -- y = z + exp(cs_i) Yo, rounded once to bf16, staged in the x region of the
         //          stage (free once S and Yo are done), and stored: a row quadrant wholly inside the
         //          sequence as one bulk tensor store (kAccum: a bulk reduce-add), otherwise row by row
-        //   correction tile: z = the row's y as the window pass stored it, then the same combine with
-        //          exp(cs_i) (cs from the first window's start) and the correction product, stored
+        //   correction tile: the same combine with z = 0, exp(cs_i) (cs from the first window's start)
+        //          and the correction product, added onto the stored y (a bulk reduce-add, or row by row)
         regs_inc<kRegsEpi>();
         const int hh = (warp - kWarpEpi) >> 2, q = warp & 3, i = 32 * q + lane, ix = i & 7;
         const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
