@@ -7,6 +7,10 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
+Other workloads (--workload): the forward on the other layer shapes (long_n64, long_n256, m2_130m,
+m2_2p7b, varlen, long_n128_dtscaled), the one-token recurrent step (decode_2p7b,
+decode_2p7b_bf16state) and the block's output gate and normalization (gated_norm_long).
+
 --impl reference times the fp64 CPU oracle on the host cores on a bounded sample of
 the same workload (the slow baseline the GPU path is checked against).
 Multi-GPU (torchrun): every rank runs its own copy of the workload (independent
