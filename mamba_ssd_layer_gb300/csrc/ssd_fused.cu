@@ -268,9 +268,10 @@ __device__ __forceinline__ bool wait_par_slow(uint64_t* bars, volatile int* abor
     uint64_t* bar = bars + idx;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        // the thread sleeps until the phase completes or about 20 us pass, so that waiting warps leave
-        // the issue slots to the warps that work
-        if (mbar_try_wait_sleep(bar, par, 20000u)) return true;
+        // try_wait lets the hardware suspend the thread briefly while the phase is pending (with the
+        // default time limit: a long sleep hint made every hand-off wake later, a spin on test_wait took
+        // issue slots from the warps that work; both measured slower)
+        if (mbar_try_wait(bar, par)) return true;
         if ((it & 7u) != 0) continue;
         if (honor_abort && *w.abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
