@@ -295,8 +295,8 @@ __device__ __forceinline__ bool wait_bar(const Waiter& w, int idx, uint32_t& ph)
 }
 
 // Bounded wait like wait_bar that, while the phase is pending, keeps calling `side` (which returns true
-// once it has nothing left to do) between short sleeps; the single-thread MMA issuer uses it to issue
-// independent work as soon as that work's inputs are there.
+// once it has nothing left to do) between brief hardware suspensions; the single-thread MMA issuer uses
+// it to issue independent work as soon as that work's inputs are there.
 template <class F>
 __device__ __forceinline__ bool poll_bar(const Waiter& w, int idx, uint32_t& ph, F&& side) {
     const uint32_t par = (ph >> idx) & 1u;
@@ -308,7 +308,7 @@ __device__ __forceinline__ bool poll_bar(const Waiter& w, int idx, uint32_t& ph,
                 if (!wait_par_slow(w.bars, w.abort, w.status, idx, par, true)) return false;
                 break;
             }
-            if (mbar_try_wait_sleep(bar, par, 200u)) break;
+            if (mbar_try_wait(bar, par)) break;
             if ((it & 7u) != 0) continue;
             if (*w.abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
